@@ -1,0 +1,376 @@
+"""Pins of the CPU oracle to facts fixed outside itself (closed forms, textbook
+tables, published generator output, brute force on tiny inputs, invariants).
+
+Each test would fail on a plausible slip in the oracle: a dropped term, a
+wrong sign or index, a transposed operand, a wrong stage order or rounding.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import okvq_oracle as o
+from bit_kv_cache_rht_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F16, F32, F64 = np.float16, np.float32, np.float64
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- RHT
+
+def test_splitmix64_published_sequence():
+    g = _golden("splitmix64.json")
+    got = o.splitmix64(g["seed"], len(g["outputs_hex"]))
+    assert got == [int(h, 16) for h in g["outputs_hex"]]
+
+
+def test_hadamard_signs_are_the_stream_bits():
+    w0, w1 = o.splitmix64(7, 2)
+    s = o.hadamard_signs(7, 128)
+    assert set(np.unique(s)) <= {-1, 1}
+    for c in (0, 5, 63, 64, 100, 127):
+        bit = ((w0 if c < 64 else w1) >> (c % 64)) & 1
+        assert s[c] == (-1 if bit else 1)
+
+
+@pytest.mark.parametrize("d", [2, 4, 8, 16, 32, 64, 128])
+def test_sylvester_hadamard_orthogonality_exact(d):
+    H = o.sylvester_hadamard(d)
+    assert np.array_equal(H @ H.T, d * np.eye(d, dtype=np.int64))
+    assert np.array_equal(H, H.T)
+    assert H[0].tolist() == [1] * d and H[:, 0].tolist() == [1] * d
+
+
+def test_fwht_equals_matrix_product():
+    r = np.random.default_rng(0)
+    x = r.standard_normal((5, 128))
+    H = o.sylvester_hadamard(128).astype(F64)
+    assert np.allclose(o.fwht(x, F64), x @ H.T, atol=1e-11, rtol=0)
+
+
+def test_fwht_fp32_exact_on_integers_and_order_matters_only_by_rounding():
+    # small integers: every butterfly sum is exact, so the fp32 canonical order
+    # must give exactly the fp64 (exact) transform
+    r = np.random.default_rng(1)
+    x = r.integers(-1000, 1000, (7, 128)).astype(F32)
+    assert np.array_equal(o.fwht(x, F32).astype(F64), o.fwht(x.astype(F64), F64))
+
+
+def test_rotate_keys_f32_close_to_fp64_and_norm_preserving():
+    r = np.random.default_rng(2)
+    k = (r.standard_normal((64, 128)) * 3).astype(F16)
+    s = o.hadamard_signs(11, 128)
+    k32 = o.rotate_keys_f32(k, s)
+    k64 = o.rotate_f64(k.astype(F64), s)
+    assert k32.dtype == F32
+    assert np.max(np.abs(k32 - k64)) < 2e-5
+    assert np.allclose(np.linalg.norm(k64, axis=1), np.linalg.norm(k.astype(F64), axis=1), rtol=1e-12)
+    # a sign slip (D after H instead of before) is a different transform
+    wrong = o.fwht(k.astype(F64), F64) * s / math.sqrt(128)
+    assert np.max(np.abs(wrong - k64)) > 0.1
+
+
+# ---------------------------------------------------------------- codebook
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16])
+def test_lloyd_max_textbook(n):
+    g = _golden("lloyd_max_gaussian.json")
+    lv = o.lloyd_max_gaussian(n)
+    pos = lv[n // 2:]
+    ref = np.array(g["levels"][str(n)])
+    ulp = 10.0 ** (np.floor(np.log10(np.abs(ref))) - 3)      # 4 significant digits printed
+    assert np.all(np.abs(pos - ref) <= 0.6 * ulp)
+    assert np.allclose(lv, -lv[::-1], atol=1e-13)
+    # fixed point: each level is the Gaussian mean of its cell (closed form)
+    th = [-math.inf] + [0.5 * (lv[j] + lv[j + 1]) for j in range(n - 1)] + [math.inf]
+    for j in range(n):
+        assert abs(lv[j] - o.gaussian_cell_mean(th[j], th[j + 1])) < 1e-12
+    # mean-squared error of the quantizer, integrated in closed form per cell:
+    # E[(X-y)^2; a<X<b] = (P + a phi(a) - b phi(b)) - 2y(phi(a)-phi(b)) + y^2 P
+    mse = 0.0
+    for j in range(n):
+        a, b, y = th[j], th[j + 1], lv[j]
+        P = o._Phi(b) - o._Phi(a)
+        ta = a * o._phi(a) if math.isfinite(a) else 0.0
+        tb = b * o._phi(b) if math.isfinite(b) else 0.0
+        mse += (P + ta - tb) - 2 * y * (o._phi(a) - o._phi(b)) + y * y * P
+    if str(n) in g["mse"]:
+        ref_mse = g["mse"][str(n)]
+        assert abs(mse - ref_mse) <= 0.6 * 10.0 ** (math.floor(math.log10(ref_mse)) - 3)
+    # the closed form agrees with direct numerical integration of (x - y)^2 phi(x)
+    from scipy.integrate import quad
+    num = sum(quad(lambda x, y=lv[j]: (x - y) ** 2 * o._phi(x), max(th[j], -40.0), min(th[j + 1], 40.0),
+                   epsabs=1e-15, epsrel=1e-13)[0] for j in range(n))
+    assert abs(num - mse) < 1e-12
+
+
+def test_lloyd_max_two_level_closed_form():
+    assert abs(o.lloyd_max_gaussian(2)[1] - math.sqrt(2 / math.pi)) < 1e-13
+
+
+def test_four_level_thresholds_textbook():
+    g = _golden("lloyd_max_gaussian.json")
+    cb = o.make_codebook(2)
+    assert np.allclose(cb.vthr[1:], g["thresholds"]["4"], atol=2e-3)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_codebook_derivation(bits):
+    cb = o.make_codebook(bits)
+    n = 1 << bits
+    assert cb.levels16.dtype == F16 and len(cb.levels16) == n
+    assert np.all(np.diff(cb.levels) > 0)
+    assert np.array_equal(cb.vthr.astype(F64), (cb.levels[:-1] + cb.levels[1:]) / 2)   # exact midpoints
+    assert cb.ktab[0] == 0.0 and cb.ktab[-1] == 1.0 and np.all(np.diff(cb.ktab) > 0)
+    assert np.array_equal(cb.kthr.astype(F64), (cb.ktab[:-1] + cb.ktab[1:]) / 2)
+    # key levels are the value levels renormalised to [0, 1]
+    lam = (cb.levels - cb.levels[0]) / (cb.levels[-1] - cb.levels[0])
+    assert np.max(np.abs(cb.ktab - lam)) <= 2.0 ** -11
+
+
+# ---------------------------------------------------------------- storage roundings
+
+def test_directed_fp16_rounding():
+    r = np.random.default_rng(3)
+    x = (r.standard_normal(20000) * 5).astype(F32)
+    dn, up = o.f16_round_down(x), o.f16_round_up(x)
+    assert np.all(dn.astype(F32) <= x) and np.all(up.astype(F32) >= x)
+    # tightest: the next fp16 past each bound crosses x
+    nxt = np.nextafter(dn, F16(np.inf)).astype(F32)
+    assert np.all((dn.astype(F32) == x) | (nxt > x))
+    prv = np.nextafter(up, F16(-np.inf)).astype(F32)
+    assert np.all((up.astype(F32) == x) | (prv < x))
+
+
+# ---------------------------------------------------------------- key groups
+
+def _brute_nearest(x, levels):
+    """argmin_j |x - level_j|, ties to the lower index, by enumeration."""
+    d = np.abs(np.asarray(x, F64)[..., None] - np.asarray(levels, F64))
+    return np.argmin(d, axis=-1).astype(np.uint8)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_key_group_codes_bounds_and_brute_force(bits):
+    cb = o.make_codebook(bits)
+    r = np.random.default_rng(4 + bits)
+    s = o.hadamard_signs(3, 128)
+    k = (r.standard_normal((32, 128)) * r.uniform(0.5, 4, 128) + 0.7).astype(F16)
+    kp = o.rotate_keys_f32(k, s)
+    mn, mx, codes, bnd = o.quantize_key_group(kp, cb)
+    mn64, mx64 = mn.astype(F64), mx.astype(F64)
+    assert np.all(mn64 <= kp.min(0)) and np.all(mx64 >= kp.max(0))
+    u = (kp.astype(F64) - mn64) / (mx64 - mn64)
+    ref = _brute_nearest(u, cb.ktab)
+    ok = ~bnd
+    assert np.array_equal(codes[ok], ref[ok])
+    rec = mn64 + cb.ktab[codes] * (mx64 - mn64)
+    assert np.all(rec >= mn64 - 1e-12) and np.all(rec <= mx64 + 1e-12)
+    gap = np.max(np.diff(cb.ktab))
+    assert np.all(np.abs(rec - kp) <= (mx64 - mn64) * gap / 2 + 1e-6)
+    # every code of a wide group is used somewhere; the top and bottom levels are hit
+    assert codes.min() == 0 and codes.max() == (1 << bits) - 1
+
+
+def test_key_group_degenerate_range_gives_code_zero():
+    cb = o.make_codebook(2)
+    kp = np.full((32, 128), 1.25, F32)
+    mn, mx, codes, _ = o.quantize_key_group(kp, cb)
+    assert np.all(mn == mx) and np.all(codes == 0)
+
+
+# ---------------------------------------------------------------- values
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_value_codes_brute_force_and_error_identity(bits):
+    cb = o.make_codebook(bits)
+    r = np.random.default_rng(10 + bits)
+    v = (r.standard_normal((50, 128)) * 2 + 0.5).astype(F16)
+    R = np.linalg.qr(r.standard_normal((128, 128)))[0].astype(F32)
+    nrm, codes, bnd, nb = o.quantize_values(v, R, cb)
+    v64 = v.astype(F64)
+    n = np.linalg.norm(v64, axis=1)
+    assert np.array_equal(nrm, n.astype(F16))
+    w = math.sqrt(128) * (v64 / n[:, None]) @ R.astype(F64).T
+    ref = _brute_nearest(w, cb.levels)
+    assert np.array_equal(codes[~bnd], ref[~bnd])
+    # per-coordinate bound: half the widest gap inside the table, clipping outside
+    gap = np.max(np.diff(cb.levels))
+    err = np.abs(w - cb.levels[codes])
+    bound = np.maximum(gap / 2, np.maximum(0, np.abs(w) - cb.levels[-1]))
+    assert np.all(err <= bound + 1e-9)
+    # orthogonality: |v - v_hat| = n |u - u_hat| with u_hat = R^T l / sqrt d
+    uh = (cb.levels[codes] / math.sqrt(128)) @ R.astype(F64)
+    vh = n[:, None] * uh
+    lhs = np.linalg.norm(v64 - vh, axis=1)
+    rhs = n * np.linalg.norm(v64 / n[:, None] - uh, axis=1)
+    assert np.allclose(lhs, rhs, rtol=1e-12)
+    assert np.allclose(np.linalg.norm(uh, axis=1), np.linalg.norm(cb.levels[codes], axis=1) / math.sqrt(128))
+
+
+def test_zero_value_vector():
+    cb = o.make_codebook(2)
+    R = np.eye(128, dtype=F32)
+    nrm, codes, _, _ = o.quantize_values(np.zeros((1, 128), F16), R, cb)
+    assert nrm[0] == 0 and np.all(codes == 1)       # nearest level to 0, tie -> lower middle level
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_pack_roundtrip_and_bit_positions(bits):
+    r = np.random.default_rng(20)
+    c = r.integers(0, 1 << bits, (3, 128)).astype(np.uint8)
+    p = o.pack_codes(c, bits)
+    assert p.shape == (3, 128 * bits // 8)
+    assert np.array_equal(o.unpack_codes(p, bits), c)
+    one = np.zeros((1, 128), np.uint8)
+    one[0, 5] = (1 << bits) - 1
+    pk = o.pack_codes(one, bits)
+    if bits == 2:
+        assert pk[0, 1] == 0b00001100 and pk.sum() == 12
+    else:
+        assert pk[0, 2] == 0xF0 and pk.sum() == 0xF0
+
+
+# ---------------------------------------------------------------- attention
+
+def _unit(bits=2, G=32, T=203, seed=0, Gq=4):
+    cb = o.make_codebook(bits)
+    r = np.random.default_rng(seed)
+    R = np.stack([np.linalg.qr(r.standard_normal((128, 128)))[0] for _ in range(3)]).astype(F32)
+    u = o.OracleUnit(128, G, cb, o.hadamard_signs(99, 128), R, Gq, 1024)
+    T1 = T // 2
+    for a, b in ((0, T1), (T1, T)):
+        K = (r.standard_normal((b - a, 128)) * 2 + np.linspace(0, 1, b - a)[:, None]).astype(F16)
+        V = (r.standard_normal((b - a, 128)) * 1.5 + 0.3).astype(F16)
+        mod = r.integers(0, 3, b - a).astype(np.uint8)
+        u.append(K, V, mod)
+    return u, r
+
+
+@pytest.mark.parametrize("bits,G,T", [(2, 32, 203), (2, 64, 130), (4, 32, 96), (4, 64, 31)])
+def test_fused_scores_equal_bruteforce(bits, G, T):
+    u, r = _unit(bits, G, T, seed=bits * 100 + G + T)
+    q = (r.standard_normal((4, 128)) * 1.5).astype(F16)
+    a = u.decode(q)
+    b = u.decode_bruteforce(q)
+    assert np.max(np.abs(a - b)) < 1e-10
+
+
+def test_single_token_output_is_its_dequantized_value():
+    u, r = _unit(T=1)
+    q = r.standard_normal((4, 128)).astype(F16)
+    _, Vh = u.dequantized()
+    assert np.allclose(u.decode(q), np.broadcast_to(Vh[0], (4, 128)), atol=1e-12)
+
+
+def test_zero_query_gives_mean_value():
+    u, r = _unit(T=150)
+    _, Vh = u.dequantized()
+    out = u.decode(np.zeros((4, 128), F16))
+    assert np.allclose(out, np.broadcast_to(Vh.mean(0), (4, 128)), atol=1e-12)
+
+
+def test_empty_unit_outputs_zero():
+    cb = o.make_codebook(2)
+    R = np.stack([np.eye(128, dtype=F32)] * 3)
+    u = o.OracleUnit(128, 32, cb, o.hadamard_signs(1, 128), R, 2, 64)
+    assert np.all(u.decode(np.ones((2, 128), F16)) == 0)
+
+
+def test_grid_keys_reproduce_exact_attention():
+    """Keys built so their rotated coordinates sit on the group's grid: the codec
+    is then lossless for keys (up to the fp16 rounding of the constructed keys),
+    so the fused output must match exact attention over those keys."""
+    G, T, d = 32, 96, 128
+    cb = o.make_codebook(2)
+    r = np.random.default_rng(5)
+    s = o.hadamard_signs(42, d)
+    H = o.sylvester_hadamard(d).astype(F64)
+    codes = r.integers(0, 4, (T, d))
+    codes[0::G] = 0
+    codes[1::G] = 3                                      # every channel reaches both ends
+    mn = np.repeat(r.uniform(-3, -1, (T // G, d)), G, 0)
+    mx = mn + np.repeat(r.uniform(1, 4, (T // G, d)), G, 0)
+    kp = mn + cb.ktab[codes] * (mx - mn)
+    K = ((kp @ H.T) * s / math.sqrt(d)).astype(F16)      # k = D H^T k' / sqrt d
+    V = (r.standard_normal((T, d)) * 2).astype(F16)
+    mod = np.zeros(T, np.uint8)
+    R = np.stack([np.eye(d, dtype=F32)] * 3)
+    u = o.OracleUnit(d, G, cb, s, R, 2, T)
+    u.append(K, V, mod)
+    assert np.mean(u.kcodes[:T] == codes) > 0.97
+    q = r.standard_normal((2, d)).astype(F16)
+    _, Vh = u.dequantized()
+    sc = q.astype(F64) @ K.astype(F64).T / math.sqrt(d)
+    p = np.exp(sc - sc.max(1, keepdims=True))
+    exact = (p / p.sum(1, keepdims=True)) @ Vh
+    assert np.max(np.abs(u.decode(q) - exact)) < 5e-3
+
+
+def test_streaming_chunking_invariance():
+    w = synth.tiny(seed=7)
+    R = w.value_rotations()
+    K, V = w.session_kv(0)
+    mod = w.sessions[0].modality()
+
+    def build(bounds):
+        c = o.OracleCache(1, 1, 8, 2, 128, 32, 2, 2048, w.hadamard_seed, R)
+        for a, b in bounds:
+            c.append(0, K[a:b], V[a:b], mod[a:b])
+        return c
+
+    T = len(mod)
+    one = build([(0, T)])
+    r = np.random.default_rng(0)
+    cuts = np.sort(r.choice(np.arange(1, T), 20, replace=False))
+    rand = build(list(zip([0, *cuts], [*cuts, T])))
+    by97 = build([(a, min(a + 97, T)) for a in range(0, T, 97)])
+    for h in range(2):
+        e0 = one.units[(0, 0, h)].export()
+        for other in (rand, by97):
+            e1 = other.units[(0, 0, h)].export()
+            for key in e0:
+                assert np.array_equal(e0[key], e1[key]), key
+
+
+# ---------------------------------------------------------------- synthetic inputs
+
+def test_value_rotations_orthogonal_and_diagonalising():
+    w = synth.tiny(seed=3)
+    R = w.value_rotations().astype(F64)
+    assert R.shape == (1, 2, 3, 128, 128)
+    for h in range(2):
+        for m in range(3):
+            Rm = R[0, h, m]
+            assert np.max(np.abs(Rm @ Rm.T - np.eye(128))) < 1e-5
+    # the basis diagonalises its modality's calibration covariance
+    from bit_kv_cache_rht_gb300.synth import CALIB_TOKENS, interleave_pattern, _rng
+    mod = interleave_pattern([(0, 64), (1, 25), (2, 8)], CALIB_TOKENS)
+    _, vscale, mu = w.layer_params(0)
+    z = _rng(w.seed, "calib", 0).standard_normal((CALIB_TOKENS, 2, 128), dtype=F32)
+    Vc = (vscale[None] * z + mu[mod]).astype(F16).astype(F64)
+    X = Vc[mod == 0, 1]
+    C = np.cov(X, rowvar=False)
+    D = R[0, 1, 0] @ C @ R[0, 1, 0].T
+    off = D - np.diag(np.diag(D))
+    assert np.max(np.abs(off)) < 1e-5 * np.trace(C)
+    assert np.all(np.diff(np.diag(D)) <= 1e-6 * np.trace(C))
+
+
+def test_workload_streams():
+    w = synth.qwen3b(tokens=32768)
+    m = w.sessions[0].modality()
+    assert len(m) == 32768 and set(np.unique(m)) == {0, 1, 2}
+    c = w.sessions[0].chunks
+    assert len(c[0]) == 665 and len(c[29]) == 697
+    t = synth.tiny()
+    mt = t.sessions[0].modality()
+    assert len(mt) == 2048 and mt[:64].tolist() == [0] * 64 and mt[64:89].tolist() == [1] * 25
+    assert mt[2037:].tolist() == [0] * 11
