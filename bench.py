@@ -1,0 +1,362 @@
+#!/usr/bin/env python3
+"""Benchmark: 2-bit omni KV decode attention on one GB300 (or N replicas).
+
+Workload (default): Qwen2.5-Omni-3B-shaped decode - 36 layers, 16 query / 2 kv
+heads, head_dim 128, one session holding a 32,768-token cache built by
+appending 1-s chunks of 640 video + 25 audio tokens (a 32-token text turn
+every 30 chunks); 2-bit codes, key group 32. One step = one okvq_decode over
+all layers (the split-K fused attention kernel + the merge / inverse-rotation
+kernel). Two replicas of the cache alternate so consecutive steps never find
+their 194 MB of codes in the 129 MB L2.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_rht_gb300 import synth  # noqa: E402
+
+METRIC = "2-bit KV decode attention: context tokens/s and HBM GB/s (% of GB300 peak)"
+UNIT = "context tokens/s"
+
+
+def algorithmic_bytes(w, lengths):
+    """Decode bytes per step: codes, statistics, norms, fp16 tail keys, modality ids, q and out."""
+    sh = w.shape
+    d, b, G = sh.head_dim, sh.bits, sh.group_size
+    per_unit = 0
+    for T in lengths:
+        per_unit_T = T * (2 * d * b // 8 + 2) + (T // G) * 4 * d + (T % G) * 2 * d
+        per_unit += per_unit_T * sh.num_layers * sh.num_kv_heads
+    mod = sum(lengths)
+    qo = 2 * len(lengths) * sh.num_layers * sh.num_q_heads * d
+    rot = sh.num_layers * sh.num_kv_heads * sh.num_modalities * d * d * 4
+    return per_unit + mod + qo // 2, qo // 2, rot     # split kernel bytes, merge kernel out bytes, R bytes
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + q, "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, gpu_index=0):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[0] == str(gpu_index):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def build_cache(w, torch, device, replicas=2):
+    from bit_kv_cache_rht_gb300.okvq import Cache
+    sh = w.shape
+    R = w.value_rotations()
+    T = w.sessions[0].length
+    K = torch.empty((T, sh.num_layers, sh.num_kv_heads, sh.head_dim), dtype=torch.float16, device=device)
+    V = torch.empty_like(K)
+    for l in range(sh.num_layers):
+        k, v = w.layer_kv(0, l)
+        K[:, l] = torch.from_numpy(k).to(device)
+        V[:, l] = torch.from_numpy(v).to(device)
+    M = torch.from_numpy(w.sessions[0].modality()).to(device)
+    caches, append_ms = [], []
+    for rep in range(replicas):
+        c = Cache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, w.max_tokens, R, head_dim=sh.head_dim,
+                  group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
+                  hadamard_seed=w.hadamard_seed)
+        st = torch.cuda.current_stream()
+        ev = []
+        for a, b in w.sessions[0].chunk_bounds():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            c.append(0, K[a:b], V[a:b], M[a:b])
+            e1.record(st)
+            ev.append((e0, e1, b - a))
+        torch.cuda.synchronize()
+        if c.check_errors() != 0:
+            raise RuntimeError("device error word set after append")
+        append_ms.append([(e0.elapsed_time(e1), n) for e0, e1, n in ev])
+        caches.append(c)
+    del K, V
+    torch.cuda.empty_cache()
+    return caches, append_ms
+
+
+def cpu_baseline_child(args):
+    """Time the CPU oracle, as it stands, on a bounded sample: decode of the
+    (layer 0, kv heads 0..Hkv-1) units of the workload, single-threaded."""
+    from oracle import okvq_oracle as o
+    w = synth.WORKLOADS[args.workload]()
+    sh = w.shape
+    R = w.value_rotations()
+    oc = o.OracleCache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.group_size, sh.bits,
+                       w.max_tokens, w.hadamard_seed, R, layers=[0])
+    K, V = w.session_kv(0, [0])
+    mod = w.sessions[0].modality()
+    for a, b in w.sessions[0].chunk_bounds():
+        oc.append(0, K[a:b], V[a:b], mod[a:b], layers_in=[0])
+    Q = w.queries(0)
+    reps, t_total = 0, 0.0
+    budget = args.cpu_seconds
+    while t_total < budget or reps == 0:
+        t0 = time.perf_counter()
+        oc.decode(Q)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        if reps >= args.cpu_max_reps:
+            break
+    per_sample = t_total / reps
+    units_total = sh.num_layers * sh.num_kv_heads
+    step_s = per_sample * units_total / sh.num_kv_heads
+    T = w.sessions[0].length
+    print(json.dumps({"value": T / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+                      "sample": "oracle decode of layer 0 (%d of %d (layer, kv head) units), %d repetitions, "
+                                "%.1f s of CPU time, extrapolated linearly to all %d layers"
+                                % (sh.num_kv_heads, units_total, reps, t_total, sh.num_layers),
+                      "step_s": step_s}))
+
+
+def run_cpu_baseline(args):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload,
+           "--cpu-seconds", str(args.cpu_seconds), "--cpu-max-reps", str(args.cpu_max_reps)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    steps = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        res = run_cpu_baseline(argparse.Namespace(workload=args.workload, cpu_seconds=args.ref_seconds,
+                                                  cpu_max_reps=1))
+        if i >= args.warmup:
+            steps.append(res)
+        base = res
+    vals = [s["value"] for s in steps if s.get("value")]
+    v = statistics.median(vals) if vals else None
+    w = synth.WORKLOADS[args.workload]()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": (statistics.median([s["step_s"] for s in steps]) * 1e3) if steps else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": base["sample"] if base else None},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_of(w, args):
+    sh = w.shape
+    return {"workload": "%s: %d layers, %d q / %d kv heads, head_dim %d, %d-token cache, %d-bit codes, group %d"
+                        % (w.name, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
+                           w.sessions[0].length, sh.bits, sh.group_size),
+            "sessions": len(w.sessions), "context_tokens": w.sessions[0].length, "bits": sh.bits,
+            "group_size": sh.group_size,
+            "l2": "inputs larger than L2: two cache replicas (2 x %.0f MB) alternate between steps"
+                  % (algorithmic_bytes(w, [s.length for s in w.sessions])[0] / 1e6),
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="okvq", choices=["okvq", "reference"])
+    ap.add_argument("--workload", default="qwen3b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-max-reps", type=int, default=1000)
+    ap.add_argument("--ref-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true")
+    args = ap.parse_args()
+    if args.cpu_baseline_child:
+        return cpu_baseline_child(args)
+    if args.impl == "reference":
+        return reference_arm(args)
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    from bit_kv_cache_rht_gb300 import okvq
+    okvq.load()
+
+    w = synth.WORKLOADS[args.workload]()
+    sh = w.shape
+    caches, append_ms = build_cache(w, torch, device, replicas=2)
+    T = w.sessions[0].length
+    lengths = [s.length for s in w.sessions]
+    split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths)
+    step_bytes = split_bytes + out_bytes
+
+    Q = torch.from_numpy(w.queries(0)).to(device)
+    out = torch.empty_like(Q)
+    st = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        caches[i % 2].decode(Q, out)
+    torch.cuda.synchronize()
+    for c in caches:
+        c.profile_enable(True)
+    sampler = ClockSampler()
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        caches[i % 2].decode(Q, out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        dist.barrier()
+    split_ms, merge_ms = [], []
+    for c in caches:
+        a, b = c.profile_read()
+        split_ms += list(a)
+        merge_ms += list(b)
+        c.profile_enable(False)
+
+    # end to end: pinned host q -> device, decode, device -> pinned host out, every step
+    q_host = Q.cpu().pin_memory()
+    o_host = torch.empty(Q.shape, dtype=torch.float16).pin_memory()
+    q_dev = torch.empty_like(Q)
+    for i in range(3):
+        q_dev.copy_(q_host, non_blocking=True)
+        caches[i % 2].decode(q_dev, out)
+        o_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(st)
+    for i in range(args.steps):
+        q_dev.copy_(q_host, non_blocking=True)
+        caches[i % 2].decode(q_dev, out)
+        o_host.copy_(out, non_blocking=True)
+    f1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    clocks = sampler.stop(local) if rank == 0 else None
+
+    t_max = ms
+    e2e_max = e2e_ms
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max, e2e_max = float(t[0]), float(t[1])
+    total_tokens = world * args.steps * sum(lengths)
+    value = total_tokens / (t_max / 1e3)
+    e2e_value = total_tokens / (e2e_max / 1e3)
+
+    if rank == 0:
+        peak, peak_kind = peaks()
+        avg_split = float(np.mean(split_ms))
+        achieved = split_bytes / (avg_split / 1e3) / 1e9
+        ms_step = t_max / args.steps
+        ap_ms = sum(x for x, _ in append_ms[0])
+        ap_tokens = sum(n for _, n in append_ms[0])
+        ap_bytes_tok = sh.num_layers * sh.num_kv_heads * (2 * 2 * sh.head_dim + 2 * sh.head_dim * sh.bits // 8 + 2
+                                                           + 4 * sh.head_dim / sh.group_size) + 1
+        traffic = None
+        tp = os.path.join(ROOT, "profiles", "decode_traffic.json")
+        if os.path.exists(tp):
+            with open(tp) as f:
+                tj = json.load(f)
+            if tj.get("workload") == args.workload:
+                traffic = tj.get("bytes_per_launch")
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
+            "config": config_of(w, args),
+            "hbm_gbs_step": step_bytes / (ms_step / 1e3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel (split-K fused 2-bit attention)",
+                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "bytes_per_launch": split_bytes, "avg_launch_ms": avg_split,
+                         "merge_kernel_avg_ms": float(np.mean(merge_ms)),
+                         "with_R_frac_step": (step_bytes + rot_bytes) / (ms_step / 1e3) / 1e9 / peak},
+            "append": {"tokens_per_s": ap_tokens / (ap_ms / 1e3), "chunks": len(append_ms[0]),
+                       "gbs": ap_tokens * ap_bytes_tok / (ap_ms / 1e3) / 1e9,
+                       "frac": ap_tokens * ap_bytes_tok / (ap_ms / 1e3) / 1e9 / peak},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(Q.numel() * 2),
+                    "d2h_bytes_per_step": int(out.numel() * 2)},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = run_cpu_baseline(args)
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,588 @@
+// Host side of the okvq C ABI: configuration checks, the codebook and Hadamard
+// signs, device allocation, the decode work partition and the canonical export.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "okvq_internal.h"
+
+using namespace okvq;
+
+struct okvq_cache {
+  okvq_config cfg{};
+  int S = 0, L = 0, Hq = 0, Hkv = 0, G = 0, bits = 0, M = 0;
+  long long max_tokens = 0, P_max = 0, cap = 0, units = 0;
+  PageLayout PL{};
+  int num_sms = 0, device = 0;
+  // device memory
+  uint8_t *pages = nullptr;
+  __half *tails = nullptr;      // [2][units][G][D]
+  uint8_t *mod = nullptr;       // [S][cap]
+  uint8_t *tmask = nullptr;     // [S][cap/16]
+  float *rot = nullptr;         // [L][Hkv][M][D][D]
+  float *rot_t = nullptr;       // transposed per matrix
+  float *signs = nullptr;       // [D]
+  uint32_t *err = nullptr;
+  float *partials = nullptr;
+  int *table = nullptr;         // device work table
+  size_t table_bytes = 0;
+  long long max_segs = 0;
+  int max_cta = 0;
+  // host state
+  std::vector<long long> len;   // per session
+  std::vector<int> tail_sel;    // per session: current tail buffer
+  bool dirty = true;
+  int ncta = 0, nseg = 0;
+  void *host_table = nullptr;   // pinned staging of the work table
+  cudaEvent_t table_ev = nullptr;
+  bool table_ev_pending = false;
+  // offsets (bytes) inside the table
+  size_t off_segs = 0, off_cta = 0, off_useg = 0, off_ulen = 0, off_utail = 0;
+  // codebook
+  __half levels16[16];
+  __half klev16[16];
+  float vthr[15], kthr[15];
+  int nlev = 0;
+  // profiling
+  bool prof = false;
+  std::vector<cudaEvent_t> ev;  // triples per decode call
+  int prof_calls = 0;
+};
+
+namespace {
+
+constexpr int CTAS_PER_SM = 2;
+
+uint64_t splitmix64_next(uint64_t &state) {
+  state += 0x9E3779B97F4A7C15ull;
+  uint64_t z = state;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+double std_normal_pdf(double x) { return std::isfinite(x) ? std::exp(-0.5 * x * x) / std::sqrt(2.0 * M_PI) : 0.0; }
+double std_normal_cdf(double x) {
+  if (x == INFINITY) return 1.0;
+  if (x == -INFINITY) return 0.0;
+  return 0.5 * std::erfc(-x / std::sqrt(2.0));
+}
+
+// Lloyd-Max quantizer of N(0,1) with n levels: thresholds are midpoints of the
+// levels, levels are the conditional means of their cells; iterate to a fixed point.
+void lloyd_max(int n, double *lv) {
+  for (int j = 0; j < n; ++j) lv[j] = -2.0 + 4.0 * j / (n - 1);
+  std::vector<double> th(n + 1), nw(n);
+  for (int it = 0; it < 200000; ++it) {
+    th[0] = -INFINITY;
+    th[n] = INFINITY;
+    for (int j = 1; j < n; ++j) th[j] = 0.5 * (lv[j - 1] + lv[j]);
+    double delta = 0.0;
+    for (int j = 0; j < n; ++j) {
+      nw[j] = (std_normal_pdf(th[j]) - std_normal_pdf(th[j + 1])) / (std_normal_cdf(th[j + 1]) - std_normal_cdf(th[j]));
+      delta = std::max(delta, std::fabs(nw[j] - lv[j]));
+    }
+    for (int j = 0; j < n; ++j) lv[j] = nw[j];
+    if (delta < 1e-15) break;
+  }
+}
+
+okvq_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return OKVQ_OK;
+  if (e == cudaErrorMemoryAllocation) return OKVQ_ENOMEM;
+  return OKVQ_ECUDA;
+}
+
+#define OKVQ_TRY(expr)                              \
+  do {                                              \
+    cudaError_t e_ = (expr);                        \
+    if (e_ != cudaSuccess) return cuda_status(e_);  \
+  } while (0)
+
+okvq_status alloc_dev(void **p, size_t bytes) {
+  cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return e == cudaErrorMemoryAllocation ? OKVQ_ENOMEM : OKVQ_ECUDA;
+  }
+  return OKVQ_OK;
+}
+
+void release(okvq_cache *h) {
+  cudaFree(h->pages);
+  cudaFree(h->tails);
+  cudaFree(h->mod);
+  cudaFree(h->tmask);
+  cudaFree(h->rot);
+  cudaFree(h->rot_t);
+  cudaFree(h->signs);
+  cudaFree(h->err);
+  cudaFree(h->partials);
+  cudaFree(h->table);
+  if (h->host_table) cudaFreeHost(h->host_table);
+  if (h->table_ev) cudaEventDestroy(h->table_ev);
+  for (auto e : h->ev) cudaEventDestroy(e);
+  delete h;
+}
+
+bool valid_stream_arg(void *) { return true; }
+
+// (lane, j, e) -> bit position of the code in a lane chunk and the page-tile offset
+inline int code_bit(int bits, int j, int e) { return bits * (2 * j + e); }
+
+// Build the decode work partition: balanced page ranges over the flattened
+// (unit, page) list, cut at unit boundaries into segments.
+void build_table(okvq_cache *h) {
+  const long long U = h->units;
+  std::vector<long long> pages_u(U);
+  long long P = 0;
+  const int LH = h->L * h->Hkv;
+  for (long long u = 0; u < U; ++u) {
+    long long T = h->len[u / LH];
+    pages_u[u] = (T + PAGE - 1) / PAGE;
+    P += pages_u[u];
+  }
+  int ncta = (int)std::min<long long>(P, h->max_cta);
+  char *base = static_cast<char *>(h->host_table);
+  int *segs = reinterpret_cast<int *>(base + h->off_segs);
+  int *cta_seg = reinterpret_cast<int *>(base + h->off_cta);
+  int *unit_seg = reinterpret_cast<int *>(base + h->off_useg);
+  long long *ulen = reinterpret_cast<long long *>(base + h->off_ulen);
+  int *utail = reinterpret_cast<int *>(base + h->off_utail);
+  for (long long u = 0; u < U; ++u) {
+    ulen[u] = h->len[u / LH];
+    utail[u] = h->tail_sel[u / LH];
+  }
+  int nseg = 0;
+  long long u = 0, ustart = 0;   // ustart = flattened index of unit u's first page
+  for (int c = 0; c < ncta; ++c) {
+    long long a = (long long)c * P / ncta, b = (long long)(c + 1) * P / ncta;
+    cta_seg[c] = nseg;
+    long long x = a;
+    while (x < b) {
+      while (u < U && ustart + pages_u[u] <= x) {
+        ustart += pages_u[u];
+        ++u;
+      }
+      long long pb = x - ustart;
+      long long pe = std::min(b - ustart, pages_u[u]);
+      segs[4 * nseg + 0] = (int)u;
+      segs[4 * nseg + 1] = (int)pb;
+      segs[4 * nseg + 2] = (int)pe;
+      segs[4 * nseg + 3] = 0;
+      ++nseg;
+      x = ustart + pe;
+    }
+  }
+  cta_seg[ncta] = nseg;
+  // unit -> first segment (segments are ordered by unit)
+  int s = 0;
+  for (long long uu = 0; uu <= U; ++uu) {
+    while (s < nseg && segs[4 * s] < uu) ++s;
+    unit_seg[uu] = s;
+  }
+  h->ncta = ncta;
+  h->nseg = nseg;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *okvq_status_string(okvq_status s) {
+  switch (s) {
+    case OKVQ_OK: return "ok";
+    case OKVQ_EINVAL: return "invalid argument";
+    case OKVQ_ENOMEM: return "out of memory";
+    case OKVQ_ECAPACITY: return "capacity exceeded";
+    case OKVQ_ECUDA: return "CUDA error";
+    case OKVQ_ESTATE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) {
+  if (!cfg || !out) return OKVQ_EINVAL;
+  *out = nullptr;
+  const okvq_config &c = *cfg;
+  if (c.num_sessions < 1 || c.num_layers < 1 || c.num_kv_heads < 1 || c.num_q_heads < 1) return OKVQ_EINVAL;
+  if (c.num_q_heads % c.num_kv_heads != 0 || c.num_q_heads / c.num_kv_heads > MAXGQ) return OKVQ_EINVAL;
+  if (c.head_dim != D) return OKVQ_EINVAL;
+  if (c.group_size != 32 && c.group_size != 64) return OKVQ_EINVAL;
+  if (c.bits != 2 && c.bits != 4) return OKVQ_EINVAL;
+  if (c.num_modalities < 1 || c.num_modalities > MAXM) return OKVQ_EINVAL;
+  if (c.max_tokens < 1 || c.max_tokens > (1ll << 40)) return OKVQ_EINVAL;
+  if (!c.value_rot) return OKVQ_EINVAL;
+  const int nlev = 1 << c.bits;
+  double lv[16];
+  if (c.codebook) {
+    for (int j = 0; j < nlev; ++j) {
+      lv[j] = c.codebook[j];
+      if (!std::isfinite(lv[j])) return OKVQ_EINVAL;
+      if (j && !(lv[j] > lv[j - 1])) return OKVQ_EINVAL;
+    }
+  } else {
+    lloyd_max(nlev, lv);
+  }
+  okvq_cache *h = new (std::nothrow) okvq_cache();
+  if (!h) return OKVQ_ENOMEM;
+  h->cfg = c;
+  h->cfg.codebook = nullptr;
+  h->cfg.value_rot = nullptr;
+  h->S = c.num_sessions;
+  h->L = c.num_layers;
+  h->Hq = c.num_q_heads;
+  h->Hkv = c.num_kv_heads;
+  h->G = c.group_size;
+  h->bits = c.bits;
+  h->M = c.num_modalities;
+  h->max_tokens = c.max_tokens;
+  h->P_max = (c.max_tokens + PAGE - 1) / PAGE;
+  h->cap = h->P_max * PAGE;
+  h->units = (long long)h->S * h->L * h->Hkv;
+  h->PL = page_layout(h->bits, h->G);
+  h->len.assign(h->S, 0);
+  h->tail_sel.assign(h->S, 0);
+  // codebook: the fp16-rounded levels define it (values); key levels renormalised to [0, 1]
+  h->nlev = nlev;
+  double l16[16], k16[16];
+  for (int j = 0; j < nlev; ++j) {
+    h->levels16[j] = __double2half(lv[j]);
+    l16[j] = (double)__half2float(h->levels16[j]);
+  }
+  for (int j = 0; j < nlev; ++j) {
+    h->klev16[j] = __double2half((l16[j] - l16[0]) / (l16[nlev - 1] - l16[0]));
+    k16[j] = (double)__half2float(h->klev16[j]);
+  }
+  for (int j = 0; j + 1 < nlev; ++j) {
+    h->vthr[j] = (float)((l16[j] + l16[j + 1]) / 2.0);
+    h->kthr[j] = (float)((k16[j] + k16[j + 1]) / 2.0);
+  }
+  for (int j = nlev - 1; j < 15; ++j) h->vthr[j] = h->kthr[j] = INFINITY;
+  for (int j = nlev; j < 16; ++j) h->levels16[j] = h->klev16[j] = __float2half(0.f);
+
+  okvq_status st = OKVQ_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto fail = [&](okvq_status e) {
+    release(h);
+    return e;
+  };
+  if (cudaGetDevice(&h->device) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
+    return fail(OKVQ_ECUDA);
+  h->max_cta = h->num_sms * CTAS_PER_SM;
+  const size_t page_total = (size_t)h->units * h->P_max * h->PL.page_bytes;
+  const size_t tails = 2 * (size_t)h->units * h->G * D * sizeof(__half);
+  const size_t rot = (size_t)h->L * h->Hkv * h->M * D * D * sizeof(float);
+  h->max_segs = (long long)h->max_cta + h->units + 1;
+  const size_t partials = (size_t)h->max_segs * MAXGQ * PARTIAL_FLOATS * sizeof(float);
+  if ((st = alloc_dev((void **)&h->pages, page_total)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->tails, tails)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->mod, (size_t)h->S * h->cap)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->tmask, (size_t)h->S * (h->cap / TILE))) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->rot, rot)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->rot_t, rot)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
+  // work table: segs [max_segs][4] int | cta_seg [max_cta+1] | unit_seg [units+1] | unit_len [units] i64 | unit_tail
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 15) & ~size_t(15);
+    return o;
+  };
+  h->off_segs = take((size_t)h->max_segs * 4 * sizeof(int));
+  h->off_cta = take((size_t)(h->max_cta + 1) * sizeof(int));
+  h->off_useg = take((size_t)(h->units + 1) * sizeof(int));
+  h->off_ulen = take((size_t)h->units * sizeof(long long));
+  h->off_utail = take((size_t)h->units * sizeof(int));
+  h->table_bytes = off;
+  if ((st = alloc_dev((void **)&h->table, h->table_bytes)) != OKVQ_OK) return fail(st);
+  if (cudaMallocHost(&h->host_table, h->table_bytes) != cudaSuccess) return fail(OKVQ_ENOMEM);
+  if (cudaEventCreateWithFlags(&h->table_ev, cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
+
+  // contents
+  if (cudaMemsetAsync(h->pages, 0, page_total, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaMemsetAsync(h->tails, 0, tails, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaMemsetAsync(h->mod, 0, (size_t)h->S * h->cap, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaMemsetAsync(h->tmask, 0, (size_t)h->S * (h->cap / TILE), s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  {
+    const size_t nmat = (size_t)h->L * h->Hkv * h->M;
+    std::vector<float> rt(nmat * D * D);
+    for (size_t mtx = 0; mtx < nmat; ++mtx) {
+      const float *R = c.value_rot + mtx * D * D;
+      float *T = rt.data() + mtx * D * D;
+      for (int i = 0; i < D; ++i)
+        for (int cc = 0; cc < D; ++cc) T[cc * D + i] = R[i * D + cc];
+    }
+    if (cudaMemcpyAsync(h->rot, c.value_rot, rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+    if (cudaMemcpyAsync(h->rot_t, rt.data(), rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+    uint64_t state = c.hadamard_seed;
+    float sg[D];
+    for (int w = 0; w < D / 64; ++w) {
+      uint64_t z = splitmix64_next(state);
+      for (int b = 0; b < 64; ++b) sg[64 * w + b] = ((z >> b) & 1ull) ? -1.f : 1.f;
+    }
+    if (cudaMemcpyAsync(h->signs, sg, sizeof(sg), cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  }
+  *out = h;
+  return OKVQ_OK;
+}
+
+void okvq_free(okvq_cache *h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  release(h);
+}
+
+okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens) {
+  if (!h || !tokens || session < 0 || session >= h->S) return OKVQ_EINVAL;
+  *tokens = h->len[session];
+  return OKVQ_OK;
+}
+
+okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, const void *v, const uint8_t *modality,
+                              int32_t num_tokens, void *stream) {
+  if (!h || session < 0 || session >= h->S || num_tokens < 0) return OKVQ_EINVAL;
+  if (num_tokens == 0) return OKVQ_OK;
+  if (!k || !v || !modality) return OKVQ_EINVAL;
+  const long long T0 = h->len[session];
+  if (T0 + num_tokens > h->max_tokens) return OKVQ_ECAPACITY;
+  AppendArgs a{};
+  a.k = static_cast<const __half *>(k);
+  a.v = static_cast<const __half *>(v);
+  a.mod_in = modality;
+  a.n = num_tokens;
+  a.T0 = T0;
+  a.session = session;
+  a.L = h->L;
+  a.Hkv = h->Hkv;
+  a.M = h->M;
+  a.bits = h->bits;
+  a.G = h->G;
+  a.P_max = h->P_max;
+  a.pages = h->pages;
+  const size_t tail_buf = (size_t)h->units * h->G * D;
+  a.tail_old = h->tails + (size_t)h->tail_sel[session] * tail_buf;
+  a.tail_new = h->tails + (size_t)(1 - h->tail_sel[session]) * tail_buf;
+  a.mod = h->mod;
+  a.tmask = h->tmask;
+  a.cap = h->cap;
+  a.rot_t = h->rot_t;
+  a.signs = h->signs;
+  a.err = h->err;
+  a.page0 = T0 / PAGE;
+  a.nlev = h->nlev;
+  for (int j = 0; j < 15; ++j) {
+    a.vthr[j] = h->vthr[j];
+    a.kthr[j] = h->kthr[j];
+  }
+  const long long last = (T0 + num_tokens - 1) / PAGE;
+  const int n_pages = (int)(last - a.page0 + 1);
+  cudaError_t e = launch_append(a, n_pages, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  h->len[session] = T0 + num_tokens;
+  h->tail_sel[session] ^= 1;
+  h->dirty = true;
+  return OKVQ_OK;
+}
+
+okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
+  if (!h || !q || !out) return OKVQ_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->dirty) {
+    if (h->table_ev_pending) OKVQ_TRY(cudaEventSynchronize(h->table_ev));   // staging buffer free again
+    build_table(h);
+    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table, h->table_bytes, cudaMemcpyHostToDevice, s));
+    OKVQ_TRY(cudaEventRecord(h->table_ev, s));
+    h->table_ev_pending = true;
+    h->dirty = false;
+  }
+  const char *tb = reinterpret_cast<const char *>(h->table);
+  DecodeArgs a{};
+  a.q = static_cast<const __half *>(q);
+  a.pages = h->pages;
+  a.tails = h->tails;
+  a.mod = h->mod;
+  a.tmask = h->tmask;
+  a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
+  a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
+  a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);
+  a.unit_tail = reinterpret_cast<const int *>(tb + h->off_utail);
+  a.partials = h->partials;
+  a.L = h->L;
+  a.Hq = h->Hq;
+  a.Hkv = h->Hkv;
+  a.M = h->M;
+  a.bits = h->bits;
+  a.G = h->G;
+  a.P_max = h->P_max;
+  a.cap = h->cap;
+  a.units = h->units;
+  a.signs = h->signs;
+  a.err = h->err;
+  for (int j = 0; j < 16; ++j) {
+    a.klut_src[j] = h->klev16[j];
+    a.vlut_src[j] = h->levels16[j];
+  }
+  CombineArgs cb{};
+  cb.partials = h->partials;
+  cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
+  cb.rot = h->rot;
+  cb.out = static_cast<__half *>(out);
+  cb.L = h->L;
+  cb.Hq = h->Hq;
+  cb.Hkv = h->Hkv;
+  cb.M = h->M;
+  cb.units = h->units;
+  cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
+  if (h->prof) {
+    const size_t need = 3 * (size_t)(h->prof_calls + 1);
+    while (h->ev.size() < need) {
+      cudaEvent_t ev;
+      OKVQ_TRY(cudaEventCreate(&ev));
+      h->ev.push_back(ev);
+    }
+    e0 = h->ev[3 * h->prof_calls];
+    e1 = h->ev[3 * h->prof_calls + 1];
+    e2 = h->ev[3 * h->prof_calls + 2];
+    OKVQ_TRY(cudaEventRecord(e0, s));
+  }
+  OKVQ_TRY(launch_decode(a, h->ncta, s));
+  if (h->prof) OKVQ_TRY(cudaEventRecord(e1, s));
+  OKVQ_TRY(launch_combine(cb, s));
+  if (h->prof) {
+    OKVQ_TRY(cudaEventRecord(e2, s));
+    ++h->prof_calls;
+  }
+  return OKVQ_OK;
+}
+
+okvq_status okvq_profile_enable(okvq_cache *h, int enable) {
+  if (!h) return OKVQ_EINVAL;
+  h->prof = enable != 0;
+  h->prof_calls = 0;
+  return OKVQ_OK;
+}
+
+okvq_status okvq_profile_read(okvq_cache *h, float *split_ms, float *merge_ms, int32_t cap, int32_t *count) {
+  if (!h || !count || cap < 0) return OKVQ_EINVAL;
+  const int n = std::min<int>(cap, h->prof_calls);
+  for (int i = 0; i < n; ++i) {
+    OKVQ_TRY(cudaEventSynchronize(h->ev[3 * i + 2]));
+    float t1 = 0.f, t2 = 0.f;
+    OKVQ_TRY(cudaEventElapsedTime(&t1, h->ev[3 * i], h->ev[3 * i + 1]));
+    OKVQ_TRY(cudaEventElapsedTime(&t2, h->ev[3 * i + 1], h->ev[3 * i + 2]));
+    if (split_ms) split_ms[i] = t1;
+    if (merge_ms) merge_ms[i] = t2;
+  }
+  *count = n;
+  return OKVQ_OK;
+}
+
+okvq_status okvq_codebook(const okvq_cache *h, float *levels, float *key_levels) {
+  if (!h) return OKVQ_EINVAL;
+  for (int j = 0; j < h->nlev; ++j) {
+    if (levels) levels[j] = __half2float(h->levels16[j]);
+    if (key_levels) key_levels[j] = __half2float(h->klev16[j]);
+  }
+  return OKVQ_OK;
+}
+
+okvq_status okvq_check_errors(okvq_cache *h, void *stream, uint32_t *word) {
+  if (!h) return OKVQ_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t w = 0;
+  OKVQ_TRY(cudaStreamSynchronize(s));
+  OKVQ_TRY(cudaMemcpy(&w, h->err, sizeof(w), cudaMemcpyDeviceToHost));
+  OKVQ_TRY(cudaMemset(h->err, 0, sizeof(uint32_t)));
+  if (word) *word = w;
+  return w ? OKVQ_ESTATE : OKVQ_OK;
+}
+
+okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, size_t *bytes) {
+  if (!h || !bytes || session < 0 || session >= h->S) return OKVQ_EINVAL;
+  const long long T = h->len[session];
+  const int G = h->G, bits = h->bits;
+  const long long Tf = (T / G) * G;
+  const int B = D * bits / 8;
+  const long long LH = (long long)h->L * h->Hkv;
+  const size_t n_kc = (size_t)LH * Tf * B, n_ks = (size_t)LH * (Tf / G) * 2 * D * 2,
+               n_kt = (size_t)LH * (T - Tf) * D * 2, n_vc = (size_t)LH * T * B, n_vn = (size_t)LH * T * 2,
+               n_md = (size_t)T;
+  const size_t need = n_kc + n_ks + n_kt + n_vc + n_vn + n_md;
+  if (!host_buf) {
+    *bytes = need;
+    return OKVQ_OK;
+  }
+  if (*bytes < need) return OKVQ_EINVAL;
+  *bytes = need;
+  OKVQ_TRY(cudaDeviceSynchronize());
+  uint8_t *out = static_cast<uint8_t *>(host_buf);
+  uint8_t *o_kc = out, *o_ks = o_kc + n_kc, *o_kt = o_ks + n_ks, *o_vc = o_kt + n_kt, *o_vn = o_vc + n_vc,
+          *o_md = o_vn + n_vn;
+  std::memset(out, 0, need);
+  const long long npages = (T + PAGE - 1) / PAGE;
+  const PageLayout PL = h->PL;
+  std::vector<uint8_t> pg((size_t)npages * PL.page_bytes);
+  std::vector<__half> tail((size_t)G * D);
+  // where code (tok in tile, channel) sits: lane chunk and bit, for K and V layouts
+  std::vector<int> kpos(TILE * D), vpos(TILE * D);
+  for (int lane = 0; lane < 32; ++lane)
+    for (int j = 0; j < 32; ++j)
+      for (int e = 0; e < 2; ++e) {
+        int tok, ch;
+        k_pair_coords(lane, j, e, tok, ch);
+        kpos[tok * D + ch] = lane * PL.lane_bytes * 8 + code_bit(bits, j, e);
+        v_pair_coords(lane, j, e, tok, ch);
+        vpos[tok * D + ch] = lane * PL.lane_bytes * 8 + code_bit(bits, j, e);
+      }
+  int inv_stat[D];
+  for (int p = 0; p < D; ++p) inv_stat[stat_channel(p)] = p;
+  const uint32_t mask = (1u << bits) - 1u;
+  for (long long lh = 0; lh < LH; ++lh) {
+    const long long unit = (long long)session * LH + lh;
+    if (npages)
+      OKVQ_TRY(cudaMemcpy(pg.data(), h->pages + (unit * h->P_max) * PL.page_bytes, (size_t)npages * PL.page_bytes,
+                          cudaMemcpyDeviceToHost));
+    for (long long t = 0; t < T; ++t) {
+      const uint8_t *p = pg.data() + (t / PAGE) * PL.page_bytes;
+      const int tt = (int)(t % PAGE), tile = tt / TILE, r = tt % TILE;
+      for (int ch = 0; ch < D; ++ch) {
+        int vb = vpos[r * D + ch];
+        uint32_t vc = (p[PL.off_v + tile * PL.tile_bytes + vb / 8] >> (vb % 8)) & mask;
+        o_vc[(lh * T + t) * B + ch * bits / 8] |= (uint8_t)(vc << ((ch * bits) % 8));
+        if (t < Tf) {
+          int kbp = kpos[r * D + ch];
+          uint32_t kc = (p[tile * PL.tile_bytes + kbp / 8] >> (kbp % 8)) & mask;
+          o_kc[(lh * Tf + t) * B + ch * bits / 8] |= (uint8_t)(kc << ((ch * bits) % 8));
+        }
+      }
+      std::memcpy(o_vn + (lh * T + t) * 2, p + PL.off_norm + tt * 2, 2);
+    }
+    for (long long gi = 0; gi < Tf / G; ++gi) {
+      const uint8_t *p = pg.data() + ((gi * G) / PAGE) * PL.page_bytes + PL.off_stats + ((gi * G) % PAGE) / G * 2 * D * 2;
+      const __half *st = reinterpret_cast<const __half *>(p);
+      __half *dst = reinterpret_cast<__half *>(o_ks) + (lh * (Tf / G) + gi) * 2 * D;
+      for (int ch = 0; ch < D; ++ch) {
+        dst[ch] = st[inv_stat[ch]];
+        dst[D + ch] = st[D + inv_stat[ch]];
+      }
+    }
+    if (T > Tf) {
+      const __half *src = h->tails + ((size_t)h->tail_sel[session] * h->units + unit) * G * D;
+      OKVQ_TRY(cudaMemcpy(tail.data(), src, (size_t)(T - Tf) * D * 2, cudaMemcpyDeviceToHost));
+      std::memcpy(o_kt + (size_t)lh * (T - Tf) * D * 2, tail.data(), (size_t)(T - Tf) * D * 2);
+    }
+  }
+  if (T) OKVQ_TRY(cudaMemcpy(o_md, h->mod + (size_t)session * h->cap, (size_t)T, cudaMemcpyDeviceToHost));
+  return OKVQ_OK;
+}
+
+}  // extern "C"

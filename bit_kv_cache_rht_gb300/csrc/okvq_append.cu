@@ -1,0 +1,319 @@
+// Append kernel: rotate + quantize + pack one chunk of tokens into the cache.
+//
+// "OmniKVQuant: KV Cache Quantization for Omni-LLMs", section 2 METHOD:
+//   keys   - randomized Hadamard rotation (TurboQuant bullet), then min-max
+//            scaling within each group of consecutive tokens with stored group
+//            statistics and the shared fixed codebook (first OmniKVQuant bullet);
+//   values - magnitude/direction split (TurboQuant bullet), rotation by the
+//            token's modality eigenbasis (second OmniKVQuant bullet), the same
+//            fixed codebook; everything bit-packed.
+//
+// One CTA per (touched 64-token page, layer, kv head). Values of the new tokens
+// are quantized at once; a key group is quantized by the CTA whose page holds it
+// when its last token arrives, reading earlier members from the fp16 tail buffer.
+// The CTA owning the last touched page writes the new fp16 tail into the other
+// tail buffer, so no CTA writes memory another CTA reads.
+#include "okvq_internal.h"
+
+namespace okvq {
+
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int XT_STRIDE = PAGE + 4;        // transposed value tile row stride (floats)
+constexpr float INV_SQRT_D = 0.0883883476483184405501f;   // fp32(1/sqrt(128))
+constexpr float SQRT_D = 11.3137084989847603904f;
+
+struct Smem {
+  float rt[D * D];                 // R_m^T for one modality (c-major)
+  float xt[D * XT_STRIDE];         // value tile, transposed [c][token]; later keys [token][c]
+  uint8_t vc[PAGE * D];            // value codes of the page
+  uint8_t kc[PAGE * D];            // key codes of the page
+  float vnorm[PAGE];
+  int mod[PAGE];
+  float kmn[2][D], kmx[2][D];
+  int present[MAXM];
+};
+
+__device__ __forceinline__ int stat_pos(int c) {
+  int kb = c >> 4, r = c & 15;
+  int t = (r & 7) >> 1;
+  int i = (r & 1) | ((r >> 3) << 1);
+  return 32 * t + 4 * kb + i;
+}
+
+__device__ __forceinline__ int code_of(float x, const float *thr, int nthr) {
+  int c = 0;
+#pragma unroll 15
+  for (int j = 0; j < 15; ++j)
+    if (j < nthr && x > thr[j]) ++c;
+  return c;
+}
+
+// Pack the codes of tile `tile` (16 tokens) from codes[64][128] into lane chunks.
+// `kind` 0 = K layout, 1 = V layout. Tokens >= valid_end (page-relative) pack as 0.
+__device__ void pack_tile(const uint8_t *codes, uint8_t *dst, int tile, int bits, int kind, int valid_end,
+                          int tid, int nthreads) {
+  const int words_per_lane = bits * 2;         // 16 B or 32 B per lane
+  for (int w = tid; w < 32 * words_per_lane; w += nthreads) {
+    int lane = w / words_per_lane, wi = w % words_per_lane;
+    uint32_t word = 0;
+    const int codes_per_word = 32 / bits;
+    for (int q = 0; q < codes_per_word; ++q) {
+      int bitpos = wi * 32 + q * bits;         // position in the lane chunk
+      int j = bitpos / (2 * bits), e = (bitpos / bits) & 1;
+      int tok, ch;
+      if (kind == 0) k_pair_coords(lane, j, e, tok, ch);
+      else v_pair_coords(lane, j, e, tok, ch);
+      tok += 16 * tile;
+      uint32_t c = tok < valid_end ? codes[tok * D + ch] : 0u;
+      word |= c << (q * bits);
+    }
+    reinterpret_cast<uint32_t *>(dst)[lane * words_per_lane + wi] = word;
+  }
+}
+
+// Inverse of pack_tile for tokens < keep_end (page-relative): fill codes[][] from dst.
+__device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int bits, int kind, int keep_end,
+                            int tid, int nthreads) {
+  const int words_per_lane = bits * 2;
+  const uint32_t mask = (1u << bits) - 1u;
+  for (int w = tid; w < 32 * words_per_lane; w += nthreads) {
+    int lane = w / words_per_lane, wi = w % words_per_lane;
+    uint32_t word = reinterpret_cast<const uint32_t *>(src)[lane * words_per_lane + wi];
+    const int codes_per_word = 32 / bits;
+    for (int q = 0; q < codes_per_word; ++q) {
+      int bitpos = wi * 32 + q * bits;
+      int j = bitpos / (2 * bits), e = (bitpos / bits) & 1;
+      int tok, ch;
+      if (kind == 0) k_pair_coords(lane, j, e, tok, ch);
+      else v_pair_coords(lane, j, e, tok, ch);
+      tok += 16 * tile;
+      if (tok < keep_end) codes[tok * D + ch] = (uint8_t)((word >> (q * bits)) & mask);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const PageLayout PL = page_layout(a.bits, a.G);
+
+  const long long page = a.page0 + blockIdx.x;
+  const int lh = blockIdx.y;                       // layer * Hkv + kv head
+  const int layer = lh / a.Hkv;
+  const long long unit = (long long)a.session * a.L * a.Hkv + lh;
+  const long long P0 = page * PAGE;
+  const long long T0 = a.T0, T1 = a.T0 + a.n;
+  const int ta = (int)(max(P0, T0) - P0);          // new tokens [ta, tb) page-relative
+  const int tb = (int)(min(P0 + PAGE, T1) - P0);
+  const int row_stride = a.L * a.Hkv * D;          // between tokens in the input
+  uint8_t *pg = a.pages + (unit * a.P_max + page) * (long long)PL.page_bytes;
+
+  // ---- modality ids of the new tokens (validated) ----
+  for (int t = tid; t < PAGE; t += THREADS) {
+    int m = 0;
+    if (t >= ta && t < tb) {
+      m = a.mod_in[P0 + t - T0];
+      if (m >= a.M) {
+        if (lh == 0) atomicOr(a.err, ERR_MODALITY);
+        m = 0;
+      }
+    }
+    S.mod[t] = m;
+  }
+  if (tid < MAXM) S.present[tid] = 0;
+  __syncthreads();
+  for (int t = ta + tid; t < tb; t += THREADS) S.present[S.mod[t]] = 1;
+  if (lh == 0) {
+    uint8_t *mod = a.mod + (long long)a.session * a.cap;
+    for (int t = ta + tid; t < tb; t += THREADS) mod[P0 + t] = (uint8_t)S.mod[t];
+    if (tid < PAGE / TILE) {
+      int t0 = tid * TILE, t1 = t0 + TILE;
+      if (t1 > ta && t0 < tb) {
+        uint8_t *tm = a.tmask + (long long)a.session * (a.cap / TILE) + P0 / TILE + tid;
+        uint8_t bitsm = (t0 < ta) ? *tm : 0;      // tile already partly filled
+        for (int t = max(t0, ta); t < min(t1, tb); ++t) bitsm |= (uint8_t)(1u << S.mod[t]);
+        *tm = bitsm;
+      }
+    }
+  }
+
+  // ---- values: load transposed tile + norms ----
+  for (int i = tid; i < D * XT_STRIDE; i += THREADS) S.xt[i] = 0.f;
+  // keep codes of older tokens that share a 16-token tile with the first new token
+  if (ta % TILE != 0) unpack_tile(S.vc, pg + PL.off_v + (ta / TILE) * PL.tile_bytes, ta / TILE, a.bits, 1, ta,
+                                  tid, THREADS);
+  __syncthreads();
+  for (int t = ta + warp; t < tb; t += THREADS / 32) {
+    const __half *src = a.v + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int c = lane + 32 * k;
+      float x = __half2float(src[c]);
+      S.xt[c * XT_STRIDE + t] = x;
+      ss = fmaf(x, x, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    float n = sqrtf(ss);
+    if (lane == 0) {
+      S.vnorm[t] = n;
+      reinterpret_cast<__half *>(pg + PL.off_norm)[t] = __float2half_rn(n);
+    }
+  }
+  __syncthreads();
+
+  // ---- values: w = sqrt(d) * R_m v / |v| per modality present, then codes ----
+  const int tt = warp;            // tokens 8*tt .. 8*tt+7
+  const int ii = lane;            // outputs 4*ii .. 4*ii+3
+  for (int m = 0; m < a.M; ++m) {
+    if (!S.present[m]) continue;  // uniform: smem flag read after a barrier
+    const float4 *rsrc = reinterpret_cast<const float4 *>(a.rot_t + (((long long)lh * a.M + m) * D * D));
+    float4 *rdst = reinterpret_cast<float4 *>(S.rt);
+    for (int i = tid; i < D * D / 4; i += THREADS) rdst[i] = rsrc[i];
+    __syncthreads();
+    float acc[8][4];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[r][k] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < D; ++c) {
+      const float4 x0 = *reinterpret_cast<const float4 *>(&S.xt[c * XT_STRIDE + 8 * tt]);
+      const float4 x1 = *reinterpret_cast<const float4 *>(&S.xt[c * XT_STRIDE + 8 * tt + 4]);
+      const float4 rv = *reinterpret_cast<const float4 *>(&S.rt[c * D + 4 * ii]);
+      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[r][k] = fmaf(xs[r], rs[k], acc[r][k]);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      int t = 8 * tt + r;
+      if (t >= ta && t < tb && S.mod[t] == m) {
+        float n = S.vnorm[t];
+        float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float w = acc[r][k] * sc;
+          S.vc[t * D + 4 * ii + k] = (uint8_t)code_of(w, a.vthr, a.nlev - 1);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // write the value tiles that got new tokens
+  for (int tile = ta / TILE; tile * TILE < tb; ++tile)
+    pack_tile(S.vc, pg + PL.off_v + tile * PL.tile_bytes, tile, a.bits, 1, tb, tid, THREADS);
+
+  // ---- keys: groups that complete with this chunk ----
+  const int G = a.G;
+  float *xk = S.xt;               // keys as [token][c], row stride D
+  __syncthreads();
+  bool any_group = false;
+  for (int g0 = 0; g0 < PAGE; g0 += G) {
+    long long gend = P0 + g0 + G;
+    bool complete_now = gend > T0 && gend <= T1;
+    any_group |= complete_now;
+    if (!complete_now) continue;
+    const __half *told = a.tail_old + unit * (long long)G * D;
+    // rotate every member: warp per token, lane holds channels 4*lane .. 4*lane+3
+    for (int r = warp; r < G; r += THREADS / 32) {
+      long long t = P0 + g0 + r;
+      const __half *src = t < T0 ? told + (t - (P0 + g0)) * D
+                                 : a.k + (t - T0) * (long long)row_stride + (long long)lh * D;
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = __half2float(src[4 * lane + j]) * a.signs[4 * lane + j];
+      // stride 1 and 2 inside the lane
+      float y0 = __fadd_rn(x[0], x[1]), y1 = __fsub_rn(x[0], x[1]);
+      float y2 = __fadd_rn(x[2], x[3]), y3 = __fsub_rn(x[2], x[3]);
+      x[0] = __fadd_rn(y0, y2); x[2] = __fsub_rn(y0, y2);
+      x[1] = __fadd_rn(y1, y3); x[3] = __fsub_rn(y1, y3);
+      // strides 4 .. 64 across lanes
+#pragma unroll
+      for (int sm = 1; sm < 32; sm <<= 1) {
+        const bool upper = (lane & sm) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float p = __shfl_xor_sync(0xffffffffu, x[j], sm);
+          x[j] = upper ? __fsub_rn(p, x[j]) : __fadd_rn(x[j], p);
+        }
+      }
+      float4 o = make_float4(__fmul_rn(x[0], INV_SQRT_D), __fmul_rn(x[1], INV_SQRT_D), __fmul_rn(x[2], INV_SQRT_D),
+                             __fmul_rn(x[3], INV_SQRT_D));
+      *reinterpret_cast<float4 *>(&xk[(g0 + r) * D + 4 * lane]) = o;
+    }
+    __syncthreads();
+    // per-channel statistics of the group
+    const int gi = g0 / G;
+    for (int c = tid; c < D; c += THREADS) {
+      float mn = xk[g0 * D + c], mx = mn;
+      for (int r = 1; r < G; ++r) {
+        float v = xk[(g0 + r) * D + c];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+      __half hmn = __float2half_rd(mn), hmx = __float2half_ru(mx);
+      S.kmn[gi][c] = __half2float(hmn);
+      S.kmx[gi][c] = __half2float(hmx);
+      __half *st = reinterpret_cast<__half *>(pg + PL.off_stats + gi * 2 * D * 2);
+      st[stat_pos(c)] = hmn;
+      st[D + stat_pos(c)] = hmx;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += THREADS) {
+      int r = i / D, c = i % D;
+      float mn = S.kmn[gi][c], mx = S.kmx[gi][c];
+      float rng = __fsub_rn(mx, mn);
+      int code = 0;
+      if (rng != 0.f) {
+        float u = __fdiv_rn(__fsub_rn(xk[(g0 + r) * D + c], mn), rng);
+        code = code_of(u, a.kthr, a.nlev - 1);
+      }
+      S.kc[(g0 + r) * D + c] = (uint8_t)code;
+    }
+    __syncthreads();
+    for (int tile = g0 / TILE; tile < (g0 + G) / TILE; ++tile)
+      pack_tile(S.kc, pg + tile * PL.tile_bytes, tile, a.bits, 0, PAGE, tid, THREADS);
+    __syncthreads();
+  }
+  (void)any_group;
+
+  // ---- new fp16 tail (only the CTA of the last touched page) ----
+  if (blockIdx.x == gridDim.x - 1) {
+    long long tstart = (T1 / G) * G;
+    const __half *told = a.tail_old + unit * (long long)G * D;
+    __half *tnew = a.tail_new + unit * (long long)G * D;
+    int ntail = (int)(T1 - tstart);
+    for (int i = tid; i < ntail * D; i += THREADS) {
+      int r = i / D, c = i % D;
+      long long t = tstart + r;
+      __half v = t < T0 ? told[(t - (T0 / G) * G) * D + c]
+                        : a.k[(t - T0) * (long long)row_stride + (long long)lh * D + c];
+      tnew[r * D + c] = v;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s) {
+  static bool attr_done = false;
+  size_t smem = sizeof(Smem);
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid(n_pages, a.L * a.Hkv);
+  append_kernel<<<grid, THREADS, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace okvq

@@ -1,0 +1,145 @@
+// Internal definitions of libokvq: device layout of the cache and the kernel
+// launch interface shared by the host API and the kernels.
+//
+// Device layout (everything allocated once by okvq_create):
+//   unit u = (session * L + layer) * Hkv + kv_head owns P_max = ceil(max_tokens/64)
+//   pages of 64 tokens, contiguous: page p of unit u starts at
+//   pages + (u * P_max + p) * page_bytes. A page holds, in order,
+//     K codes  4 tiles of 16 tokens, each tile 32 lane chunks of 16 B (2-bit) or 32 B (4-bit)
+//     V codes  same shape
+//     norms    64 fp16, token order
+//     stats    64/G groups, each [mn 128 fp16 | mx 128 fp16] in the stat channel order
+//   so one decode warp streams one contiguous block per page with a single bulk copy.
+//
+// Lane chunks: the 32 lanes of a warp running mma.m16n8k16 hold A fragments of
+// 16x16 fp16 blocks; lane l owns 32 code pairs j = 0..31 (blk = j/4, reg = j%4),
+// each pair being the two fp16 halves of one A-fragment register:
+//   K tile (A = tokens x channels):  token   = l/4 + 8*(reg&1),
+//                                    channel = 16*blk + 2*(l%4) + 8*(reg>>1) + e
+//   V tile (A = channels x tokens):  token   = 2*(l%4) + 8*(reg>>1) + e,
+//                                    channel = 16*blk + l/4 + 8*(reg&1)
+// with e = 0/1 the half. In the chunk, code e of pair j sits at bit
+// bits*(2*j + e) (2-bit: nibble j, 4-bit: byte j).
+//
+// Stat channel order: position p = 32*t + 4*kb + i (t = 0..3, kb = 0..7, i = 0..3)
+// holds channel 16*kb + 2*t + (i&1) + 8*(i>>1), i.e. the channels lane group t
+// needs for its B fragments, contiguous.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "okvq.h"
+
+namespace okvq {
+
+constexpr int D = 128;
+constexpr int PAGE = 64;
+constexpr int TILE = 16;
+constexpr int MAXM = 3;
+constexpr int MAXGQ = 8;
+
+enum : uint32_t { ERR_MODALITY = 1u, ERR_WAIT = 2u };
+
+struct PageLayout {
+  int bits, G;
+  int lane_bytes;   // 16 or 32
+  int tile_bytes;   // 32 * lane_bytes
+  int off_v;        // 4 tiles of K codes
+  int off_norm;
+  int off_stats;
+  int page_bytes;
+};
+
+__host__ __device__ inline PageLayout page_layout(int bits, int G) {
+  PageLayout L;
+  L.bits = bits;
+  L.G = G;
+  L.lane_bytes = bits * 8;                 // 64 codes * bits / 8
+  L.tile_bytes = 32 * L.lane_bytes;
+  L.off_v = 4 * L.tile_bytes;
+  L.off_norm = 2 * L.off_v;
+  L.off_stats = L.off_norm + PAGE * 2;
+  L.page_bytes = L.off_stats + (PAGE / G) * 2 * D * 2;
+  return L;
+}
+
+// token/channel of code e of pair j in lane l's chunk (see header comment)
+__host__ __device__ inline void k_pair_coords(int lane, int j, int e, int &tok, int &ch) {
+  int blk = j >> 2, reg = j & 3;
+  tok = (lane >> 2) + 8 * (reg & 1);
+  ch = 16 * blk + 2 * (lane & 3) + 8 * (reg >> 1) + e;
+}
+__host__ __device__ inline void v_pair_coords(int lane, int j, int e, int &tok, int &ch) {
+  int blk = j >> 2, reg = j & 3;
+  tok = 2 * (lane & 3) + 8 * (reg >> 1) + e;
+  ch = 16 * blk + (lane >> 2) + 8 * (reg & 1);
+}
+__host__ __device__ inline int stat_channel(int p) {
+  int t = p >> 5, kb = (p >> 2) & 7, i = p & 3;
+  return 16 * kb + 2 * t + (i & 1) + 8 * (i >> 1);
+}
+
+struct AppendArgs {
+  const __half *k;          // [n][L][Hkv][D]
+  const __half *v;
+  const uint8_t *mod_in;    // [n]
+  int n;                    // tokens in this chunk
+  long long T0;             // session length before the append
+  int session;
+  int L, Hkv, M, bits, G;
+  long long P_max;
+  uint8_t *pages;           // all units
+  __half *tail_old;         // [units][G][D] buffer read (current)
+  __half *tail_new;         // [units][G][D] buffer written (next)
+  uint8_t *mod;             // [S][cap] session modality ids
+  uint8_t *tmask;           // [S][cap/16] per 16-token tile modality bits
+  long long cap;            // max_tokens rounded up to a page
+  const float *rot_t;       // [L][Hkv][M][D][D]  (c, i) = R[i][c]
+  const float *signs;       // [D] +-1 Hadamard signs
+  uint32_t *err;
+  long long page0;          // first page touched
+  int nlev;
+  float vthr[15];           // fp32 value thresholds (midpoints of the fp16 levels)
+  float kthr[15];           // fp32 key thresholds (midpoints of the fp16 key levels)
+};
+
+struct DecodeArgs {
+  const __half *q;          // [S][L][Hq][D]
+  const uint8_t *pages;
+  const __half *tails;      // [2][units][G][D]
+  const uint8_t *mod;       // [S][cap]
+  const uint8_t *tmask;     // [S][cap/16]
+  const int *segs;          // [nseg][4] = unit, page_begin, page_end, 0
+  const int *cta_seg;       // [ncta+1]
+  const long long *unit_len;// [units] token count
+  const int *unit_tail;     // [units] 0/1 current tail buffer
+  float *partials;          // [nseg][MAXGQ][2 + MAXM*D]
+  int L, Hq, Hkv, M, bits, G;
+  long long P_max, cap;
+  long long units;
+  uint64_t unused;
+  const float *signs;       // [D] +-1
+  uint32_t *err;
+  __half klut_src[16];      // key levels lambda_j (fp16)
+  __half vlut_src[16];      // value levels l_j (fp16)
+};
+
+struct CombineArgs {
+  const float *partials;
+  const int *unit_seg;      // [units+1]
+  const float *rot;         // [L][Hkv][M][D][D] R[j][i]
+  __half *out;              // [S][L][Hq][D]
+  int L, Hq, Hkv, M;
+  long long units;
+};
+
+constexpr int PARTIAL_FLOATS = 2 + MAXM * D;   // m, l, o[M][D]
+
+cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+size_t decode_smem_bytes(int bits, int G);
+
+}  // namespace okvq

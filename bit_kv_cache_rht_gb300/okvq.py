@@ -1,0 +1,255 @@
+"""Python binding of libokvq (ctypes): argument marshalling only.
+
+The functions carry the C ABI's names (okvq_create, okvq_append_chunk,
+okvq_decode, okvq_free, ...); ``Cache`` wraps them for torch tensors. All
+compute runs in the library's CUDA kernels; there is no fallback: if
+libokvq.so is missing or fails to load, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libokvq.so")
+
+OKVQ_OK, OKVQ_EINVAL, OKVQ_ENOMEM, OKVQ_ECAPACITY, OKVQ_ECUDA, OKVQ_ESTATE = range(6)
+
+# every function the header declares (checked against include/okvq.h by the tests)
+EXPORTS = (
+    "okvq_create", "okvq_free", "okvq_append_chunk", "okvq_decode", "okvq_length", "okvq_export_state",
+    "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
+)
+
+
+class OkvqConfig(ctypes.Structure):
+    _fields_ = [
+        ("num_sessions", ctypes.c_int32),
+        ("num_layers", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("group_size", ctypes.c_int32),
+        ("bits", ctypes.c_int32),
+        ("num_modalities", ctypes.c_int32),
+        ("max_tokens", ctypes.c_int64),
+        ("hadamard_seed", ctypes.c_uint64),
+        ("codebook", ctypes.POINTER(ctypes.c_float)),
+        ("value_rot", ctypes.POINTER(ctypes.c_float)),
+    ]
+
+
+class OkvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (what, status_string(status), status))
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libokvq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libokvq.so is not built (run bit_kv_cache_rht_gb300.build.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+    L.okvq_create.argtypes = [ctypes.POINTER(OkvqConfig), vp, ctypes.POINTER(vp)]
+    L.okvq_free.argtypes = [vp]
+    L.okvq_free.restype = None
+    L.okvq_append_chunk.argtypes = [vp, i32, vp, vp, vp, i32, vp]
+    L.okvq_decode.argtypes = [vp, vp, vp, vp]
+    L.okvq_length.argtypes = [vp, i32, ctypes.POINTER(i64)]
+    L.okvq_export_state.argtypes = [vp, i32, vp, ctypes.POINTER(ctypes.c_size_t)]
+    L.okvq_codebook.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
+    L.okvq_check_errors.argtypes = [vp, vp, ctypes.POINTER(u32)]
+    L.okvq_profile_enable.argtypes = [vp, ctypes.c_int]
+    L.okvq_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float), i32,
+                                    ctypes.POINTER(i32)]
+    L.okvq_status_string.argtypes = [ctypes.c_int]
+    L.okvq_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name not in ("okvq_free", "okvq_status_string"):
+            getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(s: int) -> str:
+    return load().okvq_status_string(int(s)).decode()
+
+
+def _check(status: int, what: str):
+    if status != OKVQ_OK:
+        raise OkvqError(status, what)
+
+
+# ---- the C entry points, same names (status codes returned, not raised) ----
+
+def okvq_create(cfg: OkvqConfig, stream: int = 0):
+    h = ctypes.c_void_p()
+    st = load().okvq_create(ctypes.byref(cfg), ctypes.c_void_p(stream), ctypes.byref(h))
+    return st, h
+
+
+def okvq_free(h) -> None:
+    load().okvq_free(h)
+
+
+def okvq_append_chunk(h, session: int, k_ptr: int, v_ptr: int, mod_ptr: int, num_tokens: int, stream: int = 0) -> int:
+    return load().okvq_append_chunk(h, session, ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                    ctypes.c_void_p(mod_ptr), num_tokens, ctypes.c_void_p(stream))
+
+
+def okvq_decode(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
+    return load().okvq_decode(h, ctypes.c_void_p(q_ptr), ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream))
+
+
+def okvq_length(h, session: int):
+    n = ctypes.c_int64()
+    st = load().okvq_length(h, session, ctypes.byref(n))
+    return st, n.value
+
+
+def okvq_status_string(s: int) -> str:
+    return status_string(s)
+
+
+# ---- torch-facing wrapper ----
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Cache:
+    """A multi-session 2/4-bit omni KV cache on the current CUDA device."""
+
+    def __init__(self, num_sessions: int, num_layers: int, num_q_heads: int, num_kv_heads: int, max_tokens: int,
+                 value_rot: np.ndarray, head_dim: int = 128, group_size: int = 32, bits: int = 2,
+                 num_modalities: int = 3, hadamard_seed: int = 0, codebook: Optional[np.ndarray] = None,
+                 stream=None):
+        self._h = None
+        R = np.ascontiguousarray(value_rot, dtype=np.float32)
+        expect = (num_layers, num_kv_heads, num_modalities, head_dim, head_dim)
+        if R.shape != expect:
+            raise ValueError("value_rot must have shape %s, got %s" % (expect, R.shape))
+        self._R = R
+        cb = None
+        if codebook is not None:
+            cb = np.ascontiguousarray(codebook, dtype=np.float32)
+            self._cb = cb
+        cfg = OkvqConfig(num_sessions, num_layers, num_q_heads, num_kv_heads, head_dim, group_size, bits,
+                         num_modalities, max_tokens, hadamard_seed & ((1 << 64) - 1),
+                         cb.ctypes.data_as(ctypes.POINTER(ctypes.c_float)) if cb is not None else None,
+                         R.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+        st, h = okvq_create(cfg, _stream_handle(stream))
+        _check(st, "okvq_create")
+        self._h = h
+        self.num_sessions, self.num_layers = num_sessions, num_layers
+        self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
+        self.group_size, self.bits, self.num_modalities, self.max_tokens = group_size, bits, num_modalities, max_tokens
+
+    def close(self):
+        if self._h is not None:
+            okvq_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def append(self, session: int, k, v, modality, stream=None):
+        """k, v: cuda fp16 [T][L][Hkv][128]; modality: cuda uint8 [T]."""
+        import torch
+        T = int(modality.shape[0])
+        shp = (T, self.num_layers, self.num_kv_heads, self.head_dim)
+        for name, x, dt in (("k", k, torch.float16), ("v", v, torch.float16)):
+            if tuple(x.shape) != shp or x.dtype != dt or not x.is_cuda or not x.is_contiguous():
+                raise ValueError("%s must be a contiguous cuda fp16 tensor of shape %s" % (name, shp))
+        if modality.dtype != torch.uint8 or not modality.is_cuda or not modality.is_contiguous():
+            raise ValueError("modality must be a contiguous cuda uint8 tensor")
+        st = okvq_append_chunk(self._h, session, k.data_ptr(), v.data_ptr(), modality.data_ptr(), T,
+                               _stream_handle(stream))
+        _check(st, "okvq_append_chunk")
+
+    def decode(self, q, out=None, stream=None):
+        """q: cuda fp16 [S][L][Hq][128] -> out (same shape, fp16)."""
+        import torch
+        shp = (self.num_sessions, self.num_layers, self.num_q_heads, self.head_dim)
+        if tuple(q.shape) != shp or q.dtype != torch.float16 or not q.is_cuda or not q.is_contiguous():
+            raise ValueError("q must be a contiguous cuda fp16 tensor of shape %s" % (shp,))
+        if out is None:
+            out = torch.empty_like(q)
+        st = okvq_decode(self._h, q.data_ptr(), out.data_ptr(), _stream_handle(stream))
+        _check(st, "okvq_decode")
+        return out
+
+    def length(self, session: int) -> int:
+        st, n = okvq_length(self._h, session)
+        _check(st, "okvq_length")
+        return n
+
+    def codebook(self):
+        n = 1 << self.bits
+        lv = (ctypes.c_float * n)()
+        kl = (ctypes.c_float * n)()
+        _check(load().okvq_codebook(self._h, lv, kl), "okvq_codebook")
+        return np.array(lv[:], np.float32), np.array(kl[:], np.float32)
+
+    def check_errors(self, stream=None) -> int:
+        w = ctypes.c_uint32()
+        st = load().okvq_check_errors(self._h, ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(w))
+        if st not in (OKVQ_OK, OKVQ_ESTATE):
+            _check(st, "okvq_check_errors")
+        return int(w.value)
+
+    def profile_enable(self, on: bool = True):
+        _check(load().okvq_profile_enable(self._h, int(on)), "okvq_profile_enable")
+
+    def profile_read(self, cap: int = 4096):
+        a = (ctypes.c_float * cap)()
+        b = (ctypes.c_float * cap)()
+        n = ctypes.c_int32()
+        _check(load().okvq_profile_read(self._h, a, b, cap, ctypes.byref(n)), "okvq_profile_read")
+        return np.array(a[:n.value]), np.array(b[:n.value])
+
+    def export_state(self, session: int) -> dict:
+        """Canonical state of one session (layout documented in include/okvq.h)."""
+        L = load()
+        nbytes = ctypes.c_size_t(0)
+        _check(L.okvq_export_state(self._h, session, None, ctypes.byref(nbytes)), "okvq_export_state")
+        buf = np.zeros(nbytes.value, np.uint8)
+        _check(L.okvq_export_state(self._h, session, buf.ctypes.data_as(ctypes.c_void_p), ctypes.byref(nbytes)),
+               "okvq_export_state")
+        T = self.length(session)
+        G, d = self.group_size, self.head_dim
+        Tf = (T // G) * G
+        B = d * self.bits // 8
+        LH = (self.num_layers, self.num_kv_heads)
+        out, off = {}, 0
+
+        def take(name, count, dtype, shape):
+            nonlocal off
+            nb = count * np.dtype(dtype).itemsize
+            out[name] = buf[off:off + nb].view(dtype).reshape(shape)
+            off += nb
+
+        n = LH[0] * LH[1]
+        take("kcodes", n * Tf * B, np.uint8, (*LH, Tf, B))
+        take("kstats", n * (Tf // G) * 2 * d, np.float16, (*LH, Tf // G, 2, d))
+        take("ktail", n * (T - Tf) * d, np.float16, (*LH, T - Tf, d))
+        take("vcodes", n * T * B, np.uint8, (*LH, T, B))
+        take("vnorm", n * T, np.float16, (*LH, T))
+        take("mod", T, np.uint8, (T,))
+        return out

@@ -1,0 +1,157 @@
+/*
+ * okvq.h - C ABI of libokvq: a 2/4-bit omni-modal KV cache with fused decode
+ * attention for one GB300 (sm_103a).
+ *
+ * The operations follow "OmniKVQuant: KV Cache Quantization for Omni-LLMs"
+ * (paperlayer.ai summary of arXiv 2609.11582):
+ *   - section 2 METHOD, TurboQuant bullet: keys and values are rotated toward
+ *     a Gaussian-like coordinate law with a randomized Hadamard transform, the
+ *     magnitude is split from the direction, and a fixed codebook quantizes
+ *     the rotated coordinates;
+ *   - section 2, first OmniKVQuant bullet: rotated keys are min-max scaled
+ *     within short groups of consecutive tokens, the group statistics are
+ *     stored, and the shared fixed codebook quantizes the scaled values;
+ *   - section 2, second OmniKVQuant bullet: values use one orthogonal
+ *     eigenbasis rotation per modality;
+ *   - section 1 INTRODUCTION, Implementation bullet: the fused decode unpacks
+ *     the quantized cache inside attention without building a dense FP16
+ *     cache, rotates the query once per head, and batches the inverse value
+ *     rotations after attention aggregation.
+ *
+ * Readings of what the page leaves open (all fixed here, identically in the
+ * library and in its test oracle):
+ *   - head_dim is 128; the Hadamard matrix is Sylvester-ordered; the random
+ *     signs are bit c of the SplitMix64 stream seeded with hadamard_seed
+ *     (bit set -> -1), shared by every session, layer and head;
+ *   - keys: k' = fp32(1/sqrt(d)) * FWHT(s o k) in fp32 with butterfly strides
+ *     1, 2, ..., 64; groups of group_size consecutive tokens aligned to the
+ *     absolute token index; per channel the group min is stored as fp16
+ *     rounded down and the max as fp16 rounded up; u = (k'-mn)/(mx-mn) in
+ *     fp32 is coded to the nearest of the key levels
+ *     lambda_j = (l_j - l_0) / (l_last - l_0); mx == mn gives code 0;
+ *     the keys of an incomplete trailing group stay in fp16 and are attended
+ *     exactly until the group completes;
+ *   - values: n = |v| stored fp16 (round to nearest even);
+ *     w = sqrt(d) * R_m * v/n is coded to the nearest level l_j, with R_m the
+ *     rotation of the token's modality (rows = basis vectors);
+ *   - codebook: 2^bits ascending levels, rounded once to fp16 (the fp16
+ *     values define the codebook); the default is the Lloyd-Max quantizer of
+ *     N(0, 1); decisions compare fp32 values with fp32 midpoints of adjacent
+ *     fp16 levels, a value equal to a midpoint taking the lower code;
+ *   - decode attends every cached token of a session with one softmax
+ *     (scale 1/sqrt(d)); query head h uses kv head h / (num_q_heads /
+ *     num_kv_heads); the output is (sum_m R_m^T o_m) / l where o_m
+ *     accumulates p_t * n_t * l(code_t) / sqrt(d) over tokens of modality m.
+ *
+ * Threading: a handle is not thread-safe; use one per thread or lock.
+ * Streams: every call that takes a stream (a cudaStream_t passed as void*,
+ * NULL = the legacy default stream) only enqueues work on it; caller buffers
+ * must stay valid until that work has run.
+ */
+#ifndef OKVQ_H
+#define OKVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct okvq_cache okvq_cache; /* opaque, owned by the library */
+
+typedef enum {
+  OKVQ_OK = 0,
+  OKVQ_EINVAL = 1,    /* bad argument, shape or configuration; nothing was changed */
+  OKVQ_ENOMEM = 2,    /* a device or host allocation failed */
+  OKVQ_ECAPACITY = 3, /* the append would exceed max_tokens; nothing was written */
+  OKVQ_ECUDA = 4,     /* a CUDA call or kernel launch failed */
+  OKVQ_ESTATE = 5     /* the device error word was set (e.g. a modality id out of range,
+                         a bounded wait that gave up); see okvq_check_errors */
+} okvq_status;
+
+typedef struct {
+  int32_t num_sessions;   /* independent streams held by the cache, >= 1 */
+  int32_t num_layers;     /* >= 1 */
+  int32_t num_q_heads;    /* multiple of num_kv_heads, at most 8 query heads per kv head */
+  int32_t num_kv_heads;   /* >= 1 */
+  int32_t head_dim;       /* must be 128 */
+  int32_t group_size;     /* key group size: 32 or 64 tokens */
+  int32_t bits;           /* code width for keys and values: 2 or 4 */
+  int32_t num_modalities; /* 1..3; modality ids are 0..num_modalities-1 */
+  int64_t max_tokens;     /* per-session capacity; all storage is allocated by okvq_create */
+  uint64_t hadamard_seed; /* seed of the shared random sign vector */
+  const float *codebook;  /* host, 2^bits strictly ascending levels, or NULL for Lloyd-Max N(0,1);
+                             copied at create */
+  const float *value_rot; /* host, fp32 [num_layers][num_kv_heads][num_modalities][128][128],
+                             row-major, row i = i-th basis vector; should be orthogonal (not
+                             checked); copied at create */
+} okvq_config;
+
+/* Allocate a cache. Validates cfg (OKVQ_EINVAL), allocates device storage
+ * (OKVQ_ENOMEM) and uploads the codebook and rotations on `stream`, then
+ * synchronizes it. On success *out owns everything until okvq_free. */
+okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out);
+
+/* Release a cache and all its device memory (synchronizes the device). NULL is a no-op. */
+void okvq_free(okvq_cache *h);
+
+/* Append num_tokens tokens to `session` (section 2: values are quantized at
+ * once; each key group is quantized when its last token arrives).
+ *   k, v      device fp16 [num_tokens][num_layers][num_kv_heads][128], token-major
+ *   modality  device uint8 [num_tokens], each < num_modalities (checked on the
+ *             device: a bad id sets the error word and is stored as modality 0)
+ * Shapes and capacity are checked on the host before any launch
+ * (OKVQ_EINVAL / OKVQ_ECAPACITY, state unchanged). num_tokens == 0 is a no-op.
+ * One kernel launch, asynchronous on `stream`. */
+okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, const void *v,
+                              const uint8_t *modality, int32_t num_tokens, void *stream);
+
+/* One decode step for every session and layer (section 1, Implementation):
+ *   q    device fp16 [num_sessions][num_layers][num_q_heads][128]
+ *   out  device fp16 [num_sessions][num_layers][num_q_heads][128]
+ * An empty session yields zeros. Two kernel launches (split-K fused
+ * attention, then the merge + inverse value rotations), asynchronous on
+ * `stream`; the work list is re-uploaded on `stream` after appends changed
+ * the lengths. */
+okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
+
+/* Number of tokens held by `session`. */
+okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
+
+/* Copy the stored state of `session` to host memory in the canonical layout
+ * (synchronizes the device). With host_buf == NULL only *bytes is set. With
+ * T tokens, Tf = T - T % group_size, B = 128*bits/8, the buffer holds, in order:
+ *   kcodes  uint8 [L][Hkv][Tf][B]   channel c at byte c*bits/8, bit (c*bits)%8
+ *   kstats  fp16  [L][Hkv][Tf/group_size][2][128]   (min, max)
+ *   ktail   fp16  [L][Hkv][T-Tf][128]               (unquantized trailing keys)
+ *   vcodes  uint8 [L][Hkv][T][B]
+ *   vnorm   fp16  [L][Hkv][T]
+ *   mod     uint8 [T]
+ * *bytes must hold the buffer size on entry (OKVQ_EINVAL if too small). */
+okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, size_t *bytes);
+
+/* The fp16-rounded value levels in use (2^bits floats) and the key levels
+ * lambda_j (2^bits floats); either pointer may be NULL. */
+okvq_status okvq_codebook(const okvq_cache *h, float *levels, float *key_levels);
+
+/* Synchronize `stream`, read and clear the device error word. OKVQ_OK if it
+ * was clear, OKVQ_ESTATE otherwise (*word, if non-NULL, receives its bits:
+ * 1 = bad modality id, 2 = a bounded wait gave up). */
+okvq_status okvq_check_errors(okvq_cache *h, void *stream, uint32_t *word);
+
+/* Per-kernel timing with CUDA events recorded around each launch of
+ * okvq_decode on its stream. enable != 0 clears and starts the record.
+ * okvq_profile_read synchronizes, then returns the number of decode calls
+ * recorded (at most `cap`) and their split-K kernel and merge kernel times
+ * in milliseconds. */
+okvq_status okvq_profile_enable(okvq_cache *h, int enable);
+okvq_status okvq_profile_read(okvq_cache *h, float *split_ms, float *merge_ms, int32_t cap, int32_t *count);
+
+/* Static description of a status code. */
+const char *okvq_status_string(okvq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OKVQ_H */

@@ -1,0 +1,119 @@
+"""Shared helpers for the parity tests: build the oracle and the CUDA cache from
+the same seeded workload and compare them."""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import okvq_oracle as o
+
+ATOL, RTOL = 2e-3, 1e-2        # fp16 output vs fp64 oracle: |gpu - ref| <= ATOL + RTOL |ref|
+
+
+def ensure_built():
+    from bit_kv_cache_rht_gb300 import okvq
+    import os
+    if not os.path.exists(okvq.LIB_PATH):
+        from bit_kv_cache_rht_gb300 import build
+        build.build()
+    return okvq.load()
+
+
+def oracle_cache(w, layers=None, sessions=None):
+    sh = w.shape
+    layers = list(range(sh.num_layers)) if layers is None else list(layers)
+    R = w.value_rotations()
+    return o.OracleCache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
+                         sh.group_size, sh.bits, w.max_tokens, w.hadamard_seed, R, layers=layers), R
+
+
+def feed_oracle(oc, w, bounds=None, layers=None, sessions=None):
+    layers = oc.layers if layers is None else layers
+    sessions = range(len(w.sessions)) if sessions is None else sessions
+    for s in sessions:
+        K, V = w.session_kv(s, layers)
+        mod = w.sessions[s].modality()
+        bl = w.sessions[s].chunk_bounds() if bounds is None else bounds[s]
+        for a, b in bl:
+            oc.append(s, K[a:b], V[a:b], mod[a:b], layers_in=layers)
+
+
+def gpu_cache(w, R=None, bounds=None, sessions=None, max_tokens=None):
+    import torch
+    from bit_kv_cache_rht_gb300.okvq import Cache
+    sh = w.shape
+    R = w.value_rotations() if R is None else R
+    c = Cache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads,
+              w.max_tokens if max_tokens is None else max_tokens, R, head_dim=sh.head_dim,
+              group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
+              hadamard_seed=w.hadamard_seed)
+    sessions = range(len(w.sessions)) if sessions is None else sessions
+    for s in sessions:
+        K, V = w.session_kv(s)
+        mod = w.sessions[s].modality()
+        Kd = torch.from_numpy(K).cuda()
+        Vd = torch.from_numpy(V).cuda()
+        Md = torch.from_numpy(mod).cuda()
+        bl = w.sessions[s].chunk_bounds() if bounds is None else bounds[s]
+        for a, b in bl:
+            c.append(s, Kd[a:b], Vd[a:b], Md[a:b])
+    torch.cuda.synchronize()
+    return c
+
+
+def compare_state(gpu_state: dict, oc, session: int, layers_gpu_index, bits: int):
+    """Compare the exported state of `session` with the oracle's units.
+
+    Returns counts: boundary code mismatches (allowed) and strict mismatches
+    (must be 0) for keys/values/norms, plus stats/tail/mod equality flags."""
+    res = dict(k_strict=0, k_bnd=0, v_strict=0, v_bnd=0, n_strict=0, n_bnd=0, stats_ok=True, tail_ok=True,
+               mod_ok=True, k_codes=0, v_codes=0)
+    for i, l in enumerate(oc.layers):
+        li = layers_gpu_index[i]
+        for h in range(oc.Hkv):
+            e = oc.units[(session, l, h)].export()
+            gk = o.unpack_codes(gpu_state["kcodes"][li, h], bits)
+            ok_ = o.unpack_codes(e["kcodes"], bits)
+            diff = gk != ok_
+            res["k_strict"] += int(np.sum(diff & ~e["kbnd"]))
+            res["k_bnd"] += int(np.sum(diff & e["kbnd"]))
+            res["k_codes"] += diff.size
+            gv = o.unpack_codes(gpu_state["vcodes"][li, h], bits)
+            ov = o.unpack_codes(e["vcodes"], bits)
+            diff = gv != ov
+            res["v_strict"] += int(np.sum(diff & ~e["vbnd"]))
+            res["v_bnd"] += int(np.sum(diff & e["vbnd"]))
+            res["v_codes"] += diff.size
+            gn, on = gpu_state["vnorm"][li, h], e["vnorm"]
+            nd = gn.view(np.uint16) != on.view(np.uint16)
+            one_ulp = np.abs(gn.view(np.uint16).astype(np.int32) - on.view(np.uint16).astype(np.int32)) <= 1
+            res["n_strict"] += int(np.sum(nd & ~(e["nbnd"] & one_ulp)))
+            res["n_bnd"] += int(np.sum(nd & e["nbnd"] & one_ulp))
+            if not np.array_equal(gpu_state["kstats"][li, h].view(np.uint16), e["kstats"].view(np.uint16)):
+                res["stats_ok"] = False
+            if not np.array_equal(gpu_state["ktail"][li, h].view(np.uint16), e["ktail"].view(np.uint16)):
+                res["tail_ok"] = False
+    T = oc.units[(session, oc.layers[0], 0)].T
+    if not np.array_equal(gpu_state["mod"], oc.units[(session, oc.layers[0], 0)].mod[:T]):
+        res["mod_ok"] = False
+    return res
+
+
+def assert_state_matches(res):
+    assert res["stats_ok"], "key group statistics differ"
+    assert res["tail_ok"], "fp16 key tail differs"
+    assert res["mod_ok"], "modality ids differ"
+    assert res["k_strict"] == 0, res
+    assert res["v_strict"] == 0, res
+    assert res["n_strict"] == 0, res
+
+
+def assert_outputs_close(gpu_out, ref, what=""):
+    g = np.asarray(gpu_out, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(g)), "non-finite output " + what
+    err = np.abs(g - r)
+    bound = ATOL + RTOL * np.abs(r)
+    bad = err > bound
+    assert not bad.any(), "%s: %d/%d outside tolerance, max err %.3g (max |ref| %.3g)" % (
+        what, int(bad.sum()), bad.size, float(err.max()), float(np.abs(r).max()))
+    return float(err.max())

@@ -1,0 +1,142 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs. Codes and statistics must match bit for bit except counted
+boundary codes; decode outputs within |gpu - ref| <= 2e-3 + 1e-2 |ref|."""
+import numpy as np
+import pytest
+
+from bit_kv_cache_rht_gb300 import synth
+from oracle import okvq_oracle as o
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pu.ensure_built()
+
+
+def _full_check(w, bounds=None, layers_check=None, steps=(0,)):
+    import torch
+    oc, R = pu.oracle_cache(w, layers=layers_check)
+    pu.feed_oracle(oc, w, bounds=bounds)
+    c = pu.gpu_cache(w, R=R, bounds=bounds)
+    assert c.check_errors() == 0
+    li = oc.layers
+    for s in range(len(w.sessions)):
+        res = pu.compare_state(c.export_state(s), oc, s, li, w.shape.bits)
+        pu.assert_state_matches(res)
+    errs = []
+    for step in steps:
+        Q = w.queries(step)
+        out = c.decode(torch.from_numpy(Q).cuda()).cpu().numpy()
+        ref = oc.decode(Q)
+        errs.append(pu.assert_outputs_close(out[:, li], ref, "step %d" % step))
+    return c, oc, errs
+
+
+@pytest.mark.parametrize("bits,G", [(2, 32), (2, 64), (4, 32), (4, 64)])
+def test_tiny_one_chunk(bits, G):
+    w = synth.tiny(seed=10 + bits + G, bits=bits, group_size=G)
+    _full_check(w, bounds=[[(0, 2048)]], steps=(0, 1))
+
+
+def test_tiny_streamed_in_odd_chunks_matches_oracle_and_single_chunk():
+    w = synth.tiny(seed=21)
+    T = 2048
+    r = np.random.default_rng(3)
+    cuts = sorted(r.choice(np.arange(1, T), 30, replace=False).tolist())
+    bounds = [list(zip([0, *cuts], [*cuts, T]))]
+    c1, _, _ = _full_check(w, bounds=bounds)
+    c2 = pu.gpu_cache(w, bounds=[[(0, T)]])
+    s1, s2 = c1.export_state(0), c2.export_state(0)
+    for k in s1:
+        assert np.array_equal(s1[k].view(np.uint8), s2[k].view(np.uint8)), k
+
+
+def test_tiny_97_token_chunks():
+    w = synth.tiny(seed=22)
+    _full_check(w, bounds=[[(a, min(a + 97, 2048)) for a in range(0, 2048, 97)]])
+
+
+@pytest.mark.parametrize("T", [1, 5, 16, 31, 32, 33, 63, 64, 65, 100, 130])
+def test_short_sessions_and_tails(T):
+    w = synth.tiny(seed=30 + T, tokens=T)
+    _full_check(w, bounds=[[(0, T)]], steps=(0,))
+
+
+def test_qwen3b_shape_streamed_chunks():
+    w = synth.qwen3b(seed=40, tokens=5000, layers=3)
+    _full_check(w, steps=(0, 1))
+
+
+def test_qwen7b_shape_seven_heads_per_kv():
+    w = synth.qwen7b(seed=41, tokens=3000, layers=2)
+    _full_check(w, steps=(0,))
+
+
+def test_multisession_mixed_lengths_and_empty():
+    w = synth.multisession(seed=42, sessions=5, lo=40, hi=3000, layers=2)
+    w.sessions[2] = synth.Session([])          # an empty session decodes to zeros
+    c, oc, _ = _full_check(w, steps=(0,))
+    import torch
+    out = c.decode(torch.from_numpy(w.queries(0)).cuda()).cpu().numpy()
+    assert np.all(out[2] == 0)
+
+
+@pytest.mark.parametrize("bits,G", [(2, 64), (4, 32)])
+def test_multisession_variants(bits, G):
+    w = synth.multisession(seed=43, sessions=3, lo=500, hi=2500, layers=2, bits=bits, group_size=G)
+    _full_check(w, steps=(0,))
+
+
+def test_capacity_and_argument_errors():
+    import torch
+    from bit_kv_cache_rht_gb300 import okvq
+    w = synth.tiny(seed=50, tokens=100)
+    c = pu.gpu_cache(w, max_tokens=128)
+    K = torch.zeros((40, 1, 2, 128), dtype=torch.float16, device="cuda")
+    M = torch.zeros(40, dtype=torch.uint8, device="cuda")
+    with pytest.raises(okvq.OkvqError) as e:
+        c.append(0, K, K, M)
+    assert e.value.status == okvq.OKVQ_ECAPACITY
+    assert c.length(0) == 100                   # unchanged
+    st = okvq.okvq_append_chunk(c._h, 1, K.data_ptr(), K.data_ptr(), M.data_ptr(), 4)
+    assert st == okvq.OKVQ_EINVAL               # no such session
+
+
+def test_bad_modality_sets_error_word():
+    import torch
+    w = synth.tiny(seed=51, tokens=64)
+    c = pu.gpu_cache(w, max_tokens=256)
+    K = torch.randn((8, 1, 2, 128), device="cuda").half()
+    M = torch.full((8,), 7, dtype=torch.uint8, device="cuda")
+    c.append(0, K, K, M)
+    assert c.check_errors() & 1
+    assert c.check_errors() == 0                # cleared by the read
+
+
+def test_codebook_matches_oracle():
+    w = synth.tiny(seed=52, tokens=16)
+    for bits in (2, 4):
+        w2 = synth.tiny(seed=52, tokens=16, bits=bits)
+        c = pu.gpu_cache(w2)
+        lv, kl = c.codebook()
+        cb = o.make_codebook(bits)
+        assert np.array_equal(lv.astype(np.float16), cb.levels16)
+        assert np.array_equal(kl.astype(np.float16), cb.ktab16)
+
+
+def test_decode_is_repeatable_and_query_dependent():
+    import torch
+    w = synth.tiny(seed=53)
+    c = pu.gpu_cache(w)
+    q = torch.from_numpy(w.queries(0)).cuda()
+    a = c.decode(q).cpu().numpy()
+    b = c.decode(q).cpu().numpy()
+    assert np.array_equal(a, b)
+    q2 = torch.from_numpy(w.queries(1)).cuda()
+    assert not np.array_equal(a, c.decode(q2).cpu().numpy())
