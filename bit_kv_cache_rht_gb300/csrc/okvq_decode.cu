@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
       }
     }
 
-    uint32_t bk[8][2];      // score B fragments of the current group
+    uint32_t bk[8][2];      // score B fragments of the current group (fp16 high part)
+    uint32_t bl[8][2];      // and the fp16 residual
     float beta0 = 0.f, beta1 = 0.f;
 
     for (int k = 0; k < my_n; ++k) {
@@ -281,8 +282,15 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
               const float2 mn23 = __half22float2(*reinterpret_cast<const __half2 *>(&mnr.y));
               const float2 mx01 = __half22float2(*reinterpret_cast<const __half2 *>(&mxr.x));
               const float2 mx23 = __half22float2(*reinterpret_cast<const __half2 *>(&mxr.y));
-              bk[kb][0] = pack_h2(qv.x * (mx01.x - mn01.x), qv.y * (mx01.y - mn01.y));
-              bk[kb][1] = pack_h2(qv.z * (mx23.x - mn23.x), qv.w * (mx23.y - mn23.y));
+              const float a0 = qv.x * (mx01.x - mn01.x), a1 = qv.y * (mx01.y - mn01.y);
+              const float a2 = qv.z * (mx23.x - mn23.x), a3 = qv.w * (mx23.y - mn23.y);
+              bk[kb][0] = pack_h2(a0, a1);
+              bk[kb][1] = pack_h2(a2, a3);
+              // fp16 residuals: the score MMA runs on hi and lo so a keeps ~22 significant bits
+              const float2 h01 = __half22float2(*reinterpret_cast<const __half2 *>(&bk[kb][0]));
+              const float2 h23 = __half22float2(*reinterpret_cast<const __half2 *>(&bk[kb][1]));
+              bl[kb][0] = pack_h2(a0 - h01.x, a1 - h01.y);
+              bl[kb][1] = pack_h2(a2 - h23.x, a3 - h23.y);
               bp = fmaf(qv.x, mn01.x, bp);
               bp = fmaf(qv.y, mn01.y, bp);
               bp = fmaf(qv.z, mn23.x, bp);
@@ -306,6 +314,7 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
 #pragma unroll
             for (int r = 0; r < 4; ++r) A[r] = lut_get<BITS>(klut, pair_index<BITS>(kw, 4 * kb + r), lane);
             mma16816(sc, A, bk[kb][0], bk[kb][1]);
+            mma16816(sc, A, bl[kb][0], bl[kb][1]);
           }
         } else {
           // trailing keys of an incomplete group: exact fp16 keys, unrotated query
