@@ -54,7 +54,7 @@ struct okvq_cache {
 
 namespace {
 
-constexpr int CTAS_PER_SM = 2;
+constexpr int CTAS_PER_SM = 1;   // the decode kernel holds one 8-warp CTA per SM
 
 uint64_t splitmix64_next(uint64_t &state) {
   state += 0x9E3779B97F4A7C15ull;
@@ -127,11 +127,6 @@ void release(okvq_cache *h) {
   for (auto e : h->ev) cudaEventDestroy(e);
   delete h;
 }
-
-bool valid_stream_arg(void *) { return true; }
-
-// (lane, j, e) -> bit position of the code in a lane chunk and the page-tile offset
-inline int code_bit(int bits, int j, int e) { return bits * (2 * j + e); }
 
 // Build the decode work partition: balanced page ranges over the flattened
 // (unit, page) list, cut at unit boundaries into segments.
@@ -539,9 +534,9 @@ okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, si
       for (int e = 0; e < 2; ++e) {
         int tok, ch;
         k_pair_coords(lane, j, e, tok, ch);
-        kpos[tok * D + ch] = lane * PL.lane_bytes * 8 + code_bit(bits, j, e);
+        kpos[tok * D + ch] = lane * PL.lane_bytes * 8 + k_code_bit(bits, j, e);
         v_pair_coords(lane, j, e, tok, ch);
-        vpos[tok * D + ch] = lane * PL.lane_bytes * 8 + code_bit(bits, j, e);
+        vpos[tok * D + ch] = lane * PL.lane_bytes * 8 + v_code_bit(bits, j, e);
       }
   int inv_stat[D];
   for (int p = 0; p < D; ++p) inv_stat[stat_channel(p)] = p;

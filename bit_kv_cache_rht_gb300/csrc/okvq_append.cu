@@ -31,7 +31,7 @@ struct Smem {
   uint8_t kc[PAGE * D];            // key codes of the page
   float vnorm[PAGE];
   int mod[PAGE];
-  float kmn[2][D], kmx[2][D];
+  float kmn[2][D], kmx[2][D];     // group min and range (fp16 values held as fp32)
   int present[MAXM];
 };
 
@@ -56,18 +56,16 @@ __device__ void pack_tile(const uint8_t *codes, uint8_t *dst, int tile, int bits
                           int tid, int nthreads) {
   const int words_per_lane = bits * 2;         // 16 B or 32 B per lane
   for (int w = tid; w < 32 * words_per_lane; w += nthreads) {
-    int lane = w / words_per_lane, wi = w % words_per_lane;
+    const int lane = w / words_per_lane, wi = w % words_per_lane;
     uint32_t word = 0;
-    const int codes_per_word = 32 / bits;
-    for (int q = 0; q < codes_per_word; ++q) {
-      int bitpos = wi * 32 + q * bits;         // position in the lane chunk
-      int j = bitpos / (2 * bits), e = (bitpos / bits) & 1;
-      int tok, ch;
+    for (int b = 0; b < 32; b += bits) {
+      int j, e, tok, ch;
+      chunk_code_at(kind, bits, wi, b, j, e);
       if (kind == 0) k_pair_coords(lane, j, e, tok, ch);
       else v_pair_coords(lane, j, e, tok, ch);
       tok += 16 * tile;
-      uint32_t c = tok < valid_end ? codes[tok * D + ch] : 0u;
-      word |= c << (q * bits);
+      const uint32_t c = tok < valid_end ? codes[tok * D + ch] : 0u;
+      word |= c << b;
     }
     reinterpret_cast<uint32_t *>(dst)[lane * words_per_lane + wi] = word;
   }
@@ -79,17 +77,15 @@ __device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int bi
   const int words_per_lane = bits * 2;
   const uint32_t mask = (1u << bits) - 1u;
   for (int w = tid; w < 32 * words_per_lane; w += nthreads) {
-    int lane = w / words_per_lane, wi = w % words_per_lane;
-    uint32_t word = reinterpret_cast<const uint32_t *>(src)[lane * words_per_lane + wi];
-    const int codes_per_word = 32 / bits;
-    for (int q = 0; q < codes_per_word; ++q) {
-      int bitpos = wi * 32 + q * bits;
-      int j = bitpos / (2 * bits), e = (bitpos / bits) & 1;
-      int tok, ch;
+    const int lane = w / words_per_lane, wi = w % words_per_lane;
+    const uint32_t word = reinterpret_cast<const uint32_t *>(src)[lane * words_per_lane + wi];
+    for (int b = 0; b < 32; b += bits) {
+      int j, e, tok, ch;
+      chunk_code_at(kind, bits, wi, b, j, e);
       if (kind == 0) k_pair_coords(lane, j, e, tok, ch);
       else v_pair_coords(lane, j, e, tok, ch);
       tok += 16 * tile;
-      if (tok < keep_end) codes[tok * D + ch] = (uint8_t)((word >> (q * bits)) & mask);
+      if (tok < keep_end) codes[tok * D + ch] = (uint8_t)((word >> b) & mask);
     }
   }
 }
@@ -102,7 +98,6 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
 
   const long long page = a.page0 + blockIdx.x;
   const int lh = blockIdx.y;                       // layer * Hkv + kv head
-  const int layer = lh / a.Hkv;
   const long long unit = (long long)a.session * a.L * a.Hkv + lh;
   const long long P0 = page * PAGE;
   const long long T0 = a.T0, T1 = a.T0 + a.n;
@@ -250,7 +245,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       *reinterpret_cast<float4 *>(&xk[(g0 + r) * D + 4 * lane]) = o;
     }
     __syncthreads();
-    // per-channel statistics of the group
+    // per-channel statistics of the group: min rounded down, range rounded up
     const int gi = g0 / G;
     for (int c = tid; c < D; c += THREADS) {
       float mn = xk[g0 * D + c], mx = mn;
@@ -259,18 +254,18 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
       }
-      __half hmn = __float2half_rd(mn), hmx = __float2half_ru(mx);
+      const __half hmn = __float2half_rd(mn);
+      const __half hrg = __float2half_ru(__fsub_ru(mx, __half2float(hmn)));
       S.kmn[gi][c] = __half2float(hmn);
-      S.kmx[gi][c] = __half2float(hmx);
+      S.kmx[gi][c] = __half2float(hrg);
       __half *st = reinterpret_cast<__half *>(pg + PL.off_stats + gi * 2 * D * 2);
       st[stat_pos(c)] = hmn;
-      st[D + stat_pos(c)] = hmx;
+      st[D + stat_pos(c)] = hrg;
     }
     __syncthreads();
     for (int i = tid; i < G * D; i += THREADS) {
       int r = i / D, c = i % D;
-      float mn = S.kmn[gi][c], mx = S.kmx[gi][c];
-      float rng = __fsub_rn(mx, mn);
+      const float mn = S.kmn[gi][c], rng = S.kmx[gi][c];
       int code = 0;
       if (rng != 0.f) {
         float u = __fdiv_rn(__fsub_rn(xk[(g0 + r) * D + c], mn), rng);

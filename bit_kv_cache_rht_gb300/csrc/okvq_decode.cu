@@ -4,17 +4,22 @@
 // rotated once per head, and the inverse value rotations are batched after
 // aggregation).
 //
-// decode_kernel - split-K over the token axis. A CTA (4 warps) owns a balanced
-//   range of 64-token pages of the flattened (session, layer, kv head, page)
-//   list, cut into segments at unit boundaries. Each warp streams whole pages
-//   with one bulk copy each into a private shared-memory ring (mbarrier
-//   completion), and for every 16-token tile runs
-//     scores  S[16 tok x 8 heads] = beta_g + Lambda[tok x 128] * (q' o (mx-mn))   (mma m16n8k16)
+// decode_kernel - split-K over the token axis, one CTA (8 warps) per SM. A CTA
+//   owns a balanced range of 64-token pages of the flattened (session, layer,
+//   kv head, page) list, cut into segments at unit boundaries. Each warp streams
+//   whole pages, one bulk copy each, into a private shared-memory ring (mbarrier
+//   completion) and works on 32-token half pages:
+//     scores  S^T[16 x 8 tok] = [a_hi; a_lo][16 x 128] * Lambda^T[128 x 8 tok] + [beta; 0]
+//             (mma m16n8k16; rows 0-7 / 8-15 = the 8 query heads' fp16 high and
+//             residual parts of a = q' o range, so the sum is exact to ~2^-22)
 //     softmax online, base 2, fp32 (m, l per head)
-//     values  O_m[128 ch x 8 heads] += Lcode[ch x tok] * (p * n)[tok x heads]     (mma m16n8k16)
-//   with the code -> fp16 level lookups done in registers from shared tables,
-//   one accumulator set per modality (rotated value domain). Warps merge in
-//   shared memory; one partial (m, l, o_m) per segment and head goes to global.
+//     values  O_m[128 ch x 8 heads] += Lcode[ch x 16 tok] * (p * n)[16 tok x 8 heads]
+//   The score output fragment is already the value MMA's B fragment. Key codes
+//   become fp16 levels in registers (mask -> fp32 fma builds a byte-permute
+//   selector -> prmt from a 4-entry table); value codes through a
+//   shared-memory table indexed by a whole code byte (one 8-byte load per 4
+//   codes). One accumulator set per modality (rotated value domain); warps merge
+//   in shared memory; one partial (m, l, o_m) per segment and head goes out.
 // combine_kernel - per (unit, 32 output channels): log-sum-exp merge of the
 //   unit's partials, O = (sum_m R_m^T o_m) / (l sqrt d), fp16 store.
 #include "okvq_internal.h"
@@ -23,25 +28,24 @@ namespace okvq {
 
 namespace {
 
-constexpr int WARPS = 4;
+constexpr int WARPS = 8;
 constexpr int THREADS = WARPS * 32;
 constexpr float LOG2E = 1.4426950408889634074f;
 constexpr float INV_D = 1.0f / 128.0f;                      // (1/sqrt d) rotation * (1/sqrt d) softmax
 constexpr float INV_SQRT_D = 0.0883883476483184405501f;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr long long WAIT_LIMIT = 1ll << 26;
+constexpr int LUT_BYTES = 256 * 256;   // 256 code bytes x [K half | V half], 128 B each
 
 template <int BITS>
 struct Cfg;
 template <>
 struct Cfg<2> {
-  static constexpr int STAGES = 4;
-  static constexpr int LUT_WORDS = 16 * 32;   // 4-bit pair index, replicated per lane
+  static constexpr int STAGES = 3;
 };
 template <>
 struct Cfg<4> {
   static constexpr int STAGES = 2;
-  static constexpr int LUT_WORDS = 256;       // 8-bit pair index
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -64,7 +68,7 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 
 // bounded wait on an mbarrier phase; returns false if it gave up
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t addr = smem_u32(bar);
+  const uint32_t addr = smem_u32(bar);
   for (long long it = 0; it < WAIT_LIMIT; ++it) {
     uint32_t done;
     asm volatile(
@@ -93,41 +97,40 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
 }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// pair j of a lane chunk -> lut index
-template <int BITS>
-__device__ __forceinline__ uint32_t pair_index(const uint32_t *w, int j) {
-  if (BITS == 2) return (w[j >> 3] >> (4 * (j & 7))) & 0xFu;
-  return (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t &a, uint32_t &b) {
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
 
-template <int BITS>
-__device__ __forceinline__ uint32_t lut_get(const uint32_t *lut, uint32_t idx, int lane) {
-  if (BITS == 2) return lut[(idx << 5) | lane];
-  return lut[idx];
+// 2-bit key pair from the register-table layout: `src` holds the pair's two
+// codes at bits s and s+8 (s = 0, 2, 4, 6). Mask it into the mantissa of
+// 2^23 + (x << s) + (y << (s+8)); one fp32 fma turns that into
+// 2^23 + 0x4040 + 0x11*x + 0x1100*y, whose low 16 bits are the byte-permute
+// selector [x, x+4, y, y+4] over the table {lo bytes of the 4 levels, hi bytes}.
+__device__ __forceinline__ uint32_t kreg_pair(uint32_t src, int s, uint32_t lutlo, uint32_t luthi) {
+  constexpr float MUL[4] = {17.0f, 4.25f, 1.0625f, 0.265625f};
+  constexpr float ADD[4] = {-134201280.0f, -27246528.0f, -507840.0f, 6176832.0f};
+  const uint32_t t = (src & (0x0303u << s)) | 0x4B000000u;
+  const float f = fmaf(__uint_as_float(t), MUL[s >> 1], ADD[s >> 1]);
+  return __byte_perm(lutlo, luthi, __float_as_uint(f));
 }
 
-// value tile: acc[mt] += Lcode[16 ch x 16 tok] * P[16 tok x 8 heads]
-template <int BITS>
-__device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw, const uint32_t *vlut, int lane,
-                                          uint32_t b0, uint32_t b1) {
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    uint32_t A[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) A[r] = lut_get<BITS>(vlut, pair_index<BITS>(vw, 4 * mt + r), lane);
-    mma16816(acc[mt], A, b0, b1);
-  }
+// shared-memory table address for code byte `B` (0..3) of word w:
+// byte << 8 | lane part (laneoff holds it in its low byte)
+template <int B>
+__device__ __forceinline__ uint32_t lut_addr(uint32_t laneoff, uint32_t w) {
+  return __byte_perm(laneoff, w, 0x1100u | ((4u + B) << 4));
 }
 
 struct Merge {
@@ -136,8 +139,62 @@ struct Merge {
   float o[WARPS][MAXM][MAXGQ][D];
 };
 
+// value tile of one modality: acc[mt] += Lcode[16 ch x 16 tok] * P
+template <int BITS>
+__device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw, uint32_t lut_v, uint32_t laneoff,
+                                          uint32_t b0, uint32_t b1) {
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    uint32_t A[4];
+    if (BITS == 2) {
+      const uint32_t w = vw[mt >> 1];
+      const uint32_t a0 = (mt & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
+      const uint32_t a1 = (mt & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
+      lds64(lut_v + a0, A[0], A[1]);
+      lds64(lut_v + a1, A[2], A[3]);
+    } else {
+      const uint32_t w = vw[mt];
+      A[0] = lds32(lut_v + lut_addr<0>(laneoff, w));
+      A[1] = lds32(lut_v + lut_addr<1>(laneoff, w));
+      A[2] = lds32(lut_v + lut_addr<2>(laneoff, w));
+      A[3] = lds32(lut_v + lut_addr<3>(laneoff, w));
+    }
+    mma16816(acc[mt], A, b0, b1);
+  }
+}
+
+// key B fragments of one kb block for one 16-token tile:
+// n-tile 0 (tokens 0-7): (pair 4kb, pair 4kb+2); n-tile 1: (pair 4kb+1, pair 4kb+3)
+template <int BITS>
+__device__ __forceinline__ void key_frags(const uint32_t *kw, const uint32_t *kwh, int kb, uint32_t lutlo,
+                                          uint32_t luthi, uint32_t lut_k, uint32_t laneoff, uint32_t (&bf)[4]) {
+  if (BITS == 2) {
+    if ((KREG_WORDS >> (kb >> 1)) & 1u) {
+      const uint32_t src = (kb & 1) ? kwh[kb >> 1] : kw[kb >> 1];
+      bf[0] = kreg_pair(src, 0, lutlo, luthi);
+      bf[1] = kreg_pair(src, 4, lutlo, luthi);
+      bf[2] = kreg_pair(src, 2, lutlo, luthi);
+      bf[3] = kreg_pair(src, 6, lutlo, luthi);
+    } else {
+      const uint32_t w = kw[kb >> 1];
+      uint32_t p0, p1, p2, p3;
+      const uint32_t a0 = (kb & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
+      const uint32_t a1 = (kb & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
+      lds64(lut_k + a0, p0, p1);   // pairs 4kb, 4kb+1
+      lds64(lut_k + a1, p2, p3);   // pairs 4kb+2, 4kb+3
+      bf[0] = p0; bf[1] = p2; bf[2] = p1; bf[3] = p3;
+    }
+  } else {
+    const uint32_t w = kw[kb];
+    bf[0] = lds32(lut_k + lut_addr<0>(laneoff, w));
+    bf[1] = lds32(lut_k + lut_addr<2>(laneoff, w));
+    bf[2] = lds32(lut_k + lut_addr<1>(laneoff, w));
+    bf[3] = lds32(lut_k + lut_addr<3>(laneoff, w));
+  }
+}
+
 template <int BITS, int G>
-__global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) {
   constexpr int STAGES = Cfg<BITS>::STAGES;
   constexpr int LANE_WORDS = BITS * 2;        // 32-bit words per lane chunk
   const PageLayout PL = page_layout(BITS, G);
@@ -145,33 +202,54 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
   const int g = lane >> 2, t4 = lane & 3;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  uint32_t *klut = reinterpret_cast<uint32_t *>(smem);
-  uint32_t *vlut = klut + Cfg<BITS>::LUT_WORDS;
-  float *qr = reinterpret_cast<float *>(vlut + Cfg<BITS>::LUT_WORDS);    // [8][128] stat order, scaled
-  __half *qraw = reinterpret_cast<__half *>(qr + MAXGQ * D);             // [8][128] natural order
-  uint64_t *bars = reinterpret_cast<uint64_t *>(qraw + MAXGQ * D);       // [WARPS][STAGES]
+  unsigned char *lut = smem;                                            // LUT_BYTES
+  float *qr = reinterpret_cast<float *>(smem + LUT_BYTES);              // [8][128] stat order, scaled
+  __half *qraw = reinterpret_cast<__half *>(qr + MAXGQ * D);            // [8][128] natural order
+  uint64_t *bars = reinterpret_cast<uint64_t *>(qraw + MAXGQ * D);      // [WARPS][STAGES]
   unsigned char *stages = reinterpret_cast<unsigned char *>(bars + WARPS * STAGES);
   stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
   Merge &MG = *reinterpret_cast<Merge *>(stages);
   unsigned char *my_stage0 = stages + (size_t)warp * STAGES * PL.page_bytes;
   uint64_t *my_bars = bars + warp * STAGES;
 
-  // code -> fp16 level tables (a pair of codes -> one half2)
-  for (int i = tid; i < Cfg<BITS>::LUT_WORDS; i += THREADS) {
-    uint32_t e = BITS == 2 ? (uint32_t)(i >> 5) : (uint32_t)i;
-    uint32_t c0 = e & ((1u << BITS) - 1), c1 = e >> BITS;
-    __half2 k2 = __halves2half2(a.klut_src[c0], a.klut_src[c1]);
-    __half2 v2 = __halves2half2(a.vlut_src[c0], a.vlut_src[c1]);
-    klut[i] = *reinterpret_cast<uint32_t *>(&k2);
-    vlut[i] = *reinterpret_cast<uint32_t *>(&v2);
+  // code byte -> fp16 level table; entry e = [K part 128 B | V part 128 B].
+  // 2-bit: byte = 2 pairs -> 8 B, replicated for the 16 lanes of a half warp;
+  // 4-bit: byte = 1 pair -> 4 B, replicated for 32 lanes.
+  for (int i = tid; i < 256 * 32; i += THREADS) {
+    const int e = i >> 5, c = i & 31;
+    if (BITS == 2) {
+      if (c >= 16) continue;
+      const uint32_t k0 = h2u(__halves2half2(a.klut_src[e & 3], a.klut_src[(e >> 2) & 3]));
+      const uint32_t k1 = h2u(__halves2half2(a.klut_src[(e >> 4) & 3], a.klut_src[(e >> 6) & 3]));
+      const uint32_t v0 = h2u(__halves2half2(a.vlut_src[e & 3], a.vlut_src[(e >> 2) & 3]));
+      const uint32_t v1 = h2u(__halves2half2(a.vlut_src[(e >> 4) & 3], a.vlut_src[(e >> 6) & 3]));
+      *reinterpret_cast<uint2 *>(lut + e * 256 + c * 8) = make_uint2(k0, k1);
+      *reinterpret_cast<uint2 *>(lut + e * 256 + 128 + c * 8) = make_uint2(v0, v1);
+    } else {
+      *reinterpret_cast<uint32_t *>(lut + e * 256 + c * 4) =
+          h2u(__halves2half2(a.klut_src[e & 15], a.klut_src[e >> 4]));
+      *reinterpret_cast<uint32_t *>(lut + e * 256 + 128 + c * 4) =
+          h2u(__halves2half2(a.vlut_src[e & 15], a.vlut_src[e >> 4]));
+    }
   }
   if (lane == 0)
     for (int s = 0; s < STAGES; ++s) mbar_init(&my_bars[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
+  const uint32_t lut_k = smem_u32(lut), lut_v = lut_k + 128;
+  const uint32_t laneoff = BITS == 2 ? (uint32_t)((lane & 15) << 3) : (uint32_t)(lane << 2);
+  // 4-entry key level table in registers (2-bit register path)
+  uint32_t lutlo = 0, luthi = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t hv = __half_as_ushort(a.klut_src[j]);
+    lutlo |= (hv & 0xFFu) << (8 * j);
+    luthi |= (hv >> 8) << (8 * j);
+  }
+
   const int gq = a.Hq / a.Hkv;
-  long long consumed = 0;                      // pages consumed by this warp so far (phase tracking)
+  long long consumed = 0;
   bool wait_failed = false;
 
   const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
@@ -184,40 +262,53 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
     const long long T = a.unit_len[unit];
     const long long Tf = (T / G) * G;
     const unsigned char *unit_pages = a.pages + (long long)unit * a.P_max * PL.page_bytes;
+    const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
 
-    // ---- rotate the query group once: q' = H (s o q) / d, in log2 units ----
+    // ---- rotate the query group once: q' = H (s o q) / d, in log2 units (warp = head) ----
     {
       const __half *qsrc = a.q + (((long long)session * a.L + layer) * a.Hq + (long long)kvh * gq) * D;
-      for (int hh = warp; hh < MAXGQ; hh += WARPS) {
-        float x[4];
+      const int hh = warp;
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * lane + j;
+        const __half hv = hh < gq ? qsrc[hh * D + c] : __float2half(0.f);
+        qraw[hh * D + c] = hv;
+        x[j] = __half2float(hv) * a.signs[c];
+      }
+      float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
+      x[0] = y0 + y2; x[2] = y0 - y2; x[1] = y1 + y3; x[3] = y1 - y3;
+#pragma unroll
+      for (int sm = 1; sm < 32; sm <<= 1) {
+        const bool upper = (lane & sm) != 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          int c = 4 * lane + j;
-          __half hv = hh < gq ? qsrc[hh * D + c] : __float2half(0.f);
-          qraw[hh * D + c] = hv;
-          x[j] = __half2float(hv) * a.signs[c];
+          const float p = __shfl_xor_sync(FULL, x[j], sm);
+          x[j] = upper ? p - x[j] : x[j] + p;
         }
-        float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
-        x[0] = y0 + y2; x[2] = y0 - y2; x[1] = y1 + y3; x[3] = y1 - y3;
+      }
 #pragma unroll
-        for (int sm = 1; sm < 32; sm <<= 1) {
-          const bool upper = (lane & sm) != 0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float p = __shfl_xor_sync(FULL, x[j], sm);
-            x[j] = upper ? p - x[j] : x[j] + p;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          int c = 4 * lane + j;
-          int kb = c >> 4, r = c & 15;
-          int pos = 32 * ((r & 7) >> 1) + 4 * kb + ((r & 1) | ((r >> 3) << 1));
-          qr[hh * D + pos] = x[j] * (INV_D * LOG2E);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * lane + j;
+        const int kb = c >> 4, r = c & 15;
+        const int pos = 32 * ((r & 7) >> 1) + 4 * kb + ((r & 1) | ((r >> 3) << 1));
+        qr[hh * D + pos] = x[j] * (INV_D * LOG2E);
       }
     }
     __syncthreads();
+
+    // this lane's query fragments (head g, its 32 channels): fp16 high + residual
+    uint32_t qh[8][2], ql[8][2];
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const float4 v = *reinterpret_cast<const float4 *>(qr + g * D + 32 * t4 + 4 * kb);
+      const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+      qh[kb][0] = h2u(h01);
+      qh[kb][1] = h2u(h23);
+      ql[kb][0] = pack_h2(v.x - f01.x, v.y - f01.y);
+      ql[kb][1] = pack_h2(v.z - f23.x, v.w - f23.y);
+    }
 
     // ---- per-warp state ----
     float acc[MAXM][8][4];
@@ -227,24 +318,23 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[m][mt][r] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;     // head g
 
     const int npages = pe - pb;
     const int my_n = npages > warp ? (npages - warp + WARPS - 1) / WARPS : 0;
-    // prologue
     if (lane == 0) {
       for (int k = 0; k < min(my_n, STAGES); ++k) {
-        long long c = consumed + k;
-        int st = (int)(c % STAGES);
+        const long long c = consumed + k;
+        const int st = (int)(c % STAGES);
         fence_async_smem();
         bulk_load(my_stage0 + (size_t)st * PL.page_bytes,
                   unit_pages + (long long)(pb + warp + k * WARPS) * PL.page_bytes, PL.page_bytes, &my_bars[st]);
       }
     }
 
-    uint32_t bk[8][2];      // score B fragments of the current group (fp16 high part)
-    uint32_t bl[8][2];      // and the fp16 residual
-    float beta0 = 0.f, beta1 = 0.f;
+    uint32_t af[8][4];       // score A fragments of the current group: [a_hi ; a_lo]
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) af[kb][0] = af[kb][1] = af[kb][2] = af[kb][3] = 0u;
 
     for (int k = 0; k < my_n; ++k) {
       const long long c = consumed + k;
@@ -258,142 +348,186 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
       const unsigned char *sp = my_stage0 + (size_t)st * PL.page_bytes;
       const int page = pb + warp + k * WARPS;
       const long long tok0 = (long long)page * PAGE;
-      const __half *norms = reinterpret_cast<const __half *>(sp + PL.off_norm);
+
+      // group offsets beta(head g, group) = q' . min for the page's groups (tensor cores)
+      float beta_g0 = 0.f, beta_g1 = 0.f;
+      if (tok0 < Tf) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          uint32_t b0 = 0u, b1 = 0u;
+          if (g < PAGE / G) {
+            const __half *mn = reinterpret_cast<const __half *>(sp + PL.off_stats + g * 2 * D * 2);
+            const uint2 v = *reinterpret_cast<const uint2 *>(mn + 32 * t4 + 4 * kb);
+            b0 = v.x;
+            b1 = v.y;
+          }
+          const uint32_t A[4] = {qh[kb][0], ql[kb][0], qh[kb][1], ql[kb][1]};
+          mma16816(d, A, b0, b1);
+        }
+        beta_g0 = __shfl_sync(FULL, d[0] + d[2], 4 * g);
+        beta_g1 = __shfl_sync(FULL, d[1] + d[3], 4 * g);
+      }
 
 #pragma unroll 1
-      for (int tile = 0; tile < PAGE / TILE; ++tile) {
-        const long long ts = tok0 + tile * TILE;
-        if (ts >= T) break;
-        float sc[4];
-        if (ts < Tf) {
-          if ((tile * TILE) % G == 0) {
-            // new group: B = q' o (mx - mn) (fp16), beta = q' . mn
-            const int gi = (tile * TILE) / G;
-            const __half *st_mn = reinterpret_cast<const __half *>(sp + PL.off_stats + gi * 2 * D * 2);
-            const __half *st_mx = st_mn + D;
-            const float *qh = qr + g * D + 32 * t4;
-            float bp = 0.f;
+      for (int hp = 0; hp < 2; ++hp) {
+        const long long hs = tok0 + 32 * hp;       // half-page start
+        if (hs >= T) break;
+        float sacc[4][4];                           // n-tiles (tile, nt); rows [hi | lo]
+        if (hs < Tf) {
+          if ((32 * hp) % G == 0) {
+            // new group: a = q' o range as an exact fp16 pair (TwoProduct), fragments [a_hi ; a_lo]
+            const __half *rg =
+                reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
 #pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
-              const float4 qv = *reinterpret_cast<const float4 *>(qh + 4 * kb);
-              const uint2 mnr = *reinterpret_cast<const uint2 *>(st_mn + 32 * t4 + 4 * kb);
-              const uint2 mxr = *reinterpret_cast<const uint2 *>(st_mx + 32 * t4 + 4 * kb);
-              const float2 mn01 = __half22float2(*reinterpret_cast<const __half2 *>(&mnr.x));
-              const float2 mn23 = __half22float2(*reinterpret_cast<const __half2 *>(&mnr.y));
-              const float2 mx01 = __half22float2(*reinterpret_cast<const __half2 *>(&mxr.x));
-              const float2 mx23 = __half22float2(*reinterpret_cast<const __half2 *>(&mxr.y));
-              const float a0 = qv.x * (mx01.x - mn01.x), a1 = qv.y * (mx01.y - mn01.y);
-              const float a2 = qv.z * (mx23.x - mn23.x), a3 = qv.w * (mx23.y - mn23.y);
-              bk[kb][0] = pack_h2(a0, a1);
-              bk[kb][1] = pack_h2(a2, a3);
-              // fp16 residuals: the score MMA runs on hi and lo so a keeps ~22 significant bits
-              const float2 h01 = __half22float2(*reinterpret_cast<const __half2 *>(&bk[kb][0]));
-              const float2 h23 = __half22float2(*reinterpret_cast<const __half2 *>(&bk[kb][1]));
-              bl[kb][0] = pack_h2(a0 - h01.x, a1 - h01.y);
-              bl[kb][1] = pack_h2(a2 - h23.x, a3 - h23.y);
-              bp = fmaf(qv.x, mn01.x, bp);
-              bp = fmaf(qv.y, mn01.y, bp);
-              bp = fmaf(qv.z, mn23.x, bp);
-              bp = fmaf(qv.w, mn23.y, bp);
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * t4 + 8 * k2);
+              const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int kb = 2 * k2 + u;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const __half2 r2 = u2h(rr[2 * u + h]);
+                  const __half2 hi = __hmul2(u2h(qh[kb][h]), r2);
+                  const __half2 er = __hfma2(u2h(qh[kb][h]), r2, __hneg2(hi));
+                  const __half2 lo = __hfma2(u2h(ql[kb][h]), r2, er);
+                  af[kb][2 * h] = h2u(hi);
+                  af[kb][2 * h + 1] = h2u(lo);
+                }
+              }
             }
-            bp += __shfl_xor_sync(FULL, bp, 1);
-            bp += __shfl_xor_sync(FULL, bp, 2);
-            beta0 = __shfl_sync(FULL, bp, 8 * t4);        // head 2*t4 lives in lanes 8*t4 .. +3
-            beta1 = __shfl_sync(FULL, bp, 8 * t4 + 4);    // head 2*t4+1
           }
-          uint32_t kw[LANE_WORDS];
+          const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
 #pragma unroll
-          for (int i = 0; i < LANE_WORDS; i += 4) {
-            const uint4 v4 = *reinterpret_cast<const uint4 *>(sp + tile * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
-            kw[i] = v4.x; kw[i + 1] = v4.y; kw[i + 2] = v4.z; kw[i + 3] = v4.w;
+          for (int n = 0; n < 4; ++n) {
+            sacc[n][0] = beta; sacc[n][1] = beta; sacc[n][2] = 0.f; sacc[n][3] = 0.f;
           }
-          sc[0] = beta0; sc[1] = beta1; sc[2] = beta0; sc[3] = beta1;
+          uint32_t kw[2][LANE_WORDS], kwh[2][LANE_WORDS];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+#pragma unroll
+            for (int i = 0; i < LANE_WORDS; i += 4) {
+              const uint4 v4 = *reinterpret_cast<const uint4 *>(sp + (2 * hp + t) * PL.tile_bytes +
+                                                                lane * PL.lane_bytes + 4 * i);
+              kw[t][i] = v4.x; kw[t][i + 1] = v4.y; kw[t][i + 2] = v4.z; kw[t][i + 3] = v4.w;
+            }
+#pragma unroll
+            for (int i = 0; i < LANE_WORDS; ++i) kwh[t][i] = BITS == 2 ? __byte_perm(kw[t][i], 0u, 0x4432u) : 0u;
+          }
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
-            uint32_t A[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) A[r] = lut_get<BITS>(klut, pair_index<BITS>(kw, 4 * kb + r), lane);
-            mma16816(sc, A, bk[kb][0], bk[kb][1]);
-            mma16816(sc, A, bl[kb][0], bl[kb][1]);
+            for (int t = 0; t < 2; ++t) {
+              uint32_t bf[4];
+              key_frags<BITS>(kw[t], kwh[t], kb, lutlo, luthi, lut_k, laneoff, bf);
+              mma16816(sacc[2 * t + 0], af[kb], bf[0], bf[1]);
+              mma16816(sacc[2 * t + 1], af[kb], bf[2], bf[3]);
+            }
           }
         } else {
           // trailing keys of an incomplete group: exact fp16 keys, unrotated query
-          const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
-          const int r0 = (int)(ts - Tf) + g, r1 = r0 + 8;
-          const int nt = (int)(T - Tf);
-          sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+          const int nt_valid = (int)(T - Tf);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
             const int c0 = 16 * kb + 2 * t4;
-            uint32_t A[4];
-            A[0] = r0 < nt ? *reinterpret_cast<const uint32_t *>(tail + r0 * D + c0) : 0u;
-            A[1] = r1 < nt ? *reinterpret_cast<const uint32_t *>(tail + r1 * D + c0) : 0u;
-            A[2] = r0 < nt ? *reinterpret_cast<const uint32_t *>(tail + r0 * D + c0 + 8) : 0u;
-            A[3] = r1 < nt ? *reinterpret_cast<const uint32_t *>(tail + r1 * D + c0 + 8) : 0u;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(qraw + g * D + c0);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(qraw + g * D + c0 + 8);
-            mma16816(sc, A, b0, b1);
+            const uint32_t A[4] = {*reinterpret_cast<const uint32_t *>(qraw + g * D + c0), 0u,
+                                   *reinterpret_cast<const uint32_t *>(qraw + g * D + c0 + 8), 0u};
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+              const int row = (int)(hs - Tf) + 8 * n + g;
+              const bool ok = row < nt_valid;
+              const uint32_t b0 = ok ? *reinterpret_cast<const uint32_t *>(tail + row * D + c0) : 0u;
+              const uint32_t b1 = ok ? *reinterpret_cast<const uint32_t *>(tail + row * D + c0 + 8) : 0u;
+              mma16816(sacc[n], A, b0, b1);
+            }
           }
 #pragma unroll
-          for (int r = 0; r < 4; ++r) sc[r] *= LOG2E * INV_SQRT_D;
+          for (int n = 0; n < 4; ++n) {
+            sacc[n][0] *= LOG2E * INV_SQRT_D;
+            sacc[n][1] *= LOG2E * INV_SQRT_D;
+          }
         }
-        // tokens past the end do not exist
-        if (ts + g >= T) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-        if (ts + g + 8 >= T) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
-
-        // ---- online softmax (base 2), heads 2*t4 and 2*t4+1 ----
-        float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
+        // scores of head g for tokens hs + 8n + 2*t4 + e
+        float s[4][2];
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, o));
-          x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, o));
-        }
-        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-        if (__any_sync(FULL, n0 > m0 || n1 > m1)) {
-          const float s0 = ex2(m0 - n0), s1 = ex2(m1 - n1);
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const long long tk = hs + 8 * n + 2 * t4 + e;
+            s[n][e] = tk < T ? sacc[n][e] + sacc[n][2 + e] : -INFINITY;
+          }
+
+        // ---- online softmax (base 2) for head g ----
+        float mx = s[0][0];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mx = fmaxf(mx, fmaxf(s[n][0], s[n][1]));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        if (__any_sync(FULL, m_new > m_run)) {
+          const float sf = ex2(m_run - m_new);
+          const float sf0 = __shfl_sync(FULL, sf, 8 * t4), sf1 = __shfl_sync(FULL, sf, 8 * t4 + 4);
 #pragma unroll
           for (int m = 0; m < MAXM; ++m)
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-              acc[m][mt][0] *= s0; acc[m][mt][2] *= s0;
-              acc[m][mt][1] *= s1; acc[m][mt][3] *= s1;
+              acc[m][mt][0] *= sf0; acc[m][mt][2] *= sf0;
+              acc[m][mt][1] *= sf1; acc[m][mt][3] *= sf1;
             }
-          l0 *= s0; l1 *= s1;
-          m0 = n0; m1 = n1;
+          l_run *= sf;
+          m_run = m_new;
         }
-        const float p0 = ex2(sc[0] - m0), p1 = ex2(sc[1] - m1);
-        const float p2 = ex2(sc[2] - m0), p3 = ex2(sc[3] - m1);
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        const float na = ts + g < T ? __half2float(norms[tile * TILE + g]) : 0.f;
-        const float nb = ts + g + 8 < T ? __half2float(norms[tile * TILE + g + 8]) : 0.f;
+        float p[4][2];
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            p[n][e] = ex2(s[n][e] - m_run);
+            l_run += p[n][e];
+          }
 
-        uint32_t vw[LANE_WORDS];
+        // ---- values, tile by tile ----
+        const __half *norms = reinterpret_cast<const __half *>(sp + PL.off_norm);
 #pragma unroll
-        for (int i = 0; i < LANE_WORDS; i += 4) {
-          const uint4 v4 =
-              *reinterpret_cast<const uint4 *>(sp + PL.off_v + tile * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
-          vw[i] = v4.x; vw[i + 1] = v4.y; vw[i + 2] = v4.z; vw[i + 3] = v4.w;
-        }
-        const uint32_t tmask = a.tmask[(long long)session * (a.cap / TILE) + ts / TILE];
-        if (__popc(tmask) == 1) {
-          const uint32_t b0 = transpose8x8(pack_h2(p0 * na, p1 * na));
-          const uint32_t b1 = transpose8x8(pack_h2(p2 * nb, p3 * nb));
-          const int m = __ffs(tmask) - 1;
-          if (m == 0) value_mma<BITS>(acc[0], vw, vlut, lane, b0, b1);
-          else if (m == 1) value_mma<BITS>(acc[1], vw, vlut, lane, b0, b1);
-          else value_mma<BITS>(acc[2], vw, vlut, lane, b0, b1);
-        } else {
-          const uint8_t *modp = a.mod + (long long)session * a.cap + ts;
-          const int ma = (ts + g < T) ? modp[g] : -1;
-          const int mb = (ts + g + 8 < T) ? modp[g + 8] : -1;
+        for (int t = 0; t < 2; ++t) {
+          const int tile = 2 * hp + t;
+          const long long ts = tok0 + 16 * tile;
+          if (ts >= T) break;
+          const int r0 = 16 * tile + 2 * t4;        // page-relative tokens r0, r0+1, r0+8, r0+9
+          const float2 n01 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0));
+          const float2 n89 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0 + 8));
+          const bool v0 = ts + 2 * t4 < T, v1 = ts + 2 * t4 + 1 < T, v8 = ts + 2 * t4 + 8 < T,
+                     v9 = ts + 2 * t4 + 9 < T;
+          const float w0 = v0 ? p[2 * t][0] * n01.x : 0.f, w1 = v1 ? p[2 * t][1] * n01.y : 0.f;
+          const float w8 = v8 ? p[2 * t + 1][0] * n89.x : 0.f, w9 = v9 ? p[2 * t + 1][1] * n89.y : 0.f;
+          uint32_t vw[LANE_WORDS];
 #pragma unroll
-          for (int m = 0; m < MAXM; ++m) {
-            if (!(tmask & (1u << m))) continue;
-            const float fa = ma == m ? na : 0.f, fb = mb == m ? nb : 0.f;
-            const uint32_t b0 = transpose8x8(pack_h2(p0 * fa, p1 * fa));
-            const uint32_t b1 = transpose8x8(pack_h2(p2 * fb, p3 * fb));
-            value_mma<BITS>(acc[m], vw, vlut, lane, b0, b1);
+          for (int i = 0; i < LANE_WORDS; i += 4) {
+            const uint4 v4 = *reinterpret_cast<const uint4 *>(sp + PL.off_v + tile * PL.tile_bytes +
+                                                              lane * PL.lane_bytes + 4 * i);
+            vw[i] = v4.x; vw[i + 1] = v4.y; vw[i + 2] = v4.z; vw[i + 3] = v4.w;
+          }
+          const uint32_t tmask = a.tmask[(long long)session * (a.cap / TILE) + ts / TILE];
+          if (__popc(tmask) == 1) {
+            const uint32_t b0 = pack_h2(w0, w1), b1 = pack_h2(w8, w9);
+            const int m = __ffs(tmask) - 1;
+            if (m == 0) value_mma<BITS>(acc[0], vw, lut_v, laneoff, b0, b1);
+            else if (m == 1) value_mma<BITS>(acc[1], vw, lut_v, laneoff, b0, b1);
+            else value_mma<BITS>(acc[2], vw, lut_v, laneoff, b0, b1);
+          } else {
+            const uint8_t *modp = a.mod + (long long)session * a.cap + ts + 2 * t4;
+            const int m0 = v0 ? modp[0] : -1, m1 = v1 ? modp[1] : -1;
+            const int m8 = v8 ? modp[8] : -1, m9 = v9 ? modp[9] : -1;
+#pragma unroll
+            for (int m = 0; m < MAXM; ++m) {
+              if (!(tmask & (1u << m))) continue;
+              const uint32_t b0 = pack_h2(m0 == m ? w0 : 0.f, m1 == m ? w1 : 0.f);
+              const uint32_t b1 = pack_h2(m8 == m ? w8 : 0.f, m9 == m ? w9 : 0.f);
+              value_mma<BITS>(acc[m], vw, lut_v, laneoff, b0, b1);
+            }
           }
         }
       }
@@ -417,16 +551,12 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
     }
     consumed += my_n;
 
-    // ---- per-warp totals ----
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(FULL, l0, o);
-      l1 += __shfl_xor_sync(FULL, l1, o);
-    }
-    __syncthreads();              // all warps done with their stage buffers
-    if (g == 0) {
-      MG.m[warp][2 * t4] = m0; MG.m[warp][2 * t4 + 1] = m1;
-      MG.l[warp][2 * t4] = l0; MG.l[warp][2 * t4 + 1] = l1;
+    // ---- per-warp totals: head g lives in lanes 4g..4g+3 ----
+    l_run += __shfl_xor_sync(FULL, l_run, 1);
+    l_run += __shfl_xor_sync(FULL, l_run, 2);
+    if (t4 == 0) {
+      MG.m[warp][g] = m_run;
+      MG.l[warp][g] = l_run;
     }
 #pragma unroll
     for (int m = 0; m < MAXM; ++m)
@@ -466,48 +596,62 @@ __global__ void __launch_bounds__(THREADS, 2) decode_kernel(const DecodeArgs a) 
   }
 }
 
+// One CTA per (unit, 32 output channels): merge the unit's partials by
+// log-sum-exp, then O = (sum_m R_m^T o_m) / (l sqrt d) with the R block staged in
+// shared memory.
+constexpr int CB_CH = 32;
+constexpr int CB_MAXSEG = 64;
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  extern __shared__ __align__(16) float csm[];
+  float *Rs = csm;                                   // [M * D rows][CB_CH]
+  float *osh = Rs + MAXM * D * CB_CH;                // [MAXGQ][M * D]
+  float *wsh = osh + MAXGQ * MAXM * D;               // [MAXGQ][CB_MAXSEG] segment weights
   __shared__ float Msh[MAXGQ], Lsh[MAXGQ];
-  __shared__ float osh[MAXGQ][MAXM][D];
   const int unit = blockIdx.x, cb = blockIdx.y;
   const int tid = threadIdx.x;
   const int gq = a.Hq / a.Hkv;
   const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
+  const int lh = unit % (a.L * a.Hkv);
+  const float *R = a.rot + (long long)lh * a.M * D * D;
+  for (int i = tid; i < a.M * D * (CB_CH / 4); i += blockDim.x) {
+    const int row = i / (CB_CH / 4), q = i % (CB_CH / 4);
+    reinterpret_cast<float4 *>(Rs)[row * (CB_CH / 4) + q] =
+        *reinterpret_cast<const float4 *>(R + (long long)row * D + cb * CB_CH + 4 * q);
+  }
   if (tid < MAXGQ) {
     float M = -INFINITY, L = 0.f;
     for (int s = s0; s < s1; ++s) M = fmaxf(M, a.partials[((long long)s * MAXGQ + tid) * PARTIAL_FLOATS]);
     for (int s = s0; s < s1; ++s) {
       const float *p = a.partials + ((long long)s * MAXGQ + tid) * PARTIAL_FLOATS;
-      if (p[0] != -INFINITY) L += ex2(p[0] - M) * p[1];
+      const float w = p[0] == -INFINITY ? 0.f : ex2(p[0] - M);
+      if (s - s0 < CB_MAXSEG) wsh[tid * CB_MAXSEG + (s - s0)] = w;
+      L += w * p[1];
     }
     Msh[tid] = M;
     Lsh[tid] = L;
   }
   __syncthreads();
-  for (int i = tid; i < MAXGQ * a.M * D; i += blockDim.x) {
-    const int hh = i / (a.M * D), m = (i / D) % a.M, j = i % D;
+  for (int i = tid; i < gq * a.M * D; i += blockDim.x) {
+    const int hh = i / (a.M * D), rest = i % (a.M * D);
     float o = 0.f;
-    if (hh < gq) {
-      for (int s = s0; s < s1; ++s) {
-        const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
-        if (p[0] != -INFINITY) o += ex2(p[0] - Msh[hh]) * p[2 + m * D + j];
-      }
+    for (int s = s0; s < s1; ++s) {
+      const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
+      const float w = s - s0 < CB_MAXSEG ? wsh[hh * CB_MAXSEG + (s - s0)]
+                                         : (p[0] == -INFINITY ? 0.f : ex2(p[0] - Msh[hh]));
+      o += w * p[2 + rest];
     }
-    osh[hh][m][j] = o;
+    osh[hh * MAXM * D + rest] = o;
   }
   __syncthreads();
-  const int hh = tid >> 5, ci = cb * 32 + (tid & 31);
   const int session = unit / (a.L * a.Hkv);
-  const int lh = unit % (a.L * a.Hkv);
   const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-  if (hh < gq) {
-    const float *R = a.rot + (long long)lh * a.M * D * D;
+  for (int i = tid; i < gq * CB_CH; i += blockDim.x) {
+    const int hh = i / CB_CH, cc = i % CB_CH;
     float acc = 0.f;
-    for (int m = 0; m < a.M; ++m)
-      for (int j = 0; j < D; ++j) acc = fmaf(R[((long long)m * D + j) * D + ci], osh[hh][m][j], acc);
+    for (int r = 0; r < a.M * D; ++r) acc = fmaf(Rs[r * CB_CH + cc], osh[hh * MAXM * D + r], acc);
     const float L = Lsh[hh];
     const float y = L > 0.f ? acc / (L * 11.3137084989847603904f) : 0.f;
-    a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + ci] = __float2half_rn(y);
+    a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb * CB_CH + cc] = __float2half_rn(y);
   }
 }
 
@@ -530,8 +674,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 size_t decode_smem_bytes(int bits, int G) {
   const PageLayout PL = page_layout(bits, G);
   const int stages = bits == 2 ? Cfg<2>::STAGES : Cfg<4>::STAGES;
-  const int lut = bits == 2 ? Cfg<2>::LUT_WORDS : Cfg<4>::LUT_WORDS;
-  size_t head = 2 * lut * 4 + MAXGQ * D * 4 + MAXGQ * D * 2 + WARPS * stages * 8;
+  size_t head = LUT_BYTES + MAXGQ * D * 4 + MAXGQ * D * 2 + WARPS * stages * 8;
   size_t ring = (size_t)WARPS * stages * PL.page_bytes;
   if (ring < sizeof(Merge)) ring = sizeof(Merge);
   return head + 128 + ring;
@@ -547,8 +690,15 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
   if (a.units <= 0) return cudaSuccess;
-  dim3 grid((unsigned)a.units, D / 32);
-  combine_kernel<<<grid, 256, 0, s>>>(a);
+  static bool attr_done = false;
+  const size_t smem = (MAXM * D * CB_CH + MAXGQ * MAXM * D + MAXGQ * CB_MAXSEG) * sizeof(float);
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid((unsigned)a.units, D / CB_CH);
+  combine_kernel<<<grid, 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -8,22 +8,28 @@
 //     K codes  4 tiles of 16 tokens, each tile 32 lane chunks of 16 B (2-bit) or 32 B (4-bit)
 //     V codes  same shape
 //     norms    64 fp16, token order
-//     stats    64/G groups, each [mn 128 fp16 | mx 128 fp16] in the stat channel order
+//     stats    64/G groups, each [min 128 fp16 | range 128 fp16] in the stat channel order
 //   so one decode warp streams one contiguous block per page with a single bulk copy.
 //
-// Lane chunks: the 32 lanes of a warp running mma.m16n8k16 hold A fragments of
-// 16x16 fp16 blocks; lane l owns 32 code pairs j = 0..31 (blk = j/4, reg = j%4),
-// each pair being the two fp16 halves of one A-fragment register:
-//   K tile (A = tokens x channels):  token   = l/4 + 8*(reg&1),
-//                                    channel = 16*blk + 2*(l%4) + 8*(reg>>1) + e
-//   V tile (A = channels x tokens):  token   = 2*(l%4) + 8*(reg>>1) + e,
-//                                    channel = 16*blk + l/4 + 8*(reg&1)
-// with e = 0/1 the half. In the chunk, code e of pair j sits at bit
-// bits*(2*j + e) (2-bit: nibble j, 4-bit: byte j).
+// Lane chunks: the 32 lanes of a warp running mma.m16n8k16 hold 16x16 / 16x8
+// fp16 fragments; lane l owns 32 code pairs j = 0..31 (blk = j/4, r = j%4), each
+// pair being the two fp16 halves of one fragment register:
+//   K tile (score MMA B operand, channels x tokens; blk = 16-channel block):
+//        token = l/4 + 8*(r&1),   channel = 16*blk + 2*(l%4) + 8*(r>>1) + e
+//   V tile (value MMA A operand, channels x tokens; blk = 16-channel block):
+//        token = 2*(l%4) + 8*(r>>1) + e,   channel = 16*blk + l/4 + 8*(r&1)
+// with e = 0/1 the half. Bit position of code e of pair j inside the chunk:
+//   4-bit: 8*j + 4*e (pair j = byte j).
+//   2-bit V, and 2-bit K words not in KREG_WORDS: 4*j + 2*e (pair j = nibble j);
+//        a byte holds two pairs and indexes the shared-memory level table.
+//   2-bit K words in KREG_WORDS (register table path): word i = j/8 holds pairs
+//        q = j%8 with code e at bit 16*(q/4) + 2*(q%4) + 8*e, so one mask picks a
+//        pair as two 2-bit fields 8 bits apart, ready to become a byte-permute
+//        selector.
 //
 // Stat channel order: position p = 32*t + 4*kb + i (t = 0..3, kb = 0..7, i = 0..3)
 // holds channel 16*kb + 2*t + (i&1) + 8*(i>>1), i.e. the channels lane group t
-// needs for its B fragments, contiguous.
+// needs for its fragments, contiguous. Each group stores [min 128 fp16 | range 128 fp16].
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -76,6 +82,36 @@ __host__ __device__ inline void v_pair_coords(int lane, int j, int e, int &tok, 
   tok = 2 * (lane & 3) + 8 * (reg >> 1) + e;
   ch = 16 * blk + (lane >> 2) + 8 * (reg & 1);
 }
+// 2-bit K chunk words that use the register table layout (bit w = word w)
+constexpr unsigned KREG_WORDS = 0xFu;
+
+__host__ __device__ inline int k_code_bit(int bits, int j, int e) {
+  if (bits == 4) return 8 * j + 4 * e;
+  const int word = j >> 3;
+  if ((KREG_WORDS >> word) & 1u) {
+    const int q = j & 7;
+    return 32 * word + 16 * (q >> 2) + 2 * (q & 3) + 8 * e;
+  }
+  return 4 * j + 2 * e;
+}
+__host__ __device__ inline int v_code_bit(int bits, int j, int e) { return bits == 4 ? 8 * j + 4 * e : 4 * j + 2 * e; }
+
+// Inverse of k_code_bit / v_code_bit: the (pair, half) whose code starts at bit b
+// of chunk word wi (b a multiple of bits).
+__host__ __device__ inline void chunk_code_at(int kind, int bits, int wi, int b, int &j, int &e) {
+  if (bits == 4) {
+    j = (32 * wi + b) >> 3;
+    e = (b >> 2) & 1;
+  } else if (kind == 0 && ((KREG_WORDS >> wi) & 1u)) {
+    const int half = b >> 4, bb = b & 15;
+    e = bb >> 3;
+    j = 8 * wi + 4 * half + ((bb & 7) >> 1);
+  } else {
+    j = (32 * wi + b) >> 2;
+    e = (b >> 1) & 1;
+  }
+}
+
 __host__ __device__ inline int stat_channel(int p) {
   int t = p >> 5, kb = (p >> 2) & 7, i = p & 3;
   return 16 * kb + 2 * t + (i & 1) + 8 * (i >> 1);

@@ -25,10 +25,11 @@
  *     (bit set -> -1), shared by every session, layer and head;
  *   - keys: k' = fp32(1/sqrt(d)) * FWHT(s o k) in fp32 with butterfly strides
  *     1, 2, ..., 64; groups of group_size consecutive tokens aligned to the
- *     absolute token index; per channel the group min is stored as fp16
- *     rounded down and the max as fp16 rounded up; u = (k'-mn)/(mx-mn) in
+ *     absolute token index; per channel the group statistics are the min,
+ *     stored fp16 rounded down, and the range max - min, stored fp16 rounded
+ *     up, so [min, min + range] contains every member; u = (k'-min)/range in
  *     fp32 is coded to the nearest of the key levels
- *     lambda_j = (l_j - l_0) / (l_last - l_0); mx == mn gives code 0;
+ *     lambda_j = (l_j - l_0) / (l_last - l_0); range 0 gives code 0;
  *     the keys of an incomplete trailing group stay in fp16 and are attended
  *     exactly until the group completes;
  *   - values: n = |v| stored fp16 (round to nearest even);
@@ -123,7 +124,7 @@ okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
  * (synchronizes the device). With host_buf == NULL only *bytes is set. With
  * T tokens, Tf = T - T % group_size, B = 128*bits/8, the buffer holds, in order:
  *   kcodes  uint8 [L][Hkv][Tf][B]   channel c at byte c*bits/8, bit (c*bits)%8
- *   kstats  fp16  [L][Hkv][Tf/group_size][2][128]   (min, max)
+ *   kstats  fp16  [L][Hkv][Tf/group_size][2][128]   (min, range)
  *   ktail   fp16  [L][Hkv][T-Tf][128]               (unquantized trailing keys)
  *   vcodes  uint8 [L][Hkv][T][B]
  *   vnorm   fp16  [L][Hkv][T]

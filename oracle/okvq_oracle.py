@@ -20,9 +20,11 @@ narrower precision so that both sides decide identically:
 * the key Hadamard rotation is the canonical fp32 butterfly (stride 1, 2, ...,
   d/2; a+b / a-b, round-to-nearest, no fused multiply-add) followed by one
   fp32 multiply by fp32(1/sqrt(d));
-* key group statistics are fp16, min rounded toward -inf and max toward +inf;
-* the key code decision is u = (k' - mn) / (mx - mn) in fp32, compared with
-  fp32 midpoint thresholds (ties go to the lower code);
+* key group statistics are the group minimum and range, both fp16: the minimum
+  rounded toward -inf, the range (max - stored min, exact) rounded toward +inf,
+  so the stored interval [mn, mn + rg] contains every member;
+* the key code decision is u = (k' - mn) / rg in fp32, compared with fp32
+  midpoint thresholds (ties go to the lower code);
 * the value code decision compares fp32(w) with fp32 thresholds, w computed
   in fp64; codes whose fp64 w lies within 1e-5 of a threshold are flagged as
   boundary codes (another correct implementation may round them the other way).
@@ -226,26 +228,33 @@ def f16_near_midpoint(x64: np.ndarray, rel: float = NORM_BAND_REL) -> np.ndarray
 # append-time quantization (section 2, OmniKVQuant bullets)
 # ---------------------------------------------------------------------------
 
+def f16_round_up_f64(x64: np.ndarray) -> np.ndarray:
+    """Smallest fp16 >= x (x given exactly in fp64)."""
+    x64 = np.asarray(x64, F64)
+    h = x64.astype(F16)
+    return np.where(h.astype(F64) < x64, np.nextafter(h, F16(np.inf)), h).astype(F16)
+
+
 def quantize_key_group(kp32: np.ndarray, cb: Codebook):
     """One group of G consecutive rotated keys kp32 [G][d] (fp32).
 
-    Per channel: mn = min over the group rounded down to fp16, mx = max
-    rounded up (the stored range contains every member); u = (k'-mn)/(mx-mn)
-    in fp32; code = nearest normalized key level.  mx == mn gives code 0.
-    Returns mn16 [d], mx16 [d], codes [G][d], boundary mask [G][d].
+    Per channel the group statistics are mn = min over the group rounded down
+    to fp16 and rg = (max - mn) rounded up to fp16, so [mn, mn + rg] contains
+    every member; u = (k' - mn) / rg in fp32; code = nearest normalized key
+    level.  rg == 0 gives code 0.
+    Returns mn16 [d], rg16 [d], codes [G][d], boundary mask [G][d].
     """
     mn = f16_round_down(kp32.min(axis=0))
-    mx = f16_round_up(kp32.max(axis=0))
-    mn32, mx32 = mn.astype(F32), mx.astype(F32)
-    rng = (mx32 - mn32).astype(F32)
-    flat = rng == 0
-    safe = np.where(flat, F32(1), rng).astype(F32)
+    rg = f16_round_up_f64(kp32.max(axis=0).astype(F64) - mn.astype(F64))
+    mn32, rg32 = mn.astype(F32), rg.astype(F32)
+    flat = rg32 == 0
+    safe = np.where(flat, F32(1), rg32).astype(F32)
     u = ((kp32 - mn32[None]).astype(F32) / safe[None]).astype(F32)
     codes = nearest_code(u, cb.kthr)
     codes[:, flat] = 0
     bnd = near_threshold(u, cb.kthr)
     bnd[:, flat] = False
-    return mn, mx, codes, bnd
+    return mn, rg, codes, bnd
 
 
 def quantize_values(v16: np.ndarray, R: np.ndarray, cb: Codebook):
@@ -298,7 +307,7 @@ class OracleUnit:
         self.kcodes = np.zeros((cap, d), np.uint8)
         self.kbnd = np.zeros((cap, d), bool)
         self.kmn = np.zeros((-(-cap // group_size), d), F16)
-        self.kmx = np.zeros_like(self.kmn)
+        self.krg = np.zeros_like(self.kmn)
         self.keys16 = np.zeros((cap, d), F16)          # fp16 inputs kept for the trailing (tail) group
         self.vcodes = np.zeros((cap, d), np.uint8)
         self.vbnd = np.zeros((cap, d), bool)
@@ -328,8 +337,8 @@ class OracleUnit:
         G = self.G
         for g in range(t0 // G, t1 // G):
             kp = rotate_keys_f32(self.keys16[g * G:(g + 1) * G], self.signs)
-            mn, mx, codes, bnd = quantize_key_group(kp, self.cb)
-            self.kmn[g], self.kmx[g] = mn, mx
+            mn, rg, codes, bnd = quantize_key_group(kp, self.cb)
+            self.kmn[g], self.krg[g] = mn, rg
             self.kcodes[g * G:(g + 1) * G] = codes
             self.kbnd[g * G:(g + 1) * G] = bnd
         self.T = t1
@@ -340,7 +349,7 @@ class OracleUnit:
         b = self.cb.bits
         return {
             "kcodes": pack_codes(self.kcodes[:Tf], b),
-            "kstats": np.stack([self.kmn[:Tf // G], self.kmx[:Tf // G]], axis=1),   # [T/G][2][d]
+            "kstats": np.stack([self.kmn[:Tf // G], self.krg[:Tf // G]], axis=1),   # [T/G][2][d] (min, range)
             "ktail": self.keys16[Tf:T].copy(),
             "vcodes": pack_codes(self.vcodes[:T], b),
             "vnorm": self.vnorm[:T].copy(),
@@ -354,7 +363,7 @@ class OracleUnit:
         """Fused-score decode of the q_per_kv heads [Gq][d] -> fp64 [Gq][d].
 
         q' = (1/sqrt d) H D q, scaled by the softmax factor 1/sqrt d.  A quantized
-        token t in group g scores beta_g + sum_c (q'_c * (mx-mn)_{g,c}) lambda(code);
+        token t in group g scores beta_g + sum_c (q'_c * rg_{g,c}) lambda(code);
         beta_g = sum_c q'_c mn_{g,c}.  A tail token scores q.k/sqrt d from its fp16 key.
         One softmax over all tokens; o_m accumulates p_t * n_t * l(vcode)/sqrt d in the
         rotated value domain of modality m; O = (sum_m R_m^T o_m) / sum p.
@@ -370,7 +379,7 @@ class OracleUnit:
         if Tf:
             ng = Tf // G
             mn = self.kmn[:ng].astype(F64)
-            dl = self.kmx[:ng].astype(F64) - mn
+            dl = self.krg[:ng].astype(F64)
             lam = self.cb.ktab[self.kcodes[:Tf]].reshape(ng, G, d)           # [g][t][c]
             beta = qr @ mn.T                                                 # [Gq][g]
             a = qr[:, None, :] * dl[None]                                    # [Gq][g][c]
@@ -399,8 +408,8 @@ class OracleUnit:
         if Tf:
             g = np.arange(Tf) // G
             mn = self.kmn[g].astype(F64)
-            mx = self.kmx[g].astype(F64)
-            kp = mn + self.cb.ktab[self.kcodes[:Tf]] * (mx - mn)             # rotated domain
+            rg = self.krg[g].astype(F64)
+            kp = mn + self.cb.ktab[self.kcodes[:Tf]] * rg                    # rotated domain
             Kh[:Tf] = (kp @ H.T) * self.signs.astype(F64)[None] / math.sqrt(d)   # D H^T k'/sqrt d
         Kh[Tf:] = self.keys16[Tf:T].astype(F64)
         R64 = self.R.astype(F64)

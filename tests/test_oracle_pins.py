@@ -164,17 +164,20 @@ def test_key_group_codes_bounds_and_brute_force(bits):
     s = o.hadamard_signs(3, 128)
     k = (r.standard_normal((32, 128)) * r.uniform(0.5, 4, 128) + 0.7).astype(F16)
     kp = o.rotate_keys_f32(k, s)
-    mn, mx, codes, bnd = o.quantize_key_group(kp, cb)
-    mn64, mx64 = mn.astype(F64), mx.astype(F64)
-    assert np.all(mn64 <= kp.min(0)) and np.all(mx64 >= kp.max(0))
-    u = (kp.astype(F64) - mn64) / (mx64 - mn64)
+    mn, rg, codes, bnd = o.quantize_key_group(kp, cb)
+    mn64, rg64 = mn.astype(F64), rg.astype(F64)
+    # the stored interval contains every member, and both ends are the tightest fp16
+    assert np.all(mn64 <= kp.min(0)) and np.all(mn64 + rg64 >= kp.max(0))
+    assert np.all(np.nextafter(mn, F16(np.inf)).astype(F64) > kp.min(0))
+    assert np.all(mn64 + np.nextafter(rg, F16(-np.inf)).astype(F64) < kp.max(0))
+    u = (kp.astype(F64) - mn64) / rg64
     ref = _brute_nearest(u, cb.ktab)
     ok = ~bnd
     assert np.array_equal(codes[ok], ref[ok])
-    rec = mn64 + cb.ktab[codes] * (mx64 - mn64)
-    assert np.all(rec >= mn64 - 1e-12) and np.all(rec <= mx64 + 1e-12)
+    rec = mn64 + cb.ktab[codes] * rg64
+    assert np.all(rec >= mn64 - 1e-12) and np.all(rec <= mn64 + rg64 + 1e-12)
     gap = np.max(np.diff(cb.ktab))
-    assert np.all(np.abs(rec - kp) <= (mx64 - mn64) * gap / 2 + 1e-6)
+    assert np.all(np.abs(rec - kp) <= rg64 * gap / 2 + 1e-6)
     # every code of a wide group is used somewhere; the top and bottom levels are hit
     assert codes.min() == 0 and codes.max() == (1 << bits) - 1
 
@@ -182,8 +185,14 @@ def test_key_group_codes_bounds_and_brute_force(bits):
 def test_key_group_degenerate_range_gives_code_zero():
     cb = o.make_codebook(2)
     kp = np.full((32, 128), 1.25, F32)
-    mn, mx, codes, _ = o.quantize_key_group(kp, cb)
-    assert np.all(mn == mx) and np.all(codes == 0)
+    mn, rg, codes, _ = o.quantize_key_group(kp, cb)
+    assert np.all(rg == 0) and np.all(codes == 0)
+
+
+def test_f16_round_up_of_exact_values():
+    x = np.array([0.0, 1.0, 1.0 + 2.0 ** -12, 3.0 - 2.0 ** -30, 65504.0], F64)
+    up = o.f16_round_up_f64(x).astype(F64)
+    assert up.tolist() == [0.0, 1.0, 1.0 + 2.0 ** -10, 3.0, 65504.0]
 
 
 # ---------------------------------------------------------------- values
