@@ -209,7 +209,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if (c.group_size != 32 && c.group_size != 64) return OKVQ_EINVAL;
   if (c.bits != 2 && c.bits != 4) return OKVQ_EINVAL;
   if (c.num_modalities < 1 || c.num_modalities > MAXM) return OKVQ_EINVAL;
-  if (c.max_tokens < 1 || c.max_tokens > (1ll << 40)) return OKVQ_EINVAL;
+  if (c.max_tokens < 1 || c.max_tokens > (1ll << 31) - PAGE) return OKVQ_EINVAL;   // token indices are 32-bit
   if (!c.value_rot) return OKVQ_EINVAL;
   const int nlev = 1 << c.bits;
   double lv[16];

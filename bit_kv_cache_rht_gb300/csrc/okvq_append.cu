@@ -35,13 +35,6 @@ struct Smem {
   int present[MAXM];
 };
 
-__device__ __forceinline__ int stat_pos(int c) {
-  int kb = c >> 4, r = c & 15;
-  int t = (r & 7) >> 1;
-  int i = (r & 1) | ((r >> 3) << 1);
-  return 32 * t + 4 * kb + i;
-}
-
 __device__ __forceinline__ int code_of(float x, const float *thr, int nthr) {
   int c = 0;
 #pragma unroll 15

@@ -90,7 +90,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -104,13 +104,15 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
+// the level table lives at the start of dynamic shared memory; table reads are
+// plain loads so the compiler can schedule them and fold the base address
+__device__ __forceinline__ uint32_t lut32(const unsigned char *lut, uint32_t off) {
+  return *reinterpret_cast<const uint32_t *>(lut + off);
 }
-__device__ __forceinline__ void lds64(uint32_t addr, uint32_t &a, uint32_t &b) {
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+__device__ __forceinline__ void lut64(const unsigned char *lut, uint32_t off, uint32_t &a, uint32_t &b) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(lut + off);
+  a = v.x;
+  b = v.y;
 }
 
 // 2-bit key pair from the register-table layout: `src` holds the pair's two
@@ -141,8 +143,8 @@ struct Merge {
 
 // value tile of one modality: acc[mt] += Lcode[16 ch x 16 tok] * P
 template <int BITS>
-__device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw, uint32_t lut_v, uint32_t laneoff,
-                                          uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw, const unsigned char *lut_v,
+                                          uint32_t laneoff, uint32_t b0, uint32_t b1) {
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t A[4];
@@ -150,14 +152,14 @@ __device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw
       const uint32_t w = vw[mt >> 1];
       const uint32_t a0 = (mt & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
       const uint32_t a1 = (mt & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
-      lds64(lut_v + a0, A[0], A[1]);
-      lds64(lut_v + a1, A[2], A[3]);
+      lut64(lut_v, a0, A[0], A[1]);
+      lut64(lut_v, a1, A[2], A[3]);
     } else {
       const uint32_t w = vw[mt];
-      A[0] = lds32(lut_v + lut_addr<0>(laneoff, w));
-      A[1] = lds32(lut_v + lut_addr<1>(laneoff, w));
-      A[2] = lds32(lut_v + lut_addr<2>(laneoff, w));
-      A[3] = lds32(lut_v + lut_addr<3>(laneoff, w));
+      A[0] = lut32(lut_v, lut_addr<0>(laneoff, w));
+      A[1] = lut32(lut_v, lut_addr<1>(laneoff, w));
+      A[2] = lut32(lut_v, lut_addr<2>(laneoff, w));
+      A[3] = lut32(lut_v, lut_addr<3>(laneoff, w));
     }
     mma16816(acc[mt], A, b0, b1);
   }
@@ -167,7 +169,8 @@ __device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw
 // n-tile 0 (tokens 0-7): (pair 4kb, pair 4kb+2); n-tile 1: (pair 4kb+1, pair 4kb+3)
 template <int BITS>
 __device__ __forceinline__ void key_frags(const uint32_t *kw, const uint32_t *kwh, int kb, uint32_t lutlo,
-                                          uint32_t luthi, uint32_t lut_k, uint32_t laneoff, uint32_t (&bf)[4]) {
+                                          uint32_t luthi, const unsigned char *lut_k, uint32_t laneoff,
+                                          uint32_t (&bf)[4]) {
   if (BITS == 2) {
     if ((KREG_WORDS >> (kb >> 1)) & 1u) {
       const uint32_t src = (kb & 1) ? kwh[kb >> 1] : kw[kb >> 1];
@@ -180,16 +183,16 @@ __device__ __forceinline__ void key_frags(const uint32_t *kw, const uint32_t *kw
       uint32_t p0, p1, p2, p3;
       const uint32_t a0 = (kb & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
       const uint32_t a1 = (kb & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
-      lds64(lut_k + a0, p0, p1);   // pairs 4kb, 4kb+1
-      lds64(lut_k + a1, p2, p3);   // pairs 4kb+2, 4kb+3
+      lut64(lut_k, a0, p0, p1);   // pairs 4kb, 4kb+1
+      lut64(lut_k, a1, p2, p3);   // pairs 4kb+2, 4kb+3
       bf[0] = p0; bf[1] = p2; bf[2] = p1; bf[3] = p3;
     }
   } else {
     const uint32_t w = kw[kb];
-    bf[0] = lds32(lut_k + lut_addr<0>(laneoff, w));
-    bf[1] = lds32(lut_k + lut_addr<2>(laneoff, w));
-    bf[2] = lds32(lut_k + lut_addr<1>(laneoff, w));
-    bf[3] = lds32(lut_k + lut_addr<3>(laneoff, w));
+    bf[0] = lut32(lut_k, lut_addr<0>(laneoff, w));
+    bf[1] = lut32(lut_k, lut_addr<2>(laneoff, w));
+    bf[2] = lut32(lut_k, lut_addr<1>(laneoff, w));
+    bf[3] = lut32(lut_k, lut_addr<3>(laneoff, w));
   }
 }
 
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
-  const uint32_t lut_k = smem_u32(lut), lut_v = lut_k + 128;
+  const unsigned char *lut_k = lut, *lut_v = lut + 128;
   const uint32_t laneoff = BITS == 2 ? (uint32_t)((lane & 15) << 3) : (uint32_t)(lane << 2);
   // 4-entry key level table in registers (2-bit register path)
   uint32_t lutlo = 0, luthi = 0;
@@ -249,7 +252,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
   }
 
   const int gq = a.Hq / a.Hkv;
-  long long consumed = 0;
+  int ring_st = 0;          // stage of the next page this warp consumes
+  uint32_t ring_par = 0;    // its mbarrier phase parity
   bool wait_failed = false;
 
   const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     const int session = unit / (a.L * a.Hkv);
     const int lh = unit % (a.L * a.Hkv);
     const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-    const long long T = a.unit_len[unit];
-    const long long Tf = (T / G) * G;
+    const int T = (int)a.unit_len[unit];
+    const int Tf = (T / G) * G;
     const unsigned char *unit_pages = a.pages + (long long)unit * a.P_max * PL.page_bytes;
     const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
 
@@ -290,9 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = 4 * lane + j;
-        const int kb = c >> 4, r = c & 15;
-        const int pos = 32 * ((r & 7) >> 1) + 4 * kb + ((r & 1) | ((r >> 3) << 1));
-        qr[hh * D + pos] = x[j] * (INV_D * LOG2E);
+        qr[hh * D + stat_pos(c)] = x[j] * (INV_D * LOG2E);
       }
     }
     __syncthreads();
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     uint32_t qh[8][2], ql[8][2];
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb) {
-      const float4 v = *reinterpret_cast<const float4 *>(qr + g * D + 32 * t4 + 4 * kb);
+      const float4 v = *reinterpret_cast<const float4 *>(qr + g * D + 32 * (kb >> 1) + 8 * t4 + 4 * (kb & 1));
       const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
       const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
       qh[kb][0] = h2u(h01);
@@ -324,8 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     const int my_n = npages > warp ? (npages - warp + WARPS - 1) / WARPS : 0;
     if (lane == 0) {
       for (int k = 0; k < min(my_n, STAGES); ++k) {
-        const long long c = consumed + k;
-        const int st = (int)(c % STAGES);
+        const int st = (ring_st + k) % STAGES;
         fence_async_smem();
         bulk_load(my_stage0 + (size_t)st * PL.page_bytes,
                   unit_pages + (long long)(pb + warp + k * WARPS) * PL.page_bytes, PL.page_bytes, &my_bars[st]);
@@ -337,17 +338,19 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     for (int kb = 0; kb < 8; ++kb) af[kb][0] = af[kb][1] = af[kb][2] = af[kb][3] = 0u;
 
     for (int k = 0; k < my_n; ++k) {
-      const long long c = consumed + k;
-      const int st = (int)(c % STAGES);
-      const uint32_t par = (uint32_t)((c / STAGES) & 1);
-      if (!mbar_wait(&my_bars[st], par)) {
+      const int st = ring_st;
+      if (!mbar_wait(&my_bars[st], ring_par)) {
         wait_failed = true;
         break;
+      }
+      if (++ring_st == STAGES) {
+        ring_st = 0;
+        ring_par ^= 1u;
       }
       __syncwarp();
       const unsigned char *sp = my_stage0 + (size_t)st * PL.page_bytes;
       const int page = pb + warp + k * WARPS;
-      const long long tok0 = (long long)page * PAGE;
+      const int tok0 = page * PAGE;
 
       // group offsets beta(head g, group) = q' . min for the page's groups (tensor cores)
       float beta_g0 = 0.f, beta_g1 = 0.f;
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
           uint32_t b0 = 0u, b1 = 0u;
           if (g < PAGE / G) {
             const __half *mn = reinterpret_cast<const __half *>(sp + PL.off_stats + g * 2 * D * 2);
-            const uint2 v = *reinterpret_cast<const uint2 *>(mn + 32 * t4 + 4 * kb);
+            const uint2 v = *reinterpret_cast<const uint2 *>(mn + 32 * (kb >> 1) + 8 * t4 + 4 * (kb & 1));
             b0 = v.x;
             b1 = v.y;
           }
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
 
 #pragma unroll 1
       for (int hp = 0; hp < 2; ++hp) {
-        const long long hs = tok0 + 32 * hp;       // half-page start
+        const int hs = tok0 + 32 * hp;             // half-page start
         if (hs >= T) break;
         float sacc[4][4];                           // n-tiles (tile, nt); rows [hi | lo]
         if (hs < Tf) {
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
                 reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
-              const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * t4 + 8 * k2);
+              const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
               const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int u = 0; u < 2; ++u) {
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
           }
         } else {
           // trailing keys of an incomplete group: exact fp16 keys, unrotated query
-          const int nt_valid = (int)(T - Tf);
+          const int nt_valid = T - Tf;
 #pragma unroll
           for (int n = 0; n < 4; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
 #pragma unroll
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
                                    *reinterpret_cast<const uint32_t *>(qraw + g * D + c0 + 8), 0u};
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
-              const int row = (int)(hs - Tf) + 8 * n + g;
+              const int row = hs - Tf + 8 * n + g;
               const bool ok = row < nt_valid;
               const uint32_t b0 = ok ? *reinterpret_cast<const uint32_t *>(tail + row * D + c0) : 0u;
               const uint32_t b1 = ok ? *reinterpret_cast<const uint32_t *>(tail + row * D + c0 + 8) : 0u;
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
         for (int n = 0; n < 4; ++n)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const long long tk = hs + 8 * n + 2 * t4 + e;
+            const int tk = hs + 8 * n + 2 * t4 + e;
             s[n][e] = tk < T ? sacc[n][e] + sacc[n][2 + e] : -INFINITY;
           }
 
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int tile = 2 * hp + t;
-          const long long ts = tok0 + 16 * tile;
+          const int ts = tok0 + 16 * tile;
           if (ts >= T) break;
           const int r0 = 16 * tile + 2 * t4;        // page-relative tokens r0, r0+1, r0+8, r0+9
           const float2 n01 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0));
@@ -545,11 +548,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
       // chance to land, and leave this CTA's partials unwritten
       if (tid == 0) atomicOr(a.err, ERR_WAIT);
       if (lane == 0)
-        for (long long c2 = consumed; c2 < consumed + min(my_n, STAGES); ++c2)
-          (void)mbar_wait(&my_bars[c2 % STAGES], (uint32_t)((c2 / STAGES) & 1));
+        for (int s2 = 0; s2 < STAGES; ++s2) (void)mbar_wait(&my_bars[(ring_st + s2) % STAGES], ring_par ^ (s2 + ring_st >= STAGES ? 1u : 0u));
       return;
     }
-    consumed += my_n;
 
     // ---- per-warp totals: head g lives in lanes 4g..4g+3 ----
     l_run += __shfl_xor_sync(FULL, l_run, 1);

@@ -27,9 +27,12 @@
 //        pair as two 2-bit fields 8 bits apart, ready to become a byte-permute
 //        selector.
 //
-// Stat channel order: position p = 32*t + 4*kb + i (t = 0..3, kb = 0..7, i = 0..3)
-// holds channel 16*kb + 2*t + (i&1) + 8*(i>>1), i.e. the channels lane group t
-// needs for its fragments, contiguous. Each group stores [min 128 fp16 | range 128 fp16].
+// Stat channel order: position p = 32*(kb/2) + 8*t + 4*(kb%2) + i (t = 0..3,
+// kb = 0..7, i = 0..3) holds channel 16*kb + 2*t + (i&1) + 8*(i>>1): the 8
+// channels lane group t needs from a pair of 16-channel blocks are one 16-byte
+// chunk, and the four lane groups' chunks are adjacent (one 128-bit shared load
+// serves the warp without bank conflicts). Each group stores
+// [min 128 fp16 | range 128 fp16].
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -113,8 +116,13 @@ __host__ __device__ inline void chunk_code_at(int kind, int bits, int wi, int b,
 }
 
 __host__ __device__ inline int stat_channel(int p) {
-  int t = p >> 5, kb = (p >> 2) & 7, i = p & 3;
-  return 16 * kb + 2 * t + (i & 1) + 8 * (i >> 1);
+  const int k2 = p >> 5, t = (p >> 3) & 3, u = (p >> 2) & 1, i = p & 3;
+  return 16 * (2 * k2 + u) + 2 * t + (i & 1) + 8 * (i >> 1);
+}
+__host__ __device__ inline int stat_pos(int c) {
+  const int kb = c >> 4, r = c & 15;
+  const int t = (r & 7) >> 1, i = (r & 1) | ((r >> 3) << 1);
+  return 32 * (kb >> 1) + 8 * t + 4 * (kb & 1) + i;
 }
 
 struct AppendArgs {

@@ -80,7 +80,7 @@ typedef struct {
   int32_t group_size;     /* key group size: 32 or 64 tokens */
   int32_t bits;           /* code width for keys and values: 2 or 4 */
   int32_t num_modalities; /* 1..3; modality ids are 0..num_modalities-1 */
-  int64_t max_tokens;     /* per-session capacity; all storage is allocated by okvq_create */
+  int64_t max_tokens;     /* per-session capacity, 1 .. 2^31 - 64; all storage is allocated by okvq_create */
   uint64_t hadamard_seed; /* seed of the shared random sign vector */
   const float *codebook;  /* host, 2^bits strictly ascending levels, or NULL for Lloyd-Max N(0,1);
                              copied at create */
