@@ -123,16 +123,22 @@ __device__ __forceinline__ void lut64(const unsigned char *lut, uint32_t off, ui
 __device__ __forceinline__ uint32_t kreg_pair(uint32_t src, int s, uint32_t lutlo, uint32_t luthi) {
   constexpr float MUL[4] = {17.0f, 4.25f, 1.0625f, 0.265625f};
   constexpr float ADD[4] = {-134201280.0f, -27246528.0f, -507840.0f, 6176832.0f};
-  const uint32_t t = (src & (0x0303u << s)) | 0x4B000000u;
-  const float f = fmaf(__uint_as_float(t), MUL[s >> 1], ADD[s >> 1]);
-  return __byte_perm(lutlo, luthi, __float_as_uint(f));
+  uint32_t t, r;
+  float f;
+  // single lop3 / fma / prmt (the plain C++ form compiles to about twice as many ops)
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(src), "r"(0x0303u << s), "r"(0x4B000000u));
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(f) : "f"(__uint_as_float(t)), "f"(MUL[s >> 1]), "f"(ADD[s >> 1]));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lutlo), "r"(luthi), "r"(__float_as_uint(f)));
+  return r;
 }
 
 // shared-memory table address for code byte `B` (0..3) of word w:
 // byte << 8 | lane part (laneoff holds it in its low byte)
 template <int B>
 __device__ __forceinline__ uint32_t lut_addr(uint32_t laneoff, uint32_t w) {
-  return __byte_perm(laneoff, w, 0x1100u | ((4u + B) << 4));
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(laneoff), "r"(w), "n"(0x1100u | ((4u + B) << 4)));
+  return r;
 }
 
 struct Merge {
@@ -168,12 +174,12 @@ __device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw
 // key B fragments of one kb block for one 16-token tile:
 // n-tile 0 (tokens 0-7): (pair 4kb, pair 4kb+2); n-tile 1: (pair 4kb+1, pair 4kb+3)
 template <int BITS>
-__device__ __forceinline__ void key_frags(const uint32_t *kw, const uint32_t *kwh, int kb, uint32_t lutlo,
-                                          uint32_t luthi, const unsigned char *lut_k, uint32_t laneoff,
-                                          uint32_t (&bf)[4]) {
+__device__ __forceinline__ void key_frags(const uint32_t *kw, int kb, uint32_t lutlo, uint32_t luthi,
+                                          const unsigned char *lut_k, uint32_t laneoff, uint32_t (&bf)[4]) {
   if (BITS == 2) {
     if ((KREG_WORDS >> (kb >> 1)) & 1u) {
-      const uint32_t src = (kb & 1) ? kwh[kb >> 1] : kw[kb >> 1];
+      uint32_t src = kw[kb >> 1];
+      if (kb & 1) asm("prmt.b32 %0, %1, 0, 0x4432;" : "=r"(src) : "r"(kw[kb >> 1]));
       bf[0] = kreg_pair(src, 0, lutlo, luthi);
       bf[1] = kreg_pair(src, 4, lutlo, luthi);
       bf[2] = kreg_pair(src, 2, lutlo, luthi);
@@ -196,6 +202,183 @@ __device__ __forceinline__ void key_frags(const uint32_t *kw, const uint32_t *kw
   }
 }
 
+// Everything one warp needs to process 32-token half pages of one unit.
+struct HalfPageCtx {
+  const unsigned char *lut_k, *lut_v;
+  const uint4 *qfrag;        // [8 kb][32 lanes]: (q_hi(ch 2t..), q_lo(ch 2t..), q_hi(ch 2t+8..), q_lo(..))
+  const __half *qraw;        // [8][128] natural order
+  const __half *tail;        // this unit's fp16 trailing keys
+  const uint8_t *tmask;      // this session's 16-token tile masks
+  const uint8_t *mod;        // this session's modality ids
+  uint32_t laneoff, lutlo, luthi;
+  int T, Tf;
+};
+
+// One 32-token half page (two 16-token tiles) starting at page-relative token
+// 32*hp of the staged page sp. FULLV: all 32 tokens exist and are quantized.
+template <int BITS, int G, bool FULLV>
+__device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout &PL, const unsigned char *sp,
+                                          int tok0, int hp, float beta, uint32_t (&af)[8][4],
+                                          float (&acc)[MAXM][8][4], float &m_run, float &l_run) {
+  constexpr int LANE_WORDS = BITS * 2;
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int hs = tok0 + 32 * hp;
+  float sacc[4][4];                           // n-tiles (tile, nt); rows [hi | lo]
+  if (FULLV || hs < c.Tf) {
+    if ((32 * hp) % G == 0) {
+      // new group: a = q' o range as an exact fp16 pair (TwoProduct), fragments [a_hi ; a_lo]
+      const __half *rg = reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
+        const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int kb = 2 * k2 + u;
+          const uint4 q = c.qfrag[kb * 32 + lane];
+          const uint32_t qh[2] = {q.x, q.z}, ql[2] = {q.y, q.w};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const __half2 r2 = u2h(rr[2 * u + h]);
+            const __half2 hi = __hmul2(u2h(qh[h]), r2);
+            const __half2 er = __hfma2(u2h(qh[h]), r2, __hneg2(hi));
+            const __half2 lo = __hfma2(u2h(ql[h]), r2, er);
+            af[kb][2 * h] = h2u(hi);
+            af[kb][2 * h + 1] = h2u(lo);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      sacc[n][0] = beta; sacc[n][1] = beta; sacc[n][2] = 0.f; sacc[n][3] = 0.f;
+    }
+    uint32_t kw[2][LANE_WORDS];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int i = 0; i < LANE_WORDS; i += 4) {
+        const uint4 v4 =
+            *reinterpret_cast<const uint4 *>(sp + (2 * hp + t) * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
+        kw[t][i] = v4.x; kw[t][i + 1] = v4.y; kw[t][i + 2] = v4.z; kw[t][i + 3] = v4.w;
+      }
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t bf[4];
+        key_frags<BITS>(kw[t], kb, c.lutlo, c.luthi, c.lut_k, c.laneoff, bf);
+        mma16816(sacc[2 * t + 0], af[kb], bf[0], bf[1]);
+        mma16816(sacc[2 * t + 1], af[kb], bf[2], bf[3]);
+      }
+    }
+  } else {
+    // trailing keys of an incomplete group: exact fp16 keys, unrotated query
+    const int nt_valid = c.T - c.Tf;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const int c0 = 16 * kb + 2 * t4;
+      const uint32_t A[4] = {*reinterpret_cast<const uint32_t *>(c.qraw + g * D + c0), 0u,
+                             *reinterpret_cast<const uint32_t *>(c.qraw + g * D + c0 + 8), 0u};
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int row = hs - c.Tf + 8 * n + g;
+        const bool ok = row < nt_valid;
+        const uint32_t b0 = ok ? *reinterpret_cast<const uint32_t *>(c.tail + row * D + c0) : 0u;
+        const uint32_t b1 = ok ? *reinterpret_cast<const uint32_t *>(c.tail + row * D + c0 + 8) : 0u;
+        mma16816(sacc[n], A, b0, b1);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      sacc[n][0] *= LOG2E * INV_SQRT_D;
+      sacc[n][1] *= LOG2E * INV_SQRT_D;
+    }
+  }
+  // scores of head g for tokens hs + 8n + 2*t4 + e
+  float s[4][2];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float v = sacc[n][e] + sacc[n][2 + e];
+      s[n][e] = (FULLV || hs + 8 * n + 2 * t4 + e < c.T) ? v : -INFINITY;
+    }
+
+  // ---- online softmax (base 2) for head g ----
+  float mx = s[0][0];
+#pragma unroll
+  for (int n = 0; n < 4; ++n) mx = fmaxf(mx, fmaxf(s[n][0], s[n][1]));
+  mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  if (__any_sync(FULL, m_new > m_run)) {
+    const float sf = ex2(m_run - m_new);
+    const float sf0 = __shfl_sync(FULL, sf, 8 * t4), sf1 = __shfl_sync(FULL, sf, 8 * t4 + 4);
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[m][mt][0] *= sf0; acc[m][mt][2] *= sf0;
+        acc[m][mt][1] *= sf1; acc[m][mt][3] *= sf1;
+      }
+    l_run *= sf;
+    m_run = m_new;
+  }
+  float p[4][2];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      p[n][e] = ex2(s[n][e] - m_run);
+      l_run += p[n][e];
+    }
+
+  // ---- values, tile by tile ----
+  const __half *norms = reinterpret_cast<const __half *>(sp + PL.off_norm);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int tile = 2 * hp + t;
+    const int ts = tok0 + 16 * tile;
+    if (!FULLV && ts >= c.T) break;
+    const int r0 = 16 * tile + 2 * t4;        // page-relative tokens r0, r0+1, r0+8, r0+9
+    const float2 n01 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0));
+    const float2 n89 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0 + 8));
+    const bool v0 = FULLV || ts + 2 * t4 < c.T, v1 = FULLV || ts + 2 * t4 + 1 < c.T;
+    const bool v8 = FULLV || ts + 2 * t4 + 8 < c.T, v9 = FULLV || ts + 2 * t4 + 9 < c.T;
+    const float w0 = v0 ? p[2 * t][0] * n01.x : 0.f, w1 = v1 ? p[2 * t][1] * n01.y : 0.f;
+    const float w8 = v8 ? p[2 * t + 1][0] * n89.x : 0.f, w9 = v9 ? p[2 * t + 1][1] * n89.y : 0.f;
+    uint32_t vw[LANE_WORDS];
+#pragma unroll
+    for (int i = 0; i < LANE_WORDS; i += 4) {
+      const uint4 v4 =
+          *reinterpret_cast<const uint4 *>(sp + PL.off_v + tile * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
+      vw[i] = v4.x; vw[i + 1] = v4.y; vw[i + 2] = v4.z; vw[i + 3] = v4.w;
+    }
+    const uint32_t tmask = c.tmask[ts / TILE];
+    if (__popc(tmask) == 1) {
+      const uint32_t b0 = pack_h2(w0, w1), b1 = pack_h2(w8, w9);
+      const int m = __ffs(tmask) - 1;
+      if (m == 0) value_mma<BITS>(acc[0], vw, c.lut_v, c.laneoff, b0, b1);
+      else if (m == 1) value_mma<BITS>(acc[1], vw, c.lut_v, c.laneoff, b0, b1);
+      else value_mma<BITS>(acc[2], vw, c.lut_v, c.laneoff, b0, b1);
+    } else {
+      const uint8_t *modp = c.mod + ts + 2 * t4;
+      const int m0 = v0 ? modp[0] : -1, m1 = v1 ? modp[1] : -1;
+      const int m8 = v8 ? modp[8] : -1, m9 = v9 ? modp[9] : -1;
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m) {
+        if (!(tmask & (1u << m))) continue;
+        const uint32_t b0 = pack_h2(m0 == m ? w0 : 0.f, m1 == m ? w1 : 0.f);
+        const uint32_t b1 = pack_h2(m8 == m ? w8 : 0.f, m9 == m ? w9 : 0.f);
+        value_mma<BITS>(acc[m], vw, c.lut_v, c.laneoff, b0, b1);
+      }
+    }
+  }
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) {
   constexpr int STAGES = Cfg<BITS>::STAGES;
@@ -208,7 +391,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
   unsigned char *lut = smem;                                            // LUT_BYTES
   float *qr = reinterpret_cast<float *>(smem + LUT_BYTES);              // [8][128] stat order, scaled
   __half *qraw = reinterpret_cast<__half *>(qr + MAXGQ * D);            // [8][128] natural order
-  uint64_t *bars = reinterpret_cast<uint64_t *>(qraw + MAXGQ * D);      // [WARPS][STAGES]
+  uint4 *qfrag = reinterpret_cast<uint4 *>(qraw + MAXGQ * D);           // [8 kb][32 lanes]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(qfrag + 8 * 32);        // [WARPS][STAGES]
   unsigned char *stages = reinterpret_cast<unsigned char *>(bars + WARPS * STAGES);
   stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
   Merge &MG = *reinterpret_cast<Merge *>(stages);
@@ -299,18 +483,31 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     }
     __syncthreads();
 
-    // this lane's query fragments (head g, its 32 channels): fp16 high + residual
-    uint32_t qh[8][2], ql[8][2];
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {
+    // query fragments for the score and offset MMAs, one kb block per warp:
+    // lane (g, t4) gets head g, channels 16kb + 2t4 + {0,1} and + 8 + {0,1}, fp16 high + residual
+    {
+      const int kb = warp;
       const float4 v = *reinterpret_cast<const float4 *>(qr + g * D + 32 * (kb >> 1) + 8 * t4 + 4 * (kb & 1));
       const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
       const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-      qh[kb][0] = h2u(h01);
-      qh[kb][1] = h2u(h23);
-      ql[kb][0] = pack_h2(v.x - f01.x, v.y - f01.y);
-      ql[kb][1] = pack_h2(v.z - f23.x, v.w - f23.y);
+      qfrag[kb * 32 + lane] = make_uint4(h2u(h01), pack_h2(v.x - f01.x, v.y - f01.y), h2u(h23),
+                                         pack_h2(v.z - f23.x, v.w - f23.y));
     }
+    __syncthreads();
+
+    HalfPageCtx hc;
+    hc.lut_k = lut_k;
+    hc.lut_v = lut_v;
+    hc.qfrag = qfrag;
+    hc.qraw = qraw;
+    hc.tail = tail;
+    hc.tmask = a.tmask + (long long)session * (a.cap / TILE);
+    hc.mod = a.mod + (long long)session * a.cap;
+    hc.laneoff = laneoff;
+    hc.lutlo = lutlo;
+    hc.luthi = luthi;
+    hc.T = T;
+    hc.Tf = Tf;
 
     // ---- per-warp state ----
     float acc[MAXM][8][4];
@@ -365,7 +562,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
             b0 = v.x;
             b1 = v.y;
           }
-          const uint32_t A[4] = {qh[kb][0], ql[kb][0], qh[kb][1], ql[kb][1]};
+          const uint4 q = qfrag[kb * 32 + lane];
+          const uint32_t A[4] = {q.x, q.y, q.z, q.w};
           mma16816(d, A, b0, b1);
         }
         beta_g0 = __shfl_sync(FULL, d[0] + d[2], 4 * g);
@@ -374,165 +572,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
 
 #pragma unroll 1
       for (int hp = 0; hp < 2; ++hp) {
-        const int hs = tok0 + 32 * hp;             // half-page start
+        const int hs = tok0 + 32 * hp;
         if (hs >= T) break;
-        float sacc[4][4];                           // n-tiles (tile, nt); rows [hi | lo]
-        if (hs < Tf) {
-          if ((32 * hp) % G == 0) {
-            // new group: a = q' o range as an exact fp16 pair (TwoProduct), fragments [a_hi ; a_lo]
-            const __half *rg =
-                reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
-              const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int kb = 2 * k2 + u;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const __half2 r2 = u2h(rr[2 * u + h]);
-                  const __half2 hi = __hmul2(u2h(qh[kb][h]), r2);
-                  const __half2 er = __hfma2(u2h(qh[kb][h]), r2, __hneg2(hi));
-                  const __half2 lo = __hfma2(u2h(ql[kb][h]), r2, er);
-                  af[kb][2 * h] = h2u(hi);
-                  af[kb][2 * h + 1] = h2u(lo);
-                }
-              }
-            }
-          }
-          const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            sacc[n][0] = beta; sacc[n][1] = beta; sacc[n][2] = 0.f; sacc[n][3] = 0.f;
-          }
-          uint32_t kw[2][LANE_WORDS], kwh[2][LANE_WORDS];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-#pragma unroll
-            for (int i = 0; i < LANE_WORDS; i += 4) {
-              const uint4 v4 = *reinterpret_cast<const uint4 *>(sp + (2 * hp + t) * PL.tile_bytes +
-                                                                lane * PL.lane_bytes + 4 * i);
-              kw[t][i] = v4.x; kw[t][i + 1] = v4.y; kw[t][i + 2] = v4.z; kw[t][i + 3] = v4.w;
-            }
-#pragma unroll
-            for (int i = 0; i < LANE_WORDS; ++i) kwh[t][i] = BITS == 2 ? __byte_perm(kw[t][i], 0u, 0x4432u) : 0u;
-          }
-#pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              uint32_t bf[4];
-              key_frags<BITS>(kw[t], kwh[t], kb, lutlo, luthi, lut_k, laneoff, bf);
-              mma16816(sacc[2 * t + 0], af[kb], bf[0], bf[1]);
-              mma16816(sacc[2 * t + 1], af[kb], bf[2], bf[3]);
-            }
-          }
-        } else {
-          // trailing keys of an incomplete group: exact fp16 keys, unrotated query
-          const int nt_valid = T - Tf;
-#pragma unroll
-          for (int n = 0; n < 4; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-#pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-            const int c0 = 16 * kb + 2 * t4;
-            const uint32_t A[4] = {*reinterpret_cast<const uint32_t *>(qraw + g * D + c0), 0u,
-                                   *reinterpret_cast<const uint32_t *>(qraw + g * D + c0 + 8), 0u};
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-              const int row = hs - Tf + 8 * n + g;
-              const bool ok = row < nt_valid;
-              const uint32_t b0 = ok ? *reinterpret_cast<const uint32_t *>(tail + row * D + c0) : 0u;
-              const uint32_t b1 = ok ? *reinterpret_cast<const uint32_t *>(tail + row * D + c0 + 8) : 0u;
-              mma16816(sacc[n], A, b0, b1);
-            }
-          }
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            sacc[n][0] *= LOG2E * INV_SQRT_D;
-            sacc[n][1] *= LOG2E * INV_SQRT_D;
-          }
-        }
-        // scores of head g for tokens hs + 8n + 2*t4 + e
-        float s[4][2];
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tk = hs + 8 * n + 2 * t4 + e;
-            s[n][e] = tk < T ? sacc[n][e] + sacc[n][2 + e] : -INFINITY;
-          }
-
-        // ---- online softmax (base 2) for head g ----
-        float mx = s[0][0];
-#pragma unroll
-        for (int n = 0; n < 4; ++n) mx = fmaxf(mx, fmaxf(s[n][0], s[n][1]));
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        if (__any_sync(FULL, m_new > m_run)) {
-          const float sf = ex2(m_run - m_new);
-          const float sf0 = __shfl_sync(FULL, sf, 8 * t4), sf1 = __shfl_sync(FULL, sf, 8 * t4 + 4);
-#pragma unroll
-          for (int m = 0; m < MAXM; ++m)
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              acc[m][mt][0] *= sf0; acc[m][mt][2] *= sf0;
-              acc[m][mt][1] *= sf1; acc[m][mt][3] *= sf1;
-            }
-          l_run *= sf;
-          m_run = m_new;
-        }
-        float p[4][2];
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            p[n][e] = ex2(s[n][e] - m_run);
-            l_run += p[n][e];
-          }
-
-        // ---- values, tile by tile ----
-        const __half *norms = reinterpret_cast<const __half *>(sp + PL.off_norm);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int tile = 2 * hp + t;
-          const int ts = tok0 + 16 * tile;
-          if (ts >= T) break;
-          const int r0 = 16 * tile + 2 * t4;        // page-relative tokens r0, r0+1, r0+8, r0+9
-          const float2 n01 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0));
-          const float2 n89 = __half22float2(*reinterpret_cast<const __half2 *>(norms + r0 + 8));
-          const bool v0 = ts + 2 * t4 < T, v1 = ts + 2 * t4 + 1 < T, v8 = ts + 2 * t4 + 8 < T,
-                     v9 = ts + 2 * t4 + 9 < T;
-          const float w0 = v0 ? p[2 * t][0] * n01.x : 0.f, w1 = v1 ? p[2 * t][1] * n01.y : 0.f;
-          const float w8 = v8 ? p[2 * t + 1][0] * n89.x : 0.f, w9 = v9 ? p[2 * t + 1][1] * n89.y : 0.f;
-          uint32_t vw[LANE_WORDS];
-#pragma unroll
-          for (int i = 0; i < LANE_WORDS; i += 4) {
-            const uint4 v4 = *reinterpret_cast<const uint4 *>(sp + PL.off_v + tile * PL.tile_bytes +
-                                                              lane * PL.lane_bytes + 4 * i);
-            vw[i] = v4.x; vw[i + 1] = v4.y; vw[i + 2] = v4.z; vw[i + 3] = v4.w;
-          }
-          const uint32_t tmask = a.tmask[(long long)session * (a.cap / TILE) + ts / TILE];
-          if (__popc(tmask) == 1) {
-            const uint32_t b0 = pack_h2(w0, w1), b1 = pack_h2(w8, w9);
-            const int m = __ffs(tmask) - 1;
-            if (m == 0) value_mma<BITS>(acc[0], vw, lut_v, laneoff, b0, b1);
-            else if (m == 1) value_mma<BITS>(acc[1], vw, lut_v, laneoff, b0, b1);
-            else value_mma<BITS>(acc[2], vw, lut_v, laneoff, b0, b1);
-          } else {
-            const uint8_t *modp = a.mod + (long long)session * a.cap + ts + 2 * t4;
-            const int m0 = v0 ? modp[0] : -1, m1 = v1 ? modp[1] : -1;
-            const int m8 = v8 ? modp[8] : -1, m9 = v9 ? modp[9] : -1;
-#pragma unroll
-            for (int m = 0; m < MAXM; ++m) {
-              if (!(tmask & (1u << m))) continue;
-              const uint32_t b0 = pack_h2(m0 == m ? w0 : 0.f, m1 == m ? w1 : 0.f);
-              const uint32_t b1 = pack_h2(m8 == m ? w8 : 0.f, m9 == m ? w9 : 0.f);
-              value_mma<BITS>(acc[m], vw, lut_v, laneoff, b0, b1);
-            }
-          }
-        }
+        const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
+        if (hs + 32 <= Tf)
+          half_page<BITS, G, true>(hc, PL, sp, tok0, hp, beta, af, acc, m_run, l_run);
+        else
+          half_page<BITS, G, false>(hc, PL, sp, tok0, hp, beta, af, acc, m_run, l_run);
       }
       __syncwarp();
       // refill this stage with the page STAGES ahead
@@ -675,7 +721,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 size_t decode_smem_bytes(int bits, int G) {
   const PageLayout PL = page_layout(bits, G);
   const int stages = bits == 2 ? Cfg<2>::STAGES : Cfg<4>::STAGES;
-  size_t head = LUT_BYTES + MAXGQ * D * 4 + MAXGQ * D * 2 + WARPS * stages * 8;
+  size_t head = LUT_BYTES + MAXGQ * D * 4 + MAXGQ * D * 2 + 8 * 32 * 16 + WARPS * stages * 8;
   size_t ring = (size_t)WARPS * stages * PL.page_bytes;
   if (ring < sizeof(Merge)) ring = sizeof(Merge);
   return head + 128 + ring;
