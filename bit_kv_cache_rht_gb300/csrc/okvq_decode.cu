@@ -379,6 +379,61 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   }
 }
 
+// The last CTA to finish a unit merges the unit's partials (log-sum-exp over
+// segments) and applies the inverse value rotations:
+//   O[h] = (sum_m R_m^T o_m[h]) / (l[h] sqrt d), fp16 store.
+// scratch: shared memory free at this point (>= 12 KB + 96 KB).
+__device__ void combine_unit(const DecodeArgs &a, int unit, float *scratch) {
+  const int tid = threadIdx.x;
+  const int gq = a.Hq / a.Hkv;
+  const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
+  float *osh = scratch;                              // [MAXGQ][MAXM * D]
+  float *Lsh = osh + MAXGQ * MAXM * D;               // [MAXGQ]
+  float *Msh = Lsh + MAXGQ;                          // [MAXGQ]
+  float *Rs = Msh + MAXGQ;                           // [MAXM * D rows][64]
+  if (tid < MAXGQ) {
+    float M = -INFINITY, L = 0.f;
+    for (int s = s0; s < s1; ++s) M = fmaxf(M, a.partials[((long long)s * MAXGQ + tid) * PARTIAL_FLOATS]);
+    for (int s = s0; s < s1; ++s) {
+      const float *p = a.partials + ((long long)s * MAXGQ + tid) * PARTIAL_FLOATS;
+      if (p[0] != -INFINITY) L += ex2(p[0] - M) * p[1];
+    }
+    Msh[tid] = M;
+    Lsh[tid] = L;
+  }
+  __syncthreads();
+  for (int i = tid; i < gq * a.M * D; i += THREADS) {
+    const int hh = i / (a.M * D), rest = i % (a.M * D);
+    float o = 0.f;
+    for (int s = s0; s < s1; ++s) {
+      const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
+      if (p[0] != -INFINITY) o += ex2(p[0] - Msh[hh]) * p[2 + rest];
+    }
+    osh[hh * MAXM * D + rest] = o;
+  }
+  const int lh = unit % (a.L * a.Hkv);
+  const int session = unit / (a.L * a.Hkv);
+  const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
+  const float *R = a.rot + (long long)lh * a.M * D * D;
+  for (int cb = 0; cb < D; cb += 64) {
+    __syncthreads();
+    for (int i = tid; i < a.M * D * 16; i += THREADS) {
+      const int row = i >> 4, q = i & 15;
+      reinterpret_cast<float4 *>(Rs)[row * 16 + q] = *reinterpret_cast<const float4 *>(R + (long long)row * D + cb + 4 * q);
+    }
+    __syncthreads();
+    for (int i = tid; i < gq * 64; i += THREADS) {
+      const int hh = i >> 6, cc = i & 63;
+      float acc = 0.f;
+      for (int r = 0; r < a.M * D; ++r) acc = fmaf(Rs[r * 64 + cc], osh[hh * MAXM * D + r], acc);
+      const float L = Lsh[hh];
+      const float y = L > 0.f ? acc / (L * 11.3137084989847603904f) : 0.f;
+      a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb + cc] = __float2half_rn(y);
+    }
+  }
+  __syncthreads();
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) {
   constexpr int STAGES = Cfg<BITS>::STAGES;
@@ -639,66 +694,22 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
         ph[2 + m * D + ch] = o;
       }
     }
+    // the last segment of a unit to finish combines the unit (no waiting: a ticket)
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_last;
+    if (tid == 0) {
+      const int nsu = a.unit_seg[unit + 1] - a.unit_seg[unit];
+      const int prev = atomicAdd(&a.unit_done[unit], 1);
+      s_last = prev + 1 == nsu;
+      if (s_last) a.unit_done[unit] = 0;      // ready for the next launch
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      combine_unit(a, unit, reinterpret_cast<float *>(stages));
+    }
     __syncthreads();              // merge area is the stage ring of the next segment
-  }
-}
-
-// One CTA per (unit, 32 output channels): merge the unit's partials by
-// log-sum-exp, then O = (sum_m R_m^T o_m) / (l sqrt d) with the R block staged in
-// shared memory.
-constexpr int CB_CH = 32;
-constexpr int CB_MAXSEG = 64;
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
-  extern __shared__ __align__(16) float csm[];
-  float *Rs = csm;                                   // [M * D rows][CB_CH]
-  float *osh = Rs + MAXM * D * CB_CH;                // [MAXGQ][M * D]
-  float *wsh = osh + MAXGQ * MAXM * D;               // [MAXGQ][CB_MAXSEG] segment weights
-  __shared__ float Msh[MAXGQ], Lsh[MAXGQ];
-  const int unit = blockIdx.x, cb = blockIdx.y;
-  const int tid = threadIdx.x;
-  const int gq = a.Hq / a.Hkv;
-  const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
-  const int lh = unit % (a.L * a.Hkv);
-  const float *R = a.rot + (long long)lh * a.M * D * D;
-  for (int i = tid; i < a.M * D * (CB_CH / 4); i += blockDim.x) {
-    const int row = i / (CB_CH / 4), q = i % (CB_CH / 4);
-    reinterpret_cast<float4 *>(Rs)[row * (CB_CH / 4) + q] =
-        *reinterpret_cast<const float4 *>(R + (long long)row * D + cb * CB_CH + 4 * q);
-  }
-  if (tid < MAXGQ) {
-    float M = -INFINITY, L = 0.f;
-    for (int s = s0; s < s1; ++s) M = fmaxf(M, a.partials[((long long)s * MAXGQ + tid) * PARTIAL_FLOATS]);
-    for (int s = s0; s < s1; ++s) {
-      const float *p = a.partials + ((long long)s * MAXGQ + tid) * PARTIAL_FLOATS;
-      const float w = p[0] == -INFINITY ? 0.f : ex2(p[0] - M);
-      if (s - s0 < CB_MAXSEG) wsh[tid * CB_MAXSEG + (s - s0)] = w;
-      L += w * p[1];
-    }
-    Msh[tid] = M;
-    Lsh[tid] = L;
-  }
-  __syncthreads();
-  for (int i = tid; i < gq * a.M * D; i += blockDim.x) {
-    const int hh = i / (a.M * D), rest = i % (a.M * D);
-    float o = 0.f;
-    for (int s = s0; s < s1; ++s) {
-      const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
-      const float w = s - s0 < CB_MAXSEG ? wsh[hh * CB_MAXSEG + (s - s0)]
-                                         : (p[0] == -INFINITY ? 0.f : ex2(p[0] - Msh[hh]));
-      o += w * p[2 + rest];
-    }
-    osh[hh * MAXM * D + rest] = o;
-  }
-  __syncthreads();
-  const int session = unit / (a.L * a.Hkv);
-  const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-  for (int i = tid; i < gq * CB_CH; i += blockDim.x) {
-    const int hh = i / CB_CH, cc = i % CB_CH;
-    float acc = 0.f;
-    for (int r = 0; r < a.M * D; ++r) acc = fmaf(Rs[r * CB_CH + cc], osh[hh * MAXM * D + r], acc);
-    const float L = Lsh[hh];
-    const float y = L > 0.f ? acc / (L * 11.3137084989847603904f) : 0.f;
-    a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb * CB_CH + cc] = __float2half_rn(y);
   }
 }
 
@@ -733,20 +744,6 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
   if (a.bits == 2 && a.G == 64) return launch_decode_t<2, 64>(a, n_cta, s);
   if (a.bits == 4 && a.G == 32) return launch_decode_t<4, 32>(a, n_cta, s);
   return launch_decode_t<4, 64>(a, n_cta, s);
-}
-
-cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
-  if (a.units <= 0) return cudaSuccess;
-  static bool attr_done = false;
-  const size_t smem = (MAXM * D * CB_CH + MAXGQ * MAXM * D + MAXGQ * CB_MAXSEG) * sizeof(float);
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  dim3 grid((unsigned)a.units, D / CB_CH);
-  combine_kernel<<<grid, 256, smem, s>>>(a);
-  return cudaGetLastError();
 }
 
 }  // namespace okvq
