@@ -27,7 +27,6 @@ struct okvq_cache {
   float *signs = nullptr;       // [D]
   uint32_t *err = nullptr;
   float *partials = nullptr;
-  int *unit_done = nullptr;     // [units] per-launch segment tickets
   int *table = nullptr;         // device work table
   size_t table_bytes = 0;
   long long max_segs = 0;
@@ -122,7 +121,6 @@ void release(okvq_cache *h) {
   cudaFree(h->signs);
   cudaFree(h->err);
   cudaFree(h->partials);
-  cudaFree(h->unit_done);
   cudaFree(h->table);
   if (h->host_table) cudaFreeHost(h->host_table);
   if (h->table_ev) cudaEventDestroy(h->table_ev);
@@ -285,7 +283,6 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
-  if ((st = alloc_dev((void **)&h->unit_done, (size_t)h->units * sizeof(int))) != OKVQ_OK) return fail(st);
   // work table: segs [max_segs][4] int | cta_seg [max_cta+1] | unit_seg [units+1] | unit_len [units] i64 | unit_tail
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -309,7 +306,6 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if (cudaMemsetAsync(h->mod, 0, (size_t)h->S * h->cap, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->tmask, 0, (size_t)h->S * (h->cap / TILE), s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) return fail(OKVQ_ECUDA);
-  if (cudaMemsetAsync(h->unit_done, 0, (size_t)h->units * sizeof(int), s) != cudaSuccess) return fail(OKVQ_ECUDA);
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
     std::vector<float> rt(nmat * D * D);
@@ -430,10 +426,16 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
     a.klut_src[j] = h->klev16[j];
     a.vlut_src[j] = h->levels16[j];
   }
-  a.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
-  a.unit_done = h->unit_done;
-  a.rot = h->rot;
-  a.out = static_cast<__half *>(out);
+  CombineArgs cb{};
+  cb.partials = h->partials;
+  cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
+  cb.rot = h->rot;
+  cb.out = static_cast<__half *>(out);
+  cb.L = h->L;
+  cb.Hq = h->Hq;
+  cb.Hkv = h->Hkv;
+  cb.M = h->M;
+  cb.units = h->units;
   cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
   if (h->prof) {
     const size_t need = 3 * (size_t)(h->prof_calls + 1);
@@ -445,14 +447,11 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
     e0 = h->ev[3 * h->prof_calls];
     e1 = h->ev[3 * h->prof_calls + 1];
     e2 = h->ev[3 * h->prof_calls + 2];
+    OKVQ_TRY(cudaEventRecord(e0, s));
   }
-  // sessions without tokens have no segments: their output is zero
-  const size_t sess_out = (size_t)h->L * h->Hq * D * sizeof(__half);
-  for (int ss = 0; ss < h->S; ++ss)
-    if (h->len[ss] == 0) OKVQ_TRY(cudaMemsetAsync(static_cast<char *>(out) + ss * sess_out, 0, sess_out, s));
-  if (h->prof) OKVQ_TRY(cudaEventRecord(e0, s));
   OKVQ_TRY(launch_decode(a, h->ncta, s));
   if (h->prof) OKVQ_TRY(cudaEventRecord(e1, s));
+  OKVQ_TRY(launch_combine(cb, s));
   if (h->prof) {
     OKVQ_TRY(cudaEventRecord(e2, s));
     ++h->prof_calls;

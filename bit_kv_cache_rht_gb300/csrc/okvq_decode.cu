@@ -379,61 +379,6 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   }
 }
 
-// The last CTA to finish a unit merges the unit's partials (log-sum-exp over
-// segments) and applies the inverse value rotations:
-//   O[h] = (sum_m R_m^T o_m[h]) / (l[h] sqrt d), fp16 store.
-// scratch: shared memory free at this point (>= 12 KB + 96 KB).
-__device__ void combine_unit(const DecodeArgs &a, int unit, float *scratch) {
-  const int tid = threadIdx.x;
-  const int gq = a.Hq / a.Hkv;
-  const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
-  float *osh = scratch;                              // [MAXGQ][MAXM * D]
-  float *Lsh = osh + MAXGQ * MAXM * D;               // [MAXGQ]
-  float *Msh = Lsh + MAXGQ;                          // [MAXGQ]
-  float *Rs = Msh + MAXGQ;                           // [MAXM * D rows][64]
-  if (tid < MAXGQ) {
-    float M = -INFINITY, L = 0.f;
-    for (int s = s0; s < s1; ++s) M = fmaxf(M, a.partials[((long long)s * MAXGQ + tid) * PARTIAL_FLOATS]);
-    for (int s = s0; s < s1; ++s) {
-      const float *p = a.partials + ((long long)s * MAXGQ + tid) * PARTIAL_FLOATS;
-      if (p[0] != -INFINITY) L += ex2(p[0] - M) * p[1];
-    }
-    Msh[tid] = M;
-    Lsh[tid] = L;
-  }
-  __syncthreads();
-  for (int i = tid; i < gq * a.M * D; i += THREADS) {
-    const int hh = i / (a.M * D), rest = i % (a.M * D);
-    float o = 0.f;
-    for (int s = s0; s < s1; ++s) {
-      const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
-      if (p[0] != -INFINITY) o += ex2(p[0] - Msh[hh]) * p[2 + rest];
-    }
-    osh[hh * MAXM * D + rest] = o;
-  }
-  const int lh = unit % (a.L * a.Hkv);
-  const int session = unit / (a.L * a.Hkv);
-  const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-  const float *R = a.rot + (long long)lh * a.M * D * D;
-  for (int cb = 0; cb < D; cb += 64) {
-    __syncthreads();
-    for (int i = tid; i < a.M * D * 16; i += THREADS) {
-      const int row = i >> 4, q = i & 15;
-      reinterpret_cast<float4 *>(Rs)[row * 16 + q] = *reinterpret_cast<const float4 *>(R + (long long)row * D + cb + 4 * q);
-    }
-    __syncthreads();
-    for (int i = tid; i < gq * 64; i += THREADS) {
-      const int hh = i >> 6, cc = i & 63;
-      float acc = 0.f;
-      for (int r = 0; r < a.M * D; ++r) acc = fmaf(Rs[r * 64 + cc], osh[hh * MAXM * D + r], acc);
-      const float L = Lsh[hh];
-      const float y = L > 0.f ? acc / (L * 11.3137084989847603904f) : 0.f;
-      a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb + cc] = __float2half_rn(y);
-    }
-  }
-  __syncthreads();
-}
-
 template <int BITS, int G>
 __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) {
   constexpr int STAGES = Cfg<BITS>::STAGES;
@@ -477,6 +422,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
   if (lane == 0)
     for (int s = 0; s < STAGES; ++s) mbar_init(&my_bars[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  // the merge kernel may be scheduled as SMs free up; it waits for this grid's memory
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
 
   const unsigned char *lut_k = lut, *lut_v = lut + 128;
@@ -694,22 +641,79 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
         ph[2 + m * D + ch] = o;
       }
     }
-    // the last segment of a unit to finish combines the unit (no waiting: a ticket)
-    __threadfence();
-    __syncthreads();
-    __shared__ int s_last;
-    if (tid == 0) {
-      const int nsu = a.unit_seg[unit + 1] - a.unit_seg[unit];
-      const int prev = atomicAdd(&a.unit_done[unit], 1);
-      s_last = prev + 1 == nsu;
-      if (s_last) a.unit_done[unit] = 0;      // ready for the next launch
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      combine_unit(a, unit, reinterpret_cast<float *>(stages));
-    }
     __syncthreads();              // merge area is the stage ring of the next segment
+  }
+}
+
+// One CTA per (unit, 32 output channels), warp w = query head w: merge the
+// unit's partials by log-sum-exp, then O = (sum_m R_m^T o_m) / (l sqrt d) with
+// the R block staged in shared memory. Every global load is issued in bulk
+// (R and the partials are L2/HBM-latency bound, the arithmetic is tiny).
+constexpr int CB_CH = 32;
+__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  extern __shared__ __align__(16) float csm[];
+  float *Rs = csm;                                   // [M * D rows][CB_CH]
+  float *osh = Rs + MAXM * D * CB_CH;                // [MAXGQ][M * D]
+  __shared__ float Lsh[MAXGQ];
+  const int unit = blockIdx.x, cb = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, hh = tid >> 5;
+  const int gq = a.Hq / a.Hkv;
+  const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
+  const int lh = unit % (a.L * a.Hkv);
+  const float *R = a.rot + (long long)lh * a.M * D * D;
+  constexpr int RPER = MAXM * D * (CB_CH / 4) / 256;
+  const int rtotal = a.M * D * (CB_CH / 4);
+  float4 rt[RPER];
+#pragma unroll
+  for (int k = 0; k < RPER; ++k) {
+    const int i = tid + 256 * k;
+    if (i < rtotal) rt[k] = *reinterpret_cast<const float4 *>(R + (long long)(i >> 3) * D + cb * CB_CH + 4 * (i & 7));
+  }
+  // everything above only reads the rotations; the partials come from the decode grid
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int OPER = MAXM * D / 32;
+  float o[OPER];
+#pragma unroll
+  for (int k = 0; k < OPER; ++k) o[k] = 0.f;
+  float L = 0.f;
+  if (hh < gq) {
+    // head hh: reference max over the unit's segments (lanes take segments)
+    float M = -INFINITY;
+    for (int s = s0 + lane; s < s1; s += 32) M = fmaxf(M, a.partials[((long long)s * MAXGQ + hh) * PARTIAL_FLOATS]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int s = s0; s < s1; ++s) {
+      const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
+      const float m = p[0];
+      const float w = m == -INFINITY ? 0.f : ex2(m - M);
+      L = fmaf(w, p[1], L);
+#pragma unroll
+      for (int k = 0; k < OPER; ++k)
+        if (32 * k < a.M * D) o[k] = fmaf(w, p[2 + lane + 32 * k], o[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < RPER; ++k) {
+    const int i = tid + 256 * k;
+    if (i < rtotal) reinterpret_cast<float4 *>(Rs)[i] = rt[k];
+  }
+  if (hh < gq) {
+#pragma unroll
+    for (int k = 0; k < OPER; ++k)
+      if (32 * k < a.M * D) osh[hh * MAXM * D + lane + 32 * k] = o[k];
+    if (lane == 0) Lsh[hh] = L;
+  }
+  __syncthreads();
+  if (hh < gq) {
+    float acc = 0.f;
+    const float *oh = osh + hh * MAXM * D;
+#pragma unroll 8
+    for (int r = 0; r < a.M * D; ++r) acc = fmaf(Rs[r * CB_CH + lane], oh[r], acc);
+    const float Lh = Lsh[hh];
+    const float y = Lh > 0.f ? acc / (Lh * 11.3137084989847603904f) : 0.f;
+    const int session = unit / (a.L * a.Hkv);
+    const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
+    a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb * CB_CH + lane] = __float2half_rn(y);
   }
 }
 
@@ -744,6 +748,31 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
   if (a.bits == 2 && a.G == 64) return launch_decode_t<2, 64>(a, n_cta, s);
   if (a.bits == 4 && a.G == 32) return launch_decode_t<4, 32>(a, n_cta, s);
   return launch_decode_t<4, 64>(a, n_cta, s);
+}
+
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
+  if (a.units <= 0) return cudaSuccess;
+  static bool attr_done = false;
+  const size_t smem = (MAXM * D * CB_CH + MAXGQ * MAXM * D) * sizeof(float);
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // same shared/L1 split as the decode kernel: no reconfiguration between the two
+    e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.units, D / CB_CH);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace okvq

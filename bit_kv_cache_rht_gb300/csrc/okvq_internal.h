@@ -160,23 +160,30 @@ struct DecodeArgs {
   const long long *unit_len;// [units] token count
   const int *unit_tail;     // [units] 0/1 current tail buffer
   float *partials;          // [nseg][MAXGQ][2 + MAXM*D]
-  const int *unit_seg;      // [units+1] first segment of each unit
-  int *unit_done;           // [units] segments finished in this launch (reset by the combining CTA)
-  const float *rot;         // [L][Hkv][M][D][D] R[j][i]
-  __half *out;              // [S][L][Hq][D]
   int L, Hq, Hkv, M, bits, G;
   long long P_max, cap;
   long long units;
+  uint64_t unused;
   const float *signs;       // [D] +-1
   uint32_t *err;
   __half klut_src[16];      // key levels lambda_j (fp16)
   __half vlut_src[16];      // value levels l_j (fp16)
 };
 
+struct CombineArgs {
+  const float *partials;
+  const int *unit_seg;      // [units+1]
+  const float *rot;         // [L][Hkv][M][D][D] R[j][i]
+  __half *out;              // [S][L][Hq][D]
+  int L, Hq, Hkv, M;
+  long long units;
+};
+
 constexpr int PARTIAL_FLOATS = 2 + MAXM * D;   // m, l, o[M][D]
 
 cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 size_t decode_smem_bytes(int bits, int G);
 
 }  // namespace okvq

@@ -111,11 +111,10 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
 /* One decode step for every session and layer (section 1, Implementation):
  *   q    device fp16 [num_sessions][num_layers][num_q_heads][128]
  *   out  device fp16 [num_sessions][num_layers][num_q_heads][128]
- * An empty session yields zeros. One kernel launch (split-K fused attention;
- * the last CTA to finish a (session, layer, kv head) merges its partials and
- * applies the inverse value rotations), plus a memset per empty session,
- * asynchronous on `stream`; the work list is re-uploaded on `stream` after
- * appends changed the lengths. */
+ * An empty session yields zeros. Two kernel launches (split-K fused
+ * attention, then the merge + inverse value rotations), asynchronous on
+ * `stream`; the work list is re-uploaded on `stream` after appends changed
+ * the lengths. */
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
 
 /* Number of tokens held by `session`. */
@@ -142,12 +141,11 @@ okvq_status okvq_codebook(const okvq_cache *h, float *levels, float *key_levels)
  * 1 = bad modality id, 2 = a bounded wait gave up). */
 okvq_status okvq_check_errors(okvq_cache *h, void *stream, uint32_t *word);
 
-/* Kernel timing with CUDA events recorded around the decode kernel of each
- * okvq_decode call on its stream. enable != 0 clears and starts the record.
+/* Per-kernel timing with CUDA events recorded around each launch of
+ * okvq_decode on its stream. enable != 0 clears and starts the record.
  * okvq_profile_read synchronizes, then returns the number of decode calls
- * recorded (at most `cap`), the decode kernel time of each in milliseconds
- * (split_ms, merge included) and merge_ms = 0 (the merge runs inside the
- * decode kernel); either array may be NULL. */
+ * recorded (at most `cap`) and their split-K kernel and merge kernel times
+ * in milliseconds. */
 okvq_status okvq_profile_enable(okvq_cache *h, int enable);
 okvq_status okvq_profile_read(okvq_cache *h, float *split_ms, float *merge_ms, int32_t cap, int32_t *count);
 
