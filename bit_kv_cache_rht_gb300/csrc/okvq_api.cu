@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -128,6 +129,33 @@ void release(okvq_cache *h) {
   delete h;
 }
 
+// Split-K partials of okvq_decode_static_scratch: one fixed array per device,
+// shared by every call of that entry point (no allocation at call time).
+constexpr size_t STATIC_SEG_FLOATS = (size_t)MAXGQ * PARTIAL_FLOATS;
+static __device__ __align__(256) float g_static_partials[(size_t)OKVQ_STATIC_SCRATCH_SEGMENTS * STATIC_SEG_FLOATS];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_static_mu;
+float *g_static_addr[MAX_DEVICES] = {};   // device address of g_static_partials, per device
+
+// Look up (once per device, with that device current) the address of the static partials array.
+okvq_status static_partials(int device, float **out) {
+  if (device < 0 || device >= MAX_DEVICES) return OKVQ_EINVAL;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[device]) {
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return OKVQ_ECUDA;
+    if (cur != device && cudaSetDevice(device) != cudaSuccess) return OKVQ_ECUDA;
+    void *addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_static_partials);
+    if (cur != device && cudaSetDevice(cur) != cudaSuccess) return OKVQ_ECUDA;
+    if (e != cudaSuccess || !addr) return OKVQ_ECUDA;
+    g_static_addr[device] = static_cast<float *>(addr);
+  }
+  *out = g_static_addr[device];
+  return OKVQ_OK;
+}
+
 // Build the decode work partition: balanced page ranges over the flattened
 // (unit, page) list, cut at unit boundaries into segments.
 void build_table(okvq_cache *h) {
@@ -195,6 +223,7 @@ const char *okvq_status_string(okvq_status s) {
     case OKVQ_ECAPACITY: return "capacity exceeded";
     case OKVQ_ECUDA: return "CUDA error";
     case OKVQ_ESTATE: return "device error word set";
+    case OKVQ_ESCRATCH: return "decode work list exceeds the static scratch array";
   }
   return "unknown status";
 }
@@ -456,6 +485,64 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
     OKVQ_TRY(cudaEventRecord(e2, s));
     ++h->prof_calls;
   }
+  return OKVQ_OK;
+}
+
+okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream) {
+  if (!h || !q || !out) return OKVQ_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *scratch = nullptr;
+  okvq_status st = static_partials(h->device, &scratch);
+  if (st != OKVQ_OK) return st;
+  if (h->dirty) {
+    if (h->table_ev_pending) OKVQ_TRY(cudaEventSynchronize(h->table_ev));   // staging buffer free again
+    build_table(h);
+    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table, h->table_bytes, cudaMemcpyHostToDevice, s));
+    OKVQ_TRY(cudaEventRecord(h->table_ev, s));
+    h->table_ev_pending = true;
+    h->dirty = false;
+  }
+  if (h->nseg > OKVQ_STATIC_SCRATCH_SEGMENTS) return OKVQ_ESCRATCH;
+  // the same launches as okvq_decode, with the partials in the static array
+  const char *tb = reinterpret_cast<const char *>(h->table);
+  DecodeArgs a{};
+  a.q = static_cast<const __half *>(q);
+  a.pages = h->pages;
+  a.tails = h->tails;
+  a.mod = h->mod;
+  a.tmask = h->tmask;
+  a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
+  a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
+  a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);
+  a.unit_tail = reinterpret_cast<const int *>(tb + h->off_utail);
+  a.partials = scratch;
+  a.L = h->L;
+  a.Hq = h->Hq;
+  a.Hkv = h->Hkv;
+  a.M = h->M;
+  a.bits = h->bits;
+  a.G = h->G;
+  a.P_max = h->P_max;
+  a.cap = h->cap;
+  a.units = h->units;
+  a.signs = h->signs;
+  a.err = h->err;
+  for (int j = 0; j < 16; ++j) {
+    a.klut_src[j] = h->klev16[j];
+    a.vlut_src[j] = h->levels16[j];
+  }
+  CombineArgs cb{};
+  cb.partials = scratch;
+  cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
+  cb.rot = h->rot;
+  cb.out = static_cast<__half *>(out);
+  cb.L = h->L;
+  cb.Hq = h->Hq;
+  cb.Hkv = h->Hkv;
+  cb.M = h->M;
+  cb.units = h->units;
+  OKVQ_TRY(launch_decode(a, h->ncta, s));
+  OKVQ_TRY(launch_combine(cb, s));
   return OKVQ_OK;
 }
 

@@ -16,12 +16,14 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libokvq.so")
 
-OKVQ_OK, OKVQ_EINVAL, OKVQ_ENOMEM, OKVQ_ECAPACITY, OKVQ_ECUDA, OKVQ_ESTATE = range(6)
+OKVQ_OK, OKVQ_EINVAL, OKVQ_ENOMEM, OKVQ_ECAPACITY, OKVQ_ECUDA, OKVQ_ESTATE, OKVQ_ESCRATCH = range(7)
+OKVQ_STATIC_SCRATCH_SEGMENTS = 512   # work-list segments held by okvq_decode_static_scratch's array
 
 # every function the header declares (checked against include/okvq.h by the tests)
 EXPORTS = (
     "okvq_create", "okvq_free", "okvq_append_chunk", "okvq_decode", "okvq_length", "okvq_export_state",
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
+    "okvq_decode_static_scratch",
 )
 
 
@@ -65,6 +67,7 @@ def load() -> ctypes.CDLL:
     L.okvq_free.restype = None
     L.okvq_append_chunk.argtypes = [vp, i32, vp, vp, vp, i32, vp]
     L.okvq_decode.argtypes = [vp, vp, vp, vp]
+    L.okvq_decode_static_scratch.argtypes = [vp, vp, vp, vp]
     L.okvq_length.argtypes = [vp, i32, ctypes.POINTER(i64)]
     L.okvq_export_state.argtypes = [vp, i32, vp, ctypes.POINTER(ctypes.c_size_t)]
     L.okvq_codebook.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
@@ -109,6 +112,11 @@ def okvq_append_chunk(h, session: int, k_ptr: int, v_ptr: int, mod_ptr: int, num
 
 def okvq_decode(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
     return load().okvq_decode(h, ctypes.c_void_p(q_ptr), ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream))
+
+
+def okvq_decode_static_scratch(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
+    return load().okvq_decode_static_scratch(h, ctypes.c_void_p(q_ptr), ctypes.c_void_p(out_ptr),
+                                             ctypes.c_void_p(stream))
 
 
 def okvq_length(h, session: int):
@@ -193,6 +201,19 @@ class Cache:
             out = torch.empty_like(q)
         st = okvq_decode(self._h, q.data_ptr(), out.data_ptr(), _stream_handle(stream))
         _check(st, "okvq_decode")
+        return out
+
+    def decode_static_scratch(self, q, out, stream=None):
+        """okvq_decode_static_scratch: as decode, with the split-K partials in the
+        library's one static device array (shared by all calls; see include/okvq.h).
+        `out` must be given: the call allocates nothing."""
+        import torch
+        shp = (self.num_sessions, self.num_layers, self.num_q_heads, self.head_dim)
+        for name, x in (("q", q), ("out", out)):
+            if tuple(x.shape) != shp or x.dtype != torch.float16 or not x.is_cuda or not x.is_contiguous():
+                raise ValueError("%s must be a contiguous cuda fp16 tensor of shape %s" % (name, shp))
+        st = okvq_decode_static_scratch(self._h, q.data_ptr(), out.data_ptr(), _stream_handle(stream))
+        _check(st, "okvq_decode_static_scratch")
         return out
 
     def length(self, session: int) -> int:

@@ -67,8 +67,10 @@ typedef enum {
   OKVQ_ENOMEM = 2,    /* a device or host allocation failed */
   OKVQ_ECAPACITY = 3, /* the append would exceed max_tokens; nothing was written */
   OKVQ_ECUDA = 4,     /* a CUDA call or kernel launch failed */
-  OKVQ_ESTATE = 5     /* the device error word was set (e.g. a modality id out of range,
+  OKVQ_ESTATE = 5,    /* the device error word was set (e.g. a modality id out of range,
                          a bounded wait that gave up); see okvq_check_errors */
+  OKVQ_ESCRATCH = 6   /* okvq_decode_static_scratch: the decode work list has more than
+                         OKVQ_STATIC_SCRATCH_SEGMENTS segments; nothing was launched */
 } okvq_status;
 
 typedef struct {
@@ -116,6 +118,41 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
  * `stream`; the work list is re-uploaded on `stream` after appends changed
  * the lengths. */
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
+
+/* Capacity, in work-list segments, of the static scratch array used by
+ * okvq_decode_static_scratch: 512 segments of 8 heads x (2 + 3*128) floats,
+ * 6,324,224 bytes of device memory reserved when the library's device code is
+ * loaded on a device. A decode's work list has at most
+ * (SM count + num_sessions*num_layers*num_kv_heads) segments. */
+#define OKVQ_STATIC_SCRATCH_SEGMENTS 512
+
+/* okvq_decode without per-call scratch memory of its own. The OmniKVQuant
+ * page has no counterpart of this call: it is an engineering variant of
+ * okvq_decode (same arguments, same kernels, same results) whose split-K
+ * partials go to one file-scope device array of OKVQ_STATIC_SCRATCH_SEGMENTS
+ * segments instead of the handle's partials buffer, and which never creates
+ * CUDA events (okvq_profile_* record okvq_decode only). It allocates nothing:
+ * no cudaMalloc, cudaFree, event or library allocation.
+ * It is meant for callers that must not allocate device memory, or let a
+ * library allocate for them, during the call. One example is a serving loop
+ * whose device memory is handed out by its own allocator or a fixed budget.
+ * Another is a latency-critical decode step that must keep the device
+ * allocator, and the synchronisation cudaFree implies, out of its path.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress with the handle's device made current, then the
+ * previous device restored), once per device for the process; OKVQ_ECUDA if
+ * that fails (retried on the next call). Make that first call before any
+ * stream capture.
+ * Sharing: every call, from every handle on a device, uses the same array.
+ * It keeps the last call's contents; nothing in it needs to start at zero,
+ * because each call writes every partial it reads. Calls whose work overlaps
+ * on the device (different streams, or threads without ordering) race on the
+ * array and give undefined results: order them on one stream or serialise them.
+ * Errors: OKVQ_EINVAL for NULL arguments; OKVQ_ESCRATCH, with nothing launched,
+ * when the current work list has more than OKVQ_STATIC_SCRATCH_SEGMENTS
+ * segments (the work list itself, shared with okvq_decode, may have been
+ * rebuilt and uploaded on `stream`); otherwise as okvq_decode. */
+okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream);
 
 /* Number of tokens held by `session`. */
 okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
