@@ -30,12 +30,15 @@ namespace {
 
 constexpr int WARPS = 8;
 constexpr int THREADS = WARPS * 32;
+// warp w rotates query head w and builds query fragment block w (8 blocks of 16 channels)
+static_assert(WARPS == MAXGQ && WARPS == D / 16, "one warp per query head and per fragment block");
 constexpr float LOG2E = 1.4426950408889634074f;
 constexpr float INV_D = 1.0f / 128.0f;                      // (1/sqrt d) rotation * (1/sqrt d) softmax
 constexpr float INV_SQRT_D = 0.0883883476483184405501f;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr long long WAIT_LIMIT = 1ll << 26;
 constexpr int LUT_BYTES = 256 * 256;   // 256 code bytes x [K half | V half], 128 B each
+constexpr float SOFTMAX_HEADROOM = 6.0f;   // log2 units
 
 template <int BITS>
 struct Cfg;
@@ -313,8 +316,12 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   for (int n = 0; n < 4; ++n) mx = fmaxf(mx, fmaxf(s[n][0], s[n][1]));
   mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-  const float m_new = fmaxf(m_run, mx);
-  if (__any_sync(FULL, m_new > m_run)) {
+  // lazy reference: m_run moves only when a score passes it, and then to the new
+  // maximum plus headroom, so later small increases need no rescale; every
+  // p = 2^(s - m_run) stays <= 1 and the largest stays >= 2^-headroom
+  const bool up = mx > m_run;
+  if (__any_sync(FULL, up)) {
+    const float m_new = up ? mx + SOFTMAX_HEADROOM : m_run;
     const float sf = ex2(m_run - m_new);
     const float sf0 = __shfl_sync(FULL, sf, 8 * t4), sf1 = __shfl_sync(FULL, sf, 8 * t4 + 4);
 #pragma unroll
