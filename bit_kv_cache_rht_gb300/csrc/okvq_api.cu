@@ -22,7 +22,6 @@ struct okvq_cache {
   uint8_t *pages = nullptr;
   __half *tails = nullptr;      // [2][units][G][D]
   uint8_t *mod = nullptr;       // [S][cap]
-  uint8_t *tmask = nullptr;     // [S][cap/16]
   float *rot = nullptr;         // [L][Hkv][M][D][D]
   float *rot_t = nullptr;       // transposed per matrix
   float *signs = nullptr;       // [D]
@@ -116,7 +115,6 @@ void release(okvq_cache *h) {
   cudaFree(h->pages);
   cudaFree(h->tails);
   cudaFree(h->mod);
-  cudaFree(h->tmask);
   cudaFree(h->rot);
   cudaFree(h->rot_t);
   cudaFree(h->signs);
@@ -306,7 +304,6 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->pages, page_total)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->tails, tails)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->mod, (size_t)h->S * h->cap)) != OKVQ_OK) return fail(st);
-  if ((st = alloc_dev((void **)&h->tmask, (size_t)h->S * (h->cap / TILE))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->rot, rot)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->rot_t, rot)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
@@ -333,7 +330,6 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if (cudaMemsetAsync(h->pages, 0, page_total, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->tails, 0, tails, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->mod, 0, (size_t)h->S * h->cap, s) != cudaSuccess) return fail(OKVQ_ECUDA);
-  if (cudaMemsetAsync(h->tmask, 0, (size_t)h->S * (h->cap / TILE), s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) return fail(OKVQ_ECUDA);
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
@@ -396,7 +392,6 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   a.tail_old = h->tails + (size_t)h->tail_sel[session] * tail_buf;
   a.tail_new = h->tails + (size_t)(1 - h->tail_sel[session]) * tail_buf;
   a.mod = h->mod;
-  a.tmask = h->tmask;
   a.cap = h->cap;
   a.rot_t = h->rot_t;
   a.signs = h->signs;
@@ -434,7 +429,6 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
   a.pages = h->pages;
   a.tails = h->tails;
   a.mod = h->mod;
-  a.tmask = h->tmask;
   a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
   a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
   a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);
@@ -510,7 +504,6 @@ okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, 
   a.pages = h->pages;
   a.tails = h->tails;
   a.mod = h->mod;
-  a.tmask = h->tmask;
   a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
   a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
   a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);

@@ -117,14 +117,15 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   if (lh == 0) {
     uint8_t *mod = a.mod + (long long)a.session * a.cap;
     for (int t = ta + tid; t < tb; t += THREADS) mod[P0 + t] = (uint8_t)S.mod[t];
-    if (tid < PAGE / TILE) {
-      int t0 = tid * TILE, t1 = t0 + TILE;
-      if (t1 > ta && t0 < tb) {
-        uint8_t *tm = a.tmask + (long long)a.session * (a.cap / TILE) + P0 / TILE + tid;
-        uint8_t bitsm = (t0 < ta) ? *tm : 0;      // tile already partly filled
-        for (int t = max(t0, ta); t < min(t1, tb); ++t) bitsm |= (uint8_t)(1u << S.mod[t]);
-        *tm = bitsm;
-      }
+  }
+  // the page's own copy of its tile modality masks (decode reads them with the page)
+  if (tid < PAGE / TILE) {
+    const int t0 = tid * TILE, t1 = t0 + TILE;
+    if (t1 > ta && t0 < tb) {
+      uint8_t *tm = pg + PL.off_tmask + tid;
+      uint8_t bitsm = (t0 < ta) ? *tm : 0;        // tile already partly filled
+      for (int t = max(t0, ta); t < min(t1, tb); ++t) bitsm |= (uint8_t)(1u << S.mod[t]);
+      *tm = bitsm;
     }
   }
 

@@ -211,7 +211,6 @@ struct HalfPageCtx {
   const uint4 *qfrag;        // [8 kb][32 lanes]: (q_hi(ch 2t..), q_lo(ch 2t..), q_hi(ch 2t+8..), q_lo(..))
   const __half *qraw;        // [8][128] natural order
   const __half *tail;        // this unit's fp16 trailing keys
-  const uint8_t *tmask;      // this session's 16-token tile masks
   const uint8_t *mod;        // this session's modality ids
   uint32_t laneoff, lutlo, luthi;
   int T, Tf;
@@ -364,7 +363,7 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
           *reinterpret_cast<const uint4 *>(sp + PL.off_v + tile * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
       vw[i] = v4.x; vw[i + 1] = v4.y; vw[i + 2] = v4.z; vw[i + 3] = v4.w;
     }
-    const uint32_t tmask = c.tmask[ts / TILE];
+    const uint32_t tmask = sp[PL.off_tmask + tile];
     if (__popc(tmask) == 1) {
       const uint32_t b0 = pack_h2(w0, w1), b1 = pack_h2(w8, w9);
       const int m = __ffs(tmask) - 1;
@@ -510,7 +509,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     hc.qfrag = qfrag;
     hc.qraw = qraw;
     hc.tail = tail;
-    hc.tmask = a.tmask + (long long)session * (a.cap / TILE);
     hc.mod = a.mod + (long long)session * a.cap;
     hc.laneoff = laneoff;
     hc.lutlo = lutlo;

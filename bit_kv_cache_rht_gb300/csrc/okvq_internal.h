@@ -9,6 +9,8 @@
 //     V codes  same shape
 //     norms    64 fp16, token order
 //     stats    64/G groups, each [min 128 fp16 | range 128 fp16] in the stat channel order
+//     tmask    4 bytes, bit m of byte i set when tile i holds a token of modality m,
+//              then 12 bytes of padding (page size stays a multiple of 16 B)
 //   so one decode warp streams one contiguous block per page with a single bulk copy.
 //
 // Lane chunks: the 32 lanes of a warp running mma.m16n8k16 hold 16x16 / 16x8
@@ -58,6 +60,7 @@ struct PageLayout {
   int off_v;        // 4 tiles of K codes
   int off_norm;
   int off_stats;
+  int off_tmask;    // 4 tile modality masks
   int page_bytes;
 };
 
@@ -70,7 +73,8 @@ __host__ __device__ inline PageLayout page_layout(int bits, int G) {
   L.off_v = 4 * L.tile_bytes;
   L.off_norm = 2 * L.off_v;
   L.off_stats = L.off_norm + PAGE * 2;
-  L.page_bytes = L.off_stats + (PAGE / G) * 2 * D * 2;
+  L.off_tmask = L.off_stats + (PAGE / G) * 2 * D * 2;
+  L.page_bytes = L.off_tmask + 16;
   return L;
 }
 
@@ -138,7 +142,6 @@ struct AppendArgs {
   __half *tail_old;         // [units][G][D] buffer read (current)
   __half *tail_new;         // [units][G][D] buffer written (next)
   uint8_t *mod;             // [S][cap] session modality ids
-  uint8_t *tmask;           // [S][cap/16] per 16-token tile modality bits
   long long cap;            // max_tokens rounded up to a page
   const float *rot_t;       // [L][Hkv][M][D][D]  (c, i) = R[i][c]
   const float *signs;       // [D] +-1 Hadamard signs
@@ -154,7 +157,6 @@ struct DecodeArgs {
   const uint8_t *pages;
   const __half *tails;      // [2][units][G][D]
   const uint8_t *mod;       // [S][cap]
-  const uint8_t *tmask;     // [S][cap/16]
   const int *segs;          // [nseg][4] = unit, page_begin, page_end, 0
   const int *cta_seg;       // [ncta+1]
   const long long *unit_len;// [units] token count
