@@ -28,10 +28,8 @@ namespace okvq {
 
 namespace {
 
-constexpr int WARPS = 8;
-constexpr int THREADS = WARPS * 32;
-// warp w rotates query head w and builds query fragment block w (8 blocks of 16 channels)
-static_assert(WARPS == MAXGQ && WARPS == D / 16, "one warp per query head and per fragment block");
+// warps 0-7 rotate query head w and build query fragment block w (8 blocks of 16 channels)
+static_assert(MAXGQ == D / 16, "one warp per query head and per fragment block");
 constexpr float LOG2E = 1.4426950408889634074f;
 constexpr float INV_D = 1.0f / 128.0f;                      // (1/sqrt d) rotation * (1/sqrt d) softmax
 constexpr float INV_SQRT_D = 0.0883883476483184405501f;
@@ -39,15 +37,18 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr long long WAIT_LIMIT = 1ll << 26;
 constexpr int LUT_BYTES = 256 * 256;   // 256 code bytes x [K half | V half], 128 B each
 constexpr float SOFTMAX_HEADROOM = 6.0f;   // log2 units
+constexpr uint32_t TMEM_COLS = 512;        // parked modality accumulators: (warps / 4) x 3 x 32 columns
 
 template <int BITS>
 struct Cfg;
 template <>
 struct Cfg<2> {
-  static constexpr int STAGES = 3;
+  static constexpr int WARPS = 12;   // 3 per scheduler at 168 registers
+  static constexpr int STAGES = 2;
 };
 template <>
 struct Cfg<4> {
+  static constexpr int WARPS = 8;    // 9.4 KB pages: shared memory holds 8 warps x 2 stages
   static constexpr int STAGES = 2;
 };
 
@@ -85,6 +86,72 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Tensor memory, 32 lanes x 32 columns of 32 bits per warp access (each lane its
+// own row); warp-collective: every lane of the warp executes these.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[8][4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0][0]), "f"(v[0][1]), "f"(v[0][2]), "f"(v[0][3]), "f"(v[1][0]), "f"(v[1][1]), "f"(v[1][2]), "f"(v[1][3]),
+      "f"(v[2][0]), "f"(v[2][1]), "f"(v[2][2]), "f"(v[2][3]), "f"(v[3][0]), "f"(v[3][1]), "f"(v[3][2]), "f"(v[3][3]),
+      "f"(v[4][0]), "f"(v[4][1]), "f"(v[4][2]), "f"(v[4][3]), "f"(v[5][0]), "f"(v[5][1]), "f"(v[5][2]), "f"(v[5][3]),
+      "f"(v[6][0]), "f"(v[6][1]), "f"(v[6][2]), "f"(v[6][3]), "f"(v[7][0]), "f"(v[7][1]), "f"(v[7][2]), "f"(v[7][3])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[8][4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=f"(v[0][0]), "=f"(v[0][1]), "=f"(v[0][2]), "=f"(v[0][3]), "=f"(v[1][0]), "=f"(v[1][1]), "=f"(v[1][2]),
+        "=f"(v[1][3]), "=f"(v[2][0]), "=f"(v[2][1]), "=f"(v[2][2]), "=f"(v[2][3]), "=f"(v[3][0]), "=f"(v[3][1]),
+        "=f"(v[3][2]), "=f"(v[3][3]), "=f"(v[4][0]), "=f"(v[4][1]), "=f"(v[4][2]), "=f"(v[4][3]), "=f"(v[5][0]),
+        "=f"(v[5][1]), "=f"(v[5][2]), "=f"(v[5][3]), "=f"(v[6][0]), "=f"(v[6][1]), "=f"(v[6][2]), "=f"(v[6][3]),
+        "=f"(v[7][0]), "=f"(v[7][1]), "=f"(v[7][2]), "=f"(v[7][3])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Per-warp value accumulators, one set per modality: the set of modality `cur`
+// lives in registers, the others (once touched) wait in this warp's 32-column
+// slots of tensor memory. Calls are warp-uniform.
+struct ModAcc {
+  uint32_t slot0;   // tensor-memory address of the modality-0 slot (this warp's lanes)
+  int cur;          // modality held in registers, -1 none
+  uint32_t live;    // modalities whose slot holds sums
+};
+__device__ __forceinline__ void mod_switch(ModAcc &ma, float (&acc)[8][4], int m) {
+  if (ma.cur >= 0) {
+    tmem_st32(ma.slot0 + 32u * (uint32_t)ma.cur, acc);
+    ma.live |= 1u << ma.cur;
+  }
+  if ((ma.live >> m) & 1u) {
+    tmem_ld32(ma.slot0 + 32u * (uint32_t)m, acc);
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  }
+  ma.cur = m;
+}
+// scale the parked sets (head columns 2t4 / 2t4+1 by sf0 / sf1)
+__device__ __forceinline__ void mod_rescale_parked(const ModAcc &ma, float sf0, float sf1) {
+#pragma unroll 1
+  for (int m = 0; m < MAXM; ++m) {
+    if (m == ma.cur || !((ma.live >> m) & 1u)) continue;
+    float v[8][4];
+    tmem_ld32(ma.slot0 + 32u * (uint32_t)m, v);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      v[mt][0] *= sf0; v[mt][2] *= sf0;
+      v[mt][1] *= sf1; v[mt][3] *= sf1;
+    }
+    tmem_st32(ma.slot0 + 32u * (uint32_t)m, v);
+  }
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -144,6 +211,7 @@ __device__ __forceinline__ uint32_t lut_addr(uint32_t laneoff, uint32_t w) {
   return r;
 }
 
+template <int WARPS>
 struct Merge {
   float m[WARPS][MAXGQ];
   float l[WARPS][MAXGQ];
@@ -218,10 +286,11 @@ struct HalfPageCtx {
 
 // One 32-token half page (two 16-token tiles) starting at page-relative token
 // 32*hp of the staged page sp. FULLV: all 32 tokens exist and are quantized.
-template <int BITS, int G, bool FULLV>
+// SINGLE: every token of the page has modality ma.cur (checked by the caller).
+template <int BITS, int G, bool FULLV, bool SINGLE>
 __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout &PL, const unsigned char *sp,
                                           int tok0, int hp, float beta, uint32_t (&af)[8][4],
-                                          float (&acc)[MAXM][8][4], float &m_run, float &l_run) {
+                                          float (&acc)[8][4], ModAcc &ma, float &m_run, float &l_run) {
   constexpr int LANE_WORDS = BITS * 2;
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int hs = tok0 + 32 * hp;
@@ -253,7 +322,7 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
     }
 #pragma unroll
     for (int n = 0; n < 4; ++n) {
-      sacc[n][0] = beta; sacc[n][1] = beta; sacc[n][2] = 0.f; sacc[n][3] = 0.f;
+      sacc[n][0] = 0.f; sacc[n][1] = 0.f; sacc[n][2] = 0.f; sacc[n][3] = 0.f;
     }
     uint32_t kw[2][LANE_WORDS];
 #pragma unroll
@@ -305,7 +374,8 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   for (int n = 0; n < 4; ++n)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const float v = sacc[n][e] + sacc[n][2 + e];
+      // the group offset joins after the MMA chain (it does not wait for it)
+      const float v = sacc[n][e] + sacc[n][2 + e] + ((FULLV || hs < c.Tf) ? beta : 0.f);
       s[n][e] = (FULLV || hs + 8 * n + 2 * t4 + e < c.T) ? v : -INFINITY;
     }
 
@@ -324,12 +394,11 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
     const float sf = ex2(m_run - m_new);
     const float sf0 = __shfl_sync(FULL, sf, 8 * t4), sf1 = __shfl_sync(FULL, sf, 8 * t4 + 4);
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m)
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        acc[m][mt][0] *= sf0; acc[m][mt][2] *= sf0;
-        acc[m][mt][1] *= sf1; acc[m][mt][3] *= sf1;
-      }
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= sf0; acc[mt][2] *= sf0;
+      acc[mt][1] *= sf1; acc[mt][3] *= sf1;
+    }
+    if (ma.live & ~(ma.cur >= 0 ? 1u << ma.cur : 0u)) mod_rescale_parked(ma, sf0, sf1);
     l_run *= sf;
     m_run = m_new;
   }
@@ -363,13 +432,15 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
           *reinterpret_cast<const uint4 *>(sp + PL.off_v + tile * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
       vw[i] = v4.x; vw[i + 1] = v4.y; vw[i + 2] = v4.z; vw[i + 3] = v4.w;
     }
+    if (SINGLE) {
+      value_mma<BITS>(acc, vw, c.lut_v, c.laneoff, pack_h2(w0, w1), pack_h2(w8, w9));
+      continue;
+    }
     const uint32_t tmask = sp[PL.off_tmask + tile];
     if (__popc(tmask) == 1) {
-      const uint32_t b0 = pack_h2(w0, w1), b1 = pack_h2(w8, w9);
       const int m = __ffs(tmask) - 1;
-      if (m == 0) value_mma<BITS>(acc[0], vw, c.lut_v, c.laneoff, b0, b1);
-      else if (m == 1) value_mma<BITS>(acc[1], vw, c.lut_v, c.laneoff, b0, b1);
-      else value_mma<BITS>(acc[2], vw, c.lut_v, c.laneoff, b0, b1);
+      if (m != ma.cur) mod_switch(ma, acc, m);
+      value_mma<BITS>(acc, vw, c.lut_v, c.laneoff, pack_h2(w0, w1), pack_h2(w8, w9));
     } else {
       const uint8_t *modp = c.mod + ts + 2 * t4;
       const int m0 = v0 ? modp[0] : -1, m1 = v1 ? modp[1] : -1;
@@ -379,14 +450,18 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
         if (!(tmask & (1u << m))) continue;
         const uint32_t b0 = pack_h2(m0 == m ? w0 : 0.f, m1 == m ? w1 : 0.f);
         const uint32_t b1 = pack_h2(m8 == m ? w8 : 0.f, m9 == m ? w9 : 0.f);
-        value_mma<BITS>(acc[m], vw, c.lut_v, c.laneoff, b0, b1);
+        if (m != ma.cur) mod_switch(ma, acc, m);
+        value_mma<BITS>(acc, vw, c.lut_v, c.laneoff, b0, b1);
       }
     }
   }
 }
 
 template <int BITS, int G>
-__global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const DecodeArgs a) {
+  constexpr int WARPS = Cfg<BITS>::WARPS;
+  constexpr int THREADS = WARPS * 32;
+  static_assert(WARPS >= MAXGQ && WARPS % 4 == 0 && (WARPS / 4) * MAXM * 32 <= TMEM_COLS, "warp layout");
   constexpr int STAGES = Cfg<BITS>::STAGES;
   constexpr int LANE_WORDS = BITS * 2;        // 32-bit words per lane chunk
   const PageLayout PL = page_layout(BITS, G);
@@ -399,9 +474,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
   __half *qraw = reinterpret_cast<__half *>(qr + MAXGQ * D);            // [8][128] natural order
   uint4 *qfrag = reinterpret_cast<uint4 *>(qraw + MAXGQ * D);           // [8 kb][32 lanes]
   uint64_t *bars = reinterpret_cast<uint64_t *>(qfrag + 8 * 32);        // [WARPS][STAGES]
-  unsigned char *stages = reinterpret_cast<unsigned char *>(bars + WARPS * STAGES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + WARPS * STAGES);
+  unsigned char *stages = reinterpret_cast<unsigned char *>(tmem_slot + 4);
   stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
-  Merge &MG = *reinterpret_cast<Merge *>(stages);
+  Merge<WARPS> &MG = *reinterpret_cast<Merge<WARPS> *>(stages);
   unsigned char *my_stage0 = stages + (size_t)warp * STAGES * PL.page_bytes;
   uint64_t *my_bars = bars + warp * STAGES;
 
@@ -428,9 +504,20 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
   if (lane == 0)
     for (int s = 0; s < STAGES; ++s) mbar_init(&my_bars[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  // tensor memory for the parked modality accumulators: 2 warps per lane quarter,
+  // 3 x 32 columns each
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
   // the merge kernel may be scheduled as SMs free up; it waits for this grid's memory
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t slot0 = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(warp >> 2) * (MAXM * 32);
 
   const unsigned char *lut_k = lut, *lut_v = lut + 128;
   const uint32_t laneoff = BITS == 2 ? (uint32_t)((lane & 15) << 3) : (uint32_t)(lane << 2);
@@ -461,7 +548,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
 
     // ---- rotate the query group once: q' = H (s o q) / d, in log2 units (warp = head) ----
-    {
+    if (warp < MAXGQ) {
       const __half *qsrc = a.q + (((long long)session * a.L + layer) * a.Hq + (long long)kvh * gq) * D;
       const int hh = warp;
       float x[4];
@@ -493,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
 
     // query fragments for the score and offset MMAs, one kb block per warp:
     // lane (g, t4) gets head g, channels 16kb + 2t4 + {0,1} and + 8 + {0,1}, fp16 high + residual
-    {
+    if (warp < D / 16) {
       const int kb = warp;
       const float4 v = *reinterpret_cast<const float4 *>(qr + g * D + 32 * (kb >> 1) + 8 * t4 + 4 * (kb & 1));
       const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
@@ -517,13 +604,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
     hc.Tf = Tf;
 
     // ---- per-warp state ----
-    float acc[MAXM][8][4];
+    float acc[8][4];         // value sums of modality ma.cur (the others parked in tensor memory)
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m)
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[m][mt][r] = 0.f;
+    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    ModAcc ma{slot0, -1, 0u};
     float m_run = -INFINITY, l_run = 0.f;     // head g
 
     const int npages = pe - pb;
@@ -577,15 +661,27 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
         beta_g1 = __shfl_sync(FULL, d[1] + d[3], 4 * g);
       }
 
+      // modalities present in the page: one (the common case) runs without per-tile checks
+      const uint32_t tmw = *reinterpret_cast<const uint32_t *>(sp + PL.off_tmask);
+      const uint32_t pmask = (tmw | (tmw >> 8) | (tmw >> 16) | (tmw >> 24)) & 0xFFu;
+      const bool single = __popc(pmask) == 1;
+      if (single && __ffs(pmask) - 1 != ma.cur) mod_switch(ma, acc, __ffs(pmask) - 1);
 #pragma unroll 1
       for (int hp = 0; hp < 2; ++hp) {
         const int hs = tok0 + 32 * hp;
         if (hs >= T) break;
         const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
-        if (hs + 32 <= Tf)
-          half_page<BITS, G, true>(hc, PL, sp, tok0, hp, beta, af, acc, m_run, l_run);
-        else
-          half_page<BITS, G, false>(hc, PL, sp, tok0, hp, beta, af, acc, m_run, l_run);
+        if (single) {
+          if (hs + 32 <= Tf)
+            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+          else
+            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+        } else {
+          if (hs + 32 <= Tf)
+            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+          else
+            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+        }
       }
       __syncwarp();
       // refill this stage with the page STAGES ahead
@@ -602,7 +698,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
       if (tid == 0) atomicOr(a.err, ERR_WAIT);
       if (lane == 0)
         for (int s2 = 0; s2 < STAGES; ++s2) (void)mbar_wait(&my_bars[(ring_st + s2) % STAGES], ring_par ^ (s2 + ring_st >= STAGES ? 1u : 0u));
-      return;
+      break;
     }
 
     // ---- per-warp totals: head g lives in lanes 4g..4g+3 ----
@@ -612,15 +708,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
       MG.m[warp][g] = m_run;
       MG.l[warp][g] = l_run;
     }
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m)
+#pragma unroll 1
+    for (int m = 0; m < MAXM; ++m) {
+      const bool held = m == ma.cur || ((ma.live >> m) & 1u);
+      if (held && m != ma.cur) mod_switch(ma, acc, m);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        MG.o[warp][m][2 * t4][16 * mt + g] = acc[m][mt][0];
-        MG.o[warp][m][2 * t4 + 1][16 * mt + g] = acc[m][mt][1];
-        MG.o[warp][m][2 * t4][16 * mt + g + 8] = acc[m][mt][2];
-        MG.o[warp][m][2 * t4 + 1][16 * mt + g + 8] = acc[m][mt][3];
+        MG.o[warp][m][2 * t4][16 * mt + g] = held ? acc[mt][0] : 0.f;
+        MG.o[warp][m][2 * t4 + 1][16 * mt + g] = held ? acc[mt][1] : 0.f;
+        MG.o[warp][m][2 * t4][16 * mt + g + 8] = held ? acc[mt][2] : 0.f;
+        MG.o[warp][m][2 * t4 + 1][16 * mt + g + 8] = held ? acc[mt][3] : 0.f;
       }
+    }
     __syncthreads();
     float *part = a.partials + (long long)seg * MAXGQ * PARTIAL_FLOATS;
     for (int i = tid; i < MAXGQ * D; i += THREADS) {
@@ -647,6 +746,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_kernel(const DecodeArgs a) 
       }
     }
     __syncthreads();              // merge area is the stage ring of the next segment
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(TMEM_COLS));
   }
 }
 
@@ -732,20 +837,23 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int n_cta, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  decode_kernel<BITS, G><<<n_cta, THREADS, smem, s>>>(a);
+  decode_kernel<BITS, G><<<n_cta, Cfg<BITS>::WARPS * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int bits, int G) {
-  const PageLayout PL = page_layout(bits, G);
-  const int stages = bits == 2 ? Cfg<2>::STAGES : Cfg<4>::STAGES;
-  size_t head = LUT_BYTES + MAXGQ * D * 4 + MAXGQ * D * 2 + 8 * 32 * 16 + WARPS * stages * 8;
-  size_t ring = (size_t)WARPS * stages * PL.page_bytes;
-  if (ring < sizeof(Merge)) ring = sizeof(Merge);
+template <int BITS>
+size_t decode_smem_bytes_t(int G) {
+  const PageLayout PL = page_layout(BITS, G);
+  constexpr int W = Cfg<BITS>::WARPS, STAGES = Cfg<BITS>::STAGES;
+  size_t head = LUT_BYTES + MAXGQ * D * 4 + MAXGQ * D * 2 + 8 * 32 * 16 + W * STAGES * 8 + 16;
+  size_t ring = (size_t)W * STAGES * PL.page_bytes;
+  if (ring < sizeof(Merge<W>)) ring = sizeof(Merge<W>);
   return head + 128 + ring;
 }
+
+size_t decode_smem_bytes(int bits, int G) { return bits == 2 ? decode_smem_bytes_t<2>(G) : decode_smem_bytes_t<4>(G); }
 
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
   if (n_cta <= 0) return cudaSuccess;
