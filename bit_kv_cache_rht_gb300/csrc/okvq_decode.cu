@@ -256,13 +256,12 @@ __device__ __forceinline__ void key_frags(const uint32_t *kw, int kb, uint32_t l
       bf[2] = kreg_pair(src, 2, lutlo, luthi);
       bf[3] = kreg_pair(src, 6, lutlo, luthi);
     } else {
+      // one table entry = one B fragment: (pairs 4kb, 4kb+2), then (4kb+1, 4kb+3)
       const uint32_t w = kw[kb >> 1];
-      uint32_t p0, p1, p2, p3;
       const uint32_t a0 = (kb & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
       const uint32_t a1 = (kb & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
-      lut64(lut_k, a0, p0, p1);   // pairs 4kb, 4kb+1
-      lut64(lut_k, a1, p2, p3);   // pairs 4kb+2, 4kb+3
-      bf[0] = p0; bf[1] = p2; bf[2] = p1; bf[3] = p3;
+      lut64(lut_k, a0, bf[0], bf[1]);
+      lut64(lut_k, a1, bf[2], bf[3]);
     }
   } else {
     const uint32_t w = kw[kb];

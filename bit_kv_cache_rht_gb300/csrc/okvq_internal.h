@@ -22,8 +22,12 @@
 //        token = 2*(l%4) + 8*(r>>1) + e,   channel = 16*blk + l/4 + 8*(r&1)
 // with e = 0/1 the half. Bit position of code e of pair j inside the chunk:
 //   4-bit: 8*j + 4*e (pair j = byte j).
-//   2-bit V, and 2-bit K words not in KREG_WORDS: 4*j + 2*e (pair j = nibble j);
-//        a byte holds two pairs and indexes the shared-memory level table.
+//   2-bit V: 4*j + 2*e (pair j = nibble j); a byte holds two pairs and indexes
+//        the shared-memory level table.
+//   2-bit K words not in KREG_WORDS (table layout): pair j = 8*i + r of word i
+//        sits in byte 2*(r/4) + (r&1), nibble (r/2)&1, so the two pairs of one
+//        table entry are exactly one score-MMA B fragment (pairs 4kb and 4kb+2,
+//        or 4kb+1 and 4kb+3).
 //   2-bit K words in KREG_WORDS (register table path): word i = j/8 holds pairs
 //        q = j%8 with code e at bit 16*(q/4) + 2*(q%4) + 8*e, so one mask picks a
 //        pair as two 2-bit fields 8 bits apart, ready to become a byte-permute
@@ -90,16 +94,13 @@ __host__ __device__ inline void v_pair_coords(int lane, int j, int e, int &tok, 
   ch = 16 * blk + (lane >> 2) + 8 * (reg & 1);
 }
 // 2-bit K chunk words that use the register table layout (bit w = word w)
-constexpr unsigned KREG_WORDS = 0xFu;
+constexpr unsigned KREG_WORDS = 0x0u;
 
 __host__ __device__ inline int k_code_bit(int bits, int j, int e) {
   if (bits == 4) return 8 * j + 4 * e;
-  const int word = j >> 3;
-  if ((KREG_WORDS >> word) & 1u) {
-    const int q = j & 7;
-    return 32 * word + 16 * (q >> 2) + 2 * (q & 3) + 8 * e;
-  }
-  return 4 * j + 2 * e;
+  const int word = j >> 3, r = j & 7;
+  if ((KREG_WORDS >> word) & 1u) return 32 * word + 16 * (r >> 2) + 2 * (r & 3) + 8 * e;
+  return 32 * word + 8 * (2 * (r >> 2) + (r & 1)) + 4 * ((r >> 1) & 1) + 2 * e;
 }
 __host__ __device__ inline int v_code_bit(int bits, int j, int e) { return bits == 4 ? 8 * j + 4 * e : 4 * j + 2 * e; }
 
@@ -113,6 +114,10 @@ __host__ __device__ inline void chunk_code_at(int kind, int bits, int wi, int b,
     const int half = b >> 4, bb = b & 15;
     e = bb >> 3;
     j = 8 * wi + 4 * half + ((bb & 7) >> 1);
+  } else if (kind == 0) {
+    const int byte = b >> 3, nib = (b >> 2) & 1;
+    e = (b >> 1) & 1;
+    j = 8 * wi + 4 * (byte >> 1) + 2 * nib + (byte & 1);
   } else {
     j = (32 * wi + b) >> 2;
     e = (b >> 1) & 1;
