@@ -34,6 +34,16 @@ METRIC = "2-bit KV decode attention: context tokens/s and HBM GB/s (% of GB300 p
 UNIT = "context tokens/s"
 
 
+def decode_source_sha256():
+    """Hash of the decode kernel sources (compared with the one stored beside the ncu traffic figure)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("okvq_decode.cu", "okvq_internal.h"):
+        with open(os.path.join(ROOT, "bit_kv_cache_rht_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def algorithmic_bytes(w, lengths):
     """Decode bytes per step: codes, statistics, norms, fp16 tail keys, modality ids, q and out."""
     sh = w.shape
@@ -334,7 +344,9 @@ def main():
         if os.path.exists(tp):
             with open(tp) as f:
                 tj = json.load(f)
-            if tj.get("workload") == args.workload:
+            # DRAM bytes of one decode launch from an ncu capture, valid only while the
+            # kernel sources are the ones that capture measured
+            if tj.get("workload") == args.workload and tj.get("source_sha256") == decode_source_sha256():
                 traffic = tj.get("bytes_per_launch")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
