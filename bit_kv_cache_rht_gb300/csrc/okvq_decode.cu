@@ -45,11 +45,13 @@ template <>
 struct Cfg<2> {
   static constexpr int WARPS = 12;   // 3 per scheduler at 168 registers
   static constexpr int STAGES = 2;
+  static constexpr bool QREG = true;  // query fragments held in registers for the whole segment
 };
 template <>
 struct Cfg<4> {
   static constexpr int WARPS = 8;    // 9.4 KB pages: shared memory holds 8 warps x 2 stages
   static constexpr int STAGES = 2;
+  static constexpr bool QREG = false;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -289,7 +291,8 @@ struct HalfPageCtx {
 template <int BITS, int G, bool FULLV, bool SINGLE>
 __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout &PL, const unsigned char *sp,
                                           int tok0, int hp, float beta, uint32_t (&af)[8][4],
-                                          float (&acc)[8][4], ModAcc &ma, float &m_run, float &l_run) {
+                                          float (&acc)[8][4], ModAcc &ma, float &m_run, float &l_run,
+                                          const uint4 (&qreg)[8]) {
   constexpr int LANE_WORDS = BITS * 2;
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int hs = tok0 + 32 * hp;
@@ -305,7 +308,7 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int kb = 2 * k2 + u;
-          const uint4 q = c.qfrag[kb * 32 + lane];
+          const uint4 q = Cfg<BITS>::QREG ? qreg[kb] : c.qfrag[kb * 32 + lane];
           const uint32_t qh[2] = {q.x, q.z}, ql[2] = {q.y, q.w};
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -593,6 +596,9 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     hc.lut_k = lut_k;
     hc.lut_v = lut_v;
     hc.qfrag = qfrag;
+    uint4 qreg[8];             // this lane's query fragments (registers when Cfg::QREG)
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) qreg[kb] = Cfg<BITS>::QREG ? qfrag[kb * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
     hc.qraw = qraw;
     hc.tail = tail;
     hc.mod = a.mod + (long long)session * a.cap;
@@ -652,7 +658,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
             b0 = v.x;
             b1 = v.y;
           }
-          const uint4 q = qfrag[kb * 32 + lane];
+          const uint4 q = Cfg<BITS>::QREG ? qreg[kb] : qfrag[kb * 32 + lane];
           const uint32_t A[4] = {q.x, q.y, q.z, q.w};
           mma16816(d, A, b0, b1);
         }
@@ -672,14 +678,14 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
         const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
         if (single) {
           if (hs + 32 <= Tf)
-            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
         } else {
           if (hs + 32 <= Tf)
-            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run);
+            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
         }
       }
       __syncwarp();
