@@ -761,9 +761,11 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
 }
 
 // One CTA per (unit, 32 output channels), warp w = query head w: merge the
-// unit's partials by log-sum-exp, then O = (sum_m R_m^T o_m) / (l sqrt d) with
-// the R block staged in shared memory. Every global load is issued in bulk
-// (R and the partials are L2/HBM-latency bound, the arithmetic is tiny).
+// unit's partials by log-sum-exp, then O = (sum_m R_m^T o_m) / (l sqrt d).
+// Everything is latency bound, so: the R block streams into shared memory with
+// asynchronous copies issued before the wait on the decode grid; segment weights
+// are computed lane-parallel (lane = segment) and the per-segment loads are
+// independent; the rotation dot products run four accumulators.
 constexpr int CB_CH = 32;
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   extern __shared__ __align__(16) float csm[];
@@ -775,15 +777,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   const int gq = a.Hq / a.Hkv;
   const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
   const int lh = unit % (a.L * a.Hkv);
-  const float *R = a.rot + (long long)lh * a.M * D * D;
-  constexpr int RPER = MAXM * D * (CB_CH / 4) / 256;
-  const int rtotal = a.M * D * (CB_CH / 4);
-  float4 rt[RPER];
-#pragma unroll
-  for (int k = 0; k < RPER; ++k) {
-    const int i = tid + 256 * k;
-    if (i < rtotal) rt[k] = *reinterpret_cast<const float4 *>(R + (long long)(i >> 3) * D + cb * CB_CH + 4 * (i & 7));
+  const int nr = a.M * D;                            // rows of the stacked R_m
+  const float *R = a.rot + (long long)lh * a.M * D * D + cb * CB_CH;
+  // R rows r, channels cb*32 .. +31: 8 chunks of 16 bytes per row
+  for (int i = tid; i < nr * (CB_CH / 4); i += 256) {
+    const uint32_t dst = smem_u32(Rs + (i >> 3) * CB_CH + 4 * (i & 7));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(R + (long long)(i >> 3) * D + 4 * (i & 7))
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   // everything above only reads the rotations; the partials come from the decode grid
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int OPER = MAXM * D / 32;
@@ -792,40 +794,65 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   for (int k = 0; k < OPER; ++k) o[k] = 0.f;
   float L = 0.f;
   if (hh < gq) {
-    // head hh: reference max over the unit's segments (lanes take segments)
-    float M = -INFINITY;
-    for (int s = s0 + lane; s < s1; s += 32) M = fmaxf(M, a.partials[((long long)s * MAXGQ + hh) * PARTIAL_FLOATS]);
+    const float *pbase = a.partials + (long long)hh * PARTIAL_FLOATS;
+    auto part = [&](int s) { return pbase + (long long)s * MAXGQ * PARTIAL_FLOATS; };
+    // reference maximum and weights: lanes take segments; the first 32 segments'
+    // (m, l) are read once and kept in registers
+    float m0 = -INFINITY, l0 = 0.f;
+    if (s0 + lane < s1) {
+      const float2 ml = *reinterpret_cast<const float2 *>(part(s0 + lane));
+      m0 = ml.x;
+      l0 = ml.y;
+    }
+    float M = m0;
+    for (int s = s0 + 32 + lane; s < s1; s += 32) M = fmaxf(M, part(s)[0]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    for (int s = s0; s < s1; ++s) {
-      const float *p = a.partials + ((long long)s * MAXGQ + hh) * PARTIAL_FLOATS;
-      const float m = p[0];
-      const float w = m == -INFINITY ? 0.f : ex2(m - M);
-      L = fmaf(w, p[1], L);
+    for (int sb = s0; sb < s1; sb += 32) {
+      float w = 0.f;
+      if (sb + lane < s1) {
+        float m = m0, l = l0;
+        if (sb != s0) {
+          const float2 ml = *reinterpret_cast<const float2 *>(part(sb + lane));
+          m = ml.x;
+          l = ml.y;
+        }
+        w = m == -INFINITY ? 0.f : ex2(m - M);
+        L = fmaf(w, l, L);
+      }
+      const int n = min(32, s1 - sb);
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float ws = __shfl_sync(0xffffffffu, w, j);
+        const float *p = part(sb + j) + 2 + lane;
 #pragma unroll
-      for (int k = 0; k < OPER; ++k)
-        if (32 * k < a.M * D) o[k] = fmaf(w, p[2 + lane + 32 * k], o[k]);
+        for (int k = 0; k < OPER; ++k)
+          if (32 * k < nr) o[k] = fmaf(ws, p[32 * k], o[k]);
+      }
     }
-  }
 #pragma unroll
-  for (int k = 0; k < RPER; ++k) {
-    const int i = tid + 256 * k;
-    if (i < rtotal) reinterpret_cast<float4 *>(Rs)[i] = rt[k];
-  }
-  if (hh < gq) {
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
 #pragma unroll
     for (int k = 0; k < OPER; ++k)
-      if (32 * k < a.M * D) osh[hh * MAXM * D + lane + 32 * k] = o[k];
+      if (32 * k < nr) osh[hh * MAXM * D + lane + 32 * k] = o[k];
     if (lane == 0) Lsh[hh] = L;
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
   if (hh < gq) {
-    float acc = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const float *oh = osh + hh * MAXM * D;
-#pragma unroll 8
-    for (int r = 0; r < a.M * D; ++r) acc = fmaf(Rs[r * CB_CH + lane], oh[r], acc);
+#pragma unroll 4
+    for (int r = 0; r < nr; r += 4) {
+      const float4 ov = *reinterpret_cast<const float4 *>(oh + r);
+      acc[0] = fmaf(Rs[(r + 0) * CB_CH + lane], ov.x, acc[0]);
+      acc[1] = fmaf(Rs[(r + 1) * CB_CH + lane], ov.y, acc[1]);
+      acc[2] = fmaf(Rs[(r + 2) * CB_CH + lane], ov.z, acc[2]);
+      acc[3] = fmaf(Rs[(r + 3) * CB_CH + lane], ov.w, acc[3]);
+    }
+    const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     const float Lh = Lsh[hh];
-    const float y = Lh > 0.f ? acc / (Lh * 11.3137084989847603904f) : 0.f;
+    const float y = Lh > 0.f ? sum / (Lh * 11.3137084989847603904f) : 0.f;
     const int session = unit / (a.L * a.Hkv);
     const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
     a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb * CB_CH + lane] = __float2half_rn(y);
