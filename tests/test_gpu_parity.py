@@ -73,6 +73,15 @@ def test_qwen3b_shape_streamed_chunks():
     _full_check(w, steps=(0, 1))
 
 
+def test_bench_workload_full_size_sampled_layers():
+    """The bench workload at full size (Qwen2.5-Omni-3B shape: 36 layers, 16 q / 2 kv
+    heads, 32,768 tokens in 1-s chunks, 2-bit, G 32) through the same cache build and
+    decode launch configuration bench.py times; the oracle recomputes the first and
+    the last layer (both kv heads, all 16 query heads) and their stored state."""
+    w = synth.qwen3b()
+    _full_check(w, layers_check=[0, w.shape.num_layers - 1], steps=(0,))
+
+
 def test_qwen7b_shape_seven_heads_per_kv():
     w = synth.qwen7b(seed=41, tokens=3000, layers=2)
     _full_check(w, steps=(0,))
