@@ -22,7 +22,7 @@ struct okvq_cache {
   uint8_t *pages = nullptr;
   __half *tails = nullptr;      // [2][units][G][D]
   uint8_t *mod = nullptr;       // [S][cap]
-  float *rot = nullptr;         // [L][Hkv][M][D][D]
+  uint32_t *rot_frag = nullptr; // R^T in mma fragment order, fp16 high and residual (see CombineArgs)
   float *rot_t = nullptr;       // transposed per matrix
   float *signs = nullptr;       // [D]
   uint32_t *err = nullptr;
@@ -115,7 +115,7 @@ void release(okvq_cache *h) {
   cudaFree(h->pages);
   cudaFree(h->tails);
   cudaFree(h->mod);
-  cudaFree(h->rot);
+  cudaFree(h->rot_frag);
   cudaFree(h->rot_t);
   cudaFree(h->signs);
   cudaFree(h->err);
@@ -304,7 +304,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->pages, page_total)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->tails, tails)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->mod, (size_t)h->S * h->cap)) != OKVQ_OK) return fail(st);
-  if ((st = alloc_dev((void **)&h->rot, rot)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->rot_frag, rot)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->rot_t, rot)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
@@ -340,7 +340,28 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
       for (int i = 0; i < D; ++i)
         for (int cc = 0; cc < D; ++cc) T[cc * D + i] = R[i * D + cc];
     }
-    if (cudaMemcpyAsync(h->rot, c.value_rot, rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+    // R^T as m16n8k16 A fragments: m-tile mt (16 output channels), k-step ks (16 rows
+    // r of the stacked R_m, m = ks / 8), lane (g, t4): a0 = (c = 16mt+g, r = r0..r0+1),
+    // a1 = (c+8, r0..), a2 = (c, r0+8..), a3 = (c+8, r0+8..), r0 = 16 (ks%8) + 2 t4;
+    // each pair split into an fp16 high part and the fp16 residual
+    std::vector<uint32_t> fr(nmat * D * D);
+    const int nks = 8 * h->M;
+    for (size_t lhm = 0; lhm < (size_t)h->L * h->Hkv; ++lhm)
+      for (int mt = 0; mt < 8; ++mt)
+        for (int ks = 0; ks < nks; ++ks)
+          for (int ln = 0; ln < 32; ++ln)
+            for (int i = 0; i < 4; ++i) {
+              const int cc = 16 * mt + (ln >> 2) + 8 * (i & 1);
+              const int r0 = 16 * (ks % 8) + 2 * (ln & 3) + 8 * (i >> 1);
+              const float *Rm = c.value_rot + (lhm * h->M + ks / 8) * D * D;
+              const float v0 = Rm[r0 * D + cc], v1 = Rm[(r0 + 1) * D + cc];
+              const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+              const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
+              const size_t base = (((lhm * 8 + mt) * nks + ks) * 32 + ln) * 8;
+              fr[base + i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+              fr[base + 4 + i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            }
+    if (cudaMemcpyAsync(h->rot_frag, fr.data(), rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
     if (cudaMemcpyAsync(h->rot_t, rt.data(), rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
     uint64_t state = c.hadamard_seed;
     float sg[D];
@@ -452,7 +473,8 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
   CombineArgs cb{};
   cb.partials = h->partials;
   cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
-  cb.rot = h->rot;
+  cb.rot_frag = reinterpret_cast<const uint4 *>(h->rot_frag);
+  cb.err = h->err;
   cb.out = static_cast<__half *>(out);
   cb.L = h->L;
   cb.Hq = h->Hq;
@@ -527,7 +549,8 @@ okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, 
   CombineArgs cb{};
   cb.partials = scratch;
   cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
-  cb.rot = h->rot;
+  cb.rot_frag = reinterpret_cast<const uint4 *>(h->rot_frag);
+  cb.err = h->err;
   cb.out = static_cast<__half *>(out);
   cb.L = h->L;
   cb.Hq = h->Hq;

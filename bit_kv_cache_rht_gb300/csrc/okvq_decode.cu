@@ -760,44 +760,44 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   }
 }
 
-// One CTA per (unit, 32 output channels), warp w = query head w: merge the
-// unit's partials by log-sum-exp, then O = (sum_m R_m^T o_m) / (l sqrt d).
-// Everything is latency bound, so: the R block streams into shared memory with
-// asynchronous copies issued before the wait on the decode grid; segment weights
-// are computed lane-parallel (lane = segment) and the per-segment loads are
-// independent; the rotation dot products run four accumulators.
-constexpr int CB_CH = 32;
+// One CTA per (unit, 64 output channels): merge the unit's partials by
+// log-sum-exp (warp w = query head w), then O^T[c][h] = sum_r R^T[c][r] o[h][r] / l
+// on the tensor cores. R^T comes pre-split into fp16 high and residual parts in
+// mma fragment order (one bulk copy per CTA, issued before the wait on the decode
+// grid); o / l is split the same way, and hi*hi + hi*lo + lo*hi carries the
+// product to ~2^-22 relative (fp32 accumulation).
+constexpr int CB_CH = 64;                       // output channels per CTA (4 m-tiles of 16)
+constexpr int OSTRIDE = MAXM * D + 4;           // padded row of the merged o (floats)
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
-  extern __shared__ __align__(16) float csm[];
-  float *Rs = csm;                                   // [M * D rows][CB_CH]
-  float *osh = Rs + MAXM * D * CB_CH;                // [MAXGQ][M * D]
-  __shared__ float Lsh[MAXGQ];
-  const int unit = blockIdx.x, cb = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, hh = tid >> 5;
+  extern __shared__ __align__(128) unsigned char csm[];
+  uint4 *afr = reinterpret_cast<uint4 *>(csm);                                  // [4][8M][32][2] hi|lo
+  float *osh = reinterpret_cast<float *>(csm + 4 * 8 * MAXM * 32 * 32);           // [8][OSTRIDE]
+  float *red = osh + MAXGQ * OSTRIDE;                                             // [4][32][4]
+  __shared__ __align__(8) uint64_t bar;
+  const int unit = blockIdx.x, half = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
   const int gq = a.Hq / a.Hkv;
   const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
   const int lh = unit % (a.L * a.Hkv);
-  const int nr = a.M * D;                            // rows of the stacked R_m
-  const float *R = a.rot + (long long)lh * a.M * D * D + cb * CB_CH;
-  // R rows r, channels cb*32 .. +31: 8 chunks of 16 bytes per row
-  for (int i = tid; i < nr * (CB_CH / 4); i += 256) {
-    const uint32_t dst = smem_u32(Rs + (i >> 3) * CB_CH + 4 * (i & 7));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(R + (long long)(i >> 3) * D + 4 * (i & 7))
-                 : "memory");
+  const int nks = 8 * a.M;                                // 16-row k-steps over the stacked R_m
+  const uint32_t fbytes = (uint32_t)(4 * nks * 32 * 32);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_async_smem();
+    bulk_load(afr, a.rot_frag + ((long long)lh * 8 + 4 * half) * nks * 32 * 2, fbytes, &bar);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
   // everything above only reads the rotations; the partials come from the decode grid
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int OPER = MAXM * D / 32;
-  float o[OPER];
+  const int nr = a.M * D;
+  if (w < gq) {
+    constexpr int OPER = MAXM * D / 32;
+    float o[OPER];
 #pragma unroll
-  for (int k = 0; k < OPER; ++k) o[k] = 0.f;
-  float L = 0.f;
-  if (hh < gq) {
-    const float *pbase = a.partials + (long long)hh * PARTIAL_FLOATS;
+    for (int k = 0; k < OPER; ++k) o[k] = 0.f;
+    float L = 0.f;
+    const float *pbase = a.partials + (long long)w * PARTIAL_FLOATS;
     auto part = [&](int s) { return pbase + (long long)s * MAXGQ * PARTIAL_FLOATS; };
-    // reference maximum and weights: lanes take segments; the first 32 segments'
-    // (m, l) are read once and kept in registers
     float m0 = -INFINITY, l0 = 0.f;
     if (s0 + lane < s1) {
       const float2 ml = *reinterpret_cast<const float2 *>(part(s0 + lane));
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     for (int sb = s0; sb < s1; sb += 32) {
-      float w = 0.f;
+      float wt = 0.f;
       if (sb + lane < s1) {
         float m = m0, l = l0;
         if (sb != s0) {
@@ -817,13 +817,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
           m = ml.x;
           l = ml.y;
         }
-        w = m == -INFINITY ? 0.f : ex2(m - M);
-        L = fmaf(w, l, L);
+        wt = m == -INFINITY ? 0.f : ex2(m - M);
+        L = fmaf(wt, l, L);
       }
       const int n = min(32, s1 - sb);
 #pragma unroll 4
       for (int j = 0; j < n; ++j) {
-        const float ws = __shfl_sync(0xffffffffu, w, j);
+        const float ws = __shfl_sync(0xffffffffu, wt, j);
         const float *p = part(sb + j) + 2 + lane;
 #pragma unroll
         for (int k = 0; k < OPER; ++k)
@@ -832,30 +832,50 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
     for (int k = 0; k < OPER; ++k)
-      if (32 * k < nr) osh[hh * MAXM * D + lane + 32 * k] = o[k];
-    if (lane == 0) Lsh[hh] = L;
+      if (32 * k < nr) osh[w * OSTRIDE + lane + 32 * k] = o[k] * inv;
+  } else if (w < MAXGQ) {
+    for (int k = lane; k < nr; k += 32) osh[w * OSTRIDE + k] = 0.f;
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
-  if (hh < gq) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const float *oh = osh + hh * MAXM * D;
-#pragma unroll 4
-    for (int r = 0; r < nr; r += 4) {
-      const float4 ov = *reinterpret_cast<const float4 *>(oh + r);
-      acc[0] = fmaf(Rs[(r + 0) * CB_CH + lane], ov.x, acc[0]);
-      acc[1] = fmaf(Rs[(r + 1) * CB_CH + lane], ov.y, acc[1]);
-      acc[2] = fmaf(Rs[(r + 2) * CB_CH + lane], ov.z, acc[2]);
-      acc[3] = fmaf(Rs[(r + 3) * CB_CH + lane], ov.w, acc[3]);
+  const bool got = mbar_wait(&bar, 0);
+  if (!got && tid == 0) atomicOr(a.err, ERR_WAIT);
+  // warp w: m-tile w & 3 of this CTA's 64 channels, k-steps of half w >> 2
+  const int mtl = w & 3, kh = w >> 2, k0 = kh * (nks / 2), k1 = k0 + nks / 2;
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  if (got) {
+    for (int ks = k0; ks < k1; ++ks) {
+      const uint4 ah = afr[((mtl * nks + ks) * 32 + lane) * 2];
+      const uint4 al = afr[((mtl * nks + ks) * 32 + lane) * 2 + 1];
+      const uint32_t Ah[4] = {ah.x, ah.y, ah.z, ah.w}, Al[4] = {al.x, al.y, al.z, al.w};
+      const float2 x01 = *reinterpret_cast<const float2 *>(osh + g * OSTRIDE + 16 * ks + 2 * t4);
+      const float2 x89 = *reinterpret_cast<const float2 *>(osh + g * OSTRIDE + 16 * ks + 2 * t4 + 8);
+      const __half2 h01 = __floats2half2_rn(x01.x, x01.y), h89 = __floats2half2_rn(x89.x, x89.y);
+      const float2 f01 = __half22float2(h01), f89 = __half22float2(h89);
+      const uint32_t bh0 = h2u(h01), bh1 = h2u(h89);
+      const uint32_t bl0 = pack_h2(x01.x - f01.x, x01.y - f01.y), bl1 = pack_h2(x89.x - f89.x, x89.y - f89.y);
+      mma16816(d, Ah, bh0, bh1);
+      mma16816(d, Ah, bl0, bl1);
+      mma16816(d, Al, bh0, bh1);
     }
-    const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-    const float Lh = Lsh[hh];
-    const float y = Lh > 0.f ? sum / (Lh * 11.3137084989847603904f) : 0.f;
+  }
+  if (kh == 1)
+    *reinterpret_cast<float4 *>(red + (mtl * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+  __syncthreads();
+  if (kh == 0 && got) {
+    const float4 e = *reinterpret_cast<const float4 *>(red + (mtl * 32 + lane) * 4);
+    const float y[4] = {d[0] + e.x, d[1] + e.y, d[2] + e.z, d[3] + e.w};
     const int session = unit / (a.L * a.Hkv);
     const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-    a.out[(((long long)session * a.L + layer) * a.Hq + kvh * gq + hh) * D + cb * CB_CH + lane] = __float2half_rn(y);
+    __half *ob = a.out + (((long long)session * a.L + layer) * a.Hq + kvh * gq) * D;
+    const int c = half * CB_CH + 16 * mtl + g;
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int h = 2 * t4 + (e2 & 1), cc = c + 8 * (e2 >> 1);
+      if (h < gq) ob[h * D + cc] = __float2half_rn(y[e2] * INV_SQRT_D);
+    }
   }
 }
 
@@ -898,7 +918,7 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
   if (a.units <= 0) return cudaSuccess;
   static bool attr_done = false;
-  const size_t smem = (MAXM * D * CB_CH + MAXGQ * MAXM * D) * sizeof(float);
+  const size_t smem = (size_t)4 * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + 4 * 32 * 4) * sizeof(float);
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

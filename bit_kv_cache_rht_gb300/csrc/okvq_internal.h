@@ -180,8 +180,9 @@ struct DecodeArgs {
 struct CombineArgs {
   const float *partials;
   const int *unit_seg;      // [units+1]
-  const float *rot;         // [L][Hkv][M][D][D] R[j][i]
+  const uint4 *rot_frag;    // R^T as mma A fragments: [L*Hkv][8 m-tiles][8*M k-steps][32 lanes][hi, lo]
   __half *out;              // [S][L][Hq][D]
+  uint32_t *err;
   int L, Hq, Hkv, M;
   long long units;
 };
