@@ -290,7 +290,7 @@ struct HalfPageCtx {
 // SINGLE: every token of the page has modality ma.cur (checked by the caller).
 template <int BITS, int G, bool FULLV, bool SINGLE>
 __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout &PL, const unsigned char *sp,
-                                          int tok0, int hp, float beta, uint32_t (&af)[8][4],
+                                          int tok0, int hp, float beta,
                                           float (&acc)[8][4], ModAcc &ma, float &m_run, float &l_run,
                                           const uint4 (&qreg)[8]) {
   constexpr int LANE_WORDS = BITS * 2;
@@ -298,30 +298,6 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   const int hs = tok0 + 32 * hp;
   float sacc[4][4];                           // n-tiles (tile, nt); rows [hi | lo]
   if (FULLV || hs < c.Tf) {
-    if ((32 * hp) % G == 0) {
-      // new group: a = q' o range as an exact fp16 pair (TwoProduct), fragments [a_hi ; a_lo]
-      const __half *rg = reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
-#pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
-        const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int kb = 2 * k2 + u;
-          const uint4 q = Cfg<BITS>::QREG ? qreg[kb] : c.qfrag[kb * 32 + lane];
-          const uint32_t qh[2] = {q.x, q.z}, ql[2] = {q.y, q.w};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const __half2 r2 = u2h(rr[2 * u + h]);
-            const __half2 hi = __hmul2(u2h(qh[h]), r2);
-            const __half2 er = __hfma2(u2h(qh[h]), r2, __hneg2(hi));
-            const __half2 lo = __hfma2(u2h(ql[h]), r2, er);
-            af[kb][2 * h] = h2u(hi);
-            af[kb][2 * h + 1] = h2u(lo);
-          }
-        }
-      }
-    }
 #pragma unroll
     for (int n = 0; n < 4; ++n) {
       sacc[n][0] = 0.f; sacc[n][1] = 0.f; sacc[n][2] = 0.f; sacc[n][3] = 0.f;
@@ -335,14 +311,35 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
             *reinterpret_cast<const uint4 *>(sp + (2 * hp + t) * PL.tile_bytes + lane * PL.lane_bytes + 4 * i);
         kw[t][i] = v4.x; kw[t][i + 1] = v4.y; kw[t][i + 2] = v4.z; kw[t][i + 3] = v4.w;
       }
+    // a = q' o range of this half page's group as an exact fp16 pair (TwoProduct),
+    // fragments [a_hi ; a_lo], built per 16-channel block right before its MMAs
+    const __half *rg = reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
 #pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {
+    for (int k2 = 0; k2 < 4; ++k2) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
+      const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        uint32_t bf[4];
-        key_frags<BITS>(kw[t], kb, c.lutlo, c.luthi, c.lut_k, c.laneoff, bf);
-        mma16816(sacc[2 * t + 0], af[kb], bf[0], bf[1]);
-        mma16816(sacc[2 * t + 1], af[kb], bf[2], bf[3]);
+      for (int u = 0; u < 2; ++u) {
+        const int kb = 2 * k2 + u;
+        const uint4 q = Cfg<BITS>::QREG ? qreg[kb] : c.qfrag[kb * 32 + lane];
+        const uint32_t qh[2] = {q.x, q.z}, ql[2] = {q.y, q.w};
+        uint32_t afk[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const __half2 r2 = u2h(rr[2 * u + h]);
+          const __half2 hi = __hmul2(u2h(qh[h]), r2);
+          const __half2 er = __hfma2(u2h(qh[h]), r2, __hneg2(hi));
+          const __half2 lo = __hfma2(u2h(ql[h]), r2, er);
+          afk[2 * h] = h2u(hi);
+          afk[2 * h + 1] = h2u(lo);
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint32_t bf[4];
+          key_frags<BITS>(kw[t], kb, c.lutlo, c.luthi, c.lut_k, c.laneoff, bf);
+          mma16816(sacc[2 * t + 0], afk, bf[0], bf[1]);
+          mma16816(sacc[2 * t + 1], afk, bf[2], bf[3]);
+        }
       }
     }
   } else {
@@ -626,9 +623,6 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
       }
     }
 
-    uint32_t af[8][4];       // score A fragments of the current group: [a_hi ; a_lo]
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb) af[kb][0] = af[kb][1] = af[kb][2] = af[kb][3] = 0u;
 
     for (int k = 0; k < my_n; ++k) {
       const int st = ring_st;
@@ -678,14 +672,14 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
         const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
         if (single) {
           if (hs + 32 <= Tf)
-            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
+            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
+            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
         } else {
           if (hs + 32 <= Tf)
-            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
+            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, beta, af, acc, ma, m_run, l_run, qreg);
+            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
         }
       }
       __syncwarp();
