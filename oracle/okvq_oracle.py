@@ -29,6 +29,13 @@ narrower precision so that both sides decide identically:
   in fp64; codes whose fp64 w lies within 1e-5 of a threshold are flagged as
   boundary codes (another correct implementation may round them the other way).
 
+TurboQuant key codec (the pages' comparison point, ``key_codec="turbo"``):
+every key is coded on arrival like a value, with the shared randomized Hadamard
+rotation instead of a modality eigenbasis (norm, direction rotated, fixed
+codebook, one global scale); no group statistics and no fp16 tail.  Value
+rotations are whatever the caller passes (the Hadamard rotation for every
+modality reproduces TurboQuant's single shared value rotation).
+
 Readings where the page is silent (codebook = Lloyd-Max levels for N(0,1)
 rounded once to fp16; keys use those levels renormalised to [0, 1]; values
 quantize sqrt(d) * R_m * v/|v| against the levels directly; groups aligned to
@@ -121,6 +128,12 @@ def rotate_f64(x: np.ndarray, signs: np.ndarray) -> np.ndarray:
     """(1/sqrt(d)) H D x in fp64 (used for the query, D1)."""
     d = x.shape[-1]
     return fwht(np.asarray(x, F64) * signs.astype(F64), F64) / math.sqrt(d)
+
+
+def hadamard_rotation(signs: np.ndarray) -> np.ndarray:
+    """The randomized Hadamard rotation (1/sqrt d) H D as an orthogonal matrix (rows = basis)."""
+    d = len(signs)
+    return sylvester_hadamard(d).astype(F64) * signs.astype(F64)[None, :] / math.sqrt(d)
 
 
 # ---------------------------------------------------------------------------
@@ -274,6 +287,18 @@ def quantize_values(v16: np.ndarray, R: np.ndarray, cb: Codebook):
     return n.astype(F16), codes, bnd, f16_near_midpoint(n)
 
 
+def quantize_keys_turbo(k16: np.ndarray, signs: np.ndarray, cb: Codebook):
+    """TurboQuant keys (section 2 METHOD, TurboQuant bullet): the magnitude n = |k|
+    is split from the direction, the direction is rotated by the randomized Hadamard
+    transform toward Gaussian-like coordinates and coded with the fixed codebook, one
+    global scale for every token (no per-window ranges).  Reading: exactly the value
+    codec with the shared rotation R = (1/sqrt d) H D, so w = sqrt(d) R k/|k| is
+    coded against the same levels.  Returns norm16, codes, code boundary mask, norm
+    boundary mask, like quantize_values.
+    """
+    return quantize_values(k16, hadamard_rotation(signs), cb)
+
+
 def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
     """Canonical packing along the last axis: 2-bit channel c at byte c//4 bits 2(c%4); 4-bit low nibble = even."""
     codes = np.asarray(codes, np.uint8)
@@ -298,7 +323,10 @@ class OracleUnit:
     """The cache of one (session, layer, kv head): append and decode, step by step."""
 
     def __init__(self, d: int, group_size: int, cb: Codebook, signs: np.ndarray, R: np.ndarray,
-                 q_per_kv: int, capacity: int):
+                 q_per_kv: int, capacity: int, key_codec: str = "omni"):
+        if key_codec not in ("omni", "turbo"):
+            raise ValueError("key_codec must be 'omni' (group min-max) or 'turbo' (norm + fixed scale)")
+        self.key_codec = key_codec
         self.d, self.G, self.cb, self.signs = d, group_size, cb, signs
         self.R = np.asarray(R, F32)                  # [M][d][d] as given to the codec
         self.q_per_kv = q_per_kv
@@ -309,6 +337,8 @@ class OracleUnit:
         self.kmn = np.zeros((-(-cap // group_size), d), F16)
         self.krg = np.zeros_like(self.kmn)
         self.keys16 = np.zeros((cap, d), F16)          # fp16 inputs kept for the trailing (tail) group
+        self.knorm = np.zeros(cap, F16)                # turbo keys: |k|
+        self.knbnd = np.zeros(cap, bool)
         self.vcodes = np.zeros((cap, d), np.uint8)
         self.vbnd = np.zeros((cap, d), bool)
         self.vnorm = np.zeros(cap, F16)
@@ -317,7 +347,8 @@ class OracleUnit:
 
     @property
     def T_full(self) -> int:
-        return (self.T // self.G) * self.G
+        """Tokens whose keys are quantized (turbo keys are quantized on arrival)."""
+        return self.T if self.key_codec == "turbo" else (self.T // self.G) * self.G
 
     def append(self, K16: np.ndarray, V16: np.ndarray, mod: np.ndarray):
         """Append n tokens: values quantized now; each key group once it is complete."""
@@ -334,6 +365,11 @@ class OracleUnit:
             self.vcodes[t0 + sel] = codes
             self.vbnd[t0 + sel] = bnd
             self.nbnd[t0 + sel] = nb
+        if self.key_codec == "turbo":
+            nrm, codes, bnd, nb = quantize_keys_turbo(K16, self.signs, self.cb)
+            self.knorm[t0:t1], self.kcodes[t0:t1], self.kbnd[t0:t1], self.knbnd[t0:t1] = nrm, codes, bnd, nb
+            self.T = t1
+            return
         G = self.G
         for g in range(t0 // G, t1 // G):
             kp = rotate_keys_f32(self.keys16[g * G:(g + 1) * G], self.signs)
@@ -347,6 +383,17 @@ class OracleUnit:
     def export(self) -> dict:
         T, Tf, G = self.T, self.T_full, self.G
         b = self.cb.bits
+        if self.key_codec == "turbo":
+            return {
+                "kcodes": pack_codes(self.kcodes[:T], b),
+                "knorm": self.knorm[:T].copy(),
+                "vcodes": pack_codes(self.vcodes[:T], b),
+                "vnorm": self.vnorm[:T].copy(),
+                "kbnd": self.kbnd[:T].copy(),
+                "knbnd": self.knbnd[:T].copy(),
+                "vbnd": self.vbnd[:T].copy(),
+                "nbnd": self.nbnd[:T].copy(),
+            }
         return {
             "kcodes": pack_codes(self.kcodes[:Tf], b),
             "kstats": np.stack([self.kmn[:Tf // G], self.krg[:Tf // G]], axis=1),   # [T/G][2][d] (min, range)
@@ -376,7 +423,10 @@ class OracleUnit:
         q = q16.astype(F64)
         qr = rotate_f64(q, self.signs) / math.sqrt(d)                       # [Gq][d]
         s = np.empty((Gq, T), F64)
-        if Tf:
+        if self.key_codec == "turbo":
+            # k' = (n / sqrt d) l(code) in the rotated domain: s_t = (n_t / sqrt d) q' . l(code_t)
+            s[:] = (qr @ self.cb.levels[self.kcodes[:T]].T) * (self.knorm[:T].astype(F64) / math.sqrt(d))[None]
+        elif Tf:
             ng = Tf // G
             mn = self.kmn[:ng].astype(F64)
             dl = self.krg[:ng].astype(F64)
@@ -405,7 +455,12 @@ class OracleUnit:
         d, G, T, Tf = self.d, self.G, self.T, self.T_full
         H = sylvester_hadamard(d).astype(F64)
         Kh = np.empty((T, d), F64)
-        if Tf:
+        if self.key_codec == "turbo":
+            Rh = hadamard_rotation(self.signs)
+            lk = self.cb.levels[self.kcodes[:T]] / math.sqrt(d)
+            Kh[:] = (lk @ Rh) * self.knorm[:T].astype(F64)[:, None]               # n R^T l / sqrt d
+            Tf = T
+        elif Tf:
             g = np.arange(Tf) // G
             mn = self.kmn[g].astype(F64)
             rg = self.krg[g].astype(F64)
@@ -436,7 +491,8 @@ class OracleCache:
     """All units of a multi-session cache; mirrors the library's create/append/decode/export."""
 
     def __init__(self, num_sessions, num_layers, num_q_heads, num_kv_heads, head_dim, group_size, bits,
-                 max_tokens, hadamard_seed, value_rot, codebook_levels=None, layers=None, num_modalities=3):
+                 max_tokens, hadamard_seed, value_rot, codebook_levels=None, layers=None, num_modalities=3,
+                 key_codec="omni"):
         self.S, self.L, self.Hq, self.Hkv, self.d = num_sessions, num_layers, num_q_heads, num_kv_heads, head_dim
         self.G, self.bits, self.M = group_size, bits, num_modalities
         self.cb = make_codebook(bits, codebook_levels)
@@ -448,7 +504,7 @@ class OracleCache:
             for l in self.layers:
                 for h in range(num_kv_heads):
                     self.units[(s, l, h)] = OracleUnit(head_dim, group_size, self.cb, self.signs, R[l, h],
-                                                       num_q_heads // num_kv_heads, max_tokens)
+                                                       num_q_heads // num_kv_heads, max_tokens, key_codec)
 
     def append(self, session, K16, V16, mod, layers_in=None):
         """K16, V16 [T][L'][Hkv][d] where L' indexes ``layers_in`` (default: self.layers)."""
