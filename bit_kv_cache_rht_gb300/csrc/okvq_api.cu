@@ -15,6 +15,7 @@ using namespace okvq;
 struct okvq_cache {
   okvq_config cfg{};
   int S = 0, L = 0, Hq = 0, Hkv = 0, G = 0, bits = 0, M = 0;
+  int KG = 0;                   // kernels' group size: G, or 0 for TurboQuant keys
   long long max_tokens = 0, P_max = 0, cap = 0, units = 0;
   PageLayout PL{};
   int num_sms = 0, device = 0;
@@ -236,6 +237,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if (c.group_size != 32 && c.group_size != 64) return OKVQ_EINVAL;
   if (c.bits != 2 && c.bits != 4) return OKVQ_EINVAL;
   if (c.num_modalities < 1 || c.num_modalities > MAXM) return OKVQ_EINVAL;
+  if (c.key_codec != OKVQ_KEYS_GROUP_RANGE && c.key_codec != OKVQ_KEYS_TURBOQUANT) return OKVQ_EINVAL;
   if (c.max_tokens < 1 || c.max_tokens > (1ll << 31) - PAGE) return OKVQ_EINVAL;   // token indices are 32-bit
   if (!c.value_rot) return OKVQ_EINVAL;
   const int nlev = 1 << c.bits;
@@ -265,7 +267,8 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   h->P_max = (c.max_tokens + PAGE - 1) / PAGE;
   h->cap = h->P_max * PAGE;
   h->units = (long long)h->S * h->L * h->Hkv;
-  h->PL = page_layout(h->bits, h->G);
+  h->KG = c.key_codec == OKVQ_KEYS_TURBOQUANT ? 0 : h->G;
+  h->PL = page_layout(h->bits, h->KG);
   h->len.assign(h->S, 0);
   h->tail_sel.assign(h->S, 0);
   // codebook: the fp16-rounded levels define it (values); key levels renormalised to [0, 1]
@@ -406,7 +409,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   a.Hkv = h->Hkv;
   a.M = h->M;
   a.bits = h->bits;
-  a.G = h->G;
+  a.G = h->KG;
   a.P_max = h->P_max;
   a.pages = h->pages;
   const size_t tail_buf = (size_t)h->units * h->G * D;
@@ -460,14 +463,14 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
   a.Hkv = h->Hkv;
   a.M = h->M;
   a.bits = h->bits;
-  a.G = h->G;
+  a.G = h->KG;
   a.P_max = h->P_max;
   a.cap = h->cap;
   a.units = h->units;
   a.signs = h->signs;
   a.err = h->err;
   for (int j = 0; j < 16; ++j) {
-    a.klut_src[j] = h->klev16[j];
+    a.klut_src[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
     a.vlut_src[j] = h->levels16[j];
   }
   CombineArgs cb{};
@@ -536,14 +539,14 @@ okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, 
   a.Hkv = h->Hkv;
   a.M = h->M;
   a.bits = h->bits;
-  a.G = h->G;
+  a.G = h->KG;
   a.P_max = h->P_max;
   a.cap = h->cap;
   a.units = h->units;
   a.signs = h->signs;
   a.err = h->err;
   for (int j = 0; j < 16; ++j) {
-    a.klut_src[j] = h->klev16[j];
+    a.klut_src[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
     a.vlut_src[j] = h->levels16[j];
   }
   CombineArgs cb{};
@@ -608,10 +611,13 @@ okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, si
   if (!h || !bytes || session < 0 || session >= h->S) return OKVQ_EINVAL;
   const long long T = h->len[session];
   const int G = h->G, bits = h->bits;
-  const long long Tf = (T / G) * G;
+  const bool turbo = h->KG == 0;
+  const long long Tf = turbo ? T : (T / G) * G;
   const int B = D * bits / 8;
   const long long LH = (long long)h->L * h->Hkv;
-  const size_t n_kc = (size_t)LH * Tf * B, n_ks = (size_t)LH * (Tf / G) * 2 * D * 2,
+  // TurboQuant keys: knorm [LH][T] fp16 in the kstats slot, no tail
+  const size_t n_kc = (size_t)LH * Tf * B,
+               n_ks = turbo ? (size_t)LH * T * 2 : (size_t)LH * (Tf / G) * 2 * D * 2,
                n_kt = (size_t)LH * (T - Tf) * D * 2, n_vc = (size_t)LH * T * B, n_vn = (size_t)LH * T * 2,
                n_md = (size_t)T;
   const size_t need = n_kc + n_ks + n_kt + n_vc + n_vn + n_md;
@@ -664,7 +670,11 @@ okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, si
       }
       std::memcpy(o_vn + (lh * T + t) * 2, p + PL.off_norm + tt * 2, 2);
     }
-    for (long long gi = 0; gi < Tf / G; ++gi) {
+    if (turbo) {
+      for (long long t = 0; t < T; ++t)
+        std::memcpy(o_ks + (lh * T + t) * 2, pg.data() + (t / PAGE) * PL.page_bytes + PL.off_stats + (t % PAGE) * 2, 2);
+    }
+    for (long long gi = 0; !turbo && gi < Tf / G; ++gi) {
       const uint8_t *p = pg.data() + ((gi * G) / PAGE) * PL.page_bytes + PL.off_stats + ((gi * G) % PAGE) / G * 2 * D * 2;
       const __half *st = reinterpret_cast<const __half *>(p);
       __half *dst = reinterpret_cast<__half *>(o_ks) + (lh * (Tf / G) + gi) * 2 * D;

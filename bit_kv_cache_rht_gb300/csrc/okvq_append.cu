@@ -43,6 +43,29 @@ __device__ __forceinline__ int code_of(float x, const float *thr, int nthr) {
   return c;
 }
 
+// Canonical fp32 key rotation of one token, warp-wide: lane holds channels
+// 4*lane .. 4*lane+3 of k' = fp32(1/sqrt d) * FWHT(s o k) (butterfly strides 1 and 2
+// inside the lane, 4 .. 64 across lanes, round-to-nearest adds, no contraction).
+__device__ __forceinline__ void rotate_key_row(const __half *src, const float *signs, int lane, float (&x)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = __half2float(src[4 * lane + j]) * signs[4 * lane + j];
+  float y0 = __fadd_rn(x[0], x[1]), y1 = __fsub_rn(x[0], x[1]);
+  float y2 = __fadd_rn(x[2], x[3]), y3 = __fsub_rn(x[2], x[3]);
+  x[0] = __fadd_rn(y0, y2); x[2] = __fsub_rn(y0, y2);
+  x[1] = __fadd_rn(y1, y3); x[3] = __fsub_rn(y1, y3);
+#pragma unroll
+  for (int sm = 1; sm < 32; sm <<= 1) {
+    const bool upper = (lane & sm) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float p = __shfl_xor_sync(0xffffffffu, x[j], sm);
+      x[j] = upper ? __fsub_rn(p, x[j]) : __fadd_rn(x[j], p);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = __fmul_rn(x[j], INV_SQRT_D);
+}
+
 // Pack the codes of tile `tile` (16 tokens) from codes[64][128] into lane chunks.
 // `kind` 0 = K layout, 1 = V layout. Tokens >= valid_end (page-relative) pack as 0.
 __device__ void pack_tile(const uint8_t *codes, uint8_t *dst, int tile, int bits, int kind, int valid_end,
@@ -200,6 +223,36 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   for (int tile = ta / TILE; tile * TILE < tb; ++tile)
     pack_tile(S.vc, pg + PL.off_v + tile * PL.tile_bytes, tile, a.bits, 1, tb, tid, THREADS);
 
+  if (a.G == 0) {
+    // ---- TurboQuant keys (section 2, TurboQuant bullet): every new token now, like a
+    // value with the shared Hadamard rotation: n = |k|, w = sqrt(d) k'/n, value levels ----
+    __syncthreads();
+    // keep the codes of older tokens that share a 16-token tile with the first new token
+    if (ta % TILE != 0) unpack_tile(S.kc, pg + (ta / TILE) * PL.tile_bytes, ta / TILE, a.bits, 0, ta, tid, THREADS);
+    for (int t = ta + warp; t < tb; t += THREADS / 32) {
+      const __half *src = a.k + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float v = __half2float(src[4 * lane + j]);
+        ss = fmaf(v, v, ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float n = sqrtf(ss);
+      float x[4];
+      rotate_key_row(src, a.signs, lane, x);
+      const float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) S.kc[t * D + 4 * lane + j] = (uint8_t)code_of(x[j] * sc, a.vthr, a.nlev - 1);
+      if (lane == 0) reinterpret_cast<__half *>(pg + PL.off_stats)[t] = __float2half_rn(n);
+    }
+    __syncthreads();
+    for (int tile = ta / TILE; tile * TILE < tb; ++tile)
+      pack_tile(S.kc, pg + tile * PL.tile_bytes, tile, a.bits, 0, tb, tid, THREADS);
+    return;                       // no key groups, no fp16 tail
+  }
+
   // ---- keys: groups that complete with this chunk ----
   const int G = a.G;
   float *xk = S.xt;               // keys as [token][c], row stride D
@@ -217,26 +270,8 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       const __half *src = t < T0 ? told + (t - (P0 + g0)) * D
                                  : a.k + (t - T0) * (long long)row_stride + (long long)lh * D;
       float x[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) x[j] = __half2float(src[4 * lane + j]) * a.signs[4 * lane + j];
-      // stride 1 and 2 inside the lane
-      float y0 = __fadd_rn(x[0], x[1]), y1 = __fsub_rn(x[0], x[1]);
-      float y2 = __fadd_rn(x[2], x[3]), y3 = __fsub_rn(x[2], x[3]);
-      x[0] = __fadd_rn(y0, y2); x[2] = __fsub_rn(y0, y2);
-      x[1] = __fadd_rn(y1, y3); x[3] = __fsub_rn(y1, y3);
-      // strides 4 .. 64 across lanes
-#pragma unroll
-      for (int sm = 1; sm < 32; sm <<= 1) {
-        const bool upper = (lane & sm) != 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float p = __shfl_xor_sync(0xffffffffu, x[j], sm);
-          x[j] = upper ? __fsub_rn(p, x[j]) : __fadd_rn(x[j], p);
-        }
-      }
-      float4 o = make_float4(__fmul_rn(x[0], INV_SQRT_D), __fmul_rn(x[1], INV_SQRT_D), __fmul_rn(x[2], INV_SQRT_D),
-                             __fmul_rn(x[3], INV_SQRT_D));
-      *reinterpret_cast<float4 *>(&xk[(g0 + r) * D + 4 * lane]) = o;
+      rotate_key_row(src, a.signs, lane, x);
+      *reinterpret_cast<float4 *>(&xk[(g0 + r) * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
     }
     __syncthreads();
     // per-channel statistics of the group: min rounded down, range rounded up

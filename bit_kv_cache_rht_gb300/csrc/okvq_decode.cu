@@ -294,6 +294,8 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
                                           float (&acc)[8][4], ModAcc &ma, float &m_run, float &l_run,
                                           const uint4 (&qreg)[8]) {
   constexpr int LANE_WORDS = BITS * 2;
+  constexpr bool KT = G == 0;                 // TurboQuant keys: per-token norms, no groups
+  constexpr int GG = KT ? PAGE : G;
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int hs = tok0 + 32 * hp;
   float sacc[4][4];                           // n-tiles (tile, nt); rows [hi | lo]
@@ -312,20 +314,22 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
         kw[t][i] = v4.x; kw[t][i + 1] = v4.y; kw[t][i + 2] = v4.z; kw[t][i + 3] = v4.w;
       }
     // a = q' o range of this half page's group as an exact fp16 pair (TwoProduct),
-    // fragments [a_hi ; a_lo], built per 16-channel block right before its MMAs
-    const __half *rg = reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / G) * 2 * D * 2 + D * 2);
+    // fragments [a_hi ; a_lo], built per 16-channel block right before its MMAs.
+    // TurboQuant keys have no ranges: a = q' itself.
+    const __half *rg = reinterpret_cast<const __half *>(sp + PL.off_stats + ((32 * hp) / GG) * 2 * D * 2 + D * 2);
 #pragma unroll
     for (int k2 = 0; k2 < 4; ++k2) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (!KT) v = *reinterpret_cast<const uint4 *>(rg + 32 * k2 + 8 * t4);
       const uint32_t rr[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int kb = 2 * k2 + u;
         const uint4 q = Cfg<BITS>::QREG ? qreg[kb] : c.qfrag[kb * 32 + lane];
         const uint32_t qh[2] = {q.x, q.z}, ql[2] = {q.y, q.w};
-        uint32_t afk[4];
+        uint32_t afk[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2 && !KT; ++h) {
           const __half2 r2 = u2h(rr[2 * u + h]);
           const __half2 hi = __hmul2(u2h(qh[h]), r2);
           const __half2 er = __hfma2(u2h(qh[h]), r2, __hneg2(hi));
@@ -370,13 +374,19 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   // scores of head g for tokens hs + 8n + 2*t4 + e
   float s[4][2];
 #pragma unroll
-  for (int n = 0; n < 4; ++n)
+  for (int n = 0; n < 4; ++n) {
+    // TurboQuant keys: k' = (n_t / sqrt d) l(code), so the token's norm scales its score
+    float2 kn = make_float2(1.f, 1.f);
+    if (KT)
+      kn = __half22float2(*reinterpret_cast<const __half2 *>(sp + PL.off_stats + 2 * (32 * hp + 8 * n + 2 * t4)));
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       // the group offset joins after the MMA chain (it does not wait for it)
-      const float v = sacc[n][e] + sacc[n][2 + e] + ((FULLV || hs < c.Tf) ? beta : 0.f);
+      const float v = KT ? (sacc[n][e] + sacc[n][2 + e]) * ((e ? kn.y : kn.x) * INV_SQRT_D)
+                         : sacc[n][e] + sacc[n][2 + e] + ((FULLV || hs < c.Tf) ? beta : 0.f);
       s[n][e] = (FULLV || hs + 8 * n + 2 * t4 + e < c.T) ? v : -INFINITY;
     }
+  }
 
   // ---- online softmax (base 2) for head g ----
   float mx = s[0][0];
@@ -542,7 +552,9 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     const int lh = unit % (a.L * a.Hkv);
     const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
     const int T = (int)a.unit_len[unit];
-    const int Tf = (T / G) * G;
+    constexpr bool KT = G == 0;               // TurboQuant keys: all quantized, no groups
+    constexpr int GG = KT ? PAGE : G;
+    const int Tf = KT ? T : (T / GG) * GG;
     const unsigned char *unit_pages = a.pages + (long long)unit * a.P_max * PL.page_bytes;
     const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
 
@@ -641,12 +653,12 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
 
       // group offsets beta(head g, group) = q' . min for the page's groups (tensor cores)
       float beta_g0 = 0.f, beta_g1 = 0.f;
-      if (tok0 < Tf) {
+      if (!KT && tok0 < Tf) {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
           uint32_t b0 = 0u, b1 = 0u;
-          if (g < PAGE / G) {
+          if (g < PAGE / GG) {
             const __half *mn = reinterpret_cast<const __half *>(sp + PL.off_stats + g * 2 * D * 2);
             const uint2 v = *reinterpret_cast<const uint2 *>(mn + 32 * (kb >> 1) + 8 * t4 + 4 * (kb & 1));
             b0 = v.x;
@@ -903,6 +915,7 @@ size_t decode_smem_bytes(int bits, int G) { return bits == 2 ? decode_smem_bytes
 
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
   if (n_cta <= 0) return cudaSuccess;
+  if (a.G == 0) return a.bits == 2 ? launch_decode_t<2, 0>(a, n_cta, s) : launch_decode_t<4, 0>(a, n_cta, s);
   if (a.bits == 2 && a.G == 32) return launch_decode_t<2, 32>(a, n_cta, s);
   if (a.bits == 2 && a.G == 64) return launch_decode_t<2, 64>(a, n_cta, s);
   if (a.bits == 4 && a.G == 32) return launch_decode_t<4, 32>(a, n_cta, s);

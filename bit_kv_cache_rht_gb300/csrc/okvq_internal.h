@@ -9,6 +9,7 @@
 //     V codes  same shape
 //     norms    64 fp16, token order
 //     stats    64/G groups, each [min 128 fp16 | range 128 fp16] in the stat channel order
+//              (TurboQuant keys, G = 0 below: 64 fp16 key norms, token order)
 //     tmask    4 bytes, bit m of byte i set when tile i holds a token of modality m,
 //              then 12 bytes of padding (page size stays a multiple of 16 B)
 //   so one decode warp streams one contiguous block per page with a single bulk copy.
@@ -68,6 +69,7 @@ struct PageLayout {
   int page_bytes;
 };
 
+// G = 0 selects TurboQuant keys: per-token key norms instead of group statistics.
 __host__ __device__ inline PageLayout page_layout(int bits, int G) {
   PageLayout L;
   L.bits = bits;
@@ -77,7 +79,7 @@ __host__ __device__ inline PageLayout page_layout(int bits, int G) {
   L.off_v = 4 * L.tile_bytes;
   L.off_norm = 2 * L.off_v;
   L.off_stats = L.off_norm + PAGE * 2;
-  L.off_tmask = L.off_stats + (PAGE / G) * 2 * D * 2;
+  L.off_tmask = L.off_stats + (G ? (PAGE / G) * 2 * D * 2 : PAGE * 2);
   L.page_bytes = L.off_tmask + 16;
   return L;
 }
@@ -141,7 +143,7 @@ struct AppendArgs {
   int n;                    // tokens in this chunk
   long long T0;             // session length before the append
   int session;
-  int L, Hkv, M, bits, G;
+  int L, Hkv, M, bits, G;   // G: key group size, 0 = TurboQuant keys (per-token norms)
   long long P_max;
   uint8_t *pages;           // all units
   __half *tail_old;         // [units][G][D] buffer read (current)
@@ -167,7 +169,7 @@ struct DecodeArgs {
   const long long *unit_len;// [units] token count
   const int *unit_tail;     // [units] 0/1 current tail buffer
   float *partials;          // [nseg][MAXGQ][2 + MAXM*D]
-  int L, Hq, Hkv, M, bits, G;
+  int L, Hq, Hkv, M, bits, G;   // G: key group size, 0 = TurboQuant keys
   long long P_max, cap;
   long long units;
   uint64_t unused;

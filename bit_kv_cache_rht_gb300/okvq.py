@@ -17,7 +17,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libokvq.so")
 
 OKVQ_OK, OKVQ_EINVAL, OKVQ_ENOMEM, OKVQ_ECAPACITY, OKVQ_ECUDA, OKVQ_ESTATE, OKVQ_ESCRATCH = range(7)
-OKVQ_STATIC_SCRATCH_SEGMENTS = 512   # work-list segments held by okvq_decode_static_scratch's array
+OKVQ_STATIC_SCRATCH_SEGMENTS = 512
+OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT = 0, 1   # key codecs (okvq_config.key_codec)   # work-list segments held by okvq_decode_static_scratch's array
 
 # every function the header declares (checked against include/okvq.h by the tests)
 EXPORTS = (
@@ -41,6 +42,7 @@ class OkvqConfig(ctypes.Structure):
         ("hadamard_seed", ctypes.c_uint64),
         ("codebook", ctypes.POINTER(ctypes.c_float)),
         ("value_rot", ctypes.POINTER(ctypes.c_float)),
+        ("key_codec", ctypes.c_int32),
     ]
 
 
@@ -144,7 +146,7 @@ class Cache:
     def __init__(self, num_sessions: int, num_layers: int, num_q_heads: int, num_kv_heads: int, max_tokens: int,
                  value_rot: np.ndarray, head_dim: int = 128, group_size: int = 32, bits: int = 2,
                  num_modalities: int = 3, hadamard_seed: int = 0, codebook: Optional[np.ndarray] = None,
-                 stream=None):
+                 stream=None, key_codec: int = OKVQ_KEYS_GROUP_RANGE):
         self._h = None
         R = np.ascontiguousarray(value_rot, dtype=np.float32)
         expect = (num_layers, num_kv_heads, num_modalities, head_dim, head_dim)
@@ -158,13 +160,14 @@ class Cache:
         cfg = OkvqConfig(num_sessions, num_layers, num_q_heads, num_kv_heads, head_dim, group_size, bits,
                          num_modalities, max_tokens, hadamard_seed & ((1 << 64) - 1),
                          cb.ctypes.data_as(ctypes.POINTER(ctypes.c_float)) if cb is not None else None,
-                         R.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+                         R.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), int(key_codec))
         st, h = okvq_create(cfg, _stream_handle(stream))
         _check(st, "okvq_create")
         self._h = h
         self.num_sessions, self.num_layers = num_sessions, num_layers
         self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
         self.group_size, self.bits, self.num_modalities, self.max_tokens = group_size, bits, num_modalities, max_tokens
+        self.key_codec = int(key_codec)
 
     def close(self):
         if self._h is not None:
@@ -255,7 +258,8 @@ class Cache:
                "okvq_export_state")
         T = self.length(session)
         G, d = self.group_size, self.head_dim
-        Tf = (T // G) * G
+        turbo = self.key_codec == OKVQ_KEYS_TURBOQUANT
+        Tf = T if turbo else (T // G) * G
         B = d * self.bits // 8
         LH = (self.num_layers, self.num_kv_heads)
         out, off = {}, 0
@@ -268,8 +272,11 @@ class Cache:
 
         n = LH[0] * LH[1]
         take("kcodes", n * Tf * B, np.uint8, (*LH, Tf, B))
-        take("kstats", n * (Tf // G) * 2 * d, np.float16, (*LH, Tf // G, 2, d))
-        take("ktail", n * (T - Tf) * d, np.float16, (*LH, T - Tf, d))
+        if turbo:
+            take("knorm", n * T, np.float16, (*LH, T))
+        else:
+            take("kstats", n * (Tf // G) * 2 * d, np.float16, (*LH, Tf // G, 2, d))
+            take("ktail", n * (T - Tf) * d, np.float16, (*LH, T - Tf, d))
         take("vcodes", n * T * B, np.uint8, (*LH, T, B))
         take("vnorm", n * T, np.float16, (*LH, T))
         take("mod", T, np.uint8, (T,))

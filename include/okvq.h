@@ -73,6 +73,17 @@ typedef enum {
                          OKVQ_STATIC_SCRATCH_SEGMENTS segments; nothing was launched */
 } okvq_status;
 
+/* Key codec (okvq_config.key_codec). */
+typedef enum {
+  OKVQ_KEYS_GROUP_RANGE = 0, /* OmniKVQuant: per-group min-max of the rotated keys (section 2,
+                                first OmniKVQuant bullet); the default */
+  OKVQ_KEYS_TURBOQUANT = 1   /* TurboQuant, the pages' comparison point (section 2, TurboQuant
+                                bullet): each key coded on arrival like a value, with the
+                                shared randomized Hadamard rotation: n = |k| stored fp16,
+                                w = sqrt(d) * (1/sqrt d) H D k/n coded with the value levels;
+                                one global scale, no group statistics, no fp16 tail */
+} okvq_key_codec;
+
 typedef struct {
   int32_t num_sessions;   /* independent streams held by the cache, >= 1 */
   int32_t num_layers;     /* >= 1 */
@@ -88,7 +99,10 @@ typedef struct {
                              copied at create */
   const float *value_rot; /* host, fp32 [num_layers][num_kv_heads][num_modalities][128][128],
                              row-major, row i = i-th basis vector; should be orthogonal (not
-                             checked); copied at create */
+                             checked); copied at create. TurboQuant's single shared value
+                             rotation is the Hadamard rotation (1/sqrt d) H D for every m. */
+  int32_t key_codec;      /* okvq_key_codec; 0 (zero-initialised configs) = OmniKVQuant keys.
+                             With OKVQ_KEYS_TURBOQUANT group_size is validated but unused. */
 } okvq_config;
 
 /* Allocate a cache. Validates cfg (OKVQ_EINVAL), allocates device storage
@@ -166,6 +180,8 @@ okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
  *   vcodes  uint8 [L][Hkv][T][B]
  *   vnorm   fp16  [L][Hkv][T]
  *   mod     uint8 [T]
+ * With OKVQ_KEYS_TURBOQUANT every key is quantized (Tf = T) and kstats/ktail
+ * are replaced by knorm fp16 [L][Hkv][T] (|k|).
  * *bytes must hold the buffer size on entry (OKVQ_EINVAL if too small). */
 okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, size_t *bytes);
 

@@ -18,12 +18,13 @@ def ensure_built():
     return okvq.load()
 
 
-def oracle_cache(w, layers=None, sessions=None):
+def oracle_cache(w, layers=None, sessions=None, key_codec="omni", R=None):
     sh = w.shape
     layers = list(range(sh.num_layers)) if layers is None else list(layers)
-    R = w.value_rotations()
+    R = w.value_rotations() if R is None else R
     return o.OracleCache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
-                         sh.group_size, sh.bits, w.max_tokens, w.hadamard_seed, R, layers=layers), R
+                         sh.group_size, sh.bits, w.max_tokens, w.hadamard_seed, R, layers=layers,
+                         key_codec=key_codec), R
 
 
 def feed_oracle(oc, w, bounds=None, layers=None, sessions=None):
@@ -37,7 +38,7 @@ def feed_oracle(oc, w, bounds=None, layers=None, sessions=None):
             oc.append(s, K[a:b], V[a:b], mod[a:b], layers_in=layers)
 
 
-def gpu_cache(w, R=None, bounds=None, sessions=None, max_tokens=None):
+def gpu_cache(w, R=None, bounds=None, sessions=None, max_tokens=None, key_codec=0):
     import torch
     from bit_kv_cache_rht_gb300.okvq import Cache
     sh = w.shape
@@ -45,7 +46,7 @@ def gpu_cache(w, R=None, bounds=None, sessions=None, max_tokens=None):
     c = Cache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads,
               w.max_tokens if max_tokens is None else max_tokens, R, head_dim=sh.head_dim,
               group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
-              hadamard_seed=w.hadamard_seed)
+              hadamard_seed=w.hadamard_seed, key_codec=key_codec)
     sessions = range(len(w.sessions)) if sessions is None else sessions
     for s in sessions:
         K, V = w.session_kv(s)
@@ -67,10 +68,18 @@ def compare_state(gpu_state: dict, oc, session: int, layers_gpu_index, bits: int
     (must be 0) for keys/values/norms, plus stats/tail/mod equality flags."""
     res = dict(k_strict=0, k_bnd=0, v_strict=0, v_bnd=0, n_strict=0, n_bnd=0, stats_ok=True, tail_ok=True,
                mod_ok=True, k_codes=0, v_codes=0)
+    turbo = "knorm" in gpu_state
     for i, l in enumerate(oc.layers):
         li = layers_gpu_index[i]
         for h in range(oc.Hkv):
             e = oc.units[(session, l, h)].export()
+            if turbo:
+                # per-token key norms: fp16 round-to-nearest of |k|, one ulp allowed at a midpoint
+                gn, on = gpu_state["knorm"][li, h], e["knorm"]
+                nd = gn.view(np.uint16) != on.view(np.uint16)
+                one_ulp = np.abs(gn.view(np.uint16).astype(np.int32) - on.view(np.uint16).astype(np.int32)) <= 1
+                res["n_strict"] += int(np.sum(nd & ~(e["knbnd"] & one_ulp)))
+                res["n_bnd"] += int(np.sum(nd & e["knbnd"] & one_ulp))
             gk = o.unpack_codes(gpu_state["kcodes"][li, h], bits)
             ok_ = o.unpack_codes(e["kcodes"], bits)
             diff = gk != ok_
@@ -88,6 +97,8 @@ def compare_state(gpu_state: dict, oc, session: int, layers_gpu_index, bits: int
             one_ulp = np.abs(gn.view(np.uint16).astype(np.int32) - on.view(np.uint16).astype(np.int32)) <= 1
             res["n_strict"] += int(np.sum(nd & ~(e["nbnd"] & one_ulp)))
             res["n_bnd"] += int(np.sum(nd & e["nbnd"] & one_ulp))
+            if turbo:
+                continue
             if not np.array_equal(gpu_state["kstats"][li, h].view(np.uint16), e["kstats"].view(np.uint16)):
                 res["stats_ok"] = False
             if not np.array_equal(gpu_state["ktail"][li, h].view(np.uint16), e["ktail"].view(np.uint16)):
@@ -96,6 +107,30 @@ def compare_state(gpu_state: dict, oc, session: int, layers_gpu_index, bits: int
     if not np.array_equal(gpu_state["mod"], oc.units[(session, oc.layers[0], 0)].mod[:T]):
         res["mod_ok"] = False
     return res
+
+
+def adopt_boundary_choices(gpu_state: dict, oc, session: int, layers_gpu_index):
+    """Where the oracle flags a code (or a norm) as a boundary case, take the GPU's
+    choice into the oracle unit, so that the decode outputs are compared on the same
+    encoding.  Both choices are correct encodings; everything else stays the oracle's
+    own and must already match bit for bit (assert_state_matches)."""
+    turbo = "knorm" in gpu_state
+    for i, l in enumerate(oc.layers):
+        li = layers_gpu_index[i]
+        for h in range(oc.Hkv):
+            u = oc.units[(session, l, h)]
+            T, Tf = u.T, u.T_full
+            gk = o.unpack_codes(gpu_state["kcodes"][li, h], u.cb.bits)
+            sel = u.kbnd[:Tf] & (gk != u.kcodes[:Tf])
+            u.kcodes[:Tf][sel] = gk[sel]
+            gv = o.unpack_codes(gpu_state["vcodes"][li, h], u.cb.bits)
+            sel = u.vbnd[:T] & (gv != u.vcodes[:T])
+            u.vcodes[:T][sel] = gv[sel]
+            sel = u.nbnd[:T]
+            u.vnorm[:T][sel] = gpu_state["vnorm"][li, h][sel]
+            if turbo:
+                sel = u.knbnd[:T]
+                u.knorm[:T][sel] = gpu_state["knorm"][li, h][sel]
 
 
 def assert_state_matches(res):

@@ -64,6 +64,14 @@ def test_create_rejects_bad_configs_before_cuda(lib, bad):
     assert st == okvq.OKVQ_EINVAL and not h.value
 
 
+def test_create_rejects_unknown_key_codec(lib):
+    from bit_kv_cache_rht_gb300 import okvq
+    cfg, _keep = _cfg()
+    cfg.key_codec = 2
+    st, h = okvq.okvq_create(cfg)
+    assert st == okvq.OKVQ_EINVAL and not h.value
+
+
 def test_create_rejects_non_ascending_codebook(lib):
     from bit_kv_cache_rht_gb300 import okvq
     cfg, _keep = _cfg()

@@ -27,8 +27,9 @@ def _full_check(w, bounds=None, layers_check=None, steps=(0,)):
     assert c.check_errors() == 0
     li = oc.layers
     for s in range(len(w.sessions)):
-        res = pu.compare_state(c.export_state(s), oc, s, li, w.shape.bits)
-        pu.assert_state_matches(res)
+        st = c.export_state(s)
+        pu.assert_state_matches(pu.compare_state(st, oc, s, li, w.shape.bits))
+        pu.adopt_boundary_choices(st, oc, s, li)
     errs = []
     for step in steps:
         Q = w.queries(step)
@@ -149,3 +150,48 @@ def test_decode_is_repeatable_and_query_dependent():
     assert np.array_equal(a, b)
     q2 = torch.from_numpy(w.queries(1)).cuda()
     assert not np.array_equal(a, c.decode(q2).cpu().numpy())
+
+
+# ---------------------------------------------------------------- TurboQuant key codec
+
+def _turbo_check(w, bounds=None, steps=(0,), shared_rotation=False):
+    import torch
+    from bit_kv_cache_rht_gb300.okvq import OKVQ_KEYS_TURBOQUANT
+    R = None
+    if shared_rotation:      # TurboQuant's one value rotation: the Hadamard rotation for every modality
+        sh = w.shape
+        Rh = o.hadamard_rotation(o.hadamard_signs(w.hadamard_seed, sh.head_dim)).astype(np.float32)
+        R = np.ascontiguousarray(np.broadcast_to(Rh, (sh.num_layers, sh.num_kv_heads, sh.num_modalities,
+                                                      sh.head_dim, sh.head_dim)))
+    oc, R = pu.oracle_cache(w, key_codec="turbo", R=R)
+    pu.feed_oracle(oc, w, bounds=bounds)
+    c = pu.gpu_cache(w, R=R, bounds=bounds, key_codec=OKVQ_KEYS_TURBOQUANT)
+    assert c.check_errors() == 0
+    for s in range(len(w.sessions)):
+        st = c.export_state(s)
+        pu.assert_state_matches(pu.compare_state(st, oc, s, oc.layers, w.shape.bits))
+        pu.adopt_boundary_choices(st, oc, s, oc.layers)
+    for step in steps:
+        Q = w.queries(step)
+        out = c.decode(torch.from_numpy(Q).cuda()).cpu().numpy()
+        pu.assert_outputs_close(out[:, oc.layers], oc.decode(Q), "turbo step %d" % step)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_turbo_keys_tiny_one_chunk(bits):
+    _turbo_check(synth.tiny(seed=60 + bits, bits=bits), bounds=[[(0, 2048)]], steps=(0, 1))
+
+
+def test_turbo_keys_odd_chunks_and_shared_value_rotation():
+    w = synth.tiny(seed=63)
+    _turbo_check(w, bounds=[[(a, min(a + 97, 2048)) for a in range(0, 2048, 97)]], shared_rotation=True)
+
+
+@pytest.mark.parametrize("T", [1, 17, 64, 130])
+def test_turbo_keys_short_sessions(T):
+    _turbo_check(synth.tiny(seed=64 + T, tokens=T), bounds=[[(0, T)]])
+
+
+def test_turbo_keys_qwen3b_shape_and_multisession():
+    _turbo_check(synth.qwen3b(seed=66, tokens=3000, layers=2), steps=(0, 1))
+    _turbo_check(synth.multisession(seed=67, sessions=3, lo=100, hi=2000, layers=2))
