@@ -44,13 +44,17 @@ def decode_source_sha256():
     return h.hexdigest()
 
 
-def algorithmic_bytes(w, lengths):
-    """Decode bytes per step: codes, statistics, norms, fp16 tail keys, modality ids, q and out."""
+def algorithmic_bytes(w, lengths, key_codec="omni"):
+    """Decode bytes per step: codes, statistics, norms, fp16 tail keys, modality ids, q and out.
+    TurboQuant keys: codes and a 2-byte norm per token-head, no statistics, no tail."""
     sh = w.shape
     d, b, G = sh.head_dim, sh.bits, sh.group_size
     per_unit = 0
     for T in lengths:
-        per_unit_T = T * (2 * d * b // 8 + 2) + (T // G) * 4 * d + (T % G) * 2 * d
+        if key_codec == "turbo":
+            per_unit_T = T * (2 * d * b // 8 + 2 + 2)
+        else:
+            per_unit_T = T * (2 * d * b // 8 + 2) + (T // G) * 4 * d + (T % G) * 2 * d
         per_unit += per_unit_T * sh.num_layers * sh.num_kv_heads
     mod = sum(lengths)
     qo = 2 * len(lengths) * sh.num_layers * sh.num_q_heads * d
@@ -107,8 +111,8 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def build_cache(w, torch, device, replicas=2):
-    from bit_kv_cache_rht_gb300.okvq import Cache
+def build_cache(w, torch, device, replicas=2, key_codec="omni"):
+    from bit_kv_cache_rht_gb300.okvq import Cache, OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT
     sh = w.shape
     R = w.value_rotations()
     T = w.sessions[0].length
@@ -123,7 +127,8 @@ def build_cache(w, torch, device, replicas=2):
     for rep in range(replicas):
         c = Cache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, w.max_tokens, R, head_dim=sh.head_dim,
                   group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
-                  hadamard_seed=w.hadamard_seed)
+                  hadamard_seed=w.hadamard_seed,
+                  key_codec=OKVQ_KEYS_TURBOQUANT if key_codec == "turbo" else OKVQ_KEYS_GROUP_RANGE)
         st = torch.cuda.current_stream()
         ev = []
         for a, b in w.sessions[0].chunk_bounds():
@@ -150,7 +155,7 @@ def cpu_baseline_child(args):
     sh = w.shape
     R = w.value_rotations()
     oc = o.OracleCache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.group_size, sh.bits,
-                       w.max_tokens, w.hadamard_seed, R, layers=[0])
+                       w.max_tokens, w.hadamard_seed, R, layers=[0], key_codec=args.key_codec)
     K, V = w.session_kv(0, [0])
     mod = w.sessions[0].modality()
     for a, b in w.sessions[0].chunk_bounds():
@@ -180,7 +185,8 @@ def run_cpu_baseline(args):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload,
-           "--cpu-seconds", str(args.cpu_seconds), "--cpu-max-reps", str(args.cpu_max_reps)]
+           "--cpu-seconds", str(args.cpu_seconds), "--cpu-max-reps", str(args.cpu_max_reps),
+           "--key-codec", args.key_codec]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
@@ -195,7 +201,7 @@ def reference_arm(args):
     base = None
     for i in range(args.warmup + args.steps):
         res = run_cpu_baseline(argparse.Namespace(workload=args.workload, cpu_seconds=args.ref_seconds,
-                                                  cpu_max_reps=1))
+                                                  cpu_max_reps=1, key_codec=args.key_codec))
         if i >= args.warmup:
             steps.append(res)
         base = res
@@ -220,8 +226,11 @@ def config_of(w, args):
                            w.sessions[0].length, sh.bits, sh.group_size),
             "sessions": len(w.sessions), "context_tokens": w.sessions[0].length, "bits": sh.bits,
             "group_size": sh.group_size,
+            "key_codec": "turboquant (per-token norm, fixed scale)" if getattr(args, "key_codec", "omni") == "turbo"
+                         else "omnikvquant (per-group min-max ranges)",
             "l2": "inputs larger than L2: two cache replicas (2 x %.0f MB) alternate between steps"
-                  % (algorithmic_bytes(w, [s.length for s in w.sessions])[0] / 1e6),
+                  % (algorithmic_bytes(w, [s.length for s in w.sessions], getattr(args, "key_codec", "omni"))[0]
+                     / 1e6),
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
@@ -236,6 +245,8 @@ def main():
     ap.add_argument("--cpu-max-reps", type=int, default=1000)
     ap.add_argument("--ref-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--key-codec", default="omni", choices=["omni", "turbo"],
+                    help="omni: per-group key ranges (the method); turbo: the TurboQuant comparison codec")
     ap.add_argument("--cpu-baseline-child", action="store_true")
     args = ap.parse_args()
     if args.cpu_baseline_child:
@@ -258,10 +269,10 @@ def main():
 
     w = synth.WORKLOADS[args.workload]()
     sh = w.shape
-    caches, append_ms = build_cache(w, torch, device, replicas=2)
+    caches, append_ms = build_cache(w, torch, device, replicas=2, key_codec=args.key_codec)
     T = w.sessions[0].length
     lengths = [s.length for s in w.sessions]
-    split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths)
+    split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths, args.key_codec)
     step_bytes = split_bytes + out_bytes
 
     Q = torch.from_numpy(w.queries(0)).to(device)
@@ -346,7 +357,8 @@ def main():
                 tj = json.load(f)
             # DRAM bytes of one decode launch from an ncu capture, valid only while the
             # kernel sources are the ones that capture measured
-            if tj.get("workload") == args.workload and tj.get("source_sha256") == decode_source_sha256():
+            if (tj.get("workload") == args.workload and tj.get("source_sha256") == decode_source_sha256()
+                    and args.key_codec == "omni"):
                 traffic = tj.get("bytes_per_launch")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
