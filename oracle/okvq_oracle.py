@@ -524,3 +524,34 @@ class OracleCache:
                     q = Q16[s, l, h * gq:(h + 1) * gq]
                     out[s, i, h * gq:(h + 1) * gq] = u.decode_bruteforce(q) if brute else u.decode(q)
         return out
+
+
+# ---------------------------------------------------------------------------
+# value-rotation calibration (section 2, second OmniKVQuant bullet)
+# ---------------------------------------------------------------------------
+
+def calibrate_rotation(v16: np.ndarray, weight: Optional[np.ndarray] = None):
+    """Eigenbasis of the attention-contribution-weighted covariance of ONE modality's
+    calibration values v16 [n][d]: the directions are weighted by the tokens'
+    contributions a_t >= 0 (``weight``; None = all 1), the covariance is
+    C = sum_t a_t (v_t - mu)(v_t - mu)^T / sum_t a_t with mu the weighted mean, and
+    the rotation's rows are C's eigenvectors, in descending eigenvalue order, each
+    signed so that its largest-magnitude entry is positive.  Fewer than two tokens
+    or zero total weight give the identity (and zero eigenvalues).
+    Returns R [d][d] (fp64, rows = basis) and the eigenvalues [d] (descending).
+    """
+    v = np.asarray(v16, F64)
+    n, d = v.shape
+    a = np.ones(n, F64) if weight is None else np.asarray(weight, F64)
+    W = a.sum()
+    if n < 2 or W <= 0:
+        return np.eye(d), np.zeros(d)
+    mu = (a[:, None] * v).sum(0) / W
+    x = v - mu[None]
+    C = (x.T * a[None]) @ x / W
+    lam, U = np.linalg.eigh(C)
+    order = np.argsort(-lam, kind="stable")
+    R = U[:, order].T.copy()
+    idx = np.argmax(np.abs(R), axis=1)
+    R *= np.sign(R[np.arange(d), idx])[:, None]
+    return R, lam[order]

@@ -465,3 +465,56 @@ def test_local_key_ranges_beat_turbo_scale_on_drifted_keys():
     kt, at = _key_errors("turbo", K, V, q)
     assert ko < 0.7 * kt, (ko, kt)
     assert ao < at, (ao, at)
+
+
+# ---------------------------------------------------------------- rotation calibration
+
+def _exact_cloud(U, lam):
+    """Points +-sqrt(d lam_i) u_i (2d of them): mean 0, covariance exactly U diag(lam) U^T."""
+    d = len(lam)
+    pts = []
+    for i in range(d):
+        pts.append(np.sqrt(d * lam[i]) * U[:, i])
+        pts.append(-np.sqrt(d * lam[i]) * U[:, i])
+    return np.array(pts)
+
+
+def test_calibration_recovers_a_constructed_eigenbasis():
+    d = 128
+    r = np.random.default_rng(8)
+    U = np.linalg.qr(r.standard_normal((d, d)))[0]
+    lam = np.sort(r.uniform(0.1, 5.0, d))[::-1] + np.arange(d)[::-1] * 1e-3    # distinct, descending
+    X = _exact_cloud(U, lam)
+    R, ev = o.calibrate_rotation(X)
+    assert np.allclose(ev, lam, rtol=1e-9, atol=1e-12)
+    dots = np.abs(np.sum(R * U.T, axis=1))                   # |<r_i, u_i>|
+    assert np.all(dots > 1 - 1e-8)
+    assert np.all(R[np.arange(d), np.argmax(np.abs(R), axis=1)] > 0)   # sign convention
+
+
+def test_calibration_weights_equal_duplication_and_shift_invariance():
+    r = np.random.default_rng(9)
+    X = r.standard_normal((40, 128)) * r.uniform(0.5, 3, 128)
+    a = r.integers(1, 4, 40).astype(float)
+    Rw, ew = o.calibrate_rotation(X, a)
+    Rd, ed = o.calibrate_rotation(np.repeat(X, a.astype(int), axis=0))
+    assert np.allclose(ew, ed, rtol=1e-10, atol=1e-12)
+    Rs, es = o.calibrate_rotation(X + 7.0, a)                 # the weighted mean is removed
+    assert np.allclose(es, ew, rtol=1e-9, atol=1e-9)
+    top = ew[:-1] - ew[1:] > 1e-3 * ew[0]                     # well-separated directions are unique
+    ok = np.abs(np.sum(Rw * Rd, axis=1))[:-1][top]
+    assert np.all(ok > 1 - 1e-8)
+
+
+def test_calibration_eigen_equation_and_degenerate_cases():
+    r = np.random.default_rng(10)
+    X = r.standard_normal((300, 128)) * np.linspace(0.2, 3, 128)
+    R, ev = o.calibrate_rotation(X)
+    C = np.cov(X, rowvar=False, bias=True)
+    assert np.allclose(R @ R.T, np.eye(128), atol=1e-10)
+    assert np.allclose(R @ C @ R.T, np.diag(ev), atol=1e-9 * ev[0])
+    assert np.all(np.diff(ev) <= 1e-12)
+    R1, e1 = o.calibrate_rotation(X[:1])
+    assert np.array_equal(R1, np.eye(128)) and not e1.any()
+    R0, _ = o.calibrate_rotation(X, np.zeros(300))
+    assert np.array_equal(R0, np.eye(128))
