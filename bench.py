@@ -112,9 +112,33 @@ class ClockSampler:
 
 
 def build_cache(w, torch, device, replicas=2, key_codec="omni"):
-    from bit_kv_cache_rht_gb300.okvq import Cache, OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT
+    from bit_kv_cache_rht_gb300.okvq import Cache, OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT, calibrate_rotations
     sh = w.shape
-    R = w.value_rotations()
+    # value rotations: the calibration kernel on the workload's calibration slice
+    # (one untimed call loads the module, the second is timed)
+    Vc, modc = w.calibration_slice()
+    Vcd, Mcd = torch.from_numpy(Vc).to(device), torch.from_numpy(modc).to(device)
+    st = torch.cuda.current_stream()
+    calibrate_rotations(Vcd, Mcd, sh.num_modalities)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(st)
+    rot, _, sweeps = calibrate_rotations(Vcd, Mcd, sh.num_modalities, return_sweeps=True)
+    c1.record(st)
+    R = rot.cpu().numpy()
+    sw = sweeps.cpu().numpy().astype(np.int64)
+    if np.any(sw < 0):
+        raise RuntimeError("calibration: Jacobi did not converge for %d units" % int((sw < 0).sum()))
+    ms = c0.elapsed_time(c1)
+    # shared-memory traffic of the rotating sweeps: per round, rows p, q (2 loads + 2 stores)
+    # and columns p, q of A and V (4 + 4) for 64 pairs x 128 entries, 4 B each
+    smem_bytes = float(np.maximum(sw - 1, 0).sum()) * 127 * 64 * 128 * 12 * 4
+    smem_peak = 152 * 128 * 2.07e9 / 1e9          # GB/s: 32 banks x 4 B per clock per SM at 2.07 GHz
+    calib = {"ms": ms, "units": int(sw.size), "tokens": int(Vc.shape[0]),
+             "sweeps_mean": float(sw.mean()), "sweeps_max": int(sw.max()),
+             "roofline": {"bound": "smem", "achieved": smem_bytes / (ms / 1e3) / 1e9, "peak": smem_peak,
+                          "unit": "GB/s", "frac": smem_bytes / (ms / 1e3) / 1e9 / smem_peak,
+                          "peak_kind": "nominal (152 SMs x 128 B/clk x 2.07 GHz)"}}
+    del Vcd, Mcd, rot
     T = w.sessions[0].length
     K = torch.empty((T, sh.num_layers, sh.num_kv_heads, sh.head_dim), dtype=torch.float16, device=device)
     V = torch.empty_like(K)
@@ -144,7 +168,7 @@ def build_cache(w, torch, device, replicas=2, key_codec="omni"):
         caches.append(c)
     del K, V
     torch.cuda.empty_cache()
-    return caches, append_ms
+    return caches, append_ms, calib
 
 
 def cpu_baseline_child(args):
@@ -153,7 +177,8 @@ def cpu_baseline_child(args):
     from oracle import okvq_oracle as o
     w = synth.WORKLOADS[args.workload]()
     sh = w.shape
-    R = w.value_rotations()
+    Vc, modc = w.calibration_slice()
+    R = o.calibrate_rotations(Vc, modc, sh.num_modalities)[0].astype(np.float32)
     oc = o.OracleCache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.group_size, sh.bits,
                        w.max_tokens, w.hadamard_seed, R, layers=[0], key_codec=args.key_codec)
     K, V = w.session_kv(0, [0])
@@ -269,7 +294,7 @@ def main():
 
     w = synth.WORKLOADS[args.workload]()
     sh = w.shape
-    caches, append_ms = build_cache(w, torch, device, replicas=2, key_codec=args.key_codec)
+    caches, append_ms, calib = build_cache(w, torch, device, replicas=2, key_codec=args.key_codec)
     T = w.sessions[0].length
     lengths = [s.length for s in w.sessions]
     split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths, args.key_codec)
@@ -375,6 +400,7 @@ def main():
             "append": {"tokens_per_s": ap_tokens / (ap_ms / 1e3), "chunks": len(append_ms[0]),
                        "gbs": ap_tokens * ap_bytes_tok / (ap_ms / 1e3) / 1e9,
                        "frac": ap_tokens * ap_bytes_tok / (ap_ms / 1e3) / 1e9 / peak},
+            "calibration": dict(calib, kernel="calib_kernel (value-rotation covariance + Jacobi eigenbasis)"),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(Q.numel() * 2),
                     "d2h_bytes_per_step": int(out.numel() * 2)},
             "gpu_launches": 2 * args.steps,

@@ -328,13 +328,12 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s) {
-  static bool attr_done = false;
-  size_t smem = sizeof(Smem);
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const size_t smem = sizeof(Smem);
+  cudaError_t e = once_per_device(attr_done, [&] {
+    return cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid(n_pages, a.L * a.Hkv);
   append_kernel<<<grid, THREADS, smem, s>>>(a);
   return cudaGetLastError();

@@ -887,14 +887,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
 template <int BITS, int G>
 cudaError_t launch_decode_t(const DecodeArgs &a, int n_cta, cudaStream_t s) {
-  static bool attr_done = false;
+  static std::atomic<uint64_t> attr_done{0};
   const size_t smem = decode_smem_bytes(BITS, G);
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = once_per_device(attr_done, [&] {
+    return cudaFuncSetAttribute(decode_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   decode_kernel<BITS, G><<<n_cta, Cfg<BITS>::WARPS * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -924,16 +922,15 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
   if (a.units <= 0) return cudaSuccess;
-  static bool attr_done = false;
+  static std::atomic<uint64_t> attr_done{0};
   const size_t smem = (size_t)4 * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + 4 * 32 * 4) * sizeof(float);
-  if (!attr_done) {
+  cudaError_t ea = once_per_device(attr_done, [&] {
     cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // same shared/L1 split as the decode kernel: no reconfiguration between the two
-    e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  });
+  if (ea != cudaSuccess) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.units, D / CB_CH);
   cfg.blockDim = dim3(256);

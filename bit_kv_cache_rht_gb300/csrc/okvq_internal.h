@@ -41,6 +41,7 @@
 // serves the warp without bank conflicts). Each group stores
 // [min 128 fp16 | range 128 fp16].
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -190,6 +191,21 @@ struct CombineArgs {
 };
 
 constexpr int PARTIAL_FLOATS = 2 + MAXM * D;   // m, l, o[M][D]
+
+// Kernel attributes belong to a device: run `set` once per device ordinal (the
+// current device; ordinals >= 64 run it on every call). `done` holds one bit per
+// device.
+template <class Fn>
+cudaError_t once_per_device(std::atomic<uint64_t> &done, Fn set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);

@@ -24,7 +24,7 @@ OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT = 0, 1   # key codecs (okvq_config.k
 EXPORTS = (
     "okvq_create", "okvq_free", "okvq_append_chunk", "okvq_decode", "okvq_length", "okvq_export_state",
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
-    "okvq_decode_static_scratch",
+    "okvq_decode_static_scratch", "okvq_calibrate_rotations",
 )
 
 
@@ -70,6 +70,7 @@ def load() -> ctypes.CDLL:
     L.okvq_append_chunk.argtypes = [vp, i32, vp, vp, vp, i32, vp]
     L.okvq_decode.argtypes = [vp, vp, vp, vp]
     L.okvq_decode_static_scratch.argtypes = [vp, vp, vp, vp]
+    L.okvq_calibrate_rotations.argtypes = [i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp]
     L.okvq_length.argtypes = [vp, i32, ctypes.POINTER(i64)]
     L.okvq_export_state.argtypes = [vp, i32, vp, ctypes.POINTER(ctypes.c_size_t)]
     L.okvq_codebook.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
@@ -119,6 +120,38 @@ def okvq_decode(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
 def okvq_decode_static_scratch(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
     return load().okvq_decode_static_scratch(h, ctypes.c_void_p(q_ptr), ctypes.c_void_p(out_ptr),
                                              ctypes.c_void_p(stream))
+
+
+def okvq_calibrate_rotations(num_layers: int, num_kv_heads: int, num_modalities: int, v_ptr: int, mod_ptr: int,
+                             weight_ptr: int, num_tokens: int, rot_ptr: int, eig_ptr: int, sweeps_ptr: int = 0,
+                             stream: int = 0) -> int:
+    return load().okvq_calibrate_rotations(num_layers, num_kv_heads, num_modalities, ctypes.c_void_p(v_ptr),
+                                           ctypes.c_void_p(mod_ptr), ctypes.c_void_p(weight_ptr), num_tokens,
+                                           ctypes.c_void_p(rot_ptr), ctypes.c_void_p(eig_ptr),
+                                           ctypes.c_void_p(sweeps_ptr), ctypes.c_void_p(stream))
+
+
+def calibrate_rotations(v, modality, num_modalities: int = 3, weight=None, stream=None, return_sweeps=False):
+    """v: cuda fp16 [n][L][Hkv][128]; modality: cuda uint8 [n]; weight: cuda fp32 [n][L][Hkv] or None.
+    Returns (rot [L][Hkv][M][128][128], eig [L][Hkv][M][128]) as cuda fp32 tensors, plus the
+    int32 sweep counts [L][Hkv][M] when return_sweeps."""
+    import torch
+    n, L, Hkv, d = (int(x) for x in v.shape)
+    if d != 128 or v.dtype != torch.float16 or not v.is_cuda or not v.is_contiguous():
+        raise ValueError("v must be a contiguous cuda fp16 tensor [n][L][Hkv][128]")
+    if modality.dtype != torch.uint8 or tuple(modality.shape) != (n,) or not modality.is_cuda:
+        raise ValueError("modality must be a cuda uint8 tensor [n]")
+    if weight is not None and (weight.dtype != torch.float32 or tuple(weight.shape) != (n, L, Hkv)
+                               or not weight.is_cuda or not weight.is_contiguous()):
+        raise ValueError("weight must be a contiguous cuda fp32 tensor [n][L][Hkv]")
+    rot = torch.empty((L, Hkv, num_modalities, d, d), dtype=torch.float32, device=v.device)
+    eig = torch.empty((L, Hkv, num_modalities, d), dtype=torch.float32, device=v.device)
+    sweeps = torch.empty((L, Hkv, num_modalities), dtype=torch.int32, device=v.device)
+    st = okvq_calibrate_rotations(L, Hkv, num_modalities, v.data_ptr(), modality.data_ptr(),
+                                  weight.data_ptr() if weight is not None else 0, n, rot.data_ptr(), eig.data_ptr(),
+                                  sweeps.data_ptr(), _stream_handle(stream))
+    _check(st, "okvq_calibrate_rotations")
+    return (rot, eig, sweeps) if return_sweeps else (rot, eig)
 
 
 def okvq_length(h, session: int):

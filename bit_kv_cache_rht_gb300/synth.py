@@ -21,16 +21,13 @@ alone and the result does not depend on generation order):
   Gaussian random walk with step 0.02 per token (temporal key drift);
 * values V[t] = vscale * z + mu[mod[t]];
 * queries ~ N(0, 1);
-* value rotations: for each (layer, kv head, modality), the eigenbasis of the
-  plain covariance of that modality's values in a separate 512-token
-  calibration slice (interleave 64 video / 25 audio / 8 text), rows =
-  eigenvectors sorted by descending eigenvalue, each row's largest-magnitude
-  entry made positive.  This stands in for the offline calibration of
-  OmniKVQuant (section 2, value rotations), which is not part of the
-  append/decode path; the codec treats the matrices as an input.
+* calibration slice: a separate 512-token stream of values drawn the same
+  way (interleave 64 video / 25 audio / 8 text, its own PCG64 stream per
+  layer).  The per-modality value rotations are calibrated from it (by the
+  library's calibration kernel, or by the CPU oracle in the tests); this
+  module computes no rotation itself.
 
-Everything is cast to fp16 once (values the codec reads) or kept fp32 (the
-rotation matrices, which the codec takes as fp32).
+Everything is cast to fp16 once (the values the codec reads).
 """
 from __future__ import annotations
 
@@ -168,38 +165,20 @@ class Workload:
         q = r.standard_normal((len(self.sessions), sh.num_layers, sh.num_q_heads, sh.head_dim), dtype=np.float32)
         return q.astype(np.float16)
 
-    # ---- value rotations (codec parameter) ----
-    def value_rotations(self) -> np.ndarray:
-        """fp32 [L][Hkv][M][d][d]; row i of R is the i-th eigenvector."""
+    # ---- calibration slice (input of the value-rotation calibration) ----
+    def calibration_slice(self, layers: Optional[Sequence[int]] = None):
+        """fp16 values [CALIB_TOKENS][L'][Hkv][d] of the calibration slice and its
+        modality ids [CALIB_TOKENS] (interleave 64 video / 25 audio / 8 text)."""
         sh = self.shape
-        out = np.empty((sh.num_layers, sh.num_kv_heads, sh.num_modalities, sh.head_dim, sh.head_dim), np.float32)
+        layers = list(range(sh.num_layers)) if layers is None else list(layers)
         mod = interleave_pattern([(MOD_VIDEO, 64), (MOD_AUDIO, 25), (MOD_TEXT, 8)], CALIB_TOKENS)
-        for l in range(sh.num_layers):
+        V = np.empty((CALIB_TOKENS, len(layers), sh.num_kv_heads, sh.head_dim), np.float16)
+        for i, l in enumerate(layers):
             _, vscale, mu = self.layer_params(l)
             r = _rng(self.seed, "calib", l)
             z = r.standard_normal((CALIB_TOKENS, sh.num_kv_heads, sh.head_dim), dtype=np.float32)
-            V = (vscale[None] * z + mu[mod]).astype(np.float16).astype(np.float64)
-            for h in range(sh.num_kv_heads):
-                for m in range(sh.num_modalities):
-                    X = V[mod == m, h]
-                    out[l, h, m] = eigenbasis_rows(X)
-        return out
-
-
-def eigenbasis_rows(X: np.ndarray) -> np.ndarray:
-    """Orthonormal eigenbasis (rows) of the sample covariance of X [n][d]."""
-    d = X.shape[1]
-    if X.shape[0] >= 2:
-        C = np.cov(X, rowvar=False)
-    else:
-        C = np.eye(d)
-    w, U = np.linalg.eigh(C)
-    order = np.argsort(-w, kind="stable")
-    R = U[:, order].T.copy()
-    idx = np.argmax(np.abs(R), axis=1)
-    sgn = np.sign(R[np.arange(d), idx])
-    sgn[sgn == 0] = 1.0
-    return (R * sgn[:, None]).astype(np.float32)
+            V[:, i] = (vscale[None] * z + mu[mod]).astype(np.float16)
+        return V, mod
 
 
 # ---------------------------------------------------------------------------

@@ -202,6 +202,32 @@ okvq_status okvq_check_errors(okvq_cache *h, void *stream, uint32_t *word);
 okvq_status okvq_profile_enable(okvq_cache *h, int enable);
 okvq_status okvq_profile_read(okvq_cache *h, float *split_ms, float *merge_ms, int32_t cap, int32_t *count);
 
+/* Calibrate the per-modality value rotations (section 2, second OmniKVQuant
+ * bullet: directions weighted by their contribution to attention outputs, one
+ * covariance per modality, its eigenbasis as the rotation). For every
+ * (layer, kv head) and modality m, over the calibration tokens of modality m:
+ *   C_m = sum_t a_t (v_t - mu_m)(v_t - mu_m)^T / sum_t a_t,  mu_m the a-weighted mean,
+ * and R_m = its eigenvectors as rows, in descending eigenvalue order, each row
+ * signed so that its largest-magnitude entry is positive (fp32 cyclic Jacobi).
+ * A modality with fewer than two tokens, or zero total weight, gets the identity
+ * (eigenvalues 0). Tokens whose modality id is >= num_modalities are ignored.
+ *   v         device fp16 [num_tokens][num_layers][num_kv_heads][128], token-major
+ *   modality  device uint8 [num_tokens]
+ *   weight    device fp32 [num_tokens][num_layers][num_kv_heads] (the a_t, >= 0),
+ *             or NULL for all ones (the plain covariance)
+ *   rot_out   device fp32 [num_layers][num_kv_heads][num_modalities][128][128]: the
+ *             value_rot layout of okvq_config (copy it to the host for okvq_create)
+ *   eig_out   device fp32 [num_layers][num_kv_heads][num_modalities][128], or NULL
+ *   sweeps_out device int32 [num_layers][num_kv_heads][num_modalities], or NULL: the
+ *             Jacobi sweeps run (the last one rotated nothing); negated when 30 sweeps
+ *             did not converge (the basis is then the last iterate); 0 for identity
+ * OKVQ_EINVAL for bad sizes or NULL required pointers; one kernel launch,
+ * asynchronous on `stream`; nothing is allocated. */
+okvq_status okvq_calibrate_rotations(int32_t num_layers, int32_t num_kv_heads, int32_t num_modalities,
+                                     const void *v, const uint8_t *modality, const float *weight,
+                                     int32_t num_tokens, float *rot_out, float *eig_out, int32_t *sweeps_out,
+                                     void *stream);
+
 /* Static description of a status code. */
 const char *okvq_status_string(okvq_status s);
 

@@ -555,3 +555,23 @@ def calibrate_rotation(v16: np.ndarray, weight: Optional[np.ndarray] = None):
     idx = np.argmax(np.abs(R), axis=1)
     R *= np.sign(R[np.arange(d), idx])[:, None]
     return R, lam[order]
+
+
+def calibrate_rotations(v16: np.ndarray, modality: np.ndarray, num_modalities: int,
+                        weight: Optional[np.ndarray] = None):
+    """calibrate_rotation for every (layer, kv head) and modality of a calibration
+    stream: v16 [n][L][Hkv][d], modality ids [n] (ids >= num_modalities are
+    ignored), weight [n][L][Hkv] or None.  Returns R [L][Hkv][M][d][d] and the
+    eigenvalues [L][Hkv][M][d]."""
+    v = np.asarray(v16)
+    n, L, H, d = v.shape
+    mod = np.asarray(modality)
+    R = np.empty((L, H, num_modalities, d, d))
+    lam = np.empty((L, H, num_modalities, d))
+    for l in range(L):
+        for h in range(H):
+            for m in range(num_modalities):
+                sel = mod == m
+                a = None if weight is None else np.asarray(weight)[sel, l, h]
+                R[l, h, m], lam[l, h, m] = calibrate_rotation(v[sel, l, h], a)
+    return R, lam

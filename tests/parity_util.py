@@ -18,10 +18,23 @@ def ensure_built():
     return okvq.load()
 
 
+_ROT = {}
+
+
+def rotations(w):
+    """fp32 value rotations [L][Hkv][M][d][d]: the oracle's calibration of the
+    workload's calibration slice (one input shared by both sides)."""
+    key = (w.name, w.seed, w.shape.num_layers, w.shape.num_kv_heads, w.shape.num_modalities)
+    if key not in _ROT:
+        V, mod = w.calibration_slice()
+        _ROT[key] = o.calibrate_rotations(V, mod, w.shape.num_modalities)[0].astype(np.float32)
+    return _ROT[key]
+
+
 def oracle_cache(w, layers=None, sessions=None, key_codec="omni", R=None):
     sh = w.shape
     layers = list(range(sh.num_layers)) if layers is None else list(layers)
-    R = w.value_rotations() if R is None else R
+    R = rotations(w) if R is None else R
     return o.OracleCache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
                          sh.group_size, sh.bits, w.max_tokens, w.hadamard_seed, R, layers=layers,
                          key_codec=key_codec), R
@@ -42,7 +55,7 @@ def gpu_cache(w, R=None, bounds=None, sessions=None, max_tokens=None, key_codec=
     import torch
     from bit_kv_cache_rht_gb300.okvq import Cache
     sh = w.shape
-    R = w.value_rotations() if R is None else R
+    R = rotations(w) if R is None else R
     c = Cache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads,
               w.max_tokens if max_tokens is None else max_tokens, R, head_dim=sh.head_dim,
               group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,

@@ -249,6 +249,11 @@ def test_pack_roundtrip_and_bit_positions(bits):
 
 # ---------------------------------------------------------------- attention
 
+def _rotations(w):
+    V, mod = w.calibration_slice()
+    return o.calibrate_rotations(V, mod, w.shape.num_modalities)[0].astype(F32)
+
+
 def _unit(bits=2, G=32, T=203, seed=0, Gq=4):
     cb = o.make_codebook(bits)
     r = np.random.default_rng(seed)
@@ -325,7 +330,7 @@ def test_grid_keys_reproduce_exact_attention():
 
 def test_streaming_chunking_invariance():
     w = synth.tiny(seed=7)
-    R = w.value_rotations()
+    R = _rotations(w)
     K, V = w.session_kv(0)
     mod = w.sessions[0].modality()
 
@@ -351,26 +356,29 @@ def test_streaming_chunking_invariance():
 
 # ---------------------------------------------------------------- synthetic inputs
 
-def test_value_rotations_orthogonal_and_diagonalising():
+def test_calibrated_rotations_on_the_slice_orthogonal_and_diagonalising():
+    """The multi-unit calibration on the synthetic calibration slice: every basis is
+    orthonormal and diagonalises np.cov of its modality's tokens (the unweighted,
+    n-1 normalised covariance has the same eigenvectors)."""
     w = synth.tiny(seed=3)
-    R = w.value_rotations().astype(F64)
-    assert R.shape == (1, 2, 3, 128, 128)
+    Vc, mod = w.calibration_slice()
+    assert Vc.shape == (synth.CALIB_TOKENS, 1, 2, 128) and Vc.dtype == F16
+    R, lam = o.calibrate_rotations(Vc, mod, 3)
+    assert R.shape == (1, 2, 3, 128, 128) and lam.shape == (1, 2, 3, 128)
     for h in range(2):
         for m in range(3):
             Rm = R[0, h, m]
-            assert np.max(np.abs(Rm @ Rm.T - np.eye(128))) < 1e-5
-    # the basis diagonalises its modality's calibration covariance
-    from bit_kv_cache_rht_gb300.synth import CALIB_TOKENS, interleave_pattern, _rng
-    mod = interleave_pattern([(0, 64), (1, 25), (2, 8)], CALIB_TOKENS)
-    _, vscale, mu = w.layer_params(0)
-    z = _rng(w.seed, "calib", 0).standard_normal((CALIB_TOKENS, 2, 128), dtype=F32)
-    Vc = (vscale[None] * z + mu[mod]).astype(F16).astype(F64)
-    X = Vc[mod == 0, 1]
-    C = np.cov(X, rowvar=False)
-    D = R[0, 1, 0] @ C @ R[0, 1, 0].T
-    off = D - np.diag(np.diag(D))
-    assert np.max(np.abs(off)) < 1e-5 * np.trace(C)
-    assert np.all(np.diff(np.diag(D)) <= 1e-6 * np.trace(C))
+            assert np.max(np.abs(Rm @ Rm.T - np.eye(128))) < 1e-10
+            C = np.cov(Vc[mod == m, 0, h].astype(F64), rowvar=False)
+            D = Rm @ C @ Rm.T
+            off = D - np.diag(np.diag(D))
+            assert np.max(np.abs(off)) < 1e-10 * np.trace(C)
+            assert np.all(np.diff(np.diag(D)) <= 1e-10 * np.trace(C))
+            n = int((mod == m).sum())
+            assert np.allclose(lam[0, h, m] * n / (n - 1), np.diag(D), atol=1e-10 * np.trace(C))
+    # ids beyond the modality count are ignored
+    R2, _ = o.calibrate_rotations(Vc, np.where(mod == 2, 7, mod).astype(np.uint8), 3)
+    assert np.array_equal(R2[0, :, :2], R[0, :, :2]) and np.array_equal(R2[0, 0, 2], np.eye(128))
 
 
 def test_workload_streams():
