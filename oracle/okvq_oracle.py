@@ -29,6 +29,15 @@ narrower precision so that both sides decide identically:
   in fp64; codes whose fp64 w lies within 1e-5 of a threshold are flagged as
   boundary codes (another correct implementation may round them the other way).
 
+Eviction and compaction ("OmniTide: Co-Designing Algorithms and Systems for
+Efficient On-Device Omni-LLM Streaming", section 5.2 Applying the retention
+plan, section 6.2 Selective and efficient KV migration): deleted token ranges
+stay in their slots as holes that attention skips; the ordered-suffix mode
+packs the surviving entries of the shortest suffix that shortens the
+page-rounded span by enough pages, preserving their order.  Here the unit that
+moves is a key group (its statistics serve all its members) or, for TurboQuant
+keys, a 16-token tile.
+
 TurboQuant key codec (the pages' comparison point, ``key_codec="turbo"``):
 every key is coded on arrival like a value, with the shared randomized Hadamard
 rotation instead of a modality eigenbasis (norm, direction rotated, fixed
@@ -344,6 +353,7 @@ class OracleUnit:
         self.vnorm = np.zeros(cap, F16)
         self.nbnd = np.zeros(cap, bool)
         self.mod = np.zeros(cap, np.uint8)
+        self.dead = np.zeros(cap, bool)                # deleted tokens (holes left in place)
 
     @property
     def T_full(self) -> int:
@@ -393,6 +403,7 @@ class OracleUnit:
                 "knbnd": self.knbnd[:T].copy(),
                 "vbnd": self.vbnd[:T].copy(),
                 "nbnd": self.nbnd[:T].copy(),
+                "dead": self.dead[:T].copy(),
             }
         return {
             "kcodes": pack_codes(self.kcodes[:Tf], b),
@@ -403,6 +414,7 @@ class OracleUnit:
             "kbnd": self.kbnd[:Tf].copy(),
             "vbnd": self.vbnd[:T].copy(),
             "nbnd": self.nbnd[:T].copy(),
+            "dead": self.dead[:T].copy(),
         }
 
     # ---- decode (section 1 Implementation bullet) ----
@@ -436,6 +448,10 @@ class OracleUnit:
             s[:, :Tf] = (beta[:, :, None] + np.einsum("hgc,gtc->hgt", a, lam)).reshape(Gq, Tf)
         if T > Tf:
             s[:, Tf:] = q @ self.keys16[Tf:T].astype(F64).T / math.sqrt(d)
+        live = ~self.dead[:T]
+        if not live.any():
+            return out                                                      # nothing left to attend
+        s[:, ~live] = -np.inf                                               # deleted tokens take no part
         mmax = s.max(axis=1, keepdims=True)
         p = np.exp(s - mmax)
         l = p.sum(axis=1)
@@ -480,11 +496,68 @@ class OracleUnit:
         if self.T == 0:
             return np.zeros((Gq, d), F64)
         Kh, Vh = self.dequantized()
+        live = ~self.dead[:self.T]
+        if not live.any():
+            return np.zeros((Gq, d), F64)
+        Kh, Vh = Kh[live], Vh[live]
         s = q16.astype(F64) @ Kh.T / math.sqrt(d)
         s -= s.max(axis=1, keepdims=True)
         p = np.exp(s)
         p /= p.sum(axis=1, keepdims=True)
         return p @ Vh
+
+    # ---- eviction and compaction ("OmniTide", sections 5.2 and 6.2) ----
+    def evict(self, begin: int, end: int):
+        """Delete tokens [begin, end): they stay in their slots as holes."""
+        if not 0 <= begin <= end <= self.T:
+            raise ValueError("eviction range outside the cache")
+        self.dead[begin:end] = True
+
+    def move_granules(self, moves, granule: int, new_T: int):
+        """Apply an order-preserving move list [(src granule, dst granule)]: every
+        per-token array moves with its tokens, every key group with its granule
+        (granule = G for grouped keys); the cache then ends at new_T."""
+        for src, dst in moves:
+            a, b = src * granule, min((src + 1) * granule, self.T)
+            c = dst * granule
+            for arr in (self.kcodes, self.kbnd, self.keys16, self.knorm, self.knbnd, self.vcodes, self.vbnd,
+                        self.vnorm, self.nbnd, self.mod, self.dead):
+                arr[c:c + (b - a)] = arr[a:b]
+            if self.key_codec == "omni":
+                self.kmn[dst], self.krg[dst] = self.kmn[src], self.krg[src]
+        self.dead[new_T:self.T] = False
+        self.T = new_T
+
+
+def compaction_granule(key_codec: str, group_size: int) -> int:
+    """Tokens moved as one unit: a key group (its statistics belong to all its
+    members), or one 16-token tile for TurboQuant keys (per-token scales)."""
+    return group_size if key_codec == "omni" else 16
+
+
+def plan_suffix_compaction(dead: np.ndarray, T: int, granule: int, min_pages: int, page: int = 64):
+    """Ordered-suffix migration plan ("OmniTide", section 6.2, ordered-suffix
+    mode), at granule granularity.  Scanning suffix starts s (granule-aligned)
+    from the end of the cache backward, packing the suffix's granules that still
+    hold a live token to s, s + granule, ... in their order shortens the
+    page-rounded span from ceil(T/page) to ceil(T'/page); the first (shortest)
+    suffix that saves at least min_pages pages is the plan.  Returns None (no
+    migration) or (s_granule, T', moves) with moves [(src, dst)] for the
+    granules whose slot changes."""
+    if min_pages < 1:
+        raise ValueError("min_pages must be >= 1")
+    dead = np.asarray(dead[:T], bool)
+    ng = -(-T // granule)
+    lens = [min(granule, T - j * granule) for j in range(ng)]
+    empty = [bool(dead[j * granule:j * granule + lens[j]].all()) for j in range(ng)]
+    pages0 = -(-T // page)
+    for sg in range(ng - 1, -1, -1):
+        kept = [j for j in range(sg, ng) if not empty[j]]
+        T2 = sg * granule + sum(lens[j] for j in kept)      # only the last granule can be partial
+        if pages0 - (-(-T2 // page)) >= min_pages:
+            moves = [(j, sg + i) for i, j in enumerate(kept) if j != sg + i]
+            return sg, T2, moves
+    return None
 
 
 class OracleCache:
@@ -512,6 +585,24 @@ class OracleCache:
         for i, l in enumerate(layers_in):
             for h in range(self.Hkv):
                 self.units[(session, l, h)].append(K16[:, i, h], V16[:, i, h], mod)
+
+    def evict(self, session, begin, end):
+        """Delete tokens [begin, end) of a session in every (layer, kv head)."""
+        for (s, _, _), u in self.units.items():
+            if s == session:
+                u.evict(begin, end)
+
+    def compact(self, session, min_pages):
+        """Plan and apply the ordered-suffix compaction of a session; returns the
+        plan (see plan_suffix_compaction) or None."""
+        units = [u for (s, _, _), u in self.units.items() if s == session]
+        u0 = units[0]
+        gran = compaction_granule(u0.key_codec, self.G)
+        plan = plan_suffix_compaction(u0.dead, u0.T, gran, min_pages)
+        if plan is not None:
+            for u in units:
+                u.move_granules(plan[2], gran, plan[1])
+        return plan
 
     def decode(self, Q16, brute=False):
         """Q16 [S][L][Hq][d] -> fp64 [S][L'][Hq][d] for the oracle's layers."""

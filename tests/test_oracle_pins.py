@@ -526,3 +526,137 @@ def test_calibration_eigen_equation_and_degenerate_cases():
     assert np.array_equal(R1, np.eye(128)) and not e1.any()
     R0, _ = o.calibrate_rotation(X, np.zeros(300))
     assert np.array_equal(R0, np.eye(128))
+
+
+# ---------------------------------------------------------------- eviction and compaction
+
+def _stream(r, n):
+    K = (r.standard_normal((n, 128)) * 2 + np.linspace(0, 1, n)[:, None]).astype(F16)
+    V = (r.standard_normal((n, 128)) * 1.5 + 0.3).astype(F16)
+    return K, V, r.integers(0, 3, n).astype(np.uint8)
+
+
+def _fresh(key_codec, bits=2, G=32, seed=0):
+    cb = o.make_codebook(bits)
+    r = np.random.default_rng(seed)
+    R = np.stack([np.linalg.qr(r.standard_normal((128, 128)))[0] for _ in range(3)]).astype(F32)
+    return o.OracleUnit(128, G, cb, o.hadamard_signs(99, 128), R, 4, 2048, key_codec=key_codec)
+
+
+@pytest.mark.parametrize("key_codec,bits,G", [("omni", 2, 32), ("omni", 4, 64), ("turbo", 2, 32)])
+def test_eviction_fused_decode_equals_attention_over_live_tokens(key_codec, bits, G):
+    """Masked fused decode = brute-force softmax over the explicitly dequantized
+    live tokens; deleted tokens' data does not matter; deleting all gives zeros."""
+    r = np.random.default_rng(31)
+    u = _fresh(key_codec, bits, G)
+    K, V, mod = _stream(r, 203)
+    u.append(K[:150], V[:150], mod[:150])
+    u.append(K[150:], V[150:], mod[150:])
+    for a, b in ((0, 3), (40, 97), (130, 131), (195, 203)):     # sinks, whole groups, a tail token
+        u.evict(a, b)
+    q = (r.standard_normal((4, 128)) * 1.5).astype(F16)
+    out = u.decode(q)
+    assert np.max(np.abs(out - u.decode_bruteforce(q))) < 1e-10
+    Kh, Vh = u.dequantized()
+    live = ~u.dead[:u.T]
+    s = q.astype(F64) @ Kh[live].T / math.sqrt(128)
+    p = np.exp(s - s.max(1, keepdims=True))
+    assert np.max(np.abs(out - (p / p.sum(1, keepdims=True)) @ Vh[live])) < 1e-10
+    # a deleted token's codes can be anything
+    u.vcodes[50] ^= 1
+    u.vnorm[50] = F16(100.0)
+    u.kcodes[60] ^= 1
+    assert np.array_equal(u.decode(q), out)
+    u.evict(0, u.T)
+    assert np.all(u.decode(q) == 0) and np.all(u.decode_bruteforce(q) == 0)
+    with pytest.raises(ValueError):
+        u.evict(10, u.T + 1)
+
+
+def _brute_plan(dead, T, gran, min_pages):
+    """Every granule-aligned suffix start, packed explicitly; the largest start that
+    saves enough pages."""
+    best = None
+    for sg in range(-(-T // gran)):
+        slots = list(range(sg * gran))
+        for j in range(sg, -(-T // gran)):
+            toks = list(range(j * gran, min((j + 1) * gran, T)))
+            if not all(dead[t] for t in toks):
+                slots += toks
+        if -(-T // 64) - (-(-len(slots) // 64)) >= min_pages:
+            best = (sg, len(slots))
+    return best
+
+
+def test_suffix_plan_is_the_shortest_suffix_saving_enough_pages():
+    r = np.random.default_rng(5)
+    for trial in range(300):
+        gran = int(r.choice([16, 32, 64]))
+        T = int(r.integers(1, 700))
+        dead = np.zeros(T, bool)
+        for _ in range(int(r.integers(0, 8))):                  # runs of deletions
+            a = int(r.integers(0, T))
+            dead[a:a + int(r.integers(1, 200))] = True
+        if trial % 7 == 0:
+            dead[:] = True
+        mp = int(r.integers(1, 5))
+        plan = o.plan_suffix_compaction(dead, T, gran, mp)
+        ref = _brute_plan(dead, T, gran, mp)
+        if ref is None:
+            assert plan is None
+            continue
+        sg, T2, moves = plan
+        assert (sg, T2) == ref
+        assert all(d < s for s, d in moves) and moves == sorted(moves)
+        assert [d for _, d in moves] == sorted(set(d for _, d in moves))
+    with pytest.raises(ValueError):
+        o.plan_suffix_compaction(np.zeros(10, bool), 10, 32, 0)
+
+
+@pytest.mark.parametrize("key_codec,bits,G", [("omni", 2, 32), ("omni", 4, 64), ("turbo", 2, 32)])
+def test_compaction_equals_never_having_appended_the_removed_granules(key_codec, bits, G):
+    """Evict, compact: the state equals a cache that received only the surviving
+    granules (same partial deletions), and stays equal after further appends
+    (the trailing group continues in its new place). Decode is unchanged."""
+    r = np.random.default_rng(77 + bits + G)
+    gran = o.compaction_granule(key_codec, G)
+    n = 64 * 7 + 37                                              # ragged: the last granule is partial
+    K, V, mod = _stream(r, n + 90)
+    A = _fresh(key_codec, bits, G)
+    for a, b in ((0, 100), (100, 300), (300, n)):
+        A.append(K[a:b], V[a:b], mod[a:b])
+    ng = -(-n // gran)
+    dead = np.zeros(n, bool)
+    for j in (1, 3, 4, ng - 3):                                  # whole granules, one of them early
+        dead[j * gran:(j + 1) * gran] = True
+    dead[5:9] = True                                             # partial deletions
+    dead[6 * gran + 3:6 * gran + 7] = True
+    for t in np.nonzero(dead)[0]:
+        A.evict(int(t), int(t) + 1)
+    q = (r.standard_normal((4, 128)) * 1.5).astype(F16)
+    before = A.decode(q)
+    plan = o.plan_suffix_compaction(A.dead, A.T, gran, 1)
+    assert plan is not None
+    sg, T2, moves = plan
+    A.move_granules(moves, gran, T2)
+    assert np.allclose(A.decode(q), before, rtol=1e-12, atol=1e-12)
+    # the same tokens appended without the removed granules
+    keep = np.ones(n, bool)
+    for j in range(sg, ng):
+        if dead[j * gran:min((j + 1) * gran, n)].all():
+            keep[j * gran:(j + 1) * gran] = False
+    idx = np.nonzero(keep)[0]
+    assert len(idx) == T2
+    B = _fresh(key_codec, bits, G)
+    B.append(K[idx], V[idx], mod[idx])
+    for t in np.nonzero(dead[idx])[0]:
+        B.evict(int(t), int(t) + 1)
+    ea, eb = A.export(), B.export()
+    for key in eb:
+        assert np.array_equal(ea[key], eb[key]), key
+    A.append(K[n:], V[n:], mod[n:])
+    B.append(K[n:], V[n:], mod[n:])
+    ea, eb = A.export(), B.export()
+    for key in eb:
+        assert np.array_equal(ea[key], eb[key]), key
+    assert np.allclose(A.decode(q), B.decode(q), rtol=1e-12, atol=1e-12)
