@@ -47,6 +47,12 @@ struct okvq_cache {
   __half klev16[16];
   float vthr[15], kthr[15];
   int nlev = 0;
+  // eviction and compaction
+  std::vector<std::vector<unsigned long long>> dead;   // per session: [P_max] page deletion masks
+  unsigned long long *dead_dev = nullptr;              // [S][P_max], the source of the pages' copies
+  int *moves_dev = nullptr;                            // [cap / TILE][2] compaction move list
+  uint8_t *cscratch = nullptr;                         // compaction gather scratch
+  size_t cscratch_bytes = 0;
   // profiling
   bool prof = false;
   std::vector<cudaEvent_t> ev;  // triples per decode call
@@ -122,6 +128,9 @@ void release(okvq_cache *h) {
   cudaFree(h->err);
   cudaFree(h->partials);
   cudaFree(h->table);
+  cudaFree(h->dead_dev);
+  cudaFree(h->moves_dev);
+  cudaFree(h->cscratch);
   if (h->host_table) cudaFreeHost(h->host_table);
   if (h->table_ev) cudaEventDestroy(h->table_ev);
   for (auto e : h->ev) cudaEventDestroy(e);
@@ -210,6 +219,73 @@ void build_table(okvq_cache *h) {
   h->nseg = nseg;
 }
 
+constexpr size_t COMPACT_SCRATCH_CAP = 64ull << 20;
+
+// Bytes of one (move, unit) slot of the compaction scratch.
+int compaction_stride(const PageLayout &PL, int KG) {
+  return (std::max(granule_payload(PL, KG), compaction_granule(KG)) + 15) & ~15;
+}
+
+// Ordered-suffix compaction plan over granules ("OmniTide", section 6.2): scan
+// suffix starts from the end backward; packing the suffix's non-empty granules in
+// order to its start gives length T2; the first start that shortens the
+// page-rounded span by min_pages pages is the plan (sg < 0: none).
+struct CompactionPlan {
+  long long sg = -1, T2 = 0;
+  std::vector<int> moves;     // (source granule, destination granule) pairs, ascending
+};
+
+CompactionPlan plan_suffix(const std::vector<char> &empty, long long T, int gran, int min_pages) {
+  CompactionPlan p;
+  const long long ng = (T + gran - 1) / gran, pages0 = (T + PAGE - 1) / PAGE;
+  long long kept_tokens = 0;
+  for (long long sg = ng - 1; sg >= 0; --sg) {
+    if (!empty[sg]) kept_tokens += std::min<long long>(gran, T - sg * gran);
+    const long long T2 = sg * gran + kept_tokens;    // only the last granule can be partial
+    if (pages0 - (T2 + PAGE - 1) / PAGE >= min_pages) {
+      p.sg = sg;
+      p.T2 = T2;
+      long long dst = sg;
+      for (long long j = sg; j < ng; ++j) {
+        if (empty[j]) continue;
+        if (j != dst) {
+          p.moves.push_back((int)j);
+          p.moves.push_back((int)dst);
+        }
+        ++dst;
+      }
+      return p;
+    }
+  }
+  return p;
+}
+
+bool dead_bit(const std::vector<unsigned long long> &w, long long t) { return (w[t >> 6] >> (t & 63)) & 1ull; }
+void set_dead_bit(std::vector<unsigned long long> &w, long long t, bool v) {
+  if (v) w[t >> 6] |= 1ull << (t & 63);
+  else w[t >> 6] &= ~(1ull << (t & 63));
+}
+
+// Rewrite the deletion masks (and clear tile masks past the length) of pages
+// [p0, p1) of a session from the host copy.
+okvq_status push_page_meta(okvq_cache *h, int session, long long p0, long long p1, cudaStream_t s) {
+  if (p1 <= p0) return OKVQ_OK;
+  unsigned long long *dst = h->dead_dev + (size_t)session * h->P_max + p0;
+  // pageable source: staged before the call returns, so the host copy may change afterwards
+  OKVQ_TRY(cudaMemcpyAsync(dst, h->dead[session].data() + p0, (size_t)(p1 - p0) * 8, cudaMemcpyHostToDevice, s));
+  PageMetaArgs m{};
+  m.pages = h->pages;
+  m.dead = h->dead_dev + (size_t)session * h->P_max;
+  m.LH = h->L * h->Hkv;
+  m.session = session;
+  m.p0 = p0;
+  m.T = h->len[session];
+  m.P_max = h->P_max;
+  m.PL = h->PL;
+  OKVQ_TRY(launch_page_meta(m, (int)(p1 - p0), s));
+  return OKVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -271,6 +347,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   h->PL = page_layout(h->bits, h->KG);
   h->len.assign(h->S, 0);
   h->tail_sel.assign(h->S, 0);
+  h->dead.assign(h->S, std::vector<unsigned long long>(h->P_max, 0ull));
   // codebook: the fp16-rounded levels define it (values); key levels renormalised to [0, 1]
   h->nlev = nlev;
   double l16[16], k16[16];
@@ -312,6 +389,16 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->dead_dev, (size_t)h->S * h->P_max * 8)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->moves_dev, (size_t)(h->cap / TILE) * 2 * sizeof(int))) != OKVQ_OK) return fail(st);
+  {
+    // compaction scratch: every granule of a session, or COMPACT_SCRATCH_CAP (larger plans run in batches)
+    const int gran = compaction_granule(h->KG);
+    const size_t per_move = (size_t)(h->L * h->Hkv + 1) * compaction_stride(h->PL, h->KG);
+    h->cscratch_bytes = std::min<size_t>(COMPACT_SCRATCH_CAP, (size_t)(h->cap / gran) * per_move);
+    h->cscratch_bytes = std::max(h->cscratch_bytes, per_move);
+    if ((st = alloc_dev((void **)&h->cscratch, h->cscratch_bytes)) != OKVQ_OK) return fail(st);
+  }
   // work table: segs [max_segs][4] int | cta_seg [max_cta+1] | unit_seg [units+1] | unit_len [units] i64 | unit_tail
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -334,6 +421,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if (cudaMemsetAsync(h->tails, 0, tails, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->mod, 0, (size_t)h->S * h->cap, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaMemsetAsync(h->dead_dev, 0, (size_t)h->S * h->P_max * 8, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
     std::vector<float> rt(nmat * D * D);
@@ -607,6 +695,110 @@ okvq_status okvq_check_errors(okvq_cache *h, void *stream, uint32_t *word) {
   return w ? OKVQ_ESTATE : OKVQ_OK;
 }
 
+okvq_status okvq_evict(okvq_cache *h, int32_t session, const int64_t *ranges, int32_t num_ranges, void *stream) {
+  if (!h || session < 0 || session >= h->S || num_ranges < 0 || (num_ranges > 0 && !ranges)) return OKVQ_EINVAL;
+  const long long T = h->len[session];
+  long long p0 = -1, p1 = -1;
+  for (int i = 0; i < num_ranges; ++i) {
+    const long long b = ranges[2 * i], e = ranges[2 * i + 1];
+    if (b < 0 || e < b || e > T) return OKVQ_EINVAL;
+    if (e == b) continue;
+    p0 = p0 < 0 ? b / PAGE : std::min(p0, b / PAGE);
+    p1 = std::max(p1, (e - 1) / PAGE + 1);
+  }
+  if (p0 < 0) return OKVQ_OK;
+  for (int i = 0; i < num_ranges; ++i)
+    for (long long t = ranges[2 * i]; t < ranges[2 * i + 1]; ++t) set_dead_bit(h->dead[session], t, true);
+  return push_page_meta(h, session, p0, p1, static_cast<cudaStream_t>(stream));
+}
+
+okvq_status okvq_live_length(const okvq_cache *h, int32_t session, int64_t *tokens) {
+  if (!h || !tokens || session < 0 || session >= h->S) return OKVQ_EINVAL;
+  const long long T = h->len[session];
+  long long dead = 0;
+  for (long long p = 0; p < (T + PAGE - 1) / PAGE; ++p) dead += __builtin_popcountll(h->dead[session][p]);
+  *tokens = T - dead;
+  return OKVQ_OK;
+}
+
+okvq_status okvq_compaction_granule(const okvq_cache *h, int32_t *tokens) {
+  if (!h || !tokens) return OKVQ_EINVAL;
+  *tokens = compaction_granule(h->KG);
+  return OKVQ_OK;
+}
+
+okvq_status okvq_plan_compaction(const uint8_t *dead, int64_t length, int32_t granule, int32_t min_pages_saved,
+                                 int64_t *suffix_begin, int64_t *new_length, int32_t *num_moves) {
+  if (length < 0 || (length > 0 && !dead) || min_pages_saved < 1 || !suffix_begin || !new_length || !num_moves)
+    return OKVQ_EINVAL;
+  if (granule != 16 && granule != 32 && granule != 64) return OKVQ_EINVAL;
+  const long long ng = (length + granule - 1) / granule;
+  std::vector<char> empty(ng, 1);
+  for (long long t = 0; t < length; ++t)
+    if (!dead[t]) empty[t / granule] = 0;
+  const CompactionPlan p = plan_suffix(empty, length, granule, min_pages_saved);
+  *suffix_begin = p.sg < 0 ? -1 : p.sg * granule;
+  *new_length = p.sg < 0 ? length : p.T2;
+  *num_moves = (int32_t)(p.moves.size() / 2);
+  return OKVQ_OK;
+}
+
+okvq_status okvq_compact(okvq_cache *h, int32_t session, int32_t min_pages_saved, int64_t *new_length,
+                         int32_t *moved_granules, void *stream) {
+  if (!h || session < 0 || session >= h->S || min_pages_saved < 1) return OKVQ_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long T = h->len[session];
+  const int gran = compaction_granule(h->KG);
+  const long long ng = (T + gran - 1) / gran;
+  std::vector<char> empty(ng, 1);
+  for (long long t = 0; t < T; ++t)
+    if (!dead_bit(h->dead[session], t)) empty[t / gran] = 0;
+  const CompactionPlan p = plan_suffix(empty, T, gran, min_pages_saved);
+  const int n = (int)(p.moves.size() / 2);
+  if (new_length) *new_length = p.sg < 0 ? T : p.T2;
+  if (moved_granules) *moved_granules = n;
+  if (p.sg < 0) return OKVQ_OK;
+  const int LH = h->L * h->Hkv;
+  if (n > 0) {
+    const int stride = compaction_stride(h->PL, h->KG);
+    const size_t per_move = (size_t)(LH + 1) * stride;
+    const int batch = (int)std::min<size_t>((size_t)n, h->cscratch_bytes / per_move);
+    OKVQ_TRY(cudaMemcpyAsync(h->moves_dev, p.moves.data(), p.moves.size() * sizeof(int), cudaMemcpyHostToDevice, s));
+    MoveArgs m{};
+    m.pages = h->pages;
+    m.mod = h->mod;
+    m.scratch = h->cscratch;
+    m.LH = LH;
+    m.KG = h->KG;
+    m.session = session;
+    m.stride = stride;
+    m.P_max = h->P_max;
+    m.cap = h->cap;
+    m.PL = h->PL;
+    // every destination of a batch lies below every source of the later batches,
+    // and a batch's sources are all gathered before any of its destinations is written
+    for (int k0 = 0; k0 < n; k0 += batch) {
+      m.moves = h->moves_dev + 2 * k0;
+      m.n = std::min(batch, n - k0);
+      m.scatter = 0;
+      OKVQ_TRY(launch_move(m, s));
+      m.scatter = 1;
+      OKVQ_TRY(launch_move(m, s));
+    }
+  }
+  // the host copy of the deletion masks follows the moves
+  std::vector<unsigned long long> &w = h->dead[session];
+  for (int k = 0; k < n; ++k) {
+    const long long src = (long long)p.moves[2 * k] * gran, dst = (long long)p.moves[2 * k + 1] * gran;
+    const long long cnt = std::min<long long>(gran, T - src);
+    for (long long i = 0; i < cnt; ++i) set_dead_bit(w, dst + i, dead_bit(w, src + i));
+  }
+  for (long long t = p.T2; t < T; ++t) set_dead_bit(w, t, false);
+  h->len[session] = p.T2;
+  h->dirty = true;
+  return push_page_meta(h, session, (p.sg * gran) / PAGE, (T + PAGE - 1) / PAGE, s);
+}
+
 okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, size_t *bytes) {
   if (!h || !bytes || session < 0 || session >= h->S) return OKVQ_EINVAL;
   const long long T = h->len[session];
@@ -619,8 +811,8 @@ okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, si
   const size_t n_kc = (size_t)LH * Tf * B,
                n_ks = turbo ? (size_t)LH * T * 2 : (size_t)LH * (Tf / G) * 2 * D * 2,
                n_kt = (size_t)LH * (T - Tf) * D * 2, n_vc = (size_t)LH * T * B, n_vn = (size_t)LH * T * 2,
-               n_md = (size_t)T;
-  const size_t need = n_kc + n_ks + n_kt + n_vc + n_vn + n_md;
+               n_md = (size_t)T, n_dd = (size_t)LH * T;
+  const size_t need = n_kc + n_ks + n_kt + n_vc + n_vn + n_md + n_dd;
   if (!host_buf) {
     *bytes = need;
     return OKVQ_OK;
@@ -630,7 +822,7 @@ okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, si
   OKVQ_TRY(cudaDeviceSynchronize());
   uint8_t *out = static_cast<uint8_t *>(host_buf);
   uint8_t *o_kc = out, *o_ks = o_kc + n_kc, *o_kt = o_ks + n_ks, *o_vc = o_kt + n_kt, *o_vn = o_vc + n_vc,
-          *o_md = o_vn + n_vn;
+          *o_md = o_vn + n_vn, *o_dd = o_md + n_md;
   std::memset(out, 0, need);
   const long long npages = (T + PAGE - 1) / PAGE;
   const PageLayout PL = h->PL;
@@ -669,6 +861,9 @@ okvq_status okvq_export_state(okvq_cache *h, int32_t session, void *host_buf, si
         }
       }
       std::memcpy(o_vn + (lh * T + t) * 2, p + PL.off_norm + tt * 2, 2);
+      unsigned long long dw;
+      std::memcpy(&dw, p + PL.off_tmask + DEAD_OFF, 8);
+      o_dd[lh * T + t] = (uint8_t)((dw >> tt) & 1ull);
     }
     if (turbo) {
       for (long long t = 0; t < T; ++t)

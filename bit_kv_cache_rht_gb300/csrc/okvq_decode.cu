@@ -288,9 +288,11 @@ struct HalfPageCtx {
 // One 32-token half page (two 16-token tiles) starting at page-relative token
 // 32*hp of the staged page sp. FULLV: all 32 tokens exist and are quantized.
 // SINGLE: every token of the page has modality ma.cur (checked by the caller).
+// dead: the half page's deletion bits (bit i: token 32*hp + i was evicted); the
+// caller guarantees at least one live token.
 template <int BITS, int G, bool FULLV, bool SINGLE>
 __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout &PL, const unsigned char *sp,
-                                          int tok0, int hp, float beta,
+                                          int tok0, int hp, uint32_t dead, float beta,
                                           float (&acc)[8][4], ModAcc &ma, float &m_run, float &l_run,
                                           const uint4 (&qreg)[8]) {
   constexpr int LANE_WORDS = BITS * 2;
@@ -384,7 +386,8 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
       // the group offset joins after the MMA chain (it does not wait for it)
       const float v = KT ? (sacc[n][e] + sacc[n][2 + e]) * ((e ? kn.y : kn.x) * INV_SQRT_D)
                          : sacc[n][e] + sacc[n][2 + e] + ((FULLV || hs < c.Tf) ? beta : 0.f);
-      s[n][e] = (FULLV || hs + 8 * n + 2 * t4 + e < c.T) ? v : -INFINITY;
+      const int o = 8 * n + 2 * t4 + e;
+      s[n][e] = ((FULLV || hs + o < c.T) && !((dead >> o) & 1u)) ? v : -INFINITY;
     }
   }
 
@@ -674,6 +677,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
 
       // modalities present in the page: one (the common case) runs without per-tile checks
       const uint32_t tmw = *reinterpret_cast<const uint32_t *>(sp + PL.off_tmask);
+      const unsigned long long dead = *reinterpret_cast<const unsigned long long *>(sp + PL.off_tmask + DEAD_OFF);
       const uint32_t pmask = (tmw | (tmw >> 8) | (tmw >> 16) | (tmw >> 24)) & 0xFFu;
       const bool single = __popc(pmask) == 1;
       if (single && __ffs(pmask) - 1 != ma.cur) mod_switch(ma, acc, __ffs(pmask) - 1);
@@ -681,17 +685,23 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
       for (int hp = 0; hp < 2; ++hp) {
         const int hs = tok0 + 32 * hp;
         if (hs >= T) break;
+        const uint32_t dh = (uint32_t)(dead >> (32 * hp));
+        if (dh) {                                 // evicted tokens: skip the half page if none is live
+          const int nv = min(32, T - hs);
+          if (!((nv >= 32 ? 0xFFFFFFFFu : (1u << nv) - 1u) & ~dh)) continue;
+        }
         const float beta = (G == 32 && hp == 1) ? beta_g1 : beta_g0;
+        const bool full = hs + 32 <= Tf;
         if (single) {
-          if (hs + 32 <= Tf)
-            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
+          if (full)
+            half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
+            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
         } else {
-          if (hs + 32 <= Tf)
-            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
+          if (full)
+            half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, beta, acc, ma, m_run, l_run, qreg);
+            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
         }
       }
       __syncwarp();

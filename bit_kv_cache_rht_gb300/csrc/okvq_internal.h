@@ -11,7 +11,10 @@
 //     stats    64/G groups, each [min 128 fp16 | range 128 fp16] in the stat channel order
 //              (TurboQuant keys, G = 0 below: 64 fp16 key norms, token order)
 //     tmask    4 bytes, bit m of byte i set when tile i holds a token of modality m,
-//              then 12 bytes of padding (page size stays a multiple of 16 B)
+//              4 bytes of padding, then the 64-bit deletion mask (bit t set: page
+//              token t was evicted and is skipped by attention; the same in every
+//              (layer, kv head) of a session); the field is 16 B so the page size
+//              stays a multiple of 16 B
 //   so one decode warp streams one contiguous block per page with a single bulk copy.
 //
 // Lane chunks: the 32 lanes of a warp running mma.m16n8k16 hold 16x16 / 16x8
@@ -66,7 +69,7 @@ struct PageLayout {
   int off_v;        // 4 tiles of K codes
   int off_norm;
   int off_stats;
-  int off_tmask;    // 4 tile modality masks
+  int off_tmask;    // 4 tile modality masks, then (at +8) the 64-bit deletion mask
   int page_bytes;
 };
 
@@ -191,6 +194,42 @@ struct CombineArgs {
 };
 
 constexpr int PARTIAL_FLOATS = 2 + MAXM * D;   // m, l, o[M][D]
+constexpr int DEAD_OFF = 8;                     // deletion mask: page offset off_tmask + DEAD_OFF
+
+// Compaction granule: the tokens that move together (a key group, whose statistics
+// serve all its members, or one 16-token tile for TurboQuant keys).
+__host__ __device__ inline int compaction_granule(int KG) { return KG ? KG : TILE; }
+
+// Bytes of one granule of one (layer, kv head) in the gather scratch: K code tiles,
+// V code tiles, value norms, key statistics (one group) or key norms, tile masks;
+// rounded up to 16 B.
+__host__ __device__ inline int granule_payload(const PageLayout &PL, int KG) {
+  const int gran = compaction_granule(KG), nt = gran / TILE;
+  const int b = 2 * nt * PL.tile_bytes + 2 * gran + (KG ? 2 * D * 2 : 2 * gran) + nt;
+  return (b + 15) & ~15;
+}
+
+struct MoveArgs {
+  uint8_t *pages;
+  uint8_t *mod;             // [S][cap]
+  const int *moves;         // [n][2] (source granule, destination granule), this batch
+  uint8_t *scratch;         // [n][LH + 1][stride]: per unit payloads, then the modality ids
+  int n, LH, KG, session;
+  int stride;               // bytes per (move, unit) slot, >= granule_payload and the granule's ids
+  int scatter;              // 0: pages -> scratch, 1: scratch -> pages
+  long long P_max, cap;
+  PageLayout PL;
+};
+
+struct PageMetaArgs {
+  uint8_t *pages;
+  const unsigned long long *dead;   // [P_max] this session's deletion masks
+  int LH, session;
+  long long p0;             // first page rewritten
+  long long T;              // session length: tile masks of tiles at or past it are cleared
+  long long P_max;
+  PageLayout PL;
+};
 
 // Kernel attributes belong to a device: run `set` once per device ordinal (the
 // current device; ordinals >= 64 run it on every call). `done` holds one bit per
@@ -211,5 +250,7 @@ cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 size_t decode_smem_bytes(int bits, int G);
+cudaError_t launch_move(const MoveArgs &a, cudaStream_t s);
+cudaError_t launch_page_meta(const PageMetaArgs &a, int n_pages, cudaStream_t s);
 
 }  // namespace okvq

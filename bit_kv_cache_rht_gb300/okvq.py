@@ -24,7 +24,8 @@ OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT = 0, 1   # key codecs (okvq_config.k
 EXPORTS = (
     "okvq_create", "okvq_free", "okvq_append_chunk", "okvq_decode", "okvq_length", "okvq_export_state",
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
-    "okvq_decode_static_scratch", "okvq_calibrate_rotations",
+    "okvq_decode_static_scratch", "okvq_calibrate_rotations", "okvq_live_length", "okvq_evict",
+    "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact",
 )
 
 
@@ -71,6 +72,12 @@ def load() -> ctypes.CDLL:
     L.okvq_decode.argtypes = [vp, vp, vp, vp]
     L.okvq_decode_static_scratch.argtypes = [vp, vp, vp, vp]
     L.okvq_calibrate_rotations.argtypes = [i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp]
+    L.okvq_live_length.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
+    L.okvq_evict.argtypes = [vp, i32, vp, i32, vp]
+    L.okvq_compaction_granule.argtypes = [vp, ctypes.POINTER(i32)]
+    L.okvq_plan_compaction.argtypes = [vp, ctypes.c_int64, i32, i32, ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(i32)]
+    L.okvq_compact.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(i32), vp]
     L.okvq_length.argtypes = [vp, i32, ctypes.POINTER(i64)]
     L.okvq_export_state.argtypes = [vp, i32, vp, ctypes.POINTER(ctypes.c_size_t)]
     L.okvq_codebook.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
@@ -158,6 +165,41 @@ def okvq_length(h, session: int):
     n = ctypes.c_int64()
     st = load().okvq_length(h, session, ctypes.byref(n))
     return st, n.value
+
+
+def okvq_live_length(h, session: int):
+    n = ctypes.c_int64()
+    st = load().okvq_live_length(h, session, ctypes.byref(n))
+    return st, n.value
+
+
+def okvq_evict(h, session: int, ranges, stream: int = 0) -> int:
+    """ranges: sequence of (begin, end) slot pairs (host)."""
+    arr = np.ascontiguousarray(np.asarray(ranges, np.int64).reshape(-1, 2))
+    return load().okvq_evict(h, session, arr.ctypes.data_as(ctypes.c_void_p) if len(arr) else None, len(arr),
+                             ctypes.c_void_p(stream))
+
+
+def okvq_compaction_granule(h):
+    n = ctypes.c_int32()
+    st = load().okvq_compaction_granule(h, ctypes.byref(n))
+    return st, n.value
+
+
+def okvq_plan_compaction(dead, length: int, granule: int, min_pages_saved: int):
+    """dead: host bytes [length] (nonzero = deleted). Returns (status, suffix_begin, new_length, num_moves)."""
+    d = np.ascontiguousarray(np.asarray(dead, np.uint8))
+    sb, nl, nm = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    st = load().okvq_plan_compaction(d.ctypes.data_as(ctypes.c_void_p) if length > 0 else None, length, granule,
+                                     min_pages_saved, ctypes.byref(sb), ctypes.byref(nl), ctypes.byref(nm))
+    return st, sb.value, nl.value, nm.value
+
+
+def okvq_compact(h, session: int, min_pages_saved: int, stream: int = 0):
+    """Returns (status, new_length, moved_granules)."""
+    nl, nm = ctypes.c_int64(), ctypes.c_int32()
+    st = load().okvq_compact(h, session, min_pages_saved, ctypes.byref(nl), ctypes.byref(nm), ctypes.c_void_p(stream))
+    return st, nl.value, nm.value
 
 
 def okvq_status_string(s: int) -> str:
@@ -257,6 +299,26 @@ class Cache:
         _check(st, "okvq_length")
         return n
 
+    def live_length(self, session: int) -> int:
+        st, n = okvq_live_length(self._h, session)
+        _check(st, "okvq_live_length")
+        return n
+
+    def evict(self, session: int, ranges, stream=None) -> None:
+        """Delete [begin, end) slot ranges of a session (holes that decode skips)."""
+        _check(okvq_evict(self._h, session, ranges, _stream_handle(stream)), "okvq_evict")
+
+    def compaction_granule(self) -> int:
+        st, n = okvq_compaction_granule(self._h)
+        _check(st, "okvq_compaction_granule")
+        return n
+
+    def compact(self, session: int, min_pages_saved: int = 1, stream=None):
+        """Ordered-suffix compaction; returns (new_length, moved_granules)."""
+        st, nl, nm = okvq_compact(self._h, session, min_pages_saved, _stream_handle(stream))
+        _check(st, "okvq_compact")
+        return nl, nm
+
     def codebook(self):
         n = 1 << self.bits
         lv = (ctypes.c_float * n)()
@@ -313,4 +375,6 @@ class Cache:
         take("vcodes", n * T * B, np.uint8, (*LH, T, B))
         take("vnorm", n * T, np.float16, (*LH, T))
         take("mod", T, np.uint8, (T,))
+        take("dead", n * T, np.uint8, (*LH, T))
+        out["dead"] = out["dead"].astype(bool)
         return out

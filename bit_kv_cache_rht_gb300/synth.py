@@ -87,6 +87,28 @@ class Session:
         return out
 
 
+def retention_ranges(session: "Session", keep_recent: int = 4, sinks=(64, 8, None)) -> List[tuple]:
+    """Token ranges a unit-aware retention policy would delete (the shape of
+    OmniPick's plans, "OmniTide" section 5.1; the policy itself is not part of
+    this library): every chunk but the last ``keep_recent`` keeps, of each run of
+    one modality, only its first sinks[m] tokens (None: the whole run); the rest
+    of the run is one deletion range."""
+    out = []
+    mod = session.modality()
+    bounds = session.chunk_bounds()
+    for a, b in bounds[:max(0, len(bounds) - keep_recent)]:
+        t = a
+        while t < b:
+            e = t
+            while e < b and mod[e] == mod[t]:
+                e += 1
+            k = sinks[mod[t]]
+            if k is not None and t + k < e:
+                out.append((t + k, e))
+            t = e
+    return out
+
+
 def interleave_pattern(period: Sequence[tuple], total: int) -> np.ndarray:
     """Repeat blocks [(modality, count), ...] until ``total`` tokens."""
     block = np.concatenate([np.full(n, m, np.uint8) for m, n in period])

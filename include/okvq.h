@@ -168,8 +168,62 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
  * rebuilt and uploaded on `stream`); otherwise as okvq_decode. */
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream);
 
-/* Number of tokens held by `session`. */
+/* Number of token slots of `session`: its physical span, holes included (the
+ * next append lands at this index). */
 okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
+
+/* Slots of `session` that hold a token that was not evicted. */
+okvq_status okvq_live_length(const okvq_cache *h, int32_t session, int64_t *tokens);
+
+/* ---- eviction and compaction ("OmniTide: Co-Designing Algorithms and Systems
+ * for Efficient On-Device Omni-LLM Streaming", section 5.2 Applying the
+ * retention plan and section 6.2 Selective and efficient KV migration) ---- */
+
+/* Delete token slots of `session` in every (layer, kv head): `ranges` is a HOST
+ * array of num_ranges [begin, end) pairs of slot indices, 0 <= begin <= end <=
+ * okvq_length. Deleted tokens stay in their slots as holes that okvq_decode
+ * skips (they take no part in the softmax); a session whose every token is
+ * deleted decodes to zeros. Deleting a deleted slot again is allowed. Key group
+ * statistics are not recomputed: the survivors of a group keep its statistics,
+ * and a group still open when some of its members are deleted is completed by
+ * later appends over all its members. Logical positions (RoPE) are the caller's.
+ * Asynchronous on `stream` (one small copy and one kernel); the slot count is
+ * unchanged. OKVQ_EINVAL for a bad session, a range outside [0, length] or
+ * end < begin (nothing changes). */
+okvq_status okvq_evict(okvq_cache *h, int32_t session, const int64_t *ranges, int32_t num_ranges, void *stream);
+
+/* Tokens that compaction moves as one unit: the key group size, or 16 (one tile)
+ * with OKVQ_KEYS_TURBOQUANT. A key group moves whole because its statistics
+ * serve all its members. */
+okvq_status okvq_compaction_granule(const okvq_cache *h, int32_t *tokens);
+
+/* The ordered-suffix migration plan, on the host (no handle, no GPU): with
+ * `dead` a HOST array of `length` bytes (nonzero = deleted) and granules of
+ * `granule` slots (16, 32 or 64), scan suffix starts s (multiples of the
+ * granule) from the end backward; packing the suffix's granules that still hold
+ * a live token to s, s + granule, ... in their order gives a new length T'; the
+ * first (shortest) suffix with ceil(length/64) - ceil(T'/64) >= min_pages_saved
+ * (>= 1) is the plan. Outputs: *suffix_begin = s (-1 when no suffix saves enough:
+ * nothing moves), *new_length = T' (length when none), *num_moves = granules whose
+ * slot changes. OKVQ_EINVAL for bad sizes or NULL pointers. */
+okvq_status okvq_plan_compaction(const uint8_t *dead, int64_t length, int32_t granule, int32_t min_pages_saved,
+                                 int64_t *suffix_begin, int64_t *new_length, int32_t *num_moves);
+
+/* Plan (as okvq_plan_compaction, with the handle's granule and its deletions)
+ * and apply the ordered-suffix compaction of `session`: the moved granules'
+ * codes, statistics, norms, modality ids, masks and deletion bits are gathered
+ * into a scratch buffer, then written to their new slots (so no move overwrites
+ * another's source); the session's slot count becomes *new_length. The fp16
+ * trailing keys of an open group need no move: a granule moves by whole groups,
+ * so every token keeps its place within its group. The slot of a token that did
+ * not move is unchanged; a moved token's new slot is its old slot minus the
+ * granules removed before it. Outputs (host, may be NULL): *new_length,
+ * *moved_granules (0 when no suffix saves min_pages_saved pages: nothing changes).
+ * Asynchronous on `stream`; nothing is allocated (okvq_create reserves the
+ * scratch: room for every granule of one session, at most 64 MB, and larger
+ * plans run in batches). OKVQ_EINVAL for a bad session or min_pages_saved < 1. */
+okvq_status okvq_compact(okvq_cache *h, int32_t session, int32_t min_pages_saved, int64_t *new_length,
+                         int32_t *moved_granules, void *stream);
 
 /* Copy the stored state of `session` to host memory in the canonical layout
  * (synchronizes the device). With host_buf == NULL only *bytes is set. With
@@ -180,6 +234,8 @@ okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
  *   vcodes  uint8 [L][Hkv][T][B]
  *   vnorm   fp16  [L][Hkv][T]
  *   mod     uint8 [T]
+ *   dead    uint8 [L][Hkv][T]   1 where the token was evicted (read from each
+ *                               (layer, kv head)'s own pages)
  * With OKVQ_KEYS_TURBOQUANT every key is quantized (Tf = T) and kstats/ktail
  * are replaced by knorm fp16 [L][Hkv][T] (|k|).
  * *bytes must hold the buffer size on entry (OKVQ_EINVAL if too small). */

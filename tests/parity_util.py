@@ -80,7 +80,7 @@ def compare_state(gpu_state: dict, oc, session: int, layers_gpu_index, bits: int
     Returns counts: boundary code mismatches (allowed) and strict mismatches
     (must be 0) for keys/values/norms, plus stats/tail/mod equality flags."""
     res = dict(k_strict=0, k_bnd=0, v_strict=0, v_bnd=0, n_strict=0, n_bnd=0, stats_ok=True, tail_ok=True,
-               mod_ok=True, k_codes=0, v_codes=0)
+               mod_ok=True, dead_ok=True, k_codes=0, v_codes=0)
     turbo = "knorm" in gpu_state
     for i, l in enumerate(oc.layers):
         li = layers_gpu_index[i]
@@ -93,6 +93,8 @@ def compare_state(gpu_state: dict, oc, session: int, layers_gpu_index, bits: int
                 one_ulp = np.abs(gn.view(np.uint16).astype(np.int32) - on.view(np.uint16).astype(np.int32)) <= 1
                 res["n_strict"] += int(np.sum(nd & ~(e["knbnd"] & one_ulp)))
                 res["n_bnd"] += int(np.sum(nd & e["knbnd"] & one_ulp))
+            if not np.array_equal(gpu_state["dead"][li, h], e["dead"]):
+                res["dead_ok"] = False
             gk = o.unpack_codes(gpu_state["kcodes"][li, h], bits)
             ok_ = o.unpack_codes(e["kcodes"], bits)
             diff = gk != ok_
@@ -150,6 +152,7 @@ def assert_state_matches(res):
     assert res["stats_ok"], "key group statistics differ"
     assert res["tail_ok"], "fp16 key tail differs"
     assert res["mod_ok"], "modality ids differ"
+    assert res["dead_ok"], "deletion masks differ"
     assert res["k_strict"] == 0, res
     assert res["v_strict"] == 0, res
     assert res["n_strict"] == 0, res
