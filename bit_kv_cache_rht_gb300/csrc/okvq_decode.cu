@@ -213,11 +213,18 @@ __device__ __forceinline__ uint32_t lut_addr(uint32_t laneoff, uint32_t w) {
   return r;
 }
 
+// Cross-warp merge area of one segment (aliases the stage ring). Rows of o are
+// padded so that a warp's fragment stores (lane (g, t4) -> head 2t4 + e, channel
+// 16mt + g) hit 32 distinct banks.
+constexpr int MG_ROW = D + 4;
 template <int WARPS>
 struct Merge {
   float m[WARPS][MAXGQ];
   float l[WARPS][MAXGQ];
-  float o[WARPS][MAXM][MAXGQ][D];
+  float sc[WARPS][MAXGQ];        // exp2(m_w - M) per (warp, head)
+  float mx[MAXGQ];               // M per head
+  uint32_t held[WARPS];          // modalities each warp accumulated
+  float o[WARPS][MAXM][MAXGQ][MG_ROW];
 };
 
 // value tile of one modality: acc[mt] += Lcode[16 ch x 16 tok] * P
@@ -386,9 +393,16 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
       // the group offset joins after the MMA chain (it does not wait for it)
       const float v = KT ? (sacc[n][e] + sacc[n][2 + e]) * ((e ? kn.y : kn.x) * INV_SQRT_D)
                          : sacc[n][e] + sacc[n][2 + e] + ((FULLV || hs < c.Tf) ? beta : 0.f);
-      const int o = 8 * n + 2 * t4 + e;
-      s[n][e] = ((FULLV || hs + o < c.T) && !((dead >> o) & 1u)) ? v : -INFINITY;
+      s[n][e] = (FULLV || hs + 8 * n + 2 * t4 + e < c.T) ? v : -INFINITY;
     }
+  }
+  if (dead) {                                 // evicted tokens take no part in the softmax
+    const uint32_t dl = dead >> (2 * t4);
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if ((dl >> (8 * n + e)) & 1u) s[n][e] = -INFINITY;
   }
 
   // ---- online softmax (base 2) for head g ----
@@ -487,8 +501,10 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   uint4 *qfrag = reinterpret_cast<uint4 *>(qraw + MAXGQ * D);           // [8 kb][32 lanes]
   uint64_t *bars = reinterpret_cast<uint64_t *>(qfrag + 8 * 32);        // [WARPS][STAGES]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + WARPS * STAGES);
-  unsigned char *stages = reinterpret_cast<unsigned char *>(tmem_slot + 4);
-  stages = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
+  // 128-byte aligned stage ring, as an offset from the (aligned) shared base: a round
+  // trip through an integer would hide that these are shared-memory addresses
+  const size_t stage_off = (reinterpret_cast<unsigned char *>(tmem_slot + 4) - smem + 127) & ~size_t(127);
+  unsigned char *stages = smem + stage_off;
   Merge<WARPS> &MG = *reinterpret_cast<Merge<WARPS> *>(stages);
   unsigned char *my_stage0 = stages + (size_t)warp * STAGES * PL.page_bytes;
   uint64_t *my_bars = bars + warp * STAGES;
@@ -725,44 +741,49 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     // ---- per-warp totals: head g lives in lanes 4g..4g+3 ----
     l_run += __shfl_xor_sync(FULL, l_run, 1);
     l_run += __shfl_xor_sync(FULL, l_run, 2);
+    const uint32_t held = ma.live | (ma.cur >= 0 ? 1u << ma.cur : 0u);
     if (t4 == 0) {
       MG.m[warp][g] = m_run;
       MG.l[warp][g] = l_run;
     }
+    if (lane == 0) MG.held[warp] = held;
 #pragma unroll 1
     for (int m = 0; m < MAXM; ++m) {
-      const bool held = m == ma.cur || ((ma.live >> m) & 1u);
-      if (held && m != ma.cur) mod_switch(ma, acc, m);
+      if (!((held >> m) & 1u)) continue;       // readers skip what a warp never held
+      if (m != ma.cur) mod_switch(ma, acc, m);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        MG.o[warp][m][2 * t4][16 * mt + g] = held ? acc[mt][0] : 0.f;
-        MG.o[warp][m][2 * t4 + 1][16 * mt + g] = held ? acc[mt][1] : 0.f;
-        MG.o[warp][m][2 * t4][16 * mt + g + 8] = held ? acc[mt][2] : 0.f;
-        MG.o[warp][m][2 * t4 + 1][16 * mt + g + 8] = held ? acc[mt][3] : 0.f;
+        MG.o[warp][m][2 * t4][16 * mt + g] = acc[mt][0];
+        MG.o[warp][m][2 * t4 + 1][16 * mt + g] = acc[mt][1];
+        MG.o[warp][m][2 * t4][16 * mt + g + 8] = acc[mt][2];
+        MG.o[warp][m][2 * t4 + 1][16 * mt + g + 8] = acc[mt][3];
       }
     }
     __syncthreads();
     float *part = a.partials + (long long)seg * MAXGQ * PARTIAL_FLOATS;
+    // per-(warp, head) scales, once; then every (head, channel) sums the warps that held data
+    if (tid < MAXGQ) {
+      float M = -INFINITY, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) M = fmaxf(M, MG.m[w][tid]);
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) {
+        const float sc = MG.m[w][tid] == -INFINITY ? 0.f : ex2(MG.m[w][tid] - M);
+        MG.sc[w][tid] = sc;
+        L += sc * MG.l[w][tid];
+      }
+      part[tid * PARTIAL_FLOATS + 0] = M;
+      part[tid * PARTIAL_FLOATS + 1] = L;
+    }
+    __syncthreads();
     for (int i = tid; i < MAXGQ * D; i += THREADS) {
       const int hh = i / D, ch = i % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) M = fmaxf(M, MG.m[w][hh]);
-      float wsc[WARPS];
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) wsc[w] = MG.m[w][hh] == -INFINITY ? 0.f : ex2(MG.m[w][hh] - M);
       float *ph = part + hh * PARTIAL_FLOATS;
-      if (ch == 0) {
-        float L = 0.f;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) L += wsc[w] * MG.l[w][hh];
-        ph[0] = M;
-        ph[1] = L;
-      }
       for (int m = 0; m < a.M; ++m) {
         float o = 0.f;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) o += wsc[w] * MG.o[w][m][hh][ch];
+        for (int w = 0; w < WARPS; ++w)
+          if ((MG.held[w] >> m) & 1u) o = fmaf(MG.sc[w][hh], MG.o[w][m][hh][ch], o);
         ph[2 + m * D + ch] = o;
       }
     }
