@@ -38,6 +38,11 @@ page-rounded span by enough pages, preserving their order.  Here the unit that
 moves is a key group (its statistics serve all its members) or, for TurboQuant
 keys, a 16-token tile.
 
+Far memory ("ProtoKV: Streaming Video Understanding under Delayed Query with
+Summary-State Memory", section 3.3 Eq. (2) and Algorithm 4): pseudo tokens
+synthesized by the caller join the softmax with the additive log-mass bias
+log n_k of their prototype; the near window is this cache.
+
 TurboQuant key codec (the pages' comparison point, ``key_codec="turbo"``):
 every key is coded on arrival like a value, with the shared randomized Hadamard
 rotation instead of a modality eigenbasis (norm, direction rotated, fixed
@@ -466,6 +471,58 @@ class OracleUnit:
             out += o_m @ R64[m]                                              # R_m^T o_m for each head
         return out / l[:, None]
 
+    # ---- pseudo-token far memory ("ProtoKV: Streaming Video Understanding under
+    # Delayed Query with Summary-State Memory", section 3.3 Eq. (2), Appendix A.3
+    # Eq. (4) and Algorithm 4) ----
+    def decode_with_pseudo(self, q16: np.ndarray, kf16: np.ndarray, vf16: np.ndarray, mass: np.ndarray,
+                           per_proto: int) -> np.ndarray:
+        """One softmax over this unit's cache (the near window, bias 0, deleted
+        tokens skipped) and far pseudo tokens kf16, vf16 [n_far][d] (fp16, the
+        original key / value bases): pseudo token j belongs to prototype
+        j // per_proto, whose mass n = mass[j // per_proto] adds log n to its
+        logit q.k/sqrt d; prototypes with n = 0 are inactive and skipped.
+        Returns fp64 [Gq][d] (zeros when nothing is attended)."""
+        d, G, T, Tf = self.d, self.G, self.T, self.T_full
+        Gq = q16.shape[0]
+        q = q16.astype(F64)
+        nf = len(kf16)
+        n = np.asarray(mass, F64)[np.arange(nf) // per_proto] if nf else np.zeros(0)
+        sf = q @ np.asarray(kf16, F64).T / math.sqrt(d)                    # [Gq][n_far]
+        with np.errstate(divide="ignore"):
+            sf = sf + np.log(n)[None]                                       # log 0 = -inf: inactive
+        s = np.full((Gq, T), -np.inf)
+        if T:
+            qr = rotate_f64(q, self.signs) / math.sqrt(d)
+            if self.key_codec == "turbo":
+                s[:] = (qr @ self.cb.levels[self.kcodes[:T]].T) * (self.knorm[:T].astype(F64) / math.sqrt(d))[None]
+            elif Tf:
+                ng = Tf // G
+                lam = self.cb.ktab[self.kcodes[:Tf]].reshape(ng, G, d)
+                beta = qr @ self.kmn[:ng].astype(F64).T
+                a = qr[:, None, :] * self.krg[:ng].astype(F64)[None]
+                s[:, :Tf] = (beta[:, :, None] + np.einsum("hgc,gtc->hgt", a, lam)).reshape(Gq, Tf)
+            if T > Tf:
+                s[:, Tf:] = q @ self.keys16[Tf:T].astype(F64).T / math.sqrt(d)
+            s[:, self.dead[:T]] = -np.inf
+        mmax = max(s.max() if T else -np.inf, sf.max() if nf else -np.inf)
+        out = np.zeros((Gq, d), F64)
+        if mmax == -np.inf:
+            return out
+        mrow = np.maximum(s.max(axis=1) if T else -np.inf, sf.max(axis=1) if nf else -np.inf)[:, None]
+        p = np.exp(s - mrow)
+        pf = np.exp(sf - mrow)
+        l = p.sum(axis=1) + pf.sum(axis=1)
+        if T:
+            lv = self.cb.levels[self.vcodes[:T]] / math.sqrt(d)
+            wv = lv * self.vnorm[:T].astype(F64)[:, None]
+            R64 = self.R.astype(F64)
+            for m in range(self.R.shape[0]):
+                sel = self.mod[:T] == m
+                if sel.any():
+                    out += (p[:, sel] @ wv[sel]) @ R64[m]
+        out += pf @ np.asarray(vf16, F64)
+        return out / l[:, None]
+
     def dequantized(self):
         """Explicit K-hat, V-hat [T][d] in the original bases (for brute-force attention)."""
         d, G, T, Tf = self.d, self.G, self.T, self.T_full
@@ -603,6 +660,19 @@ class OracleCache:
             for u in units:
                 u.move_granules(plan[2], gran, plan[1])
         return plan
+
+    def decode_with_pseudo(self, Q16, KF, VF, MASS, per_proto):
+        """Q16 [S][L][Hq][d]; KF, VF [S][L][Hkv][n_far][d] fp16; MASS [S][L][Hkv][n_far / per_proto]
+        -> fp64 [S][L'][Hq][d] for the oracle's layers."""
+        gq = self.Hq // self.Hkv
+        out = np.zeros((self.S, len(self.layers), self.Hq, self.d), F64)
+        for s in range(self.S):
+            for i, l in enumerate(self.layers):
+                for h in range(self.Hkv):
+                    u = self.units[(s, l, h)]
+                    out[s, i, h * gq:(h + 1) * gq] = u.decode_with_pseudo(
+                        Q16[s, l, h * gq:(h + 1) * gq], KF[s, l, h], VF[s, l, h], MASS[s, l, h], per_proto)
+        return out
 
     def decode(self, Q16, brute=False):
         """Q16 [S][L][Hq][d] -> fp64 [S][L'][Hq][d] for the oracle's layers."""

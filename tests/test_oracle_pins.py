@@ -660,3 +660,56 @@ def test_compaction_equals_never_having_appended_the_removed_granules(key_codec,
     for key in eb:
         assert np.array_equal(ea[key], eb[key]), key
     assert np.allclose(A.decode(q), B.decode(q), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- pseudo-token far memory
+
+def _far(r, n_proto, per, scale=1.0):
+    c = r.standard_normal((n_proto, 128)) * 2.0                              # prototype centres
+    kf = (np.repeat(c, per, axis=0) + 0.3 * r.standard_normal((n_proto * per, 128))) * scale
+    vf = np.repeat(r.standard_normal((n_proto, 128)), per, axis=0) + 0.2 * r.standard_normal((n_proto * per, 128))
+    return kf.astype(F16), vf.astype(F16)
+
+
+@pytest.mark.parametrize("key_codec", ["omni", "turbo"])
+def test_log_mass_bias_equals_duplicated_pseudo_tokens(key_codec):
+    """b_k = log n_k is exactly the effect of n_k copies of each of the
+    prototype's pseudo tokens (the pages' motivation for the bias): integer masses
+    against brute-force attention over [dequantized near window; repeated far
+    tokens] with no bias; inactive prototypes (n = 0) contribute nothing."""
+    r = np.random.default_rng(41)
+    u = _fresh(key_codec)
+    K, V, mod = _stream(r, 150)
+    u.append(K, V, mod)
+    u.evict(20, 40)
+    P, S = 6, 4
+    kf, vf = _far(r, P, S)
+    mass = np.array([1, 3, 0, 7, 2, 12], np.float32)
+    q = (r.standard_normal((4, 128)) * 1.2).astype(F16)
+    out = u.decode_with_pseudo(q, kf, vf, mass, S)
+    Kh, Vh = u.dequantized()
+    live = ~u.dead[:u.T]
+    reps = np.repeat(mass.astype(int), S)
+    Kall = np.concatenate([Kh[live], np.repeat(kf.astype(F64), reps, axis=0)])
+    Vall = np.concatenate([Vh[live], np.repeat(vf.astype(F64), reps, axis=0)])
+    s = q.astype(F64) @ Kall.T / math.sqrt(128)
+    p = np.exp(s - s.max(1, keepdims=True))
+    assert np.max(np.abs(out - (p / p.sum(1, keepdims=True)) @ Vall)) < 1e-10
+
+
+def test_pseudo_decode_reduces_to_plain_decode_and_to_far_only():
+    r = np.random.default_rng(42)
+    u = _fresh("omni")
+    K, V, mod = _stream(r, 203)
+    u.append(K, V, mod)
+    q = (r.standard_normal((4, 128)) * 1.5).astype(F16)
+    kf, vf = _far(r, 5, 8)
+    assert np.max(np.abs(u.decode_with_pseudo(q, kf[:0], vf[:0], np.zeros(0), 8) - u.decode(q))) < 1e-12
+    assert np.max(np.abs(u.decode_with_pseudo(q, kf, vf, np.zeros(5), 8) - u.decode(q))) < 1e-12
+    e = _fresh("omni")                                                       # empty near window
+    mass = np.array([2.5, 1.0, 4.0, 0.5, 9.0])
+    s = q.astype(F64) @ kf.astype(F64).T / math.sqrt(128) + np.log(np.repeat(mass, 8))[None]
+    p = np.exp(s - s.max(1, keepdims=True))
+    ref = (p / p.sum(1, keepdims=True)) @ vf.astype(F64)
+    assert np.max(np.abs(e.decode_with_pseudo(q, kf, vf, mass, 8) - ref)) < 1e-12
+    assert np.all(e.decode_with_pseudo(q, kf, vf, np.zeros(5), 8) == 0)
