@@ -229,6 +229,70 @@ def compaction_leg(c, w, torch, Q, out, peak, steps):
             "decode_ms_after": tot / steps, "l2": "256 MB buffer rewritten before each decode"}
 
 
+def pseudo_leg(torch, device, peak, steps=10, near_tokens=8192, prototypes=3072, per_proto=8):
+    """ProtoKV-style far memory next to the compressed cache: a near window of the
+    last 8,192 tokens of the 3B-shaped stream (2-bit) and 3,072 prototypes x 8
+    fp16 pseudo tokens per (layer, kv head) (near : far = 1 : 3, the pages'
+    default split), drawn on the device from a seeded generator (centres ~ N(0,
+    scale^2) with per-channel scales log-uniform in [0.5, 4], residuals 0.25 of the
+    scale; masses log-uniform in [1, 300], a tenth inactive). The 0.9 GB of pseudo
+    tokens exceed L2, so every step reads them from HBM."""
+    w = synth.qwen3b(tokens=near_tokens)
+    sh = w.shape
+    caches, _, _ = build_cache(w, torch, device, replicas=1)
+    c = caches[0]
+    g = torch.Generator(device=device).manual_seed(0x50F7)
+    shp = (1, sh.num_layers, sh.num_kv_heads)
+    nf = prototypes * per_proto
+    scale = torch.exp(torch.empty(shp + (1, sh.head_dim), device=device).uniform_(math.log(0.5), math.log(4.0),
+                                                                                    generator=g))
+    kf = (scale * (torch.randn(shp + (prototypes, sh.head_dim), device=device, generator=g)
+                   .repeat_interleave(per_proto, dim=3)
+                   + 0.25 * torch.randn(shp + (nf, sh.head_dim), device=device, generator=g))).half()
+    vf = (scale * (torch.randn(shp + (prototypes, sh.head_dim), device=device, generator=g)
+                   .repeat_interleave(per_proto, dim=3)
+                   + 0.25 * torch.randn(shp + (nf, sh.head_dim), device=device, generator=g))).half()
+    mass = torch.exp(torch.empty(shp + (prototypes,), device=device).uniform_(0.0, math.log(300.0), generator=g))
+    mass = torch.where(torch.rand(shp + (prototypes,), device=device, generator=g) < 0.1, torch.zeros_like(mass),
+                       mass.round())
+    Q = torch.from_numpy(w.queries(0)).to(device)
+    out = torch.empty_like(Q)
+    for _ in range(3):
+        c.decode_pseudo(Q, kf, vf, mass, per_proto, out)
+        c.decode(Q, out)
+    torch.cuda.synchronize()
+    c.profile_enable(True)
+    for _ in range(steps):
+        c.decode(Q, out)
+    torch.cuda.synchronize()
+    near_split, near_merge = (list(x) for x in c.profile_read())
+    c.profile_enable(False)
+    c.profile_enable(True)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        c.decode_pseudo(Q, kf, vf, mass, per_proto, out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ps_split, ps_merge = (list(x) for x in c.profile_read())
+    c.profile_enable(False)
+    if c.check_errors() != 0:
+        raise RuntimeError("device error word set after the pseudo-token decode")
+    step_ms = e0.elapsed_time(e1) / steps
+    far_ms = float(np.mean(ps_split)) - float(np.mean(near_split))
+    units = sh.num_layers * sh.num_kv_heads
+    far_bytes = units * (nf * sh.head_dim * 2 * 2 + prototypes * 4) + 2 * Q.numel() * 2
+    return {"near_tokens": near_tokens, "prototypes": prototypes, "per_prototype": per_proto, "far_tokens": nf,
+            "ms_per_step": step_ms, "context_tokens_per_s": (near_tokens + nf) / (step_ms / 1e3),
+            "near_decode_ms": float(np.mean(near_split)), "near_plus_far_ms": float(np.mean(ps_split)),
+            "merge_ms": float(np.mean(ps_merge)),
+            "far_kernel_ms": far_ms, "far_bytes": far_bytes,
+            "far_roofline": {"bound": "hbm", "achieved": far_bytes / (far_ms / 1e3) / 1e9, "peak": peak,
+                             "unit": "GB/s", "frac": far_bytes / (far_ms / 1e3) / 1e9 / peak,
+                             "note": "far kernel time = (near + far kernels) - (near kernel alone), CUDA events"}}
+
+
 def cpu_baseline_child(args):
     """Time the CPU oracle, as it stands, on a bounded sample: decode of the
     (layer 0, kv heads 0..Hkv-1) units of the workload, single-threaded."""
@@ -465,6 +529,9 @@ def main():
             "clocks": clocks,
         }
         line["compaction"] = compaction_leg(caches[0], w, torch, Q, out, peak, 10)
+        del caches
+        torch.cuda.empty_cache()
+        line["pseudo_tokens"] = pseudo_leg(torch, device, peak)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = run_cpu_baseline(args)
         print(json.dumps(line))

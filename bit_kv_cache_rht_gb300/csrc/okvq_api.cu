@@ -53,6 +53,9 @@ struct okvq_cache {
   int *moves_dev = nullptr;                            // [cap / TILE][2] compaction move list
   uint8_t *cscratch = nullptr;                         // compaction gather scratch
   size_t cscratch_bytes = 0;
+  // far-memory pseudo tokens
+  float *far_partials = nullptr;                       // [units][far_nsplit][MAXGQ][FAR_PARTIAL_FLOATS]
+  int far_nsplit = 1;
   // profiling
   bool prof = false;
   std::vector<cudaEvent_t> ev;  // triples per decode call
@@ -131,6 +134,7 @@ void release(okvq_cache *h) {
   cudaFree(h->dead_dev);
   cudaFree(h->moves_dev);
   cudaFree(h->cscratch);
+  cudaFree(h->far_partials);
   if (h->host_table) cudaFreeHost(h->host_table);
   if (h->table_ev) cudaEventDestroy(h->table_ev);
   for (auto e : h->ev) cudaEventDestroy(e);
@@ -286,6 +290,83 @@ okvq_status push_page_meta(okvq_cache *h, int session, long long p0, long long p
   return OKVQ_OK;
 }
 
+// Upload the work table if the lengths changed, then launch the near-window
+// decode, the far-memory kernel (if any) and the merge. seg_limit >= 0: refuse
+// (OKVQ_ESCRATCH, nothing launched) a work list with more segments.
+okvq_status enqueue_decode(okvq_cache *h, const void *q, void *out, cudaStream_t s, float *partials, long long seg_limit,
+                           bool profile, const FarArgs *far) {
+  if (h->dirty) {
+    if (h->table_ev_pending) OKVQ_TRY(cudaEventSynchronize(h->table_ev));   // staging buffer free again
+    build_table(h);
+    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table, h->table_bytes, cudaMemcpyHostToDevice, s));
+    OKVQ_TRY(cudaEventRecord(h->table_ev, s));
+    h->table_ev_pending = true;
+    h->dirty = false;
+  }
+  if (seg_limit >= 0 && h->nseg > seg_limit) return OKVQ_ESCRATCH;
+  const char *tb = reinterpret_cast<const char *>(h->table);
+  DecodeArgs a{};
+  a.q = static_cast<const __half *>(q);
+  a.pages = h->pages;
+  a.tails = h->tails;
+  a.mod = h->mod;
+  a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
+  a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
+  a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);
+  a.unit_tail = reinterpret_cast<const int *>(tb + h->off_utail);
+  a.partials = partials;
+  a.L = h->L;
+  a.Hq = h->Hq;
+  a.Hkv = h->Hkv;
+  a.M = h->M;
+  a.bits = h->bits;
+  a.G = h->KG;
+  a.P_max = h->P_max;
+  a.cap = h->cap;
+  a.units = h->units;
+  a.signs = h->signs;
+  a.err = h->err;
+  for (int j = 0; j < 16; ++j) {
+    a.klut_src[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
+    a.vlut_src[j] = h->levels16[j];
+  }
+  CombineArgs cb{};
+  cb.partials = partials;
+  cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
+  cb.rot_frag = reinterpret_cast<const uint4 *>(h->rot_frag);
+  cb.err = h->err;
+  cb.out = static_cast<__half *>(out);
+  cb.L = h->L;
+  cb.Hq = h->Hq;
+  cb.Hkv = h->Hkv;
+  cb.M = h->M;
+  cb.units = h->units;
+  cb.far = far ? far->partials : nullptr;
+  cb.far_split = far ? far->nsplit : 0;
+  cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
+  if (profile) {
+    const size_t need = 3 * (size_t)(h->prof_calls + 1);
+    while (h->ev.size() < need) {
+      cudaEvent_t ev;
+      OKVQ_TRY(cudaEventCreate(&ev));
+      h->ev.push_back(ev);
+    }
+    e0 = h->ev[3 * h->prof_calls];
+    e1 = h->ev[3 * h->prof_calls + 1];
+    e2 = h->ev[3 * h->prof_calls + 2];
+    OKVQ_TRY(cudaEventRecord(e0, s));
+  }
+  OKVQ_TRY(launch_decode(a, h->ncta, s));
+  if (far) OKVQ_TRY(launch_far(*far, s));
+  if (profile) OKVQ_TRY(cudaEventRecord(e1, s));
+  OKVQ_TRY(launch_combine(cb, s));
+  if (profile) {
+    OKVQ_TRY(cudaEventRecord(e2, s));
+    ++h->prof_calls;
+  }
+  return OKVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -390,6 +471,11 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->dead_dev, (size_t)h->S * h->P_max * 8)) != OKVQ_OK) return fail(st);
+  // far memory: every unit's pseudo tokens split so that the far grid covers the SMs once
+  h->far_nsplit = (int)std::max<long long>(1, (long long)h->num_sms / h->units);
+  if ((st = alloc_dev((void **)&h->far_partials,
+                      (size_t)h->units * h->far_nsplit * MAXGQ * FAR_PARTIAL_FLOATS * sizeof(float))) != OKVQ_OK)
+    return fail(st);
   if ((st = alloc_dev((void **)&h->moves_dev, (size_t)(h->cap / TILE) * 2 * sizeof(int))) != OKVQ_OK) return fail(st);
   {
     // compaction scratch: every granule of a session, or COMPACT_SCRATCH_CAP (larger plans run in batches)
@@ -526,131 +612,45 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
 
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
   if (!h || !q || !out) return OKVQ_EINVAL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (h->dirty) {
-    if (h->table_ev_pending) OKVQ_TRY(cudaEventSynchronize(h->table_ev));   // staging buffer free again
-    build_table(h);
-    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table, h->table_bytes, cudaMemcpyHostToDevice, s));
-    OKVQ_TRY(cudaEventRecord(h->table_ev, s));
-    h->table_ev_pending = true;
-    h->dirty = false;
-  }
-  const char *tb = reinterpret_cast<const char *>(h->table);
-  DecodeArgs a{};
-  a.q = static_cast<const __half *>(q);
-  a.pages = h->pages;
-  a.tails = h->tails;
-  a.mod = h->mod;
-  a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
-  a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
-  a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);
-  a.unit_tail = reinterpret_cast<const int *>(tb + h->off_utail);
-  a.partials = h->partials;
-  a.L = h->L;
-  a.Hq = h->Hq;
-  a.Hkv = h->Hkv;
-  a.M = h->M;
-  a.bits = h->bits;
-  a.G = h->KG;
-  a.P_max = h->P_max;
-  a.cap = h->cap;
-  a.units = h->units;
-  a.signs = h->signs;
-  a.err = h->err;
-  for (int j = 0; j < 16; ++j) {
-    a.klut_src[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
-    a.vlut_src[j] = h->levels16[j];
-  }
-  CombineArgs cb{};
-  cb.partials = h->partials;
-  cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
-  cb.rot_frag = reinterpret_cast<const uint4 *>(h->rot_frag);
-  cb.err = h->err;
-  cb.out = static_cast<__half *>(out);
-  cb.L = h->L;
-  cb.Hq = h->Hq;
-  cb.Hkv = h->Hkv;
-  cb.M = h->M;
-  cb.units = h->units;
-  cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
-  if (h->prof) {
-    const size_t need = 3 * (size_t)(h->prof_calls + 1);
-    while (h->ev.size() < need) {
-      cudaEvent_t ev;
-      OKVQ_TRY(cudaEventCreate(&ev));
-      h->ev.push_back(ev);
-    }
-    e0 = h->ev[3 * h->prof_calls];
-    e1 = h->ev[3 * h->prof_calls + 1];
-    e2 = h->ev[3 * h->prof_calls + 2];
-    OKVQ_TRY(cudaEventRecord(e0, s));
-  }
-  OKVQ_TRY(launch_decode(a, h->ncta, s));
-  if (h->prof) OKVQ_TRY(cudaEventRecord(e1, s));
-  OKVQ_TRY(launch_combine(cb, s));
-  if (h->prof) {
-    OKVQ_TRY(cudaEventRecord(e2, s));
-    ++h->prof_calls;
-  }
-  return OKVQ_OK;
+  return enqueue_decode(h, q, out, static_cast<cudaStream_t>(stream), h->partials, -1, h->prof, nullptr);
 }
 
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream) {
   if (!h || !q || !out) return OKVQ_EINVAL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *scratch = nullptr;
   okvq_status st = static_partials(h->device, &scratch);
   if (st != OKVQ_OK) return st;
-  if (h->dirty) {
-    if (h->table_ev_pending) OKVQ_TRY(cudaEventSynchronize(h->table_ev));   // staging buffer free again
-    build_table(h);
-    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table, h->table_bytes, cudaMemcpyHostToDevice, s));
-    OKVQ_TRY(cudaEventRecord(h->table_ev, s));
-    h->table_ev_pending = true;
-    h->dirty = false;
-  }
-  if (h->nseg > OKVQ_STATIC_SCRATCH_SEGMENTS) return OKVQ_ESCRATCH;
   // the same launches as okvq_decode, with the partials in the static array
-  const char *tb = reinterpret_cast<const char *>(h->table);
-  DecodeArgs a{};
-  a.q = static_cast<const __half *>(q);
-  a.pages = h->pages;
-  a.tails = h->tails;
-  a.mod = h->mod;
-  a.segs = reinterpret_cast<const int *>(tb + h->off_segs);
-  a.cta_seg = reinterpret_cast<const int *>(tb + h->off_cta);
-  a.unit_len = reinterpret_cast<const long long *>(tb + h->off_ulen);
-  a.unit_tail = reinterpret_cast<const int *>(tb + h->off_utail);
-  a.partials = scratch;
-  a.L = h->L;
-  a.Hq = h->Hq;
-  a.Hkv = h->Hkv;
-  a.M = h->M;
-  a.bits = h->bits;
-  a.G = h->KG;
-  a.P_max = h->P_max;
-  a.cap = h->cap;
-  a.units = h->units;
-  a.signs = h->signs;
-  a.err = h->err;
-  for (int j = 0; j < 16; ++j) {
-    a.klut_src[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
-    a.vlut_src[j] = h->levels16[j];
-  }
-  CombineArgs cb{};
-  cb.partials = scratch;
-  cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);
-  cb.rot_frag = reinterpret_cast<const uint4 *>(h->rot_frag);
-  cb.err = h->err;
-  cb.out = static_cast<__half *>(out);
-  cb.L = h->L;
-  cb.Hq = h->Hq;
-  cb.Hkv = h->Hkv;
-  cb.M = h->M;
-  cb.units = h->units;
-  OKVQ_TRY(launch_decode(a, h->ncta, s));
-  OKVQ_TRY(launch_combine(cb, s));
-  return OKVQ_OK;
+  return enqueue_decode(h, q, out, static_cast<cudaStream_t>(stream), scratch, OKVQ_STATIC_SCRATCH_SEGMENTS, false,
+                        nullptr);
+}
+
+okvq_status okvq_decode_pseudo(okvq_cache *h, const void *q, const void *far_k, const void *far_v,
+                               const float *far_mass, int32_t num_prototypes, int32_t tokens_per_prototype,
+                               void *out, void *stream) {
+  if (!h || !q || !out || num_prototypes < 0 || tokens_per_prototype < 1) return OKVQ_EINVAL;
+  const long long n_far = (long long)num_prototypes * tokens_per_prototype;
+  if (n_far > (1ll << 30)) return OKVQ_EINVAL;
+  if (n_far > 0 && (!far_k || !far_v || !far_mass)) return OKVQ_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(far_k) | reinterpret_cast<uintptr_t>(far_v)) & 15u) return OKVQ_EINVAL;
+  FarArgs f{};
+  f.q = static_cast<const __half *>(q);
+  f.k = static_cast<const __half *>(far_k);
+  f.v = static_cast<const __half *>(far_v);
+  f.mass = far_mass;
+  f.partials = h->far_partials;
+  f.err = h->err;
+  f.L = h->L;
+  f.Hq = h->Hq;
+  f.Hkv = h->Hkv;
+  f.n_far = (int)n_far;
+  f.per_proto = tokens_per_prototype;
+  f.nsplit = h->far_nsplit;
+  // tokens per split, a multiple of the tokens one pass of the far kernel's warps takes
+  const long long pass = far_pass_tokens();
+  f.chunk = (int)(((n_far + h->far_nsplit - 1) / h->far_nsplit + pass - 1) / pass * pass);
+  f.units = h->units;
+  return enqueue_decode(h, q, out, static_cast<cudaStream_t>(stream), h->partials, -1, h->prof, &f);
 }
 
 okvq_status okvq_profile_enable(okvq_cache *h, int enable) {

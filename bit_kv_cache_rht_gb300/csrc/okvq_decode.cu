@@ -22,7 +22,7 @@
 //   in shared memory; one partial (m, l, o_m) per segment and head goes out.
 // combine_kernel - per (unit, 32 output channels): log-sum-exp merge of the
 //   unit's partials, O = (sum_m R_m^T o_m) / (l sqrt d), fp16 store.
-#include "okvq_internal.h"
+#include "okvq_device.h"
 
 namespace okvq {
 
@@ -30,11 +30,7 @@ namespace {
 
 // warps 0-7 rotate query head w and build query fragment block w (8 blocks of 16 channels)
 static_assert(MAXGQ == D / 16, "one warp per query head and per fragment block");
-constexpr float LOG2E = 1.4426950408889634074f;
 constexpr float INV_D = 1.0f / 128.0f;                      // (1/sqrt d) rotation * (1/sqrt d) softmax
-constexpr float INV_SQRT_D = 0.0883883476483184405501f;
-constexpr unsigned FULL = 0xffffffffu;
-constexpr long long WAIT_LIMIT = 1ll << 26;
 constexpr int LUT_BYTES = 256 * 256;   // 256 code bytes x [K half | V half], 128 B each
 constexpr float SOFTMAX_HEADROOM = 6.0f;   // log2 units
 constexpr uint32_t TMEM_COLS = 512;        // parked modality accumulators: (warps / 4) x 3 x 32 columns
@@ -54,40 +50,6 @@ struct Cfg<4> {
   static constexpr bool QREG = false;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// bounded wait on an mbarrier phase; returns false if it gave up
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  for (long long it = 0; it < WAIT_LIMIT; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -155,19 +117,6 @@ __device__ __forceinline__ void mod_rescale_parked(const ModAcc &ma, float sf0, 
   }
 }
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
@@ -805,11 +754,12 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
 // product to ~2^-22 relative (fp32 accumulation).
 constexpr int CB_CH = 64;                       // output channels per CTA (4 m-tiles of 16)
 constexpr int OSTRIDE = MAXM * D + 4;           // padded row of the merged o (floats)
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
   extern __shared__ __align__(128) unsigned char csm[];
   uint4 *afr = reinterpret_cast<uint4 *>(csm);                                  // [4][8M][32][2] hi|lo
   float *osh = reinterpret_cast<float *>(csm + 4 * 8 * MAXM * 32 * 32);           // [8][OSTRIDE]
   float *red = osh + MAXGQ * OSTRIDE;                                             // [4][32][4]
+  float *ofar = red + 4 * 32 * 4;                                                  // [8][CB_CH] far memory / l
   __shared__ __align__(8) uint64_t bar;
   const int unit = blockIdx.x, half = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
@@ -843,8 +793,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     }
     float M = m0;
     for (int s = s0 + 32 + lane; s < s1; s += 32) M = fmaxf(M, part(s)[0]);
+    // far-memory partials of this unit and head: m, l, o[D] in the original value basis
+    const float *fbase = a.far_split ? a.far + ((long long)unit * a.far_split * MAXGQ + w) * FAR_PARTIAL_FLOATS : a.far;
+    auto farp = [&](int f) { return fbase + (long long)f * MAXGQ * FAR_PARTIAL_FLOATS; };
+    for (int f = lane; f < a.far_split; f += 32) M = fmaxf(M, farp(f)[0]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float of0 = 0.f, of1 = 0.f;            // channels half * CB_CH + lane, + 32
+    for (int f = 0; f < a.far_split; ++f) {
+      const float mf = farp(f)[0];
+      const float wt = mf == -INFINITY ? 0.f : ex2(mf - M);
+      if (lane == 0) L = fmaf(wt, farp(f)[1], L);
+      of0 = fmaf(wt, farp(f)[2 + half * CB_CH + lane], of0);
+      of1 = fmaf(wt, farp(f)[2 + half * CB_CH + lane + 32], of1);
+    }
     for (int sb = s0; sb < s1; sb += 32) {
       float wt = 0.f;
       if (sb + lane < s1) {
@@ -873,8 +835,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
     for (int k = 0; k < OPER; ++k)
       if (32 * k < nr) osh[w * OSTRIDE + lane + 32 * k] = o[k] * inv;
+    ofar[w * CB_CH + lane] = of0 * inv;
+    ofar[w * CB_CH + lane + 32] = of1 * inv;
   } else if (w < MAXGQ) {
     for (int k = lane; k < nr; k += 32) osh[w * OSTRIDE + k] = 0.f;
+    ofar[w * CB_CH + lane] = 0.f;
+    ofar[w * CB_CH + lane + 32] = 0.f;
   }
   __syncthreads();
   const bool got = mbar_wait(&bar, 0);
@@ -911,7 +877,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
     for (int e2 = 0; e2 < 4; ++e2) {
       const int h = 2 * t4 + (e2 & 1), cc = c + 8 * (e2 >> 1);
-      if (h < gq) ob[h * D + cc] = __float2half_rn(y[e2] * INV_SQRT_D);
+      if (h < gq) ob[h * D + cc] = __float2half_rn(fmaf(y[e2], INV_SQRT_D, ofar[h * CB_CH + cc - half * CB_CH]));
     }
   }
 }
@@ -954,7 +920,7 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
   if (a.units <= 0) return cudaSuccess;
   static std::atomic<uint64_t> attr_done{0};
-  const size_t smem = (size_t)4 * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + 4 * 32 * 4) * sizeof(float);
+  const size_t smem = (size_t)4 * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + 4 * 32 * 4 + MAXGQ * CB_CH) * sizeof(float);
   cudaError_t ea = once_per_device(attr_done, [&] {
     cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

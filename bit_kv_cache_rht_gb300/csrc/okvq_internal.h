@@ -191,9 +191,25 @@ struct CombineArgs {
   uint32_t *err;
   int L, Hq, Hkv, M;
   long long units;
+  const float *far;         // far-memory partials [units][far_split][MAXGQ][FAR_PARTIAL_FLOATS], or null
+  int far_split;            // 0: no far memory
+};
+
+// Far-memory pseudo tokens (fp16, the original key / value bases) of every unit.
+struct FarArgs {
+  const __half *q;          // [S][L][Hq][D]
+  const __half *k, *v;      // [units][n_far][D]
+  const float *mass;        // [units][n_far / per_proto]
+  float *partials;          // [units][nsplit][MAXGQ][FAR_PARTIAL_FLOATS]
+  uint32_t *err;
+  int L, Hq, Hkv;
+  int n_far, per_proto;
+  int nsplit, chunk;        // splits per unit, tokens per split
+  long long units;
 };
 
 constexpr int PARTIAL_FLOATS = 2 + MAXM * D;   // m, l, o[M][D]
+constexpr int FAR_PARTIAL_FLOATS = 2 + D;       // m, l, o[D] (original value basis)
 constexpr int DEAD_OFF = 8;                     // deletion mask: page offset off_tmask + DEAD_OFF
 
 // Compaction granule: the tokens that move together (a key group, whose statistics
@@ -251,6 +267,8 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 size_t decode_smem_bytes(int bits, int G);
 cudaError_t launch_move(const MoveArgs &a, cudaStream_t s);
+cudaError_t launch_far(const FarArgs &a, cudaStream_t s);
+int far_pass_tokens();        // pseudo tokens one pass of the far kernel's warps takes
 cudaError_t launch_page_meta(const PageMetaArgs &a, int n_pages, cudaStream_t s);
 
 }  // namespace okvq

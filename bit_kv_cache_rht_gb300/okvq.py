@@ -25,7 +25,7 @@ EXPORTS = (
     "okvq_create", "okvq_free", "okvq_append_chunk", "okvq_decode", "okvq_length", "okvq_export_state",
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
     "okvq_decode_static_scratch", "okvq_calibrate_rotations", "okvq_live_length", "okvq_evict",
-    "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact",
+    "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact", "okvq_decode_pseudo",
 )
 
 
@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
     L.okvq_decode.argtypes = [vp, vp, vp, vp]
     L.okvq_decode_static_scratch.argtypes = [vp, vp, vp, vp]
     L.okvq_calibrate_rotations.argtypes = [i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp]
+    L.okvq_decode_pseudo.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
     L.okvq_live_length.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     L.okvq_evict.argtypes = [vp, i32, vp, i32, vp]
     L.okvq_compaction_granule.argtypes = [vp, ctypes.POINTER(i32)]
@@ -165,6 +166,13 @@ def okvq_length(h, session: int):
     n = ctypes.c_int64()
     st = load().okvq_length(h, session, ctypes.byref(n))
     return st, n.value
+
+
+def okvq_decode_pseudo(h, q_ptr: int, k_ptr: int, v_ptr: int, mass_ptr: int, num_prototypes: int,
+                       tokens_per_prototype: int, out_ptr: int, stream: int = 0) -> int:
+    return load().okvq_decode_pseudo(h, ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                                     ctypes.c_void_p(mass_ptr), num_prototypes, tokens_per_prototype,
+                                     ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream))
 
 
 def okvq_live_length(h, session: int):
@@ -298,6 +306,26 @@ class Cache:
         st, n = okvq_length(self._h, session)
         _check(st, "okvq_length")
         return n
+
+    def decode_pseudo(self, q, far_k, far_v, far_mass, tokens_per_prototype: int, out=None, stream=None):
+        """Decode with far-memory pseudo tokens: far_k, far_v cuda fp16 [S][L][Hkv][P*Sp][128],
+        far_mass cuda fp32 [S][L][Hkv][P] (Sp = tokens_per_prototype)."""
+        import torch
+        qs = (self.num_sessions, self.num_layers, self.num_q_heads, self.head_dim)
+        if tuple(q.shape) != qs or q.dtype != torch.float16 or not q.is_cuda or not q.is_contiguous():
+            raise ValueError("q must be a contiguous cuda fp16 tensor of shape %s" % (qs,))
+        shp = (self.num_sessions, self.num_layers, self.num_kv_heads)
+        P = int(far_mass.shape[-1])
+        for t, dt, shape in ((far_k, torch.float16, shp + (P * tokens_per_prototype, self.head_dim)),
+                             (far_v, torch.float16, shp + (P * tokens_per_prototype, self.head_dim)),
+                             (far_mass, torch.float32, shp + (P,))):
+            if not t.is_cuda or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError("pseudo-token tensor must be a contiguous cuda %s tensor %s" % (dt, shape))
+        if out is None:
+            out = torch.empty_like(q)
+        _check(okvq_decode_pseudo(self._h, q.data_ptr(), far_k.data_ptr(), far_v.data_ptr(), far_mass.data_ptr(), P,
+                                  tokens_per_prototype, out.data_ptr(), _stream_handle(stream)), "okvq_decode_pseudo")
+        return out
 
     def live_length(self, session: int) -> int:
         st, n = okvq_live_length(self._h, session)

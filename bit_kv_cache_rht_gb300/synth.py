@@ -43,7 +43,7 @@ CALIB_TOKENS = 512
 DRIFT_STEP = 0.02
 SCALE_LO, SCALE_HI = 0.5, 4.0
 
-_PURPOSE = {"params": 1, "kv": 2, "calib": 3, "query": 4, "plan": 5}
+_PURPOSE = {"params": 1, "kv": 2, "calib": 3, "query": 4, "plan": 5, "far": 6}
 
 
 def _rng(seed: int, purpose: str, *ids: int) -> np.random.Generator:
@@ -186,6 +186,36 @@ class Workload:
         r = _rng(self.seed, "query", step)
         q = r.standard_normal((len(self.sessions), sh.num_layers, sh.num_q_heads, sh.head_dim), dtype=np.float32)
         return q.astype(np.float16)
+
+    # ---- far-memory pseudo tokens (input of the pseudo-token decode) ----
+    def pseudo_tokens(self, num_prototypes: int, per_proto: int, inactive: float = 0.1):
+        """Pseudo tokens shaped like a prototype bank's: for every (session, layer,
+        kv head), prototype centres drawn like the layer's keys and values, and
+        per_proto tokens per prototype = centre + small residual modes (0.25 of
+        the channel scale). Masses log-uniform in [1, 300], rounded, with about
+        ``inactive`` of the prototypes at 0. Returns fp16 K, V
+        [S][L][Hkv][P*per_proto][d] and fp32 masses [S][L][Hkv][P]."""
+        sh = self.shape
+        S, P = len(self.sessions), num_prototypes
+        shp = (S, sh.num_layers, sh.num_kv_heads)
+        K = np.empty(shp + (P * per_proto, sh.head_dim), np.float16)
+        V = np.empty_like(K)
+        mass = np.empty(shp + (P,), np.float32)
+        for s in range(S):
+            for l in range(sh.num_layers):
+                kscale, vscale, _ = self.layer_params(l)
+                r = _rng(self.seed, "far", s, l)
+                for h in range(sh.num_kv_heads):
+                    ck = kscale[h] * r.standard_normal((P, sh.head_dim), dtype=np.float32)
+                    cv = vscale[h] * r.standard_normal((P, sh.head_dim), dtype=np.float32)
+                    rk = 0.25 * kscale[h] * r.standard_normal((P * per_proto, sh.head_dim), dtype=np.float32)
+                    rv = 0.25 * vscale[h] * r.standard_normal((P * per_proto, sh.head_dim), dtype=np.float32)
+                    K[s, l, h] = (np.repeat(ck, per_proto, axis=0) + rk).astype(np.float16)
+                    V[s, l, h] = (np.repeat(cv, per_proto, axis=0) + rv).astype(np.float16)
+                    n = np.round(np.exp(r.uniform(0.0, math.log(300.0), P)))
+                    n[r.random(P) < inactive] = 0.0
+                    mass[s, l, h] = n
+        return K, V, mass
 
     # ---- calibration slice (input of the value-rotation calibration) ----
     def calibration_slice(self, layers: Optional[Sequence[int]] = None):

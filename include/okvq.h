@@ -168,6 +168,30 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
  * rebuilt and uploaded on `stream`); otherwise as okvq_decode. */
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream);
 
+/* Decode with far-memory pseudo tokens ("ProtoKV: Streaming Video Understanding
+ * under Delayed Query with Summary-State Memory", section 3.3 Eq. (2), Appendix
+ * A.3 Eq. (4) and Algorithm 4): one softmax per query head over the cache (the
+ * near window, bias 0, evicted tokens skipped) and P = num_prototypes x
+ * S = tokens_per_prototype pseudo tokens per (session, layer, kv head) that the
+ * caller synthesized (prototype centre plus decoded residual modes; the
+ * synthesis itself is the caller's). Pseudo token j belongs to prototype j / S,
+ * whose mass n adds log n to its logit q.k/sqrt(d); prototypes with n = 0 are
+ * inactive and skipped. Layouts (device, row-major):
+ *   q, out     as okvq_decode
+ *   far_k      fp16 [S][L][Hkv][P*S][128]  pseudo keys, the caller's key basis
+ *              (the one okvq_append_chunk receives keys in), 16-byte aligned
+ *   far_v      fp16 [S][L][Hkv][P*S][128]  pseudo values, the original value basis, 16-byte aligned
+ *   far_mass   fp32 [S][L][Hkv][P]         n >= 0
+ * Launches the near-window decode, one far-memory kernel and the merge on
+ * `stream`; nothing is allocated (the far partials are reserved by okvq_create).
+ * P = 0 gives okvq_decode's result. A unit with no live near token and no
+ * active prototype decodes to zeros. OKVQ_EINVAL for NULL or misaligned
+ * pointers, P < 0, S < 1 or P*S > 2^30. With profiling on, okvq_profile_read's
+ * first time covers the near-window and far-memory kernels together. */
+okvq_status okvq_decode_pseudo(okvq_cache *h, const void *q, const void *far_k, const void *far_v,
+                               const float *far_mass, int32_t num_prototypes, int32_t tokens_per_prototype,
+                               void *out, void *stream);
+
 /* Number of token slots of `session`: its physical span, holes included (the
  * next append lands at this index). */
 okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
