@@ -55,6 +55,7 @@ struct okvq_cache {
   size_t cscratch_bytes = 0;
   // far-memory pseudo tokens
   float *far_partials = nullptr;                       // [units][far_nsplit][MAXGQ][FAR_PARTIAL_FLOATS]
+  unsigned char *lut = nullptr;                        // decode level table (LEVEL_TABLE_BYTES)
   int far_nsplit = 1;
   // profiling
   bool prof = false;
@@ -135,6 +136,7 @@ void release(okvq_cache *h) {
   cudaFree(h->moves_dev);
   cudaFree(h->cscratch);
   cudaFree(h->far_partials);
+  cudaFree(h->lut);
   if (h->host_table) cudaFreeHost(h->host_table);
   if (h->table_ev) cudaEventDestroy(h->table_ev);
   for (auto e : h->ev) cudaEventDestroy(e);
@@ -324,6 +326,7 @@ okvq_status enqueue_decode(okvq_cache *h, const void *q, void *out, cudaStream_t
   a.P_max = h->P_max;
   a.cap = h->cap;
   a.units = h->units;
+  a.lut = h->lut;
   a.signs = h->signs;
   a.err = h->err;
   for (int j = 0; j < 16; ++j) {
@@ -471,6 +474,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->dead_dev, (size_t)h->S * h->P_max * 8)) != OKVQ_OK) return fail(st);
+  if ((st = alloc_dev((void **)&h->lut, LEVEL_TABLE_BYTES)) != OKVQ_OK) return fail(st);
   // far memory: every unit's pseudo tokens split so that the far grid covers the SMs once
   h->far_nsplit = (int)std::max<long long>(1, (long long)h->num_sms / h->units);
   if ((st = alloc_dev((void **)&h->far_partials,
@@ -508,6 +512,15 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if (cudaMemsetAsync(h->mod, 0, (size_t)h->S * h->cap, s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaMemsetAsync(h->dead_dev, 0, (size_t)h->S * h->P_max * 8, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  {
+    LutArgs la{};
+    la.out = h->lut;
+    for (int j = 0; j < 16; ++j) {
+      la.klev[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
+      la.vlev[j] = h->levels16[j];
+    }
+    if (launch_lut(h->bits, la, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+  }
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
     std::vector<float> rt(nmat * D * D);

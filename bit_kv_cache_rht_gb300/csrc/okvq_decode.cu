@@ -432,6 +432,31 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
   }
 }
 
+// code byte -> fp16 level table; entry e = [K part 128 B | V part 128 B].
+// 2-bit: byte = 2 pairs -> 8 B, replicated for the 16 lanes of a half warp;
+// 4-bit: byte = 1 pair -> 4 B, replicated for 32 lanes. Built once per cache
+// (lut_kernel) into global memory; each decode CTA bulk-copies it.
+template <int BITS>
+__global__ void lut_kernel(const LutArgs a) {
+  unsigned char *lut = a.out;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 256 * 32; i += gridDim.x * blockDim.x) {
+    const int e = i >> 5, c = i & 31;
+    if (BITS == 2) {
+      if (c >= 16) continue;
+      const uint32_t k0 = h2u(__halves2half2(a.klev[e & 3], a.klev[(e >> 2) & 3]));
+      const uint32_t k1 = h2u(__halves2half2(a.klev[(e >> 4) & 3], a.klev[(e >> 6) & 3]));
+      const uint32_t v0 = h2u(__halves2half2(a.vlev[e & 3], a.vlev[(e >> 2) & 3]));
+      const uint32_t v1 = h2u(__halves2half2(a.vlev[(e >> 4) & 3], a.vlev[(e >> 6) & 3]));
+      *reinterpret_cast<uint2 *>(lut + e * 256 + c * 8) = make_uint2(k0, k1);
+      *reinterpret_cast<uint2 *>(lut + e * 256 + 128 + c * 8) = make_uint2(v0, v1);
+    } else {
+      *reinterpret_cast<uint32_t *>(lut + e * 256 + c * 4) = h2u(__halves2half2(a.klev[e & 15], a.klev[e >> 4]));
+      *reinterpret_cast<uint32_t *>(lut + e * 256 + 128 + c * 4) =
+          h2u(__halves2half2(a.vlev[e & 15], a.vlev[e >> 4]));
+    }
+  }
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const DecodeArgs a) {
   constexpr int WARPS = Cfg<BITS>::WARPS;
@@ -458,25 +483,13 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   unsigned char *my_stage0 = stages + (size_t)warp * STAGES * PL.page_bytes;
   uint64_t *my_bars = bars + warp * STAGES;
 
-  // code byte -> fp16 level table; entry e = [K part 128 B | V part 128 B].
-  // 2-bit: byte = 2 pairs -> 8 B, replicated for the 16 lanes of a half warp;
-  // 4-bit: byte = 1 pair -> 4 B, replicated for 32 lanes.
-  for (int i = tid; i < 256 * 32; i += THREADS) {
-    const int e = i >> 5, c = i & 31;
-    if (BITS == 2) {
-      if (c >= 16) continue;
-      const uint32_t k0 = h2u(__halves2half2(a.klut_src[e & 3], a.klut_src[(e >> 2) & 3]));
-      const uint32_t k1 = h2u(__halves2half2(a.klut_src[(e >> 4) & 3], a.klut_src[(e >> 6) & 3]));
-      const uint32_t v0 = h2u(__halves2half2(a.vlut_src[e & 3], a.vlut_src[(e >> 2) & 3]));
-      const uint32_t v1 = h2u(__halves2half2(a.vlut_src[(e >> 4) & 3], a.vlut_src[(e >> 6) & 3]));
-      *reinterpret_cast<uint2 *>(lut + e * 256 + c * 8) = make_uint2(k0, k1);
-      *reinterpret_cast<uint2 *>(lut + e * 256 + 128 + c * 8) = make_uint2(v0, v1);
-    } else {
-      *reinterpret_cast<uint32_t *>(lut + e * 256 + c * 4) =
-          h2u(__halves2half2(a.klut_src[e & 15], a.klut_src[e >> 4]));
-      *reinterpret_cast<uint32_t *>(lut + e * 256 + 128 + c * 4) =
-          h2u(__halves2half2(a.vlut_src[e & 15], a.vlut_src[e >> 4]));
-    }
+  // the level table (built once per cache) arrives by one bulk copy; it is first
+  // needed after the first segment's query rotation
+  __shared__ __align__(8) uint64_t lut_bar;
+  if (tid == 0) {
+    mbar_init(&lut_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    bulk_load(lut, a.lut, LUT_BYTES, &lut_bar);
   }
   if (lane == 0)
     for (int s = 0; s < STAGES; ++s) mbar_init(&my_bars[s], 1);
@@ -511,6 +524,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   int ring_st = 0;          // stage of the next page this warp consumes
   uint32_t ring_par = 0;    // its mbarrier phase parity
   bool wait_failed = false;
+  bool lut_ready = false;
 
   const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
   for (int seg = seg_begin; seg < seg_end; ++seg) {
@@ -525,6 +539,18 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     const int Tf = KT ? T : (T / GG) * GG;
     const unsigned char *unit_pages = a.pages + (long long)unit * a.P_max * PL.page_bytes;
     const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
+    // the segment's first pages are on their way while the query is rotated (the
+    // ring is free: the previous segment's merge ended with a barrier)
+    const int npages = pe - pb;
+    const int my_n = npages > warp ? (npages - warp + WARPS - 1) / WARPS : 0;
+    if (lane == 0) {
+      for (int k = 0; k < min(my_n, STAGES); ++k) {
+        const int st = (ring_st + k) % STAGES;
+        fence_async_smem();
+        bulk_load(my_stage0 + (size_t)st * PL.page_bytes,
+                  unit_pages + (long long)(pb + warp + k * WARPS) * PL.page_bytes, PL.page_bytes, &my_bars[st]);
+      }
+    }
 
     // ---- rotate the query group once: q' = H (s o q) / d, in log2 units (warp = head) ----
     if (warp < MAXGQ) {
@@ -592,17 +618,10 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     ModAcc ma{slot0, -1, 0u};
     float m_run = -INFINITY, l_run = 0.f;     // head g
 
-    const int npages = pe - pb;
-    const int my_n = npages > warp ? (npages - warp + WARPS - 1) / WARPS : 0;
-    if (lane == 0) {
-      for (int k = 0; k < min(my_n, STAGES); ++k) {
-        const int st = (ring_st + k) % STAGES;
-        fence_async_smem();
-        bulk_load(my_stage0 + (size_t)st * PL.page_bytes,
-                  unit_pages + (long long)(pb + warp + k * WARPS) * PL.page_bytes, PL.page_bytes, &my_bars[st]);
-      }
+    if (!lut_ready) {                         // once: the bulk copy of the level table
+      if (!mbar_wait(&lut_bar, 0u)) wait_failed = true;
+      lut_ready = true;
     }
-
 
     for (int k = 0; k < my_n; ++k) {
       const int st = ring_st;
@@ -738,6 +757,8 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     }
     __syncthreads();              // merge area is the stage ring of the next segment
   }
+  // the level table's copy must have landed before the CTA's shared memory goes away
+  if (!lut_ready && tid == 0 && !mbar_wait(&lut_bar, 0u)) atomicOr(a.err, ERR_WAIT);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -904,6 +925,12 @@ size_t decode_smem_bytes_t(int G) {
   size_t ring = (size_t)W * STAGES * PL.page_bytes;
   if (ring < sizeof(Merge<W>)) ring = sizeof(Merge<W>);
   return head + 128 + ring;
+}
+
+cudaError_t launch_lut(int bits, const LutArgs &a, cudaStream_t s) {
+  if (bits == 2) lut_kernel<2><<<32, 256, 0, s>>>(a);
+  else lut_kernel<4><<<32, 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 size_t decode_smem_bytes(int bits, int G) { return bits == 2 ? decode_smem_bytes_t<2>(G) : decode_smem_bytes_t<4>(G); }

@@ -176,11 +176,18 @@ struct DecodeArgs {
   int L, Hq, Hkv, M, bits, G;   // G: key group size, 0 = TurboQuant keys
   long long P_max, cap;
   long long units;
-  uint64_t unused;
+  const unsigned char *lut; // [256 code bytes][K 128 B | V 128 B] level table, built by launch_lut
   const float *signs;       // [D] +-1
   uint32_t *err;
   __half klut_src[16];      // key levels lambda_j (fp16)
   __half vlut_src[16];      // value levels l_j (fp16)
+};
+
+// The decode kernel's code-byte -> fp16 level table (64 KB), built once per cache.
+struct LutArgs {
+  unsigned char *out;
+  __half klev[16];          // key levels (the value levels for TurboQuant keys)
+  __half vlev[16];          // value levels
 };
 
 struct CombineArgs {
@@ -265,6 +272,8 @@ cudaError_t once_per_device(std::atomic<uint64_t> &done, Fn set) {
 cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+cudaError_t launch_lut(int bits, const LutArgs &a, cudaStream_t s);
+constexpr size_t LEVEL_TABLE_BYTES = 256 * 256;
 size_t decode_smem_bytes(int bits, int G);
 cudaError_t launch_move(const MoveArgs &a, cudaStream_t s);
 cudaError_t launch_far(const FarArgs &a, cudaStream_t s);
