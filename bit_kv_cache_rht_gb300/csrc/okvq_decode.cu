@@ -4,24 +4,29 @@
 // rotated once per head, and the inverse value rotations are batched after
 // aggregation).
 //
-// decode_kernel - split-K over the token axis, one CTA (8 warps) per SM. A CTA
-//   owns a balanced range of 64-token pages of the flattened (session, layer,
-//   kv head, page) list, cut into segments at unit boundaries. Each warp streams
-//   whole pages, one bulk copy each, into a private shared-memory ring (mbarrier
-//   completion) and works on 32-token half pages:
+// decode_kernel - split-K over the token axis, one CTA per SM (12 warps at
+//   2-bit, 8 at 4-bit). A CTA owns a balanced range of 64-token pages of the
+//   flattened (session, layer, kv head, page) list, cut into segments at unit
+//   boundaries. Each warp streams whole pages, one bulk copy each, into a private
+//   2-stage shared-memory ring (mbarrier completion, bounded waits) and works on
+//   32-token half pages:
 //     scores  S^T[16 x 8 tok] = [a_hi; a_lo][16 x 128] * Lambda^T[128 x 8 tok] + [beta; 0]
 //             (mma m16n8k16; rows 0-7 / 8-15 = the 8 query heads' fp16 high and
 //             residual parts of a = q' o range, so the sum is exact to ~2^-22)
-//     softmax online, base 2, fp32 (m, l per head)
+//     softmax online, base 2, fp32 (m, l per head), lazy reference
 //     values  O_m[128 ch x 8 heads] += Lcode[ch x 16 tok] * (p * n)[16 tok x 8 heads]
-//   The score output fragment is already the value MMA's B fragment. Key codes
-//   become fp16 levels in registers (mask -> fp32 fma builds a byte-permute
-//   selector -> prmt from a 4-entry table); value codes through a
-//   shared-memory table indexed by a whole code byte (one 8-byte load per 4
-//   codes). One accumulator set per modality (rotated value domain); warps merge
-//   in shared memory; one partial (m, l, o_m) per segment and head goes out.
-// combine_kernel - per (unit, 32 output channels): log-sum-exp merge of the
-//   unit's partials, O = (sum_m R_m^T o_m) / (l sqrt d), fp16 store.
+//   The score output fragment is already the value MMA's B fragment. Key and
+//   value codes become fp16 MMA operands through a 64 KB shared-memory table
+//   indexed by a whole code byte (built once per cache, bulk-copied per CTA);
+//   one 8-byte load yields a whole operand register pair. One accumulator set
+//   per modality in the rotated value domain: the current set in registers, the
+//   others parked in tensor memory. Evicted tokens (page deletion masks) take no
+//   part in the softmax. Warps merge in shared memory; one partial (m, l, o_m)
+//   per segment and head goes out.
+// combine_kernel - per (unit, 64 output channels): log-sum-exp merge of the
+//   unit's partials (and of the far-memory partials, if any), then
+//   O = (sum_m R_m^T o_m) / (l sqrt d) on the tensor cores, plus the far-memory
+//   values, fp16 store.
 #include "okvq_device.h"
 
 namespace okvq {
