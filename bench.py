@@ -62,6 +62,11 @@ def algorithmic_bytes(w, lengths, key_codec="omni"):
     return per_unit + mod + qo // 2, qo // 2, rot     # split kernel bytes, merge kernel out bytes, R bytes
 
 
+def make_workload(args):
+    """The named synthetic workload at the requested code width and key group size."""
+    return synth.WORKLOADS[args.workload](bits=getattr(args, "bits", 2), group_size=getattr(args, "group_size", 32))
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -111,11 +116,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def build_cache(w, torch, device, replicas=2, key_codec="omni"):
-    from bit_kv_cache_rht_gb300.okvq import Cache, OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT, calibrate_rotations
+def device_session_kv(w, s, torch, device):
+    """fp16 K, V [T][L][Hkv][d] of session s, drawn on the device with the synthetic
+    recipe: the workload's per-channel scales and modality means per layer; z ~ N(0, 1);
+    keys add a per-channel Gaussian random walk of step 0.02 per token (torch
+    generators seeded by (workload seed, session, layer); the parity tests draw the
+    same recipe with numpy)."""
     sh = w.shape
-    # value rotations: the calibration kernel on the workload's calibration slice
-    # (one untimed call loads the module, the second is timed)
+    mod = torch.from_numpy(w.sessions[s].modality()).to(device).long()
+    T = len(mod)
+    K = torch.empty((T, sh.num_layers, sh.num_kv_heads, sh.head_dim), dtype=torch.float16, device=device)
+    V = torch.empty_like(K)
+    for l in range(sh.num_layers):
+        kscale, vscale, mu = w.layer_params(l)
+        g = torch.Generator(device=device).manual_seed(((int(w.seed) * 1000003 + s) * 1009 + l) & 0x7FFFFFFF)
+        shp = (T, sh.num_kv_heads, sh.head_dim)
+        z = torch.randn(shp, device=device, generator=g)
+        drift = torch.cumsum(torch.randn(shp, device=device, generator=g) * 0.02, dim=0)
+        K[:, l] = (torch.from_numpy(kscale).to(device) * z + drift).half()
+        z = torch.randn(shp, device=device, generator=g)
+        V[:, l] = (torch.from_numpy(vscale).to(device) * z + torch.from_numpy(mu).to(device)[mod]).half()
+    return K, V
+
+
+def calibrate(w, torch, device):
+    """Value rotations of the workload from its calibration slice, by the calibration
+    kernel (one untimed call loads the module, the second is timed)."""
+    from bit_kv_cache_rht_gb300.okvq import calibrate_rotations
+    sh = w.shape
     Vc, modc = w.calibration_slice()
     Vcd, Mcd = torch.from_numpy(Vc).to(device), torch.from_numpy(modc).to(device)
     st = torch.cuda.current_stream()
@@ -139,34 +167,40 @@ def build_cache(w, torch, device, replicas=2, key_codec="omni"):
                           "unit": "GB/s", "frac": smem_bytes / (ms / 1e3) / 1e9 / smem_peak,
                           "peak_kind": "nominal (152 SMs x 128 B/clk x 2.07 GHz)"}}
     del Vcd, Mcd, rot
-    T = w.sessions[0].length
-    K = torch.empty((T, sh.num_layers, sh.num_kv_heads, sh.head_dim), dtype=torch.float16, device=device)
-    V = torch.empty_like(K)
-    for l in range(sh.num_layers):
-        k, v = w.layer_kv(0, l)
-        K[:, l] = torch.from_numpy(k).to(device)
-        V[:, l] = torch.from_numpy(v).to(device)
-    M = torch.from_numpy(w.sessions[0].modality()).to(device)
-    caches, append_ms = [], []
-    for rep in range(replicas):
-        c = Cache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, w.max_tokens, R, head_dim=sh.head_dim,
-                  group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
-                  hadamard_seed=w.hadamard_seed,
-                  key_codec=OKVQ_KEYS_TURBOQUANT if key_codec == "turbo" else OKVQ_KEYS_GROUP_RANGE)
-        st = torch.cuda.current_stream()
-        ev = []
-        for a, b in w.sessions[0].chunk_bounds():
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            c.append(0, K[a:b], V[a:b], M[a:b])
-            e1.record(st)
-            ev.append((e0, e1, b - a))
-        torch.cuda.synchronize()
+    return R, calib
+
+
+def build_cache(w, torch, device, replicas=2, key_codec="omni"):
+    from bit_kv_cache_rht_gb300.okvq import Cache, OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT
+    sh = w.shape
+    st = torch.cuda.current_stream()
+    R, calib = calibrate(w, torch, device)
+    caches = [Cache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads, w.max_tokens, R,
+                    head_dim=sh.head_dim, group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
+                    hadamard_seed=w.hadamard_seed,
+                    key_codec=OKVQ_KEYS_TURBOQUANT if key_codec == "turbo" else OKVQ_KEYS_GROUP_RANGE)
+              for _ in range(replicas)]
+    append_ms = [[] for _ in range(replicas)]
+    for s in range(len(w.sessions)):
+        if not w.sessions[s].length:
+            continue
+        K, V = device_session_kv(w, s, torch, device)
+        M = torch.from_numpy(w.sessions[s].modality()).to(device)
+        for rep, c in enumerate(caches):
+            ev = []
+            for a, b in w.sessions[s].chunk_bounds():
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                c.append(s, K[a:b], V[a:b], M[a:b])
+                e1.record(st)
+                ev.append((e0, e1, b - a))
+            torch.cuda.synchronize()
+            append_ms[rep] += [(e0.elapsed_time(e1), n) for e0, e1, n in ev]
+        del K, V, M
+    torch.cuda.synchronize()
+    for c in caches:
         if c.check_errors() != 0:
             raise RuntimeError("device error word set after append")
-        append_ms.append([(e0.elapsed_time(e1), n) for e0, e1, n in ev])
-        caches.append(c)
-    del K, V
     torch.cuda.empty_cache()
     return caches, append_ms, calib
 
@@ -293,11 +327,56 @@ def pseudo_leg(torch, device, peak, steps=10, near_tokens=8192, prototypes=3072,
                              "note": "far kernel time = (near + far kernels) - (near kernel alone), CUDA events"}}
 
 
+def streaming_run(args, torch, device, peak):
+    """The streaming configuration: 1-s chunks [2,304 video, 25 audio] of the 3B
+    shape appended one by one up to 131,072 tokens, one decode query after every
+    chunk; append and decode latency (CUDA events around each call, host work of
+    the call included) against the context length."""
+    from bit_kv_cache_rht_gb300.okvq import Cache
+    w = make_workload(args)
+    sh = w.shape
+    R, calib = calibrate(w, torch, device)
+    c = Cache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, w.max_tokens, R, head_dim=sh.head_dim,
+              group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
+              hadamard_seed=w.hadamard_seed)
+    K, V = device_session_kv(w, 0, torch, device)
+    M = torch.from_numpy(w.sessions[0].modality()).to(device)
+    Q = torch.from_numpy(w.queries(0)).to(device)
+    out = torch.empty_like(Q)
+    st = torch.cuda.current_stream()
+    rows = []
+    for a, b in w.sessions[0].chunk_bounds():
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(st)
+        c.append(0, K[a:b], V[a:b], M[a:b])
+        ev[1].record(st)
+        c.decode(Q, out)
+        ev[2].record(st)
+        rows.append((b, b - a, ev))
+    torch.cuda.synchronize()
+    if c.check_errors() != 0:
+        raise RuntimeError("device error word set in the streaming run")
+    res = [(T, n, e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for T, n, e in rows]
+    ap_tok = sum(n for _, n, _, _ in res)
+    ap_ms = sum(x for _, _, x, _ in res)
+    T_end, _, _, dec_ms = res[-1]
+    line = {"metric": METRIC, "value": T_end / (dec_ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": len(res),
+            "warmup": 0, "ms_per_step": dec_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 operands, f32 accumulate", "data": "synthetic", "config": config_of(w, args),
+            "streaming": {"chunks": len(res), "append_tokens_per_s": ap_tok / (ap_ms / 1e3),
+                          "decode_ms_at_context": [[T, round(d, 4)] for T, _, _, d in res[::8]] + [[T_end,
+                                                                                                  round(dec_ms, 4)]],
+                          "append_ms_per_chunk": float(np.median([x for _, _, x, _ in res])),
+                          "note": "first decode after each append rebuilds the work table (host) and uploads it"},
+            "calibration": calib}
+    print(json.dumps(line))
+
+
 def cpu_baseline_child(args):
     """Time the CPU oracle, as it stands, on a bounded sample: decode of the
     (layer 0, kv heads 0..Hkv-1) units of the workload, single-threaded."""
     from oracle import okvq_oracle as o
-    w = synth.WORKLOADS[args.workload]()
+    w = make_workload(args)
     sh = w.shape
     Vc, modc = w.calibration_slice()
     R = o.calibrate_rotations(Vc, modc, sh.num_modalities)[0].astype(np.float32)
@@ -319,12 +398,14 @@ def cpu_baseline_child(args):
             break
     per_sample = t_total / reps
     units_total = sh.num_layers * sh.num_kv_heads
-    step_s = per_sample * units_total / sh.num_kv_heads
-    T = w.sessions[0].length
-    print(json.dumps({"value": T / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-                      "sample": "oracle decode of layer 0 (%d of %d (layer, kv head) units), %d repetitions, "
-                                "%.1f s of CPU time, extrapolated linearly to all %d layers"
-                                % (sh.num_kv_heads, units_total, reps, t_total, sh.num_layers),
+    T0 = w.sessions[0].length
+    T_all = sum(x.length for x in w.sessions)
+    step_s = per_sample * sh.num_layers * T_all / T0      # linear in layers and in cached tokens
+    print(json.dumps({"value": T_all / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+                      "sample": "oracle decode of layer 0 of session 0 (%d of %d (layer, kv head) units), %d "
+                                "repetitions, %.1f s of CPU time, extrapolated linearly to all %d layers%s"
+                                % (sh.num_kv_heads, units_total, reps, t_total, sh.num_layers,
+                                   "" if len(w.sessions) == 1 else " and all %d sessions' tokens" % len(w.sessions)),
                       "step_s": step_s}))
 
 
@@ -332,6 +413,7 @@ def run_cpu_baseline(args):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload,
+           "--bits", str(getattr(args, "bits", 2)), "--group-size", str(getattr(args, "group_size", 32)),
            "--cpu-seconds", str(args.cpu_seconds), "--cpu-max-reps", str(args.cpu_max_reps),
            "--key-codec", args.key_codec]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
@@ -347,14 +429,15 @@ def reference_arm(args):
     steps = []
     base = None
     for i in range(args.warmup + args.steps):
-        res = run_cpu_baseline(argparse.Namespace(workload=args.workload, cpu_seconds=args.ref_seconds,
+        res = run_cpu_baseline(argparse.Namespace(workload=args.workload, bits=args.bits, group_size=args.group_size,
+                                                  cpu_seconds=args.ref_seconds,
                                                   cpu_max_reps=1, key_codec=args.key_codec))
         if i >= args.warmup:
             steps.append(res)
         base = res
     vals = [s["value"] for s in steps if s.get("value")]
     v = statistics.median(vals) if vals else None
-    w = synth.WORKLOADS[args.workload]()
+    w = make_workload(args)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": (statistics.median([s["step_s"] for s in steps]) * 1e3) if steps else None,
@@ -368,10 +451,13 @@ def reference_arm(args):
 
 def config_of(w, args):
     sh = w.shape
-    return {"workload": "%s: %d layers, %d q / %d kv heads, head_dim %d, %d-token cache, %d-bit codes, group %d"
+    lengths = [x.length for x in w.sessions]
+    cache = ("%d-token cache" % lengths[0]) if len(lengths) == 1 else (
+        "%d sessions of %d-%d tokens (%d in all)" % (len(lengths), min(lengths), max(lengths), sum(lengths)))
+    return {"workload": "%s: %d layers, %d q / %d kv heads, head_dim %d, %s, %d-bit codes, group %d"
                         % (w.name, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
-                           w.sessions[0].length, sh.bits, sh.group_size),
-            "sessions": len(w.sessions), "context_tokens": w.sessions[0].length, "bits": sh.bits,
+                           cache, sh.bits, sh.group_size),
+            "sessions": len(w.sessions), "context_tokens": sum(lengths), "bits": sh.bits,
             "group_size": sh.group_size,
             "key_codec": "turboquant (per-token norm, fixed scale)" if getattr(args, "key_codec", "omni") == "turbo"
                          else "omnikvquant (per-group min-max ranges)",
@@ -394,6 +480,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--key-codec", default="omni", choices=["omni", "turbo"],
                     help="omni: per-group key ranges (the method); turbo: the TurboQuant comparison codec")
+    ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
+    ap.add_argument("--group-size", type=int, default=32, choices=[32, 64])
     ap.add_argument("--cpu-baseline-child", action="store_true")
     args = ap.parse_args()
     if args.cpu_baseline_child:
@@ -414,7 +502,9 @@ def main():
     from bit_kv_cache_rht_gb300 import okvq
     okvq.load()
 
-    w = synth.WORKLOADS[args.workload]()
+    if args.workload == "streaming":
+        return streaming_run(args, torch, device, peaks()[0])
+    w = make_workload(args)
     sh = w.shape
     caches, append_ms, calib = build_cache(w, torch, device, replicas=2, key_codec=args.key_codec)
     T = w.sessions[0].length
@@ -491,6 +581,7 @@ def main():
     if rank == 0:
         peak, peak_kind = peaks()
         avg_split = float(np.mean(split_ms))
+        step_us = 1e3 * (np.asarray(split_ms) + np.asarray(merge_ms))
         achieved = split_bytes / (avg_split / 1e3) / 1e9
         ms_step = t_max / args.steps
         ap_ms = sum(x for x, _ in append_ms[0])
@@ -513,6 +604,8 @@ def main():
             "vs_baseline": None, "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
             "config": config_of(w, args),
             "hbm_gbs_step": step_bytes / (ms_step / 1e3) / 1e9,
+            "latency_us": {"p50": float(np.percentile(step_us, 50)), "p99": float(np.percentile(step_us, 99)),
+                           "of": "decode + merge kernels per step, profiled pass (%d steps)" % len(step_us)},
             "roofline": {"bound": "hbm", "kernel": "decode_kernel (split-K fused 2-bit attention)",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -528,10 +621,11 @@ def main():
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
         }
-        line["compaction"] = compaction_leg(caches[0], w, torch, Q, out, peak, 10)
-        del caches
-        torch.cuda.empty_cache()
-        line["pseudo_tokens"] = pseudo_leg(torch, device, peak)
+        if args.workload == "qwen3b" and sh.bits == 2 and sh.group_size == 32 and args.key_codec == "omni":
+            line["compaction"] = compaction_leg(caches[0], w, torch, Q, out, peak, 10)
+            del caches
+            torch.cuda.empty_cache()
+            line["pseudo_tokens"] = pseudo_leg(torch, device, peak)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = run_cpu_baseline(args)
         print(json.dumps(line))
