@@ -32,14 +32,16 @@ struct Smem {
   float vnorm[PAGE];
   int mod[PAGE];
   float kmn[2][D], kmx[2][D];     // group min and range (fp16 values held as fp32)
+  float red[2][2][D];              // per-half min / max of a group
   int present[MAXM];
 };
 
-__device__ __forceinline__ int code_of(float x, const float *thr, int nthr) {
+// code = number of thresholds strictly below x (NTHR = levels - 1)
+template <int NTHR>
+__device__ __forceinline__ int code_of(float x, const float *thr) {
   int c = 0;
-#pragma unroll 15
-  for (int j = 0; j < 15; ++j)
-    if (j < nthr && x > thr[j]) ++c;
+#pragma unroll
+  for (int j = 0; j < NTHR; ++j) c += x > thr[j] ? 1 : 0;
   return c;
 }
 
@@ -67,50 +69,56 @@ __device__ __forceinline__ void rotate_key_row(const __half *src, const float *s
 }
 
 // Pack the codes of tile `tile` (16 tokens) from codes[64][128] into lane chunks.
-// `kind` 0 = K layout, 1 = V layout. Tokens >= valid_end (page-relative) pack as 0.
-__device__ void pack_tile(const uint8_t *codes, uint8_t *dst, int tile, int bits, int kind, int valid_end,
-                          int tid, int nthreads) {
-  const int words_per_lane = bits * 2;         // 16 B or 32 B per lane
-  for (int w = tid; w < 32 * words_per_lane; w += nthreads) {
-    const int lane = w / words_per_lane, wi = w % words_per_lane;
+// KIND 0 = K layout, 1 = V layout. Tokens >= valid_end (page-relative) pack as 0.
+// The code slots of a word are unrolled, so their (token, channel) positions
+// reduce to a few operations on the lane and word index.
+template <int BITS, int KIND>
+__device__ void pack_tile(const uint8_t *codes, uint8_t *dst, int tile, int valid_end, int tid, int nthreads) {
+  constexpr int WPL = BITS * 2;                 // 32-bit words per lane chunk (16 B or 32 B)
+  for (int w = tid; w < 32 * WPL; w += nthreads) {
+    const int lane = w / WPL, wi = w % WPL;
     uint32_t word = 0;
-    for (int b = 0; b < 32; b += bits) {
+#pragma unroll
+    for (int b = 0; b < 32; b += BITS) {
       int j, e, tok, ch;
-      chunk_code_at(kind, bits, wi, b, j, e);
-      if (kind == 0) k_pair_coords(lane, j, e, tok, ch);
+      chunk_code_at(KIND, BITS, wi, b, j, e);
+      if (KIND == 0) k_pair_coords(lane, j, e, tok, ch);
       else v_pair_coords(lane, j, e, tok, ch);
       tok += 16 * tile;
       const uint32_t c = tok < valid_end ? codes[tok * D + ch] : 0u;
       word |= c << b;
     }
-    reinterpret_cast<uint32_t *>(dst)[lane * words_per_lane + wi] = word;
+    reinterpret_cast<uint32_t *>(dst)[lane * WPL + wi] = word;
   }
 }
 
 // Inverse of pack_tile for tokens < keep_end (page-relative): fill codes[][] from dst.
-__device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int bits, int kind, int keep_end,
-                            int tid, int nthreads) {
-  const int words_per_lane = bits * 2;
-  const uint32_t mask = (1u << bits) - 1u;
-  for (int w = tid; w < 32 * words_per_lane; w += nthreads) {
-    const int lane = w / words_per_lane, wi = w % words_per_lane;
-    const uint32_t word = reinterpret_cast<const uint32_t *>(src)[lane * words_per_lane + wi];
-    for (int b = 0; b < 32; b += bits) {
+template <int BITS, int KIND>
+__device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int keep_end, int tid, int nthreads) {
+  constexpr int WPL = BITS * 2;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  for (int w = tid; w < 32 * WPL; w += nthreads) {
+    const int lane = w / WPL, wi = w % WPL;
+    const uint32_t word = reinterpret_cast<const uint32_t *>(src)[lane * WPL + wi];
+#pragma unroll
+    for (int b = 0; b < 32; b += BITS) {
       int j, e, tok, ch;
-      chunk_code_at(kind, bits, wi, b, j, e);
-      if (kind == 0) k_pair_coords(lane, j, e, tok, ch);
+      chunk_code_at(KIND, BITS, wi, b, j, e);
+      if (KIND == 0) k_pair_coords(lane, j, e, tok, ch);
       else v_pair_coords(lane, j, e, tok, ch);
       tok += 16 * tile;
-      if (tok < keep_end) codes[tok * D + ch] = (uint8_t)((word >> b) & mask);
+      if (tok < keep_end) codes[tok * D + ch] = (uint8_t)((word >> b) & MASK);
     }
   }
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
+  constexpr int NTHR = (1 << BITS) - 1;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem &S = *reinterpret_cast<Smem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PageLayout PL = page_layout(a.bits, a.G);
+  const PageLayout PL = page_layout(BITS, a.G);
 
   const long long page = a.page0 + blockIdx.x;
   const int lh = blockIdx.y;                       // layer * Hkv + kv head
@@ -155,8 +163,8 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   // ---- values: load transposed tile + norms ----
   for (int i = tid; i < D * XT_STRIDE; i += THREADS) S.xt[i] = 0.f;
   // keep codes of older tokens that share a 16-token tile with the first new token
-  if (ta % TILE != 0) unpack_tile(S.vc, pg + PL.off_v + (ta / TILE) * PL.tile_bytes, ta / TILE, a.bits, 1, ta,
-                                  tid, THREADS);
+  if (ta % TILE != 0) unpack_tile<BITS, 1>(S.vc, pg + PL.off_v + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid,
+                                           THREADS);
   __syncthreads();
   for (int t = ta + warp; t < tb; t += THREADS / 32) {
     const __half *src = a.v + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           float w = acc[r][k] * sc;
-          S.vc[t * D + 4 * ii + k] = (uint8_t)code_of(w, a.vthr, a.nlev - 1);
+          S.vc[t * D + 4 * ii + k] = (uint8_t)code_of<NTHR>(w, a.vthr);
         }
       }
     }
@@ -221,14 +229,14 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   }
   // write the value tiles that got new tokens
   for (int tile = ta / TILE; tile * TILE < tb; ++tile)
-    pack_tile(S.vc, pg + PL.off_v + tile * PL.tile_bytes, tile, a.bits, 1, tb, tid, THREADS);
+    pack_tile<BITS, 1>(S.vc, pg + PL.off_v + tile * PL.tile_bytes, tile, tb, tid, THREADS);
 
   if (a.G == 0) {
     // ---- TurboQuant keys (section 2, TurboQuant bullet): every new token now, like a
     // value with the shared Hadamard rotation: n = |k|, w = sqrt(d) k'/n, value levels ----
     __syncthreads();
     // keep the codes of older tokens that share a 16-token tile with the first new token
-    if (ta % TILE != 0) unpack_tile(S.kc, pg + (ta / TILE) * PL.tile_bytes, ta / TILE, a.bits, 0, ta, tid, THREADS);
+    if (ta % TILE != 0) unpack_tile<BITS, 0>(S.kc, pg + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid, THREADS);
     for (int t = ta + warp; t < tb; t += THREADS / 32) {
       const __half *src = a.k + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
       float ss = 0.f;
@@ -244,12 +252,12 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       rotate_key_row(src, a.signs, lane, x);
       const float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) S.kc[t * D + 4 * lane + j] = (uint8_t)code_of(x[j] * sc, a.vthr, a.nlev - 1);
+      for (int j = 0; j < 4; ++j) S.kc[t * D + 4 * lane + j] = (uint8_t)code_of<NTHR>(x[j] * sc, a.vthr);
       if (lane == 0) reinterpret_cast<__half *>(pg + PL.off_stats)[t] = __float2half_rn(n);
     }
     __syncthreads();
     for (int tile = ta / TILE; tile * TILE < tb; ++tile)
-      pack_tile(S.kc, pg + tile * PL.tile_bytes, tile, a.bits, 0, tb, tid, THREADS);
+      pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, tb, tid, THREADS);
     return;                       // no key groups, no fp16 tail
   }
 
@@ -275,14 +283,23 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     }
     __syncthreads();
     // per-channel statistics of the group: min rounded down, range rounded up
+    // (thread (c, h) scans half h of the members; the halves meet in shared memory)
     const int gi = g0 / G;
-    for (int c = tid; c < D; c += THREADS) {
-      float mn = xk[g0 * D + c], mx = mn;
-      for (int r = 1; r < G; ++r) {
-        float v = xk[(g0 + r) * D + c];
+    {
+      const int c = tid & (D - 1), h = tid / D;
+      float mn = xk[(g0 + h * (G / 2)) * D + c], mx = mn;
+#pragma unroll 8
+      for (int r = 1; r < G / 2; ++r) {
+        const float v = xk[(g0 + h * (G / 2) + r) * D + c];
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
       }
+      S.red[h][0][c] = mn;
+      S.red[h][1][c] = mx;
+    }
+    __syncthreads();
+    for (int c = tid; c < D; c += THREADS) {
+      const float mn = fminf(S.red[0][0][c], S.red[1][0][c]), mx = fmaxf(S.red[0][1][c], S.red[1][1][c]);
       const __half hmn = __float2half_rd(mn);
       const __half hrg = __float2half_ru(__fsub_ru(mx, __half2float(hmn)));
       S.kmn[gi][c] = __half2float(hmn);
@@ -298,13 +315,13 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       int code = 0;
       if (rng != 0.f) {
         float u = __fdiv_rn(__fsub_rn(xk[(g0 + r) * D + c], mn), rng);
-        code = code_of(u, a.kthr, a.nlev - 1);
+        code = code_of<NTHR>(u, a.kthr);
       }
       S.kc[(g0 + r) * D + c] = (uint8_t)code;
     }
     __syncthreads();
     for (int tile = g0 / TILE; tile < (g0 + G) / TILE; ++tile)
-      pack_tile(S.kc, pg + tile * PL.tile_bytes, tile, a.bits, 0, PAGE, tid, THREADS);
+      pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, PAGE, tid, THREADS);
     __syncthreads();
   }
   (void)any_group;
@@ -331,11 +348,14 @@ cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s) {
   static std::atomic<uint64_t> attr_done{0};
   const size_t smem = sizeof(Smem);
   cudaError_t e = once_per_device(attr_done, [&] {
-    return cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t r = cudaFuncSetAttribute(append_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(append_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
   dim3 grid(n_pages, a.L * a.Hkv);
-  append_kernel<<<grid, THREADS, smem, s>>>(a);
+  if (a.bits == 2) append_kernel<2><<<grid, THREADS, smem, s>>>(a);
+  else append_kernel<4><<<grid, THREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 
