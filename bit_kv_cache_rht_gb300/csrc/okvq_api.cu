@@ -24,7 +24,7 @@ struct okvq_cache {
   __half *tails = nullptr;      // [2][units][G][D]
   uint8_t *mod = nullptr;       // [S][cap]
   uint32_t *rot_frag = nullptr; // R^T in mma fragment order, fp16 high and residual (see CombineArgs)
-  float *rot_t = nullptr;       // transposed per matrix
+  __half *rot_h = nullptr;      // [L*Hkv*M][2][D][ROT_ROW_H] fp16 high / residual parts of R (append)
   float *signs = nullptr;       // [D]
   uint32_t *err = nullptr;
   float *partials = nullptr;
@@ -127,7 +127,7 @@ void release(okvq_cache *h) {
   cudaFree(h->tails);
   cudaFree(h->mod);
   cudaFree(h->rot_frag);
-  cudaFree(h->rot_t);
+  cudaFree(h->rot_h);
   cudaFree(h->signs);
   cudaFree(h->err);
   cudaFree(h->partials);
@@ -469,7 +469,8 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->tails, tails)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->mod, (size_t)h->S * h->cap)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->rot_frag, rot)) != OKVQ_OK) return fail(st);
-  if ((st = alloc_dev((void **)&h->rot_t, rot)) != OKVQ_OK) return fail(st);
+  const size_t rot_h_bytes = (size_t)h->L * h->Hkv * h->M * 2 * D * ROT_ROW_H * sizeof(__half);
+  if ((st = alloc_dev((void **)&h->rot_h, rot_h_bytes)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
@@ -523,12 +524,18 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   }
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
-    std::vector<float> rt(nmat * D * D);
+    // R as fp16 high + residual parts, rows padded (the append kernel's tensor-core rotation)
+    std::vector<__half> rh(nmat * 2 * D * ROT_ROW_H, __float2half_rn(0.f));
     for (size_t mtx = 0; mtx < nmat; ++mtx) {
       const float *R = c.value_rot + mtx * D * D;
-      float *T = rt.data() + mtx * D * D;
+      __half *H = rh.data() + mtx * 2 * D * ROT_ROW_H;
       for (int i = 0; i < D; ++i)
-        for (int cc = 0; cc < D; ++cc) T[cc * D + i] = R[i * D + cc];
+        for (int cc = 0; cc < D; ++cc) {
+          const float v = R[i * D + cc];
+          const __half hi = __float2half_rn(v);
+          H[i * ROT_ROW_H + cc] = hi;
+          H[(D + i) * ROT_ROW_H + cc] = __float2half_rn(v - __half2float(hi));
+        }
     }
     // R^T as m16n8k16 A fragments: m-tile mt (16 output channels), k-step ks (16 rows
     // r of the stacked R_m, m = ks / 8), lane (g, t4): a0 = (c = 16mt+g, r = r0..r0+1),
@@ -552,7 +559,8 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
               fr[base + 4 + i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
             }
     if (cudaMemcpyAsync(h->rot_frag, fr.data(), rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
-    if (cudaMemcpyAsync(h->rot_t, rt.data(), rot, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail(OKVQ_ECUDA);
+    if (cudaMemcpyAsync(h->rot_h, rh.data(), rot_h_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return fail(OKVQ_ECUDA);
     uint64_t state = c.hadamard_seed;
     float sg[D];
     for (int w = 0; w < D / 64; ++w) {
@@ -604,7 +612,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   a.tail_new = h->tails + (size_t)(1 - h->tail_sel[session]) * tail_buf;
   a.mod = h->mod;
   a.cap = h->cap;
-  a.rot_t = h->rot_t;
+  a.rot_h = h->rot_h;
   a.signs = h->signs;
   a.err = h->err;
   a.page0 = T0 / PAGE;

@@ -20,13 +20,16 @@ namespace okvq {
 namespace {
 
 constexpr int THREADS = 256;
-constexpr int XT_STRIDE = PAGE + 4;        // transposed value tile row stride (floats)
 constexpr float INV_SQRT_D = 0.0883883476483184405501f;   // fp32(1/sqrt(128))
 constexpr float SQRT_D = 11.3137084989847603904f;
 
+constexpr int ROW_H = ROT_ROW_H;           // padded fp16 row: ldmatrix row reads hit distinct banks
+
 struct Smem {
-  float rt[D * D];                 // R_m^T for one modality (c-major)
-  float xt[D * XT_STRIDE];         // value tile, transposed [c][token]; later keys [token][c]
+  __half rh[2][D][ROW_H];          // R_m of one modality, fp16 high and residual parts, [output][channel]
+  __half vh[PAGE][ROW_H];          // the page's values, fp16 [token][channel]
+  float xt[PAGE * D];              // keys [token][c] (rotated, fp32)
+  uint64_t bar;                    // completion of the bulk copy of rh
   uint8_t vc[PAGE * D];            // value codes of the page
   uint8_t kc[PAGE * D];            // key codes of the page
   float vnorm[PAGE];
@@ -35,6 +38,33 @@ struct Smem {
   float red[2][2][D];              // per-half min / max of a group
   int present[MAXM];
 };
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// bounded wait on an mbarrier phase; false if it gave up
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity) {
+  for (long long it = 0; it < (1ll << 26); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 // code = number of thresholds strictly below x (NTHR = levels - 1)
 template <int NTHR>
@@ -160,8 +190,12 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     }
   }
 
-  // ---- values: load transposed tile + norms ----
-  for (int i = tid; i < D * XT_STRIDE; i += THREADS) S.xt[i] = 0.f;
+  // ---- values: fp16 tile + norms ----
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = tid; i < PAGE * ROW_H / 2; i += THREADS) reinterpret_cast<uint32_t *>(&S.vh[0][0])[i] = 0u;
   // keep codes of older tokens that share a 16-token tile with the first new token
   if (ta % TILE != 0) unpack_tile<BITS, 1>(S.vc, pg + PL.off_v + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid,
                                            THREADS);
@@ -172,8 +206,9 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       int c = lane + 32 * k;
-      float x = __half2float(src[c]);
-      S.xt[c * XT_STRIDE + t] = x;
+      const __half hv = src[c];
+      S.vh[t][c] = hv;
+      const float x = __half2float(hv);
       ss = fmaf(x, x, ss);
     }
 #pragma unroll
@@ -187,45 +222,66 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   __syncthreads();
 
   // ---- values: w = sqrt(d) * R_m v / |v| per modality present, then codes ----
-  const int tt = warp;            // tokens 8*tt .. 8*tt+7
-  const int ii = lane;            // outputs 4*ii .. 4*ii+3
+  // On the tensor cores: [64 tokens x 128 ch] (fp16, exact) times R_m^T, with R_m in
+  // fp16 high + residual parts (two MMAs, fp32 accumulation: ~2^-22 relative, as
+  // fp32 arithmetic). Warp w: tokens 16 (w & 3) .., outputs 64 (w >> 2) ..
+  const int mt = warp & 3, o0 = 64 * (warp >> 2);
+  const int g = lane >> 2, t4 = lane & 3;
+  uint32_t phase = 0;
   for (int m = 0; m < a.M; ++m) {
     if (!S.present[m]) continue;  // uniform: smem flag read after a barrier
-    const float4 *rsrc = reinterpret_cast<const float4 *>(a.rot_t + (((long long)lh * a.M + m) * D * D));
-    float4 *rdst = reinterpret_cast<float4 *>(S.rt);
-    for (int i = tid; i < D * D / 4; i += THREADS) rdst[i] = rsrc[i];
-    __syncthreads();
+    if (tid == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar)),
+                   "r"((uint32_t)sizeof(S.rh))
+                   : "memory");
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_addr(&S.rh[0][0][0])),
+          "l"(a.rot_h + ((long long)lh * a.M + m) * (2 * D * ROW_H)), "r"((uint32_t)sizeof(S.rh)),
+          "r"(smem_addr(&S.bar))
+          : "memory");
+    }
+    const bool failed = __syncthreads_or(!wait_bar(&S.bar, phase));
+    phase ^= 1u;
+    if (failed) {                                  // the codes of this chunk's values stay unwritten
+      if (tid == 0) atomicOr(a.err, ERR_WAIT);
+      break;
+    }
     float acc[8][4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const uint32_t va = smem_addr(&S.vh[16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+    const int bj = lane >> 3;                      // ldmatrix matrix: hi / lo x channel half
+    const uint32_t rb = smem_addr(&S.rh[bj >> 1][o0 + (lane & 7)][8 * (bj & 1)]);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc[r][k] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < D; ++c) {
-      const float4 x0 = *reinterpret_cast<const float4 *>(&S.xt[c * XT_STRIDE + 8 * tt]);
-      const float4 x1 = *reinterpret_cast<const float4 *>(&S.xt[c * XT_STRIDE + 8 * tt + 4]);
-      const float4 rv = *reinterpret_cast<const float4 *>(&S.rt[c * D + 4 * ii]);
-      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const float rs[4] = {rv.x, rv.y, rv.z, rv.w};
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t A[4];
+      ldsm4(va + 32 * kk, A);
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[r][k] = fmaf(xs[r], rs[k], acc[r][k]);
+      for (int nt = 0; nt < 8; ++nt) {
+        uint32_t B[4];
+        ldsm4(rb + (8 * nt * ROW_H) * 2 + 32 * kk, B);
+        mma16816(acc[nt], A, B[0], B[1]);
+        mma16816(acc[nt], A, B[2], B[3]);
+      }
     }
+    // rows: tokens 16 mt + g (+8); columns: outputs o0 + 8 nt + 2 t4 (+1)
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      int t = 8 * tt + r;
+    for (int r = 0; r < 2; ++r) {
+      const int t = 16 * mt + g + 8 * r;
       if (t >= ta && t < tb && S.mod[t] == m) {
-        float n = S.vnorm[t];
-        float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
+        const float n = S.vnorm[t];
+        const float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float w = acc[r][k] * sc;
-          S.vc[t * D + 4 * ii + k] = (uint8_t)code_of<NTHR>(w, a.vthr);
+        for (int nt = 0; nt < 8; ++nt) {
+          const int i = o0 + 8 * nt + 2 * t4;
+          S.vc[t * D + i] = (uint8_t)code_of<NTHR>(acc[nt][2 * r] * sc, a.vthr);
+          S.vc[t * D + i + 1] = (uint8_t)code_of<NTHR>(acc[nt][2 * r + 1] * sc, a.vthr);
         }
       }
     }
-    __syncthreads();
+    __syncthreads();                               // rh is rewritten for the next modality
   }
   // write the value tiles that got new tokens
   for (int tile = ta / TILE; tile * TILE < tb; ++tile)

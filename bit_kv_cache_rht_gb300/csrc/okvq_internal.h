@@ -59,6 +59,7 @@ constexpr int PAGE = 64;
 constexpr int TILE = 16;
 constexpr int MAXM = 3;
 constexpr int MAXGQ = 8;
+constexpr int ROT_ROW_H = D + 8;   // padded row (fp16) of the value rotations the append kernel stages
 
 enum : uint32_t { ERR_MODALITY = 1u, ERR_WAIT = 2u };
 
@@ -154,7 +155,7 @@ struct AppendArgs {
   __half *tail_new;         // [units][G][D] buffer written (next)
   uint8_t *mod;             // [S][cap] session modality ids
   long long cap;            // max_tokens rounded up to a page
-  const float *rot_t;       // [L][Hkv][M][D][D]  (c, i) = R[i][c]
+  const __half *rot_h;      // [L][Hkv][M][2][D][ROT_ROW_H]: R[i][c] as fp16 high, then residual part
   const float *signs;       // [D] +-1 Hadamard signs
   uint32_t *err;
   long long page0;          // first page touched
