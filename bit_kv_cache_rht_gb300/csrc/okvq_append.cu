@@ -26,9 +26,13 @@ constexpr float SQRT_D = 11.3137084989847603904f;
 constexpr int ROW_H = ROT_ROW_H;           // padded fp16 row: ldmatrix row reads hit distinct banks
 
 struct Smem {
-  __half rh[2][D][ROW_H];          // R_m of one modality, fp16 high and residual parts, [output][channel]
-  __half vh[PAGE][ROW_H];          // the page's values, fp16 [token][channel]
-  float xt[PAGE * D];              // keys [token][c] (rotated, fp32)
+  union {
+    struct {
+      __half rh[2][D][ROW_H];      // R_m of one modality, fp16 high and residual parts, [output][channel]
+      __half vh[PAGE][ROW_H];      // the page's values, fp16 [token][channel]
+    } v;
+    float xt[PAGE * D];            // then: keys [token][c] (rotated, fp32)
+  } u;
   uint64_t bar;                    // completion of the bulk copy of rh
   uint8_t vc[PAGE * D];            // value codes of the page
   uint8_t kc[PAGE * D];            // key codes of the page
@@ -78,9 +82,12 @@ __device__ __forceinline__ int code_of(float x, const float *thr) {
 // Canonical fp32 key rotation of one token, warp-wide: lane holds channels
 // 4*lane .. 4*lane+3 of k' = fp32(1/sqrt d) * FWHT(s o k) (butterfly strides 1 and 2
 // inside the lane, 4 .. 64 across lanes, round-to-nearest adds, no contraction).
-__device__ __forceinline__ void rotate_key_row(const __half *src, const float *signs, int lane, float (&x)[4]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) x[j] = __half2float(src[4 * lane + j]) * signs[4 * lane + j];
+__device__ __forceinline__ void rotate_key_row(uint2 raw, const float *signs, int lane, float (&x)[4]) {
+  const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x), h23 = *reinterpret_cast<const __half2 *>(&raw.y);
+  x[0] = __low2float(h01) * signs[4 * lane];
+  x[1] = __high2float(h01) * signs[4 * lane + 1];
+  x[2] = __low2float(h23) * signs[4 * lane + 2];
+  x[3] = __high2float(h23) * signs[4 * lane + 3];
   float y0 = __fadd_rn(x[0], x[1]), y1 = __fsub_rn(x[0], x[1]);
   float y2 = __fadd_rn(x[2], x[3]), y3 = __fsub_rn(x[2], x[3]);
   x[0] = __fadd_rn(y0, y2); x[2] = __fsub_rn(y0, y2);
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int i = tid; i < PAGE * ROW_H / 2; i += THREADS) reinterpret_cast<uint32_t *>(&S.vh[0][0])[i] = 0u;
+  for (int i = tid; i < PAGE * ROW_H / 2; i += THREADS) reinterpret_cast<uint32_t *>(&S.u.v.vh[0][0])[i] = 0u;
   // keep codes of older tokens that share a 16-token tile with the first new token
   if (ta % TILE != 0) unpack_tile<BITS, 1>(S.vc, pg + PL.off_v + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid,
                                            THREADS);
@@ -207,7 +214,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     for (int k = 0; k < 4; ++k) {
       int c = lane + 32 * k;
       const __half hv = src[c];
-      S.vh[t][c] = hv;
+      S.u.v.vh[t][c] = hv;
       const float x = __half2float(hv);
       ss = fmaf(x, x, ss);
     }
@@ -233,12 +240,12 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     if (tid == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar)),
-                   "r"((uint32_t)sizeof(S.rh))
+                   "r"((uint32_t)sizeof(S.u.v.rh))
                    : "memory");
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-              smem_addr(&S.rh[0][0][0])),
-          "l"(a.rot_h + ((long long)lh * a.M + m) * (2 * D * ROW_H)), "r"((uint32_t)sizeof(S.rh)),
+              smem_addr(&S.u.v.rh[0][0][0])),
+          "l"(a.rot_h + ((long long)lh * a.M + m) * (2 * D * ROW_H)), "r"((uint32_t)sizeof(S.u.v.rh)),
           "r"(smem_addr(&S.bar))
           : "memory");
     }
@@ -251,9 +258,9 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const uint32_t va = smem_addr(&S.vh[16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+    const uint32_t va = smem_addr(&S.u.v.vh[16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
     const int bj = lane >> 3;                      // ldmatrix matrix: hi / lo x channel half
-    const uint32_t rb = smem_addr(&S.rh[bj >> 1][o0 + (lane & 7)][8 * (bj & 1)]);
+    const uint32_t rb = smem_addr(&S.u.v.rh[bj >> 1][o0 + (lane & 7)][8 * (bj & 1)]);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t A[4];
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float n = sqrtf(ss);
       float x[4];
-      rotate_key_row(src, a.signs, lane, x);
+      rotate_key_row(*reinterpret_cast<const uint2 *>(src + 4 * lane), a.signs, lane, x);
       const float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) S.kc[t * D + 4 * lane + j] = (uint8_t)code_of<NTHR>(x[j] * sc, a.vthr);
@@ -317,45 +324,68 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     return;                       // no key groups, no fp16 tail
   }
 
-  // ---- keys: groups that complete with this chunk ----
+  // ---- keys: groups that complete with this chunk, all of the page's at once ----
   const int G = a.G;
-  float *xk = S.xt;               // keys as [token][c], row stride D
+  float *xk = S.u.xt;             // keys as [token][c], row stride D (the value staging is free now)
   __syncthreads();
-  bool any_group = false;
+  uint32_t gmask = 0;             // bit gi: group gi of the page completes now
   for (int g0 = 0; g0 < PAGE; g0 += G) {
-    long long gend = P0 + g0 + G;
-    bool complete_now = gend > T0 && gend <= T1;
-    any_group |= complete_now;
-    if (!complete_now) continue;
+    const long long gend = P0 + g0 + G;
+    if (gend > T0 && gend <= T1) gmask |= 1u << (g0 / G);
+  }
+  if (gmask) {
     const __half *told = a.tail_old + unit * (long long)G * D;
-    // rotate every member: warp per token, lane holds channels 4*lane .. 4*lane+3
-    for (int r = warp; r < G; r += THREADS / 32) {
-      long long t = P0 + g0 + r;
-      const __half *src = t < T0 ? told + (t - (P0 + g0)) * D
-                                 : a.k + (t - T0) * (long long)row_stride + (long long)lh * D;
+    // rotate every member: warp per token (8 tokens per warp, loads issued first),
+    // lane holds channels 4*lane .. 4*lane+3
+    constexpr int PER_WARP = PAGE / (THREADS / 32);
+    uint2 raw[PER_WARP];
+#pragma unroll
+    for (int j = 0; j < PER_WARP; ++j) {
+      const int r = warp + j * (THREADS / 32);
+      raw[j] = make_uint2(0u, 0u);
+      if ((gmask >> (r / G)) & 1u) {
+        const long long t = P0 + r, gs = P0 + (r / G) * G;
+        const __half *src = t < T0 ? told + (t - gs) * D : a.k + (t - T0) * (long long)row_stride + (long long)lh * D;
+        raw[j] = *reinterpret_cast<const uint2 *>(src + 4 * lane);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < PER_WARP; ++j) {
+      const int r = warp + j * (THREADS / 32);
+      if (!((gmask >> (r / G)) & 1u)) continue;     // warp-uniform
       float x[4];
-      rotate_key_row(src, a.signs, lane, x);
-      *reinterpret_cast<float4 *>(&xk[(g0 + r) * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
+      rotate_key_row(raw[j], a.signs, lane, x);
+      *reinterpret_cast<float4 *>(&xk[r * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
     }
     __syncthreads();
-    // per-channel statistics of the group: min rounded down, range rounded up
-    // (thread (c, h) scans half h of the members; the halves meet in shared memory)
-    const int gi = g0 / G;
+    // per-channel statistics: thread (c, h) scans 32 members (G = 32: group h;
+    // G = 64: half h of the group); then min rounded down, range rounded up
     {
       const int c = tid & (D - 1), h = tid / D;
-      float mn = xk[(g0 + h * (G / 2)) * D + c], mx = mn;
+      if ((gmask >> ((32 * h) / G)) & 1u) {
+        float mn = xk[(32 * h) * D + c], mx = mn;
 #pragma unroll 8
-      for (int r = 1; r < G / 2; ++r) {
-        const float v = xk[(g0 + h * (G / 2) + r) * D + c];
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
+        for (int r = 1; r < 32; ++r) {
+          const float v = xk[(32 * h + r) * D + c];
+          mn = fminf(mn, v);
+          mx = fmaxf(mx, v);
+        }
+        S.red[h][0][c] = mn;
+        S.red[h][1][c] = mx;
       }
-      S.red[h][0][c] = mn;
-      S.red[h][1][c] = mx;
     }
     __syncthreads();
-    for (int c = tid; c < D; c += THREADS) {
-      const float mn = fminf(S.red[0][0][c], S.red[1][0][c]), mx = fmaxf(S.red[0][1][c], S.red[1][1][c]);
+    for (int i = tid; i < (PAGE / G) * D; i += THREADS) {
+      const int gi = i / D, c = i % D;
+      if (!((gmask >> gi) & 1u)) continue;
+      float mn, mx;
+      if (G == 32) {
+        mn = S.red[gi][0][c];
+        mx = S.red[gi][1][c];
+      } else {
+        mn = fminf(S.red[0][0][c], S.red[1][0][c]);
+        mx = fmaxf(S.red[0][1][c], S.red[1][1][c]);
+      }
       const __half hmn = __float2half_rd(mn);
       const __half hrg = __float2half_ru(__fsub_ru(mx, __half2float(hmn)));
       S.kmn[gi][c] = __half2float(hmn);
@@ -365,22 +395,22 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       st[D + stat_pos(c)] = hrg;
     }
     __syncthreads();
-    for (int i = tid; i < G * D; i += THREADS) {
-      int r = i / D, c = i % D;
+    for (int i = tid; i < PAGE * D; i += THREADS) {
+      const int r = i / D, c = i % D, gi = r / G;
+      if (!((gmask >> gi) & 1u)) continue;
       const float mn = S.kmn[gi][c], rng = S.kmx[gi][c];
       int code = 0;
       if (rng != 0.f) {
-        float u = __fdiv_rn(__fsub_rn(xk[(g0 + r) * D + c], mn), rng);
+        const float u = __fdiv_rn(__fsub_rn(xk[r * D + c], mn), rng);
         code = code_of<NTHR>(u, a.kthr);
       }
-      S.kc[(g0 + r) * D + c] = (uint8_t)code;
+      S.kc[r * D + c] = (uint8_t)code;
     }
     __syncthreads();
-    for (int tile = g0 / TILE; tile < (g0 + G) / TILE; ++tile)
-      pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, PAGE, tid, THREADS);
+    for (int tile = 0; tile < PAGE / TILE; ++tile)
+      if ((gmask >> ((TILE * tile) / G)) & 1u) pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, PAGE, tid, THREADS);
     __syncthreads();
   }
-  (void)any_group;
 
   // ---- new fp16 tail (only the CTA of the last touched page) ----
   if (blockIdx.x == gridDim.x - 1) {
