@@ -132,7 +132,9 @@ def device_session_kv(w, s, torch, device):
         g = torch.Generator(device=device).manual_seed(((int(w.seed) * 1000003 + s) * 1009 + l) & 0x7FFFFFFF)
         shp = (T, sh.num_kv_heads, sh.head_dim)
         z = torch.randn(shp, device=device, generator=g)
-        drift = torch.cumsum(torch.randn(shp, device=device, generator=g) * 0.02, dim=0)
+        # the random walk along the token axis, scanned as the innermost dimension
+        steps = torch.randn((sh.num_kv_heads * sh.head_dim, T), device=device, generator=g) * 0.02
+        drift = torch.cumsum(steps, dim=1).t().reshape(shp)
         K[:, l] = (torch.from_numpy(kscale).to(device) * z + drift).half()
         z = torch.randn(shp, device=device, generator=g)
         V[:, l] = (torch.from_numpy(vscale).to(device) * z + torch.from_numpy(mu).to(device)[mod]).half()
