@@ -56,6 +56,10 @@ struct okvq_cache {
   // far-memory pseudo tokens
   float *far_partials = nullptr;                       // [units][far_nsplit][MAXGQ][FAR_PARTIAL_FLOATS]
   unsigned char *lut = nullptr;                        // decode level table (LEVEL_TABLE_BYTES)
+  __half *q_stage[2] = {}, *out_stage = nullptr;       // device staging of okvq_decode_host
+  cudaStream_t copy_stream = nullptr;                  // uploads of okvq_decode_host
+  cudaEvent_t ev_in[2] = {}, ev_used[2] = {};          // upload done / staging slot released
+  int host_calls = 0;
   int far_nsplit = 1;
   // profiling
   bool prof = false;
@@ -137,6 +141,14 @@ void release(okvq_cache *h) {
   cudaFree(h->cscratch);
   cudaFree(h->far_partials);
   cudaFree(h->lut);
+  cudaFree(h->q_stage[0]);
+  cudaFree(h->q_stage[1]);
+  cudaFree(h->out_stage);
+  for (int b = 0; b < 2; ++b) {
+    if (h->ev_in[b]) cudaEventDestroy(h->ev_in[b]);
+    if (h->ev_used[b]) cudaEventDestroy(h->ev_used[b]);
+  }
+  if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->host_table) cudaFreeHost(h->host_table);
   if (h->table_ev) cudaEventDestroy(h->table_ev);
   for (auto e : h->ev) cudaEventDestroy(e);
@@ -476,6 +488,14 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->partials, partials)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->dead_dev, (size_t)h->S * h->P_max * 8)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->lut, LEVEL_TABLE_BYTES)) != OKVQ_OK) return fail(st);
+  const size_t qo_bytes = (size_t)h->S * h->L * h->Hq * D * sizeof(__half);
+  for (int b = 0; b < 2; ++b) {
+    if ((st = alloc_dev((void **)&h->q_stage[b], qo_bytes)) != OKVQ_OK) return fail(st);
+    if (cudaEventCreateWithFlags(&h->ev_in[b], cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
+    if (cudaEventCreateWithFlags(&h->ev_used[b], cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
+  }
+  if ((st = alloc_dev((void **)&h->out_stage, qo_bytes)) != OKVQ_OK) return fail(st);
+  if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(OKVQ_ECUDA);
   // far memory: every unit's pseudo tokens split so that the far grid covers the SMs once
   h->far_nsplit = (int)std::max<long long>(1, (long long)h->num_sms / h->units);
   if ((st = alloc_dev((void **)&h->far_partials,
@@ -634,6 +654,26 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
   if (!h || !q || !out) return OKVQ_EINVAL;
   return enqueue_decode(h, q, out, static_cast<cudaStream_t>(stream), h->partials, -1, h->prof, nullptr);
+}
+
+okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, void *stream) {
+  if (!h || !q_host || !out_host) return OKVQ_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qo_bytes = (size_t)h->S * h->L * h->Hq * D * sizeof(__half);
+  // the upload runs on the handle's copy stream into one of two staging slots, so it
+  // overlaps the decode the previous call left on `stream`; the slot is reused only
+  // after the decode two calls back has read it
+  const int b = h->host_calls & 1;
+  if (h->host_calls >= 2) OKVQ_TRY(cudaStreamWaitEvent(h->copy_stream, h->ev_used[b], 0));
+  OKVQ_TRY(cudaMemcpyAsync(h->q_stage[b], q_host, qo_bytes, cudaMemcpyHostToDevice, h->copy_stream));
+  OKVQ_TRY(cudaEventRecord(h->ev_in[b], h->copy_stream));
+  OKVQ_TRY(cudaStreamWaitEvent(s, h->ev_in[b], 0));
+  okvq_status st = enqueue_decode(h, h->q_stage[b], h->out_stage, s, h->partials, -1, h->prof, nullptr);
+  if (st != OKVQ_OK) return st;
+  OKVQ_TRY(cudaEventRecord(h->ev_used[b], s));
+  OKVQ_TRY(cudaMemcpyAsync(out_host, h->out_stage, qo_bytes, cudaMemcpyDeviceToHost, s));
+  ++h->host_calls;
+  return OKVQ_OK;
 }
 
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream) {

@@ -778,14 +778,20 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
 // mma fragment order (one bulk copy per CTA, issued before the wait on the decode
 // grid); o / l is split the same way, and hi*hi + hi*lo + lo*hi carries the
 // product to ~2^-22 relative (fp32 accumulation).
-constexpr int CB_CH = 64;                       // output channels per CTA (4 m-tiles of 16)
+#ifndef OKVQ_CB_CH
+#define OKVQ_CB_CH 32
+#endif
+constexpr int CB_CH = OKVQ_CB_CH;               // output channels per CTA (32 or 64)
+constexpr int CB_MT = CB_CH / 16;               // m-tiles of 16 channels per CTA
+constexpr int CB_KS = 8 / CB_MT;                // warps sharing an m-tile, each a slice of the k-steps
+constexpr int CB_RED = (CB_KS - 1) * CB_MT * 32 * 4;   // floats of the cross-warp k-slice reduction
 constexpr int OSTRIDE = MAXM * D + 4;           // padded row of the merged o (floats)
 __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
   extern __shared__ __align__(128) unsigned char csm[];
-  uint4 *afr = reinterpret_cast<uint4 *>(csm);                                  // [4][8M][32][2] hi|lo
-  float *osh = reinterpret_cast<float *>(csm + 4 * 8 * MAXM * 32 * 32);           // [8][OSTRIDE]
-  float *red = osh + MAXGQ * OSTRIDE;                                             // [4][32][4]
-  float *ofar = red + 4 * 32 * 4;                                                  // [8][CB_CH] far memory / l
+  uint4 *afr = reinterpret_cast<uint4 *>(csm);                                  // [MT][8M][32][2] hi|lo
+  float *osh = reinterpret_cast<float *>(csm + CB_MT * 8 * MAXM * 32 * 32);       // [8][OSTRIDE]
+  float *red = osh + MAXGQ * OSTRIDE;                                             // [KS-1][MT][32][4]
+  float *ofar = red + CB_RED;                                                      // [8][CB_CH] far memory / l
   __shared__ __align__(8) uint64_t bar;
   const int unit = blockIdx.x, half = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
@@ -793,12 +799,12 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
   const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
   const int lh = unit % (a.L * a.Hkv);
   const int nks = 8 * a.M;                                // 16-row k-steps over the stacked R_m
-  const uint32_t fbytes = (uint32_t)(4 * nks * 32 * 32);
+  const uint32_t fbytes = (uint32_t)(CB_MT * nks * 32 * 32);
   if (tid == 0) {
     mbar_init(&bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
-    bulk_load(afr, a.rot_frag + ((long long)lh * 8 + 4 * half) * nks * 32 * 2, fbytes, &bar);
+    bulk_load(afr, a.rot_frag + ((long long)lh * 8 + CB_MT * half) * nks * 32 * 2, fbytes, &bar);
   }
   // everything above only reads the rotations; the partials come from the decode grid
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -825,13 +831,13 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
     for (int f = lane; f < a.far_split; f += 32) M = fmaxf(M, farp(f)[0]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float of0 = 0.f, of1 = 0.f;            // channels half * CB_CH + lane, + 32
+    float of[CB_CH / 32] = {};             // channels half * CB_CH + lane (+ 32)
     for (int f = 0; f < a.far_split; ++f) {
       const float mf = farp(f)[0];
       const float wt = mf == -INFINITY ? 0.f : ex2(mf - M);
       if (lane == 0) L = fmaf(wt, farp(f)[1], L);
-      of0 = fmaf(wt, farp(f)[2 + half * CB_CH + lane], of0);
-      of1 = fmaf(wt, farp(f)[2 + half * CB_CH + lane + 32], of1);
+#pragma unroll
+      for (int j = 0; j < CB_CH / 32; ++j) of[j] = fmaf(wt, farp(f)[2 + half * CB_CH + lane + 32 * j], of[j]);
     }
     for (int sb = s0; sb < s1; sb += 32) {
       float wt = 0.f;
@@ -861,18 +867,18 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
 #pragma unroll
     for (int k = 0; k < OPER; ++k)
       if (32 * k < nr) osh[w * OSTRIDE + lane + 32 * k] = o[k] * inv;
-    ofar[w * CB_CH + lane] = of0 * inv;
-    ofar[w * CB_CH + lane + 32] = of1 * inv;
+#pragma unroll
+    for (int j = 0; j < CB_CH / 32; ++j) ofar[w * CB_CH + lane + 32 * j] = of[j] * inv;
   } else if (w < MAXGQ) {
     for (int k = lane; k < nr; k += 32) osh[w * OSTRIDE + k] = 0.f;
-    ofar[w * CB_CH + lane] = 0.f;
-    ofar[w * CB_CH + lane + 32] = 0.f;
+#pragma unroll
+    for (int j = 0; j < CB_CH / 32; ++j) ofar[w * CB_CH + lane + 32 * j] = 0.f;
   }
   __syncthreads();
   const bool got = mbar_wait(&bar, 0);
   if (!got && tid == 0) atomicOr(a.err, ERR_WAIT);
-  // warp w: m-tile w & 3 of this CTA's 64 channels, k-steps of half w >> 2
-  const int mtl = w & 3, kh = w >> 2, k0 = kh * (nks / 2), k1 = k0 + nks / 2;
+  // warp w: m-tile w % MT of this CTA's channels, k-step slice w / MT
+  const int mtl = w % CB_MT, kh = w / CB_MT, k0 = kh * (nks / CB_KS), k1 = k0 + nks / CB_KS;
   float d[4] = {0.f, 0.f, 0.f, 0.f};
   if (got) {
     for (int ks = k0; ks < k1; ++ks) {
@@ -890,12 +896,16 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
       mma16816(d, Al, bh0, bh1);
     }
   }
-  if (kh == 1)
-    *reinterpret_cast<float4 *>(red + (mtl * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+  if (kh > 0)
+    *reinterpret_cast<float4 *>(red + (((kh - 1) * CB_MT + mtl) * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
   __syncthreads();
   if (kh == 0 && got) {
-    const float4 e = *reinterpret_cast<const float4 *>(red + (mtl * 32 + lane) * 4);
-    const float y[4] = {d[0] + e.x, d[1] + e.y, d[2] + e.z, d[3] + e.w};
+    float y[4] = {d[0], d[1], d[2], d[3]};
+#pragma unroll
+    for (int k = 1; k < CB_KS; ++k) {
+      const float4 e = *reinterpret_cast<const float4 *>(red + (((k - 1) * CB_MT + mtl) * 32 + lane) * 4);
+      y[0] += e.x; y[1] += e.y; y[2] += e.z; y[3] += e.w;
+    }
     const int session = unit / (a.L * a.Hkv);
     const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
     __half *ob = a.out + (((long long)session * a.L + layer) * a.Hq + kvh * gq) * D;
@@ -952,7 +962,7 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
   if (a.units <= 0) return cudaSuccess;
   static std::atomic<uint64_t> attr_done{0};
-  const size_t smem = (size_t)4 * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + 4 * 32 * 4 + MAXGQ * CB_CH) * sizeof(float);
+  const size_t smem = (size_t)CB_MT * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + CB_RED + MAXGQ * CB_CH) * sizeof(float);
   cudaError_t ea = once_per_device(attr_done, [&] {
     cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -25,7 +25,7 @@ EXPORTS = (
     "okvq_create", "okvq_free", "okvq_append_chunk", "okvq_decode", "okvq_length", "okvq_export_state",
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
     "okvq_decode_static_scratch", "okvq_calibrate_rotations", "okvq_live_length", "okvq_evict",
-    "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact", "okvq_decode_pseudo",
+    "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact", "okvq_decode_pseudo", "okvq_decode_host",
 )
 
 
@@ -73,6 +73,7 @@ def load() -> ctypes.CDLL:
     L.okvq_decode_static_scratch.argtypes = [vp, vp, vp, vp]
     L.okvq_calibrate_rotations.argtypes = [i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp]
     L.okvq_decode_pseudo.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
+    L.okvq_decode_host.argtypes = [vp, vp, vp, vp]
     L.okvq_live_length.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     L.okvq_evict.argtypes = [vp, i32, vp, i32, vp]
     L.okvq_compaction_granule.argtypes = [vp, ctypes.POINTER(i32)]
@@ -123,6 +124,11 @@ def okvq_append_chunk(h, session: int, k_ptr: int, v_ptr: int, mod_ptr: int, num
 
 def okvq_decode(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
     return load().okvq_decode(h, ctypes.c_void_p(q_ptr), ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream))
+
+
+def okvq_decode_host(h, q_host_ptr: int, out_host_ptr: int, stream: int = 0) -> int:
+    return load().okvq_decode_host(h, ctypes.c_void_p(q_host_ptr), ctypes.c_void_p(out_host_ptr),
+                                   ctypes.c_void_p(stream))
 
 
 def okvq_decode_static_scratch(h, q_ptr: int, out_ptr: int, stream: int = 0) -> int:
@@ -288,6 +294,18 @@ class Cache:
         st = okvq_decode(self._h, q.data_ptr(), out.data_ptr(), _stream_handle(stream))
         _check(st, "okvq_decode")
         return out
+
+    def decode_host(self, q_host, out_host, stream=None):
+        """okvq_decode_host: q_host, out_host are CPU fp16 tensors [S][L][Hq][128]
+        (pinned for asynchronous copies); the call returns before the copies finish."""
+        import torch
+        shp = (self.num_sessions, self.num_layers, self.num_q_heads, self.head_dim)
+        for name, x in (("q_host", q_host), ("out_host", out_host)):
+            if tuple(x.shape) != shp or x.dtype != torch.float16 or x.is_cuda or not x.is_contiguous():
+                raise ValueError("%s must be a contiguous CPU fp16 tensor of shape %s" % (name, shp))
+        _check(okvq_decode_host(self._h, q_host.data_ptr(), out_host.data_ptr(), _stream_handle(stream)),
+               "okvq_decode_host")
+        return out_host
 
     def decode_static_scratch(self, q, out, stream=None):
         """okvq_decode_static_scratch: as decode, with the split-K partials in the

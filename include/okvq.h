@@ -168,6 +168,19 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
  * rebuilt and uploaded on `stream`); otherwise as okvq_decode. */
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream);
 
+/* okvq_decode on HOST buffers: copies the queries (host, same layout as
+ * okvq_decode's q) into the handle's device staging, decodes, and copies the
+ * outputs back to `out_host`, all asynchronously on `stream` (the host buffers
+ * must stay valid, and `out_host` unread, until the stream reaches that point;
+ * pinned host memory makes the copies asynchronous, pageable memory makes them
+ * synchronous). The upload runs on a copy stream owned by the handle, into one
+ * of two staging slots, so it overlaps the decode a previous call left on
+ * `stream`; `stream` waits for it, so the call's effects are complete when
+ * `stream` reaches that point. Staging (3 x S*L*Hq*128 fp16), the copy stream and
+ * its events are created by okvq_create; calls on one handle must be ordered
+ * (one host thread). Errors as okvq_decode. */
+okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, void *stream);
+
 /* Decode with far-memory pseudo tokens ("ProtoKV: Streaming Video Understanding
  * under Delayed Query with Summary-State Memory", section 3.3 Eq. (2), Appendix
  * A.3 Eq. (4) and Algorithm 4): one softmax per query head over the cache (the

@@ -195,3 +195,21 @@ def test_turbo_keys_short_sessions(T):
 def test_turbo_keys_qwen3b_shape_and_multisession():
     _turbo_check(synth.qwen3b(seed=66, tokens=3000, layers=2), steps=(0, 1))
     _turbo_check(synth.multisession(seed=67, sessions=3, lo=100, hi=2000, layers=2))
+
+
+def test_decode_host_equals_decode_on_device_buffers():
+    """okvq_decode_host (pinned host queries and outputs, the uploads on the handle's
+    copy stream into alternating slots) gives okvq_decode's outputs bit for bit,
+    with four calls queued before any synchronisation."""
+    import torch
+    w = synth.multisession(seed=45, sessions=3, lo=100, hi=2500, layers=2)
+    c = pu.gpu_cache(w)
+    Qs = [w.queries(step) for step in range(4)]
+    refs = [c.decode(torch.from_numpy(Q).cuda()).cpu() for Q in Qs]
+    qh = [torch.from_numpy(Q).pin_memory() for Q in Qs]
+    oh = [torch.full(Q.shape, float("nan"), dtype=torch.float16).pin_memory() for Q in Qs]
+    for q, o in zip(qh, oh):
+        c.decode_host(q, o)
+    torch.cuda.synchronize()
+    for o, ref in zip(oh, refs):
+        assert torch.equal(o, ref)
