@@ -462,6 +462,47 @@ __global__ void lut_kernel(const LutArgs a) {
   }
 }
 
+// The rare partial half pages (a unit's last page, pages with evicted tokens) run
+// out of line, so the common path's code stays small.
+struct TailState {
+  float acc[8][4];
+  ModAcc ma;
+  float m_run, l_run;
+  uint4 qreg[8];
+  HalfPageCtx hc;
+};
+template <int BITS, int G, bool SINGLE>
+__device__ __noinline__ void half_page_partial(TailState *ts, const unsigned char *sp, int tok0, int hp, uint32_t dead,
+                                               float beta) {
+  const PageLayout PL = page_layout(BITS, G);
+  half_page<BITS, G, false, SINGLE>(ts->hc, PL, sp, tok0, hp, dead, beta, ts->acc, ts->ma, ts->m_run, ts->l_run,
+                                    ts->qreg);
+}
+template <int BITS, int G, bool SINGLE>
+__device__ __forceinline__ void call_partial(const HalfPageCtx &hc, const unsigned char *sp, int tok0, int hp,
+                                             uint32_t dead, float beta, float (&acc)[8][4], ModAcc &ma,
+                                             float &m_run, float &l_run, const uint4 (&qreg)[8]) {
+  TailState ts;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ts.acc[i][j] = acc[i][j];
+    ts.qreg[i] = qreg[i];
+  }
+  ts.ma = ma;
+  ts.m_run = m_run;
+  ts.l_run = l_run;
+  ts.hc = hc;
+  half_page_partial<BITS, G, SINGLE>(&ts, sp, tok0, hp, dead, beta);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = ts.acc[i][j];
+  ma = ts.ma;
+  m_run = ts.m_run;
+  l_run = ts.l_run;
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const DecodeArgs a) {
   constexpr int WARPS = Cfg<BITS>::WARPS;
@@ -685,12 +726,12 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
           if (full)
             half_page<BITS, G, true, true>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, true>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
+            call_partial<BITS, G, true>(hc, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
         } else {
           if (full)
             half_page<BITS, G, true, false>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
           else
-            half_page<BITS, G, false, false>(hc, PL, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
+            call_partial<BITS, G, false>(hc, sp, tok0, hp, dh, beta, acc, ma, m_run, l_run, qreg);
         }
       }
       __syncwarp();
