@@ -6,9 +6,10 @@
 // sources are gathered into scratch space before the destinations are written,
 // so that no write lands on a source another move still needs).
 //
-// move_kernel      - one CTA per (move, layer x kv head) plus one per move for the
-//                    session's modality ids: copies one granule's bytes between its
-//                    page slot and the scratch slot (gather or scatter).
+// move_kernel      - one CTA per (move, 8 layer x kv head slots; the last group
+//                    also carries the session's modality ids): copies one granule's
+//                    bytes between its page slots and the scratch slots (gather or
+//                    scatter).
 // page_meta_kernel - one CTA per (page, layer x kv head): writes the page's
 //                    deletion mask from the session's mask array and clears the
 //                    tile modality masks of tiles at or past the session length.
@@ -18,7 +19,8 @@ namespace okvq {
 
 namespace {
 
-constexpr int MOVE_THREADS = 128;
+constexpr int MOVE_THREADS = 256;
+constexpr int MOVE_UNITS = 8;          // (layer, kv head) slots per CTA
 
 // Copy `bytes` (a multiple of 16, both addresses 16-byte aligned) with 16-byte accesses.
 __device__ __forceinline__ void copy16(uint8_t *dst, const uint8_t *src, int bytes) {
@@ -26,36 +28,49 @@ __device__ __forceinline__ void copy16(uint8_t *dst, const uint8_t *src, int byt
     reinterpret_cast<uint4 *>(dst)[i] = reinterpret_cast<const uint4 *>(src)[i];
 }
 
+// One CTA per (move, group of MOVE_UNITS (layer, kv head) slots): the slots'
+// pieces form one list of 16-byte words, spread over all the CTA's threads.
 __global__ void __launch_bounds__(MOVE_THREADS) move_kernel(const MoveArgs a) {
-  const int k = blockIdx.x, lh = blockIdx.y;
+  const int k = blockIdx.x;
   const int gran = compaction_granule(a.KG), nt = gran / TILE;
   const long long gi = a.moves[2 * k + (a.scatter ? 1 : 0)];     // the page-side granule
   const long long tok = gi * gran;
-  uint8_t *slot = a.scratch + ((long long)k * (a.LH + 1) + lh) * a.stride;
-  if (lh == a.LH) {                                              // modality ids (gran is a multiple of 16)
-    uint8_t *m = a.mod + (long long)a.session * a.cap + tok;
-    if (a.scatter) copy16(m, slot, gran);
-    else copy16(slot, m, gran);
-    return;
-  }
   const PageLayout &PL = a.PL;
-  const long long unit = (long long)a.session * a.LH + lh;
-  uint8_t *pg = a.pages + (unit * a.P_max + tok / PAGE) * (long long)PL.page_bytes;
   const int tin = (int)(tok % PAGE), tb = tin / TILE;
-  // the granule's pieces inside the page, in scratch order
+  // the granule's pieces inside a page, in scratch order (lengths in 16-byte words)
   const int off[4] = {tb * PL.tile_bytes, PL.off_v + tb * PL.tile_bytes, PL.off_norm + 2 * tin,
                       PL.off_stats + (a.KG ? (tin / a.KG) * 2 * D * 2 : 2 * tin)};
-  const int len[4] = {nt * PL.tile_bytes, nt * PL.tile_bytes, 2 * gran, a.KG ? 2 * D * 2 : 2 * gran};
-  int so = 0;
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    if (a.scatter) copy16(pg + off[p], slot + so, len[p]);
-    else copy16(slot + so, pg + off[p], len[p]);
-    so += len[p];
+  const int len[4] = {nt * PL.tile_bytes / 16, nt * PL.tile_bytes / 16, 2 * gran / 16,
+                      (a.KG ? 2 * D * 2 : 2 * gran) / 16};
+  const int per = len[0] + len[1] + len[2] + len[3];
+  const int lh0 = blockIdx.y * MOVE_UNITS, lh1 = min(a.LH, lh0 + MOVE_UNITS);
+  uint8_t *scr = a.scratch + (long long)k * (a.LH + 1) * a.stride;
+  for (int idx = threadIdx.x; idx < (lh1 - lh0) * per; idx += MOVE_THREADS) {
+    const int lh = lh0 + idx / per, w = idx % per;
+    // piece of word w: cumulative bounds, no indexed arrays (they would live in local memory)
+    const int c1 = len[0], c2 = c1 + len[1], c3 = c2 + len[2];
+    const int so = w >= c3 ? c3 : w >= c2 ? c2 : w >= c1 ? c1 : 0;
+    const int po = w >= c3 ? off[3] : w >= c2 ? off[2] : w >= c1 ? off[1] : off[0];
+    const long long unit = (long long)a.session * a.LH + lh;
+    uint4 *pg = reinterpret_cast<uint4 *>(a.pages + (unit * a.P_max + tok / PAGE) * (long long)PL.page_bytes + po) +
+                (w - so);
+    uint4 *sl = reinterpret_cast<uint4 *>(scr + (long long)lh * a.stride) + w;
+    if (a.scatter) *pg = *sl;
+    else *sl = *pg;
   }
-  if (threadIdx.x < nt) {                                        // tile modality masks
-    if (a.scatter) pg[PL.off_tmask + tb + threadIdx.x] = slot[so + threadIdx.x];
-    else slot[so + threadIdx.x] = pg[PL.off_tmask + tb + threadIdx.x];
+  for (int idx = threadIdx.x; idx < (lh1 - lh0) * nt; idx += MOVE_THREADS) {   // tile modality masks
+    const int lh = lh0 + idx / nt, j = idx % nt;
+    const long long unit = (long long)a.session * a.LH + lh;
+    uint8_t *pg = a.pages + (unit * a.P_max + tok / PAGE) * (long long)PL.page_bytes + PL.off_tmask + tb + j;
+    uint8_t *sl = scr + (long long)lh * a.stride + 16 * per + j;
+    if (a.scatter) *pg = *sl;
+    else *sl = *pg;
+  }
+  if (a.LH >= lh0 && a.LH < lh0 + MOVE_UNITS) {                  // modality ids (gran is a multiple of 16)
+    uint8_t *m = a.mod + (long long)a.session * a.cap + tok;
+    uint8_t *sl = scr + (long long)a.LH * a.stride;
+    if (a.scatter) copy16(m, sl, gran);
+    else copy16(sl, m, gran);
   }
 }
 
@@ -73,7 +88,7 @@ __global__ void page_meta_kernel(const PageMetaArgs a) {
 
 cudaError_t launch_move(const MoveArgs &a, cudaStream_t s) {
   if (a.n <= 0) return cudaSuccess;
-  move_kernel<<<dim3((unsigned)a.n, (unsigned)(a.LH + 1)), MOVE_THREADS, 0, s>>>(a);
+  move_kernel<<<dim3((unsigned)a.n, (unsigned)((a.LH + 1 + MOVE_UNITS - 1) / MOVE_UNITS)), MOVE_THREADS, 0, s>>>(a);
   return cudaGetLastError();
 }
 
