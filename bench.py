@@ -62,6 +62,31 @@ def algorithmic_bytes(w, lengths, key_codec="omni"):
     return per_unit + mod + qo // 2, qo // 2, rot     # split kernel bytes, merge kernel out bytes, R bytes
 
 
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(vals, world, device):
+    """Each rank's timings -> the maximum over the ranks (the job ends with its slowest
+    replica); the identity with one rank. `device` carries the reduction (the GPU with
+    NCCL, the CPU with gloo)."""
+    if world <= 1:
+        return [float(v) for v in vals]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tokens(world, steps, lengths):
+    """Context tokens the whole job decodes: every replica decodes every session each step
+    (weak scaling: the work per GPU is fixed)."""
+    return world * steps * sum(lengths)
+
+
 def make_workload(args):
     """The named synthetic workload at the requested code width and key group size."""
     return synth.WORKLOADS[args.workload](bits=getattr(args, "bits", 2), group_size=getattr(args, "group_size", 32))
@@ -425,8 +450,7 @@ def run_cpu_baseline(args):
 
 
 def reference_arm(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if rank_env()[1] != 0:         # under a multi-rank launch, rank 0 alone times the oracle
         return
     steps = []
     base = None
@@ -494,9 +518,7 @@ def main():
 
     import torch
     import torch.distributed as dist
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
@@ -566,13 +588,8 @@ def main():
     e2e_ms = f0.elapsed_time(f1)
     clocks = sampler.stop(local) if rank == 0 else None
 
-    t_max = ms
-    e2e_max = e2e_ms
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max, e2e_max = float(t[0]), float(t[1])
-    total_tokens = world * args.steps * sum(lengths)
+    t_max, e2e_max = max_over_ranks([ms, e2e_ms], world, device)
+    total_tokens = job_tokens(world, args.steps, lengths)
     value = total_tokens / (t_max / 1e3)
     e2e_value = total_tokens / (e2e_max / 1e3)
 
