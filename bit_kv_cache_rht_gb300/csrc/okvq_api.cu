@@ -60,6 +60,8 @@ struct okvq_cache {
   cudaStream_t copy_stream = nullptr;                  // uploads of okvq_decode_host
   cudaEvent_t ev_in[2] = {}, ev_used[2] = {};          // upload done / staging slot released
   int host_calls = 0;
+  const void *dev_ok[8] = {};                          // device pointers already validated
+  int dev_ok_next = 0;
   int far_nsplit = 1;
   // profiling
   bool prof = false;
@@ -117,7 +119,18 @@ okvq_status cuda_status(cudaError_t e) {
     if (e_ != cudaSuccess) return cuda_status(e_);  \
   } while (0)
 
+// Test hook (okvq_test_fail_alloc): the n-th device allocation from now on fails
+// as if the device were out of memory; -1 = off.
+std::atomic<long long> g_fail_alloc{-1};
+
 okvq_status alloc_dev(void **p, size_t bytes) {
+  long long n = g_fail_alloc.load();
+  while (n >= 0 && !g_fail_alloc.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 0) {
+    *p = nullptr;
+    return OKVQ_ENOMEM;
+  }
   cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
   if (e != cudaSuccess) {
     *p = nullptr;
@@ -382,9 +395,33 @@ okvq_status enqueue_decode(okvq_cache *h, const void *q, void *out, cudaStream_t
   return OKVQ_OK;
 }
 
+// True for device (or managed) memory of the handle's device; the answer for the
+// last few pointers is remembered, so a decode loop on fixed buffers checks once.
+bool device_ptr(okvq_cache *h, const void *p) {
+  if (!p) return false;
+  for (const void *q : h->dev_ok)
+    if (q == p) return true;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();                          // clear the sticky-free error of the query
+    return false;
+  }
+  const bool ok = (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == h->device;
+  if (ok) {
+    h->dev_ok[h->dev_ok_next] = p;
+    h->dev_ok_next = (h->dev_ok_next + 1) % 8;
+  }
+  return ok;
+}
+
 }  // namespace
 
 extern "C" {
+
+okvq_status okvq_test_fail_alloc(int64_t n) {
+  g_fail_alloc.store(n < 0 ? -1 : n);
+  return OKVQ_OK;
+}
 
 const char *okvq_status_string(okvq_status s) {
   switch (s) {
@@ -610,7 +647,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
                               int32_t num_tokens, void *stream) {
   if (!h || session < 0 || session >= h->S || num_tokens < 0) return OKVQ_EINVAL;
   if (num_tokens == 0) return OKVQ_OK;
-  if (!k || !v || !modality) return OKVQ_EINVAL;
+  if (!device_ptr(h, k) || !device_ptr(h, v) || !device_ptr(h, modality)) return OKVQ_EINVAL;
   const long long T0 = h->len[session];
   if (T0 + num_tokens > h->max_tokens) return OKVQ_ECAPACITY;
   AppendArgs a{};
@@ -652,7 +689,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
 }
 
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
-  if (!h || !q || !out) return OKVQ_EINVAL;
+  if (!h || !device_ptr(h, q) || !device_ptr(h, out)) return OKVQ_EINVAL;
   return enqueue_decode(h, q, out, static_cast<cudaStream_t>(stream), h->partials, -1, h->prof, nullptr);
 }
 
@@ -677,7 +714,7 @@ okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, 
 }
 
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream) {
-  if (!h || !q || !out) return OKVQ_EINVAL;
+  if (!h || !device_ptr(h, q) || !device_ptr(h, out)) return OKVQ_EINVAL;
   float *scratch = nullptr;
   okvq_status st = static_partials(h->device, &scratch);
   if (st != OKVQ_OK) return st;
@@ -689,10 +726,11 @@ okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, 
 okvq_status okvq_decode_pseudo(okvq_cache *h, const void *q, const void *far_k, const void *far_v,
                                const float *far_mass, int32_t num_prototypes, int32_t tokens_per_prototype,
                                void *out, void *stream) {
-  if (!h || !q || !out || num_prototypes < 0 || tokens_per_prototype < 1) return OKVQ_EINVAL;
+  if (!h || !device_ptr(h, q) || !device_ptr(h, out) || num_prototypes < 0 || tokens_per_prototype < 1)
+    return OKVQ_EINVAL;
   const long long n_far = (long long)num_prototypes * tokens_per_prototype;
   if (n_far > (1ll << 30)) return OKVQ_EINVAL;
-  if (n_far > 0 && (!far_k || !far_v || !far_mass)) return OKVQ_EINVAL;
+  if (n_far > 0 && (!device_ptr(h, far_k) || !device_ptr(h, far_v) || !device_ptr(h, far_mass))) return OKVQ_EINVAL;
   if ((reinterpret_cast<uintptr_t>(far_k) | reinterpret_cast<uintptr_t>(far_v)) & 15u) return OKVQ_EINVAL;
   FarArgs f{};
   f.q = static_cast<const __half *>(q);

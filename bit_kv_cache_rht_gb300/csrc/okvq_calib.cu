@@ -248,7 +248,11 @@ extern "C" okvq_status okvq_calibrate_rotations(int32_t num_layers, int32_t num_
                                                  int32_t *sweeps_out, void *stream) {
   if (num_layers < 1 || num_kv_heads < 1 || num_modalities < 1 || num_modalities > MAXM || num_tokens < 0)
     return OKVQ_EINVAL;
-  if (!rot_out || (num_tokens > 0 && (!v || !modality))) return OKVQ_EINVAL;
+  if (!is_device_memory(rot_out) || (eig_out && !is_device_memory(eig_out)) ||
+      (sweeps_out && !is_device_memory(sweeps_out)))
+    return OKVQ_EINVAL;
+  if (num_tokens > 0 && (!is_device_memory(v) || !is_device_memory(modality) || (weight && !is_device_memory(weight))))
+    return OKVQ_EINVAL;
   CalibArgs a;
   a.v = static_cast<const __half *>(v);
   a.mod = modality;

@@ -255,6 +255,17 @@ struct PageMetaArgs {
   PageLayout PL;
 };
 
+// True for device or managed memory (a host query, no caching).
+inline bool is_device_memory(const void *p) {
+  if (!p) return false;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
 // Kernel attributes belong to a device: run `set` once per device ordinal (the
 // current device; ordinals >= 64 run it on every call). `done` holds one bit per
 // device.

@@ -26,6 +26,7 @@ EXPORTS = (
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
     "okvq_decode_static_scratch", "okvq_calibrate_rotations", "okvq_live_length", "okvq_evict",
     "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact", "okvq_decode_pseudo", "okvq_decode_host",
+    "okvq_test_fail_alloc",
 )
 
 
@@ -74,6 +75,7 @@ def load() -> ctypes.CDLL:
     L.okvq_calibrate_rotations.argtypes = [i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp]
     L.okvq_decode_pseudo.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
     L.okvq_decode_host.argtypes = [vp, vp, vp, vp]
+    L.okvq_test_fail_alloc.argtypes = [ctypes.c_int64]
     L.okvq_live_length.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     L.okvq_evict.argtypes = [vp, i32, vp, i32, vp]
     L.okvq_compaction_granule.argtypes = [vp, ctypes.POINTER(i32)]
@@ -214,6 +216,10 @@ def okvq_compact(h, session: int, min_pages_saved: int, stream: int = 0):
     nl, nm = ctypes.c_int64(), ctypes.c_int32()
     st = load().okvq_compact(h, session, min_pages_saved, ctypes.byref(nl), ctypes.byref(nm), ctypes.c_void_p(stream))
     return st, nl.value, nm.value
+
+
+def okvq_test_fail_alloc(n: int) -> int:
+    return load().okvq_test_fail_alloc(n)
 
 
 def okvq_status_string(s: int) -> str:

@@ -205,6 +205,12 @@ okvq_status okvq_decode_pseudo(okvq_cache *h, const void *q, const void *far_k, 
                                const float *far_mass, int32_t num_prototypes, int32_t tokens_per_prototype,
                                void *out, void *stream);
 
+/* Device pointers passed to okvq_append_chunk, okvq_decode, okvq_decode_static_scratch,
+ * okvq_decode_pseudo and okvq_calibrate_rotations are checked with
+ * cudaPointerGetAttributes: host memory (pageable or pinned) or another device's
+ * memory gives OKVQ_EINVAL with nothing launched. A handle remembers the last 8
+ * pointers it accepted, so a loop over fixed buffers pays the query once. */
+
 /* Number of token slots of `session`: its physical span, holes included (the
  * next append lands at this index). */
 okvq_status okvq_length(const okvq_cache *h, int32_t session, int64_t *tokens);
@@ -320,6 +326,12 @@ okvq_status okvq_calibrate_rotations(int32_t num_layers, int32_t num_kv_heads, i
                                      const void *v, const uint8_t *modality, const float *weight,
                                      int32_t num_tokens, float *rot_out, float *eig_out, int32_t *sweeps_out,
                                      void *stream);
+
+/* Test hook: the n-th device allocation of the library from now on (n = 0: the
+ * next one) fails as if the device were out of memory, so that the error paths of
+ * okvq_create can be exercised without exhausting a GPU; n < 0 turns it off.
+ * Process-wide; not for production use. */
+okvq_status okvq_test_fail_alloc(int64_t n);
 
 /* Static description of a status code. */
 const char *okvq_status_string(okvq_status s);

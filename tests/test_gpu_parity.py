@@ -213,3 +213,62 @@ def test_decode_host_equals_decode_on_device_buffers():
     torch.cuda.synchronize()
     for o, ref in zip(oh, refs):
         assert torch.equal(o, ref)
+
+
+def test_host_and_foreign_pointers_are_rejected_before_any_launch():
+    """Pageable and pinned host memory passed where device memory is expected:
+    OKVQ_EINVAL, nothing launched, the cache unchanged."""
+    import torch
+    from bit_kv_cache_rht_gb300 import okvq
+    w = synth.tiny(seed=51, tokens=64)
+    c = pu.gpu_cache(w)
+    before = c.export_state(0)
+    K = torch.zeros((8, 1, 2, 128), dtype=torch.float16)
+    Kp = K.pin_memory()
+    M = torch.zeros(8, dtype=torch.uint8)
+    Kd = K.cuda()
+    Md = M.cuda()
+    E = okvq.OKVQ_EINVAL
+    assert okvq.okvq_append_chunk(c._h, 0, K.data_ptr(), Kd.data_ptr(), Md.data_ptr(), 8) == E
+    assert okvq.okvq_append_chunk(c._h, 0, Kd.data_ptr(), Kp.data_ptr(), Md.data_ptr(), 8) == E
+    assert okvq.okvq_append_chunk(c._h, 0, Kd.data_ptr(), Kd.data_ptr(), M.data_ptr(), 8) == E
+    q = torch.from_numpy(w.queries(0))
+    qd, od = q.cuda(), torch.empty_like(q).cuda()
+    assert okvq.okvq_decode(c._h, q.data_ptr(), od.data_ptr()) == E
+    assert okvq.okvq_decode(c._h, qd.data_ptr(), q.pin_memory().data_ptr()) == E
+    torch.cuda.synchronize()
+    assert c.length(0) == 64 and c.check_errors() == 0
+    after = c.export_state(0)
+    for k in before:
+        assert np.array_equal(before[k].view(np.uint8), after[k].view(np.uint8)), k
+    assert okvq.okvq_decode(c._h, qd.data_ptr(), od.data_ptr()) == okvq.OKVQ_OK
+
+
+def test_injected_allocation_failures_give_enomem_without_leaks():
+    """okvq_test_fail_alloc(k) makes the k-th device allocation of okvq_create fail:
+    the call returns OKVQ_ENOMEM, frees what it had allocated and leaves no handle;
+    past the last allocation the create succeeds."""
+    import torch
+    from bit_kv_cache_rht_gb300 import okvq
+    w = synth.tiny(seed=52, tokens=64)
+    R = pu.rotations(w)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    failures = 0
+    try:
+        for k in range(40):
+            okvq.okvq_test_fail_alloc(k)
+            try:
+                c = okvq.Cache(1, 1, 8, 2, 4096, R, group_size=32, bits=2)
+            except okvq.OkvqError as e:
+                assert e.status == okvq.OKVQ_ENOMEM
+                failures += 1
+                continue
+            okvq.okvq_test_fail_alloc(-1)
+            c.close()
+            break
+    finally:
+        okvq.okvq_test_fail_alloc(-1)
+    assert 10 <= failures < 40                   # every allocation of create was made to fail once
+    torch.cuda.synchronize()
+    assert abs(torch.cuda.mem_get_info()[0] - free0) < (64 << 20)
