@@ -622,7 +622,7 @@ class OracleCache:
 
     def __init__(self, num_sessions, num_layers, num_q_heads, num_kv_heads, head_dim, group_size, bits,
                  max_tokens, hadamard_seed, value_rot, codebook_levels=None, layers=None, num_modalities=3,
-                 key_codec="omni"):
+                 key_codec="omni", sessions=None):
         self.S, self.L, self.Hq, self.Hkv, self.d = num_sessions, num_layers, num_q_heads, num_kv_heads, head_dim
         self.G, self.bits, self.M = group_size, bits, num_modalities
         self.cb = make_codebook(bits, codebook_levels)
@@ -630,7 +630,8 @@ class OracleCache:
         self.layers = list(range(num_layers)) if layers is None else list(layers)
         R = np.asarray(value_rot, F32)
         self.units = {}
-        for s in range(num_sessions):
+        self.sessions = list(range(num_sessions)) if sessions is None else list(sessions)   # the ones modelled
+        for s in self.sessions:
             for l in self.layers:
                 for h in range(num_kv_heads):
                     self.units[(s, l, h)] = OracleUnit(head_dim, group_size, self.cb, self.signs, R[l, h],
@@ -666,7 +667,7 @@ class OracleCache:
         -> fp64 [S][L'][Hq][d] for the oracle's layers."""
         gq = self.Hq // self.Hkv
         out = np.zeros((self.S, len(self.layers), self.Hq, self.d), F64)
-        for s in range(self.S):
+        for s in self.sessions:
             for i, l in enumerate(self.layers):
                 for h in range(self.Hkv):
                     u = self.units[(s, l, h)]
@@ -678,7 +679,7 @@ class OracleCache:
         """Q16 [S][L][Hq][d] -> fp64 [S][L'][Hq][d] for the oracle's layers."""
         gq = self.Hq // self.Hkv
         out = np.zeros((self.S, len(self.layers), self.Hq, self.d), F64)
-        for s in range(self.S):
+        for s in self.sessions:
             for i, l in enumerate(self.layers):
                 for h in range(self.Hkv):
                     u = self.units[(s, l, h)]

@@ -37,7 +37,7 @@ def oracle_cache(w, layers=None, sessions=None, key_codec="omni", R=None):
     R = rotations(w) if R is None else R
     return o.OracleCache(len(w.sessions), sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
                          sh.group_size, sh.bits, w.max_tokens, w.hadamard_seed, R, layers=layers,
-                         key_codec=key_codec), R
+                         key_codec=key_codec, sessions=sessions), R
 
 
 def feed_oracle(oc, w, bounds=None, layers=None, sessions=None):

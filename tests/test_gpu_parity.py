@@ -83,6 +83,38 @@ def test_bench_workload_full_size_sampled_layers():
     _full_check(w, layers_check=[0, w.shape.num_layers - 1], steps=(0,))
 
 
+def test_qwen7b_full_size_sampled_layer():
+    """The 7B-shaped long stream at full size (28 layers, 28 q / 4 kv heads, 81,920
+    tokens in 1-s chunks) through the same cache build and decode launch the
+    benchmark times; the oracle recomputes the first layer (all 4 kv heads, all 28
+    query heads) and its stored state."""
+    w = synth.qwen7b()
+    _full_check(w, layers_check=[0], steps=(0,))
+
+
+def test_multisession_full_length_mix_sampled_sessions():
+    """64 sessions with the full 4 K-64 K length mix and per-session interleaves (2
+    layers): the multi-session work partition of the decode; the oracle recomputes
+    the shortest and the longest session and one in between."""
+    import torch
+    w = synth.multisession(layers=2)
+    lens = [x.length for x in w.sessions]
+    pick = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17})
+    oc, R = pu.oracle_cache(w, sessions=pick)
+    pu.feed_oracle(oc, w, sessions=pick)
+    c = pu.gpu_cache(w, R=R)
+    assert c.check_errors() == 0
+    for s in pick:
+        st = c.export_state(s)
+        pu.assert_state_matches(pu.compare_state(st, oc, s, oc.layers, w.shape.bits))
+        pu.adopt_boundary_choices(st, oc, s, oc.layers)
+    Q = w.queries(0)
+    out = c.decode(torch.from_numpy(Q).cuda()).cpu().numpy()
+    ref = oc.decode(Q)
+    pu.assert_outputs_close(out[pick], ref[pick], "sampled sessions")
+    assert c.check_errors() == 0
+
+
 def test_qwen7b_shape_seven_heads_per_kv():
     w = synth.qwen7b(seed=41, tokens=3000, layers=2)
     _full_check(w, steps=(0,))
