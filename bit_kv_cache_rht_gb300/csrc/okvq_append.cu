@@ -202,25 +202,37 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int i = tid; i < PAGE * ROW_H / 2; i += THREADS) reinterpret_cast<uint32_t *>(&S.u.v.vh[0][0])[i] = 0u;
+  // the new tokens' values: 8 tokens per warp, all loads issued first (lane: channels
+  // 4 lane .. 4 lane + 3). Rows of other tokens are left as they are: a row only
+  // feeds its own outputs, which are discarded.
+  constexpr int VPW = PAGE / (THREADS / 32);
+  uint2 vraw[VPW];
+#pragma unroll
+  for (int j = 0; j < VPW; ++j) {
+    const int t = warp + j * (THREADS / 32);
+    vraw[j] = make_uint2(0u, 0u);
+    if (t >= ta && t < tb)
+      vraw[j] = *reinterpret_cast<const uint2 *>(a.v + (P0 + t - T0) * (long long)row_stride + (long long)lh * D +
+                                                 4 * lane);
+  }
   // keep codes of older tokens that share a 16-token tile with the first new token
   if (ta % TILE != 0) unpack_tile<BITS, 1>(S.vc, pg + PL.off_v + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid,
                                            THREADS);
   __syncthreads();
-  for (int t = ta + warp; t < tb; t += THREADS / 32) {
-    const __half *src = a.v + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
-    float ss = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      int c = lane + 32 * k;
-      const __half hv = src[c];
-      S.u.v.vh[t][c] = hv;
-      const float x = __half2float(hv);
-      ss = fmaf(x, x, ss);
-    }
+  for (int j = 0; j < VPW; ++j) {
+    const int t = warp + j * (THREADS / 32);
+    if (t < ta || t >= tb) continue;               // warp-uniform
+    *reinterpret_cast<uint2 *>(&S.u.v.vh[t][4 * lane]) = vraw[j];
+    const float2 x01 = __half22float2(*reinterpret_cast<const __half2 *>(&vraw[j].x));
+    const float2 x23 = __half22float2(*reinterpret_cast<const __half2 *>(&vraw[j].y));
+    float ss = x01.x * x01.x;
+    ss = fmaf(x01.y, x01.y, ss);
+    ss = fmaf(x23.x, x23.x, ss);
+    ss = fmaf(x23.y, x23.y, ss);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    float n = sqrtf(ss);
+    const float n = sqrtf(ss);
     if (lane == 0) {
       S.vnorm[t] = n;
       reinterpret_cast<__half *>(pg + PL.off_norm)[t] = __float2half_rn(n);
@@ -395,16 +407,18 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       st[D + stat_pos(c)] = hrg;
     }
     __syncthreads();
-    for (int i = tid; i < PAGE * D; i += THREADS) {
-      const int r = i / D, c = i % D, gi = r / G;
-      if (!((gmask >> gi) & 1u)) continue;
-      const float mn = S.kmn[gi][c], rng = S.kmx[gi][c];
-      int code = 0;
-      if (rng != 0.f) {
-        const float u = __fdiv_rn(__fsub_rn(xk[r * D + c], mn), rng);
-        code = code_of<NTHR>(u, a.kthr);
+    {
+      // thread (c, h): channel c of rows 32h .. 32h + 31, one group's statistics
+      const int c = tid & (D - 1), h = tid / D, gi = (32 * h) / G;
+      if ((gmask >> gi) & 1u) {
+        const float mn = S.kmn[gi][c], rng = S.kmx[gi][c];
+#pragma unroll 4
+        for (int r = 32 * h; r < 32 * h + 32; ++r) {
+          int code = 0;
+          if (rng != 0.f) code = code_of<NTHR>(__fdiv_rn(__fsub_rn(xk[r * D + c], mn), rng), a.kthr);
+          S.kc[r * D + c] = (uint8_t)code;
+        }
       }
-      S.kc[r * D + c] = (uint8_t)code;
     }
     __syncthreads();
     for (int tile = 0; tile < PAGE / TILE; ++tile)
