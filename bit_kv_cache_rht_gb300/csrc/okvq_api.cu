@@ -195,19 +195,84 @@ okvq_status static_partials(int device, float **out) {
   return OKVQ_OK;
 }
 
-// Build the decode work partition: balanced page ranges over the flattened
-// (unit, page) list, cut at unit boundaries into segments.
+// Decode work partition. The flattened (unit, page) list is cut into at most
+// max_cta contiguous ranges, one per CTA, and each range into segments at unit
+// boundaries. Cost model: a page costs 1, a segment seg_cost more (its query
+// rotation, the page ring it starts empty and the cross-warp merge that ends
+// it). The smallest per-CTA budget with which a greedy walk covers every page
+// is found by bisection (greedy is exact for contiguous splits of an additive
+// cost); a segment always holds at least one page. Returns the CTAs used (>= 1
+// when there are pages); segs [nseg][4] = unit, first page, end page, 0.
+struct SplitPlan {
+  int ncta = 0, nseg = 0;
+};
+SplitPlan plan_split(const long long *pages_u, long long U, int max_cta, int seg_cost, int *segs, int *cta_seg) {
+  long long P = 0;
+  for (long long u = 0; u < U; ++u) P += pages_u[u];
+  SplitPlan r;
+  if (P == 0 || max_cta < 1) {
+    cta_seg[0] = 0;
+    return r;
+  }
+  const long long sc = std::max(seg_cost, 0);
+  // CTAs a budget B needs (emit: also write the segments)
+  auto walk = [&](long long B, bool emit) -> long long {
+    long long u = 0, p = 0, c = 0;
+    int ns = 0;
+    while (u < U && pages_u[u] == 0) ++u;
+    while (u < U) {
+      if (emit) cta_seg[c] = ns;
+      long long rem = B;
+      while (u < U && rem > sc) {
+        const long long take = std::min(pages_u[u] - p, rem - sc);
+        if (emit) {
+          segs[4 * ns + 0] = (int)u;
+          segs[4 * ns + 1] = (int)p;
+          segs[4 * ns + 2] = (int)(p + take);
+          segs[4 * ns + 3] = 0;
+        }
+        ++ns;
+        rem -= sc + take;
+        p += take;
+        if (p < pages_u[u]) break;
+        p = 0;
+        ++u;
+        while (u < U && pages_u[u] == 0) ++u;
+      }
+      ++c;
+      if (!emit && c > max_cta) return c;
+    }
+    if (emit) {
+      cta_seg[c] = ns;
+      r.nseg = ns;
+    }
+    return c;
+  };
+  long long lo = std::max<long long>(sc + 1, (P + max_cta - 1) / max_cta);
+  long long hi = P + sc * (U + max_cta) + 1;    // one CTA takes everything
+  while (lo < hi) {
+    const long long mid = lo + (hi - lo) / 2;
+    if (walk(mid, false) <= max_cta) hi = mid;
+    else lo = mid + 1;
+  }
+  r.ncta = (int)walk(lo, true);
+  return r;
+}
+
+#ifndef OKVQ_SEG_COST
+#define OKVQ_SEG_COST 48
+#endif
+constexpr int SEG_COST_PAGES = OKVQ_SEG_COST;
+
+// Build the decode work table from the session lengths.
 void build_table(okvq_cache *h) {
   const long long U = h->units;
   std::vector<long long> pages_u(U);
-  long long P = 0;
   const int LH = h->L * h->Hkv;
   for (long long u = 0; u < U; ++u) {
     long long T = h->len[u / LH];
     pages_u[u] = (T + PAGE - 1) / PAGE;
-    P += pages_u[u];
   }
-  int ncta = (int)std::min<long long>(P, h->max_cta);
   char *base = static_cast<char *>(h->host_table);
   int *segs = reinterpret_cast<int *>(base + h->off_segs);
   int *cta_seg = reinterpret_cast<int *>(base + h->off_cta);
@@ -218,27 +283,8 @@ void build_table(okvq_cache *h) {
     ulen[u] = h->len[u / LH];
     utail[u] = h->tail_sel[u / LH];
   }
-  int nseg = 0;
-  long long u = 0, ustart = 0;   // ustart = flattened index of unit u's first page
-  for (int c = 0; c < ncta; ++c) {
-    long long a = (long long)c * P / ncta, b = (long long)(c + 1) * P / ncta;
-    cta_seg[c] = nseg;
-    long long x = a;
-    while (x < b) {
-      while (u < U && ustart + pages_u[u] <= x) {
-        ustart += pages_u[u];
-        ++u;
-      }
-      long long pb = x - ustart;
-      long long pe = std::min(b - ustart, pages_u[u]);
-      segs[4 * nseg + 0] = (int)u;
-      segs[4 * nseg + 1] = (int)pb;
-      segs[4 * nseg + 2] = (int)pe;
-      segs[4 * nseg + 3] = 0;
-      ++nseg;
-      x = ustart + pe;
-    }
-  }
+  const SplitPlan sp = plan_split(pages_u.data(), U, h->max_cta, SEG_COST_PAGES, segs, cta_seg);
+  const int ncta = sp.ncta, nseg = sp.nseg;
   cta_seg[ncta] = nseg;
   // unit -> first segment (segments are ordered by unit)
   int s = 0;
@@ -839,6 +885,27 @@ okvq_status okvq_plan_compaction(const uint8_t *dead, int64_t length, int32_t gr
   *suffix_begin = p.sg < 0 ? -1 : p.sg * granule;
   *new_length = p.sg < 0 ? length : p.T2;
   *num_moves = (int32_t)(p.moves.size() / 2);
+  return OKVQ_OK;
+}
+
+okvq_status okvq_plan_decode(const int64_t *unit_pages, int64_t units, int32_t max_ctas, int32_t segment_cost,
+                             int32_t *segments, int32_t *cta_first, int32_t *num_ctas, int32_t *num_segments) {
+  if (units < 0 || (units > 0 && !unit_pages) || max_ctas < 1 || segment_cost < 0 || !segments || !cta_first ||
+      !num_ctas || !num_segments)
+    return OKVQ_EINVAL;
+  if (units > INT32_MAX) return OKVQ_EINVAL;
+  std::vector<long long> pages(units);
+  for (long long u = 0; u < units; ++u) {
+    if (unit_pages[u] < 0 || unit_pages[u] > INT32_MAX) return OKVQ_EINVAL;
+    pages[u] = unit_pages[u];
+  }
+  std::vector<int> segs(4 * (size_t)(units + max_ctas) + 4);
+  const SplitPlan sp = plan_split(pages.data(), units, max_ctas, segment_cost, segs.data(), cta_first);
+  cta_first[sp.ncta] = sp.nseg;
+  for (int i = 0; i < sp.nseg; ++i)
+    for (int j = 0; j < 3; ++j) segments[3 * i + j] = segs[4 * i + j];
+  *num_ctas = sp.ncta;
+  *num_segments = sp.nseg;
   return OKVQ_OK;
 }
 

@@ -26,7 +26,7 @@ EXPORTS = (
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
     "okvq_decode_static_scratch", "okvq_calibrate_rotations", "okvq_live_length", "okvq_evict",
     "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact", "okvq_decode_pseudo", "okvq_decode_host",
-    "okvq_test_fail_alloc",
+    "okvq_test_fail_alloc", "okvq_plan_decode",
 )
 
 
@@ -82,6 +82,7 @@ def load() -> ctypes.CDLL:
     L.okvq_plan_compaction.argtypes = [vp, ctypes.c_int64, i32, i32, ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(i32)]
     L.okvq_compact.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(i32), vp]
+    L.okvq_plan_decode.argtypes = [vp, ctypes.c_int64, i32, i32, vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.okvq_length.argtypes = [vp, i32, ctypes.POINTER(i64)]
     L.okvq_export_state.argtypes = [vp, i32, vp, ctypes.POINTER(ctypes.c_size_t)]
     L.okvq_codebook.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
@@ -209,6 +210,20 @@ def okvq_plan_compaction(dead, length: int, granule: int, min_pages_saved: int):
     st = load().okvq_plan_compaction(d.ctypes.data_as(ctypes.c_void_p) if length > 0 else None, length, granule,
                                      min_pages_saved, ctypes.byref(sb), ctypes.byref(nl), ctypes.byref(nm))
     return st, sb.value, nl.value, nm.value
+
+
+def okvq_plan_decode(unit_pages, max_ctas: int, segment_cost: int):
+    """Host split of the decode work. Returns (status, segments [n][3] = (unit, first page,
+    end page), cta_first [ctas + 1])."""
+    p = np.ascontiguousarray(np.asarray(unit_pages, np.int64))
+    units = p.shape[0]
+    seg = np.zeros((units + max(max_ctas, 1), 3), np.int32)
+    first = np.zeros(max(max_ctas, 1) + 1, np.int32)
+    nc, ns = ctypes.c_int32(), ctypes.c_int32()
+    st = load().okvq_plan_decode(p.ctypes.data_as(ctypes.c_void_p) if units else None, units, max_ctas, segment_cost,
+                                 seg.ctypes.data_as(ctypes.c_void_p), first.ctypes.data_as(ctypes.c_void_p),
+                                 ctypes.byref(nc), ctypes.byref(ns))
+    return st, seg[:ns.value].copy(), first[:nc.value + 1].copy()
 
 
 def okvq_compact(h, session: int, min_pages_saved: int, stream: int = 0):

@@ -252,6 +252,23 @@ okvq_status okvq_compaction_granule(const okvq_cache *h, int32_t *tokens);
 okvq_status okvq_plan_compaction(const uint8_t *dead, int64_t length, int32_t granule, int32_t min_pages_saved,
                                  int64_t *suffix_begin, int64_t *new_length, int32_t *num_moves);
 
+/* The decode's split of the work over CTAs, on the host (no handle, no GPU):
+ * the pages of units 0..units-1 (unit_pages[u] >= 0 each, HOST array), in
+ * order, are cut into at most max_ctas contiguous ranges, one per CTA, and each
+ * range into segments at unit boundaries (one split-K partial each). A page
+ * costs 1 and a segment segment_cost more; the split minimises the largest
+ * CTA cost (the smallest budget with which a greedy walk covers every page,
+ * found by bisection), and no segment is empty. okvq_decode plans with
+ * segment_cost 48 (a segment's query rotation, its empty page ring at the
+ * start and its cross-warp merge at the end cost about that many pages).
+ * Outputs: segments [*num_segments][3] = unit, first page, end page (caller
+ * room for units + max_ctas segments); cta_first [*num_ctas + 1] = first
+ * segment of each CTA, then *num_segments (caller room for max_ctas + 1).
+ * No pages: *num_ctas = *num_segments = 0. OKVQ_EINVAL for NULL pointers,
+ * units < 0, max_ctas < 1, segment_cost < 0 or a count outside [0, 2^31). */
+okvq_status okvq_plan_decode(const int64_t *unit_pages, int64_t units, int32_t max_ctas, int32_t segment_cost,
+                             int32_t *segments, int32_t *cta_first, int32_t *num_ctas, int32_t *num_segments);
+
 /* Plan (as okvq_plan_compaction, with the handle's granule and its deletions)
  * and apply the ordered-suffix compaction of `session`: the moved granules'
  * codes, statistics, norms, modality ids, masks and deletion bits are gathered
