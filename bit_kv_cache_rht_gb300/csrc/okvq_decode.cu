@@ -518,7 +518,8 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   unsigned char *lut = smem;                                            // LUT_BYTES
   float *qr = reinterpret_cast<float *>(smem + LUT_BYTES);              // [8][128] stat order, scaled
   __half *qraw = reinterpret_cast<__half *>(qr + MAXGQ * D);            // [8][128] natural order
-  uint4 *qfrag = reinterpret_cast<uint4 *>(qraw + MAXGQ * D);           // [8 kb][32 lanes]
+  __half *qstage = qraw + MAXGQ * D;                                    // [8][128] next segment's queries
+  uint4 *qfrag = reinterpret_cast<uint4 *>(qstage + MAXGQ * D);         // [8 kb][32 lanes]
   uint64_t *bars = reinterpret_cast<uint64_t *>(qfrag + 8 * 32);        // [WARPS][STAGES]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + WARPS * STAGES);
   // 128-byte aligned stage ring, as an offset from the (aligned) shared base: a round
@@ -532,9 +533,42 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   // the level table (built once per cache) arrives by one bulk copy; it is first
   // needed after the first segment's query rotation
   __shared__ __align__(8) uint64_t lut_bar;
+  // the next segment's descriptor and queries (bulk copy) are staged while the
+  // current one runs, so a segment starts without global latency
+  __shared__ __align__(8) uint64_t q_bar;
+  __shared__ int sd_unit, sd_pb, sd_pe, sd_tail;
+  __shared__ long long sd_T;
+  const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
+  const int gq = a.Hq / a.Hkv;
+  struct SegDesc {
+    int unit, pb, pe, tail;
+    long long T;
+  };
+  auto load_desc = [&](int sg) {
+    SegDesc d;
+    d.unit = a.segs[4 * sg + 0];
+    d.pb = a.segs[4 * sg + 1];
+    d.pe = a.segs[4 * sg + 2];
+    d.T = a.unit_len[d.unit];
+    d.tail = a.unit_tail[d.unit];
+    return d;
+  };
+  auto stage_segment = [&](const SegDesc &d) {  // one thread
+    sd_unit = d.unit;
+    sd_pb = d.pb;
+    sd_pe = d.pe;
+    sd_T = d.T;
+    sd_tail = d.tail;
+    const int ss = d.unit / (a.L * a.Hkv), lh = d.unit % (a.L * a.Hkv);
+    const __half *qsrc = a.q + (((long long)ss * a.L + lh / a.Hkv) * a.Hq + (long long)(lh % a.Hkv) * gq) * D;
+    fence_async_smem();
+    bulk_load(qstage, qsrc, (uint32_t)(gq * D * sizeof(__half)), &q_bar);
+  };
   if (tid == 0) {
     mbar_init(&lut_bar, 1);
+    mbar_init(&q_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (seg_begin < seg_end) stage_segment(load_desc(seg_begin));
     bulk_load(lut, a.lut, LUT_BYTES, &lut_bar);
   }
   if (lane == 0)
@@ -566,25 +600,28 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     luthi |= (hv >> 8) << (8 * j);
   }
 
-  const int gq = a.Hq / a.Hkv;
   int ring_st = 0;          // stage of the next page this warp consumes
   uint32_t ring_par = 0;    // its mbarrier phase parity
   bool wait_failed = false;
   bool lut_ready = false;
 
-  const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
-  for (int seg = seg_begin; seg < seg_end; ++seg) {
-    const int unit = a.segs[4 * seg + 0];
-    const int pb = a.segs[4 * seg + 1], pe = a.segs[4 * seg + 2];
+  int seg = seg_begin;
+  for (; seg < seg_end; ++seg) {
+    const int unit = sd_unit;
+    const int pb = sd_pb, pe = sd_pe;
     const int session = unit / (a.L * a.Hkv);
-    const int lh = unit % (a.L * a.Hkv);
-    const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-    const int T = (int)a.unit_len[unit];
+    const int T = (int)sd_T;
+    const int tail_sel = sd_tail;
+    // the next segment's descriptor: loaded now by a thread whose warp has no head
+    // to rotate (at 2-bit), staged with its queries once the rotation is done
+    const bool stager = tid == THREADS - 32 && seg + 1 < seg_end;
+    SegDesc next{};
+    if (stager) next = load_desc(seg + 1);
     constexpr bool KT = G == 0;               // TurboQuant keys: all quantized, no groups
     constexpr int GG = KT ? PAGE : G;
     const int Tf = KT ? T : (T / GG) * GG;
     const unsigned char *unit_pages = a.pages + (long long)unit * a.P_max * PL.page_bytes;
-    const __half *tail = a.tails + ((long long)a.unit_tail[unit] * a.units + unit) * (long long)G * D;
+    const __half *tail = a.tails + ((long long)tail_sel * a.units + unit) * (long long)G * D;
     // the segment's first pages are on their way while the query is rotated (the
     // ring is free: the previous segment's merge ended with a barrier)
     const int npages = pe - pb;
@@ -599,14 +636,14 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     }
 
     // ---- rotate the query group once: q' = H (s o q) / d, in log2 units (warp = head) ----
+    if (!mbar_wait(&q_bar, (uint32_t)(seg - seg_begin) & 1u)) wait_failed = true;
     if (warp < MAXGQ) {
-      const __half *qsrc = a.q + (((long long)session * a.L + layer) * a.Hq + (long long)kvh * gq) * D;
       const int hh = warp;
       float x[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = 4 * lane + j;
-        const __half hv = hh < gq ? qsrc[hh * D + c] : __float2half(0.f);
+        const __half hv = hh < gq ? qstage[hh * D + c] : __float2half(0.f);
         qraw[hh * D + c] = hv;
         x[j] = __half2float(hv) * a.signs[c];
       }
@@ -640,6 +677,8 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
                                          pack_h2(v.z - f23.x, v.w - f23.y));
     }
     __syncthreads();
+    // the descriptor and queries of this CTA's next segment, staged while this one runs
+    if (stager) stage_segment(next);
 
     HalfPageCtx hc;
     hc.lut_k = lut_k;
@@ -803,8 +842,12 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     }
     __syncthreads();              // merge area is the stage ring of the next segment
   }
-  // the level table's copy must have landed before the CTA's shared memory goes away
+  // the level table's and a staged query copy must land before the CTA's shared
+  // memory goes away (one is left unconsumed when the loop ended early)
   if (!lut_ready && tid == 0 && !mbar_wait(&lut_bar, 0u)) atomicOr(a.err, ERR_WAIT);
+  if (seg < seg_end && tid == 0)
+    for (int s2 = seg; s2 < min(seg + 2, seg_end); ++s2)
+      if (!mbar_wait(&q_bar, (uint32_t)(s2 - seg_begin) & 1u)) atomicOr(a.err, ERR_WAIT);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -977,7 +1020,7 @@ template <int BITS>
 size_t decode_smem_bytes_t(int G) {
   const PageLayout PL = page_layout(BITS, G);
   constexpr int W = Cfg<BITS>::WARPS, STAGES = Cfg<BITS>::STAGES;
-  size_t head = LUT_BYTES + MAXGQ * D * 4 + MAXGQ * D * 2 + 8 * 32 * 16 + W * STAGES * 8 + 16;
+  size_t head = LUT_BYTES + MAXGQ * D * 4 + 2 * MAXGQ * D * 2 + 8 * 32 * 16 + W * STAGES * 8 + 16;
   size_t ring = (size_t)W * STAGES * PL.page_bytes;
   if (ring < sizeof(Merge<W>)) ring = sizeof(Merge<W>);
   return head + 128 + ring;
