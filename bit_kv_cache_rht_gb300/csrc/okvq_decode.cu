@@ -503,6 +503,77 @@ __device__ __forceinline__ void call_partial(const HalfPageCtx &hc, const unsign
   l_run = ts.l_run;
 }
 
+// The cross-warp merge of one segment, after every warp parked its modality sums
+// in tensor memory and wrote its (m, l) and held set: per-(warp, head) scales
+// (threads 0-7, which also write the partial's m and l), then the sums of each
+// lane quarter's warps (w, w + 4, w + 8 share tensor-memory rows) in tensor
+// memory, then the four quarter sums in shared memory, lane-major. Out of line:
+// its registers stay out of the page loop's allocation.
+template <int WARPS>
+__device__ __noinline__ void segment_merge(Merge<WARPS> *MG, float *part, uint32_t tbase, int nmod) {
+  constexpr int THREADS = WARPS * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, t4 = lane & 3;
+  // per-(warp, head) scales, once
+  if (tid < MAXGQ) {
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, MG->m[w][tid]);
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float sc = MG->m[w][tid] == -INFINITY ? 0.f : ex2(MG->m[w][tid] - M);
+      MG->sc[w][tid] = sc;
+      L += sc * MG->l[w][tid];
+    }
+    part[tid * PARTIAL_FLOATS + 0] = M;
+    part[tid * PARTIAL_FLOATS + 1] = L;
+  }
+  __syncthreads();
+  // warps of one lane quarter (w, w + 4, w + 8) share their tensor-memory rows:
+  // warp w sums, for modality m = w / 4 (+ WARPS / 4 ...), the scaled sets of its
+  // quarter; the four quarter sums meet in shared memory, lane-major
+  float *R4 = &MG->o[0][0][0][0];                 // [M][4 quarters][32 regs][32 lanes]
+  {
+    const int q = warp & 3;
+#pragma unroll 1
+    for (int m = warp >> 2; m < nmod; m += WARPS / 4) {
+      float sum[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) sum[mt][0] = sum[mt][1] = sum[mt][2] = sum[mt][3] = 0.f;
+#pragma unroll 1
+      for (int k = 0; k < WARPS / 4; ++k) {
+        const int src = q + 4 * k;
+        if (!((MG->held[src] >> m) & 1u)) continue;   // warp-uniform
+        float v[8][4];
+        tmem_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(k * MAXM * 32 + 32 * m), v);
+        const float s0 = MG->sc[src][2 * t4], s1 = MG->sc[src][2 * t4 + 1];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          sum[mt][0] = fmaf(s0, v[mt][0], sum[mt][0]);
+          sum[mt][1] = fmaf(s1, v[mt][1], sum[mt][1]);
+          sum[mt][2] = fmaf(s0, v[mt][2], sum[mt][2]);
+          sum[mt][3] = fmaf(s1, v[mt][3], sum[mt][3]);
+        }
+      }
+      float *dst = R4 + (size_t)(m * 4 + q) * 32 * 32 + lane;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[(4 * mt + e) * 32] = sum[mt][e];
+    }
+  }
+  tc_fence_before();                             // the slot reads are done before the next segment parks
+  __syncthreads();
+  tc_fence_after();
+  // register i = 4 mt + e of lane (g, t4): head 2 t4 + (e & 1), channel 16 mt + g + 8 (e >> 1)
+  for (int idx = tid; idx < nmod * 32 * 32; idx += THREADS) {
+    const int m = idx >> 10, i = (idx >> 5) & 31, ln = idx & 31;
+    const float *r = R4 + (size_t)m * 4 * 32 * 32 + i * 32 + ln;
+    const float o = (r[0] + r[32 * 32]) + (r[2 * 32 * 32] + r[3 * 32 * 32]);
+    const int head = 2 * (ln & 3) + (i & 1), ch = 16 * (i >> 2) + (ln >> 2) + 8 * ((i >> 1) & 1);
+    part[head * PARTIAL_FLOATS + 2 + m * D + ch] = o;
+  }
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const DecodeArgs a) {
   constexpr int WARPS = Cfg<BITS>::WARPS;
@@ -800,46 +871,12 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
       MG.l[warp][g] = l_run;
     }
     if (lane == 0) MG.held[warp] = held;
-#pragma unroll 1
-    for (int m = 0; m < MAXM; ++m) {
-      if (!((held >> m) & 1u)) continue;       // readers skip what a warp never held
-      if (m != ma.cur) mod_switch(ma, acc, m);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        MG.o[warp][m][2 * t4][16 * mt + g] = acc[mt][0];
-        MG.o[warp][m][2 * t4 + 1][16 * mt + g] = acc[mt][1];
-        MG.o[warp][m][2 * t4][16 * mt + g + 8] = acc[mt][2];
-        MG.o[warp][m][2 * t4 + 1][16 * mt + g + 8] = acc[mt][3];
-      }
-    }
+    // every modality sum of this warp goes to (or stays in) its tensor-memory slots
+    if (ma.cur >= 0) tmem_st32(ma.slot0 + 32u * (uint32_t)ma.cur, acc);
+    tc_fence_before();
     __syncthreads();
-    float *part = a.partials + (long long)seg * MAXGQ * PARTIAL_FLOATS;
-    // per-(warp, head) scales, once; then every (head, channel) sums the warps that held data
-    if (tid < MAXGQ) {
-      float M = -INFINITY, L = 0.f;
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) M = fmaxf(M, MG.m[w][tid]);
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) {
-        const float sc = MG.m[w][tid] == -INFINITY ? 0.f : ex2(MG.m[w][tid] - M);
-        MG.sc[w][tid] = sc;
-        L += sc * MG.l[w][tid];
-      }
-      part[tid * PARTIAL_FLOATS + 0] = M;
-      part[tid * PARTIAL_FLOATS + 1] = L;
-    }
-    __syncthreads();
-    for (int i = tid; i < MAXGQ * D; i += THREADS) {
-      const int hh = i / D, ch = i % D;
-      float *ph = part + hh * PARTIAL_FLOATS;
-      for (int m = 0; m < a.M; ++m) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w)
-          if ((MG.held[w] >> m) & 1u) o = fmaf(MG.sc[w][hh], MG.o[w][m][hh][ch], o);
-        ph[2 + m * D + ch] = o;
-      }
-    }
+    tc_fence_after();
+    segment_merge<WARPS>(&MG, a.partials + (long long)seg * MAXGQ * PARTIAL_FLOATS, tbase, a.M);
     __syncthreads();              // merge area is the stage ring of the next segment
   }
   // the level table's and a staged query copy must land before the CTA's shared
