@@ -167,18 +167,14 @@ __device__ __forceinline__ uint32_t lut_addr(uint32_t laneoff, uint32_t w) {
   return r;
 }
 
-// Cross-warp merge area of one segment (aliases the stage ring). Rows of o are
-// padded so that a warp's fragment stores (lane (g, t4) -> head 2t4 + e, channel
-// 16mt + g) hit 32 distinct banks.
-constexpr int MG_ROW = D + 4;
+// Cross-warp merge area of one segment (aliases the stage ring).
 template <int WARPS>
 struct Merge {
   float m[WARPS][MAXGQ];
   float l[WARPS][MAXGQ];
   float sc[WARPS][MAXGQ];        // exp2(m_w - M) per (warp, head)
-  float mx[MAXGQ];               // M per head
   uint32_t held[WARPS];          // modalities each warp accumulated
-  float o[WARPS][MAXM][MAXGQ][MG_ROW];
+  float q4[MAXM][4][32][32];     // per modality and lane quarter: the quarter's sum, [register][lane]
 };
 
 // value tile of one modality: acc[mt] += Lcode[16 ch x 16 tok] * P
@@ -531,7 +527,7 @@ __device__ __noinline__ void segment_merge(Merge<WARPS> *MG, float *part, uint32
   // warps of one lane quarter (w, w + 4, w + 8) share their tensor-memory rows:
   // warp w sums, for modality m = w / 4 (+ WARPS / 4 ...), the scaled sets of its
   // quarter; the four quarter sums meet in shared memory, lane-major
-  float *R4 = &MG->o[0][0][0][0];                 // [M][4 quarters][32 regs][32 lanes]
+  float *R4 = &MG->q4[0][0][0][0];
   {
     const int q = warp & 3;
 #pragma unroll 1
