@@ -5,9 +5,11 @@
 // aggregation).
 //
 // decode_kernel - split-K over the token axis, one CTA per SM (12 warps at
-//   2-bit, 8 at 4-bit). A CTA owns a balanced range of 64-token pages of the
-//   flattened (session, layer, kv head, page) list, cut into segments at unit
-//   boundaries. Each warp streams whole pages, one bulk copy each, into a private
+//   2-bit, 8 at 4-bit). A CTA owns a range of 64-token pages of the flattened
+//   (session, layer, kv head, page) list, cut into segments at unit boundaries
+//   (the host balances pages plus a fixed cost per segment). A segment's
+//   descriptor and queries are staged one segment ahead. Each warp streams whole
+//   pages, one bulk copy each, into a private
 //   2-stage shared-memory ring (mbarrier completion, bounded waits) and works on
 //   32-token half pages:
 //     scores  S^T[16 x 8 tok] = [a_hi; a_lo][16 x 128] * Lambda^T[128 x 8 tok] + [beta; 0]
@@ -21,8 +23,9 @@
 //   one 8-byte load yields a whole operand register pair. One accumulator set
 //   per modality in the rotated value domain: the current set in registers, the
 //   others parked in tensor memory. Evicted tokens (page deletion masks) take no
-//   part in the softmax. Warps merge in shared memory; one partial (m, l, o_m)
-//   per segment and head goes out.
+//   part in the softmax. Warps merge through tensor memory (the warps of a lane
+//   quarter) and shared memory (the four quarters); one partial (m, l, o_m) per
+//   segment and head goes out.
 // combine_kernel - per (unit, 64 output channels): log-sum-exp merge of the
 //   unit's partials (and of the far-memory partials, if any), then
 //   O = (sum_m R_m^T o_m) / (l sqrt d) on the tensor cores, plus the far-memory
