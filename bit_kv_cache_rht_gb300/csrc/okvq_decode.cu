@@ -937,6 +937,14 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
     float L = 0.f;
     const float *pbase = a.partials + (long long)w * PARTIAL_FLOATS;
     auto part = [&](int s) { return pbase + (long long)s * MAXGQ * PARTIAL_FLOATS; };
+    // the first two segments' o rows are loaded with the (m, l) pairs: one round
+    // trip to L2 fewer for the common unit of one or two segments
+    float p0[OPER], p1[OPER];
+#pragma unroll
+    for (int k = 0; k < OPER; ++k) {
+      p0[k] = (s0 < s1 && 32 * k < nr) ? part(s0)[2 + lane + 32 * k] : 0.f;
+      p1[k] = (s0 + 1 < s1 && 32 * k < nr) ? part(s0 + 1)[2 + lane + 32 * k] : 0.f;
+    }
     float m0 = -INFINITY, l0 = 0.f;
     if (s0 + lane < s1) {
       const float2 ml = *reinterpret_cast<const float2 *>(part(s0 + lane));
@@ -972,8 +980,18 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
         L = fmaf(wt, l, L);
       }
       const int n = min(32, s1 - sb);
+      int j0 = 0;
+      if (sb == s0) {                     // lane 1's weight is 0 (and p1 = 0) without a second segment
+        const float w0 = __shfl_sync(0xffffffffu, wt, 0), w1 = __shfl_sync(0xffffffffu, wt, 1);
+#pragma unroll
+        for (int k = 0; k < OPER; ++k) {
+          o[k] = fmaf(w0, p0[k], o[k]);
+          o[k] = fmaf(w1, p1[k], o[k]);
+        }
+        j0 = 2;
+      }
 #pragma unroll 4
-      for (int j = 0; j < n; ++j) {
+      for (int j = j0; j < n; ++j) {
         const float ws = __shfl_sync(0xffffffffu, wt, j);
         const float *p = part(sb + j) + 2 + lane;
 #pragma unroll
