@@ -633,8 +633,8 @@ def main():
             "calibration": dict(calib, kernel="calib_kernel (value-rotation covariance + Jacobi eigenbasis)"),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(Q.numel() * 2),
                     "d2h_bytes_per_step": int(out.numel() * 2),
-                    "how": "okvq_decode_host: pinned-host queries in, outputs out, both copies inside the "
-                           "timed region, every step"},
+                    "how": "okvq_decode_host: pinned-host queries copied in and outputs stored into pinned "
+                           "host memory by the merge kernel, inside the timed region, every step"},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
         }

@@ -441,6 +441,18 @@ okvq_status enqueue_decode(okvq_cache *h, const void *q, void *out, cudaStream_t
   return OKVQ_OK;
 }
 
+// The device address of page-locked, mapped host memory (pinned by cudaHostAlloc
+// or registered), else null (pageable memory, or a failed query). Asked on every
+// call: a freed pinned buffer's addresses may come back as pageable memory.
+void *mapped_host(void *p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 // True for device (or managed) memory of the handle's device; the answer for the
 // last few pointers is remembered, so a decode loop on fixed buffers checks once.
 bool device_ptr(okvq_cache *h, const void *p) {
@@ -751,10 +763,14 @@ okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, 
   OKVQ_TRY(cudaMemcpyAsync(h->q_stage[b], q_host, qo_bytes, cudaMemcpyHostToDevice, h->copy_stream));
   OKVQ_TRY(cudaEventRecord(h->ev_in[b], h->copy_stream));
   OKVQ_TRY(cudaStreamWaitEvent(s, h->ev_in[b], 0));
-  okvq_status st = enqueue_decode(h, h->q_stage[b], h->out_stage, s, h->partials, -1, h->prof, nullptr);
+  // page-locked output: the merge kernel stores into it directly (no copy after the
+  // decode); pageable output: device staging, then a copy
+  void *out_dev = mapped_host(out_host);
+  okvq_status st = enqueue_decode(h, h->q_stage[b], out_dev ? out_dev : h->out_stage, s, h->partials, -1, h->prof,
+                                  nullptr);
   if (st != OKVQ_OK) return st;
   OKVQ_TRY(cudaEventRecord(h->ev_used[b], s));
-  OKVQ_TRY(cudaMemcpyAsync(out_host, h->out_stage, qo_bytes, cudaMemcpyDeviceToHost, s));
+  if (!out_dev) OKVQ_TRY(cudaMemcpyAsync(out_host, h->out_stage, qo_bytes, cudaMemcpyDeviceToHost, s));
   ++h->host_calls;
   return OKVQ_OK;
 }

@@ -169,11 +169,15 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream);
 
 /* okvq_decode on HOST buffers: copies the queries (host, same layout as
- * okvq_decode's q) into the handle's device staging, decodes, and copies the
- * outputs back to `out_host`, all asynchronously on `stream` (the host buffers
- * must stay valid, and `out_host` unread, until the stream reaches that point;
- * pinned host memory makes the copies asynchronous, pageable memory makes them
- * synchronous). The upload runs on a copy stream owned by the handle, into one
+ * okvq_decode's q) into the handle's device staging, decodes, and delivers the
+ * outputs to `out_host`, all asynchronously on `stream` (the host buffers must
+ * stay valid, and `out_host` unread, until the stream reaches that point). When
+ * `out_host` is page-locked host memory (cudaHostAlloc, cudaHostRegister, a
+ * pinned torch tensor; checked with cudaPointerGetAttributes on every call), the
+ * merge kernel stores the outputs into it directly, with no copy after the
+ * decode; otherwise they go through device staging and a copy. Pinned host
+ * memory makes the query upload asynchronous, pageable memory makes it
+ * synchronous. The upload runs on a copy stream owned by the handle, into one
  * of two staging slots, so it overlaps the decode a previous call left on
  * `stream`; `stream` waits for it, so the call's effects are complete when
  * `stream` reaches that point. Staging (3 x S*L*Hq*128 fp16), the copy stream and
