@@ -247,6 +247,27 @@ def test_decode_host_equals_decode_on_device_buffers():
         assert torch.equal(o, ref)
 
 
+def test_decode_host_pageable_and_pinned_outputs_agree():
+    """Pinned outputs are stored by the merge kernel itself; pageable outputs go
+    through device staging and a copy. Both give okvq_decode's outputs bit for
+    bit, also when the two kinds alternate on one handle."""
+    import torch
+    w = synth.qwen3b(seed=46, tokens=1500, layers=2)
+    c = pu.gpu_cache(w)
+    Qs = [w.queries(step) for step in range(4)]
+    refs = [c.decode(torch.from_numpy(Q).cuda()).cpu() for Q in Qs]
+    outs = []
+    for i, Q in enumerate(Qs):
+        o = torch.full(Q.shape, float("nan"), dtype=torch.float16)
+        if i % 2:
+            o = o.pin_memory()
+        c.decode_host(torch.from_numpy(Q), o)          # pageable queries: a synchronous upload
+        outs.append(o)
+    torch.cuda.synchronize()
+    for o, ref in zip(outs, refs):
+        assert torch.equal(o, ref)
+
+
 def test_host_and_foreign_pointers_are_rejected_before_any_launch():
     """Pageable and pinned host memory passed where device memory is expected:
     OKVQ_EINVAL, nothing launched, the cache unchanged."""
