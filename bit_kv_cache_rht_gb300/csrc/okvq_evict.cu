@@ -10,9 +10,10 @@
 //                    also carries the session's modality ids): copies one granule's
 //                    bytes between its page slots and the scratch slots (gather or
 //                    scatter).
-// page_meta_kernel - one CTA per (page, layer x kv head): writes the page's
-//                    deletion mask from the session's mask array and clears the
-//                    tile modality masks of tiles at or past the session length.
+// page_meta_kernel - one thread per (page, layer x kv head), flat grid: writes the
+//                    page's deletion mask from the session's mask array and
+//                    clears the tile modality masks of tiles at or past the
+//                    session length.
 #include "okvq_internal.h"
 
 namespace okvq {
@@ -74,14 +75,19 @@ __global__ void __launch_bounds__(MOVE_THREADS) move_kernel(const MoveArgs a) {
   }
 }
 
-__global__ void page_meta_kernel(const PageMetaArgs a) {
-  const long long page = a.p0 + blockIdx.x;
-  const int lh = blockIdx.y;
+constexpr int META_THREADS = 256;
+
+__global__ void __launch_bounds__(META_THREADS) page_meta_kernel(const PageMetaArgs a, long long n) {
+  const long long i = (long long)blockIdx.x * META_THREADS + threadIdx.x;
+  if (i >= n) return;
+  const long long page = a.p0 + i / a.LH;       // consecutive threads: the units of one page
+  const int lh = (int)(i % a.LH);
   const long long unit = (long long)a.session * a.LH + lh;
   uint8_t *pg = a.pages + (unit * a.P_max + page) * (long long)a.PL.page_bytes;
-  if (threadIdx.x == 0)
-    *reinterpret_cast<unsigned long long *>(pg + a.PL.off_tmask + DEAD_OFF) = a.dead[page];
-  if (threadIdx.x < PAGE / TILE && page * PAGE + TILE * threadIdx.x >= a.T) pg[a.PL.off_tmask + threadIdx.x] = 0;
+  *reinterpret_cast<unsigned long long *>(pg + a.PL.off_tmask + DEAD_OFF) = a.dead[page];
+#pragma unroll
+  for (int t = 0; t < PAGE / TILE; ++t)
+    if (page * PAGE + TILE * t >= a.T) pg[a.PL.off_tmask + t] = 0;
 }
 
 }  // namespace
@@ -94,7 +100,8 @@ cudaError_t launch_move(const MoveArgs &a, cudaStream_t s) {
 
 cudaError_t launch_page_meta(const PageMetaArgs &a, int n_pages, cudaStream_t s) {
   if (n_pages <= 0) return cudaSuccess;
-  page_meta_kernel<<<dim3((unsigned)n_pages, (unsigned)a.LH), 32, 0, s>>>(a);
+  const long long n = (long long)n_pages * a.LH;
+  page_meta_kernel<<<(unsigned)((n + META_THREADS - 1) / META_THREADS), META_THREADS, 0, s>>>(a, n);
   return cudaGetLastError();
 }
 
