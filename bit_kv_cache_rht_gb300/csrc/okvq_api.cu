@@ -453,6 +453,9 @@ void *mapped_host(void *p) {
   return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
+// The decode stages each segment's queries by bulk copy: a 16-byte aligned source.
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 // True for device (or managed) memory of the handle's device; the answer for the
 // last few pointers is remembered, so a decode loop on fixed buffers checks once.
 bool device_ptr(okvq_cache *h, const void *p) {
@@ -747,7 +750,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
 }
 
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream) {
-  if (!h || !device_ptr(h, q) || !device_ptr(h, out)) return OKVQ_EINVAL;
+  if (!h || !aligned16(q) || !device_ptr(h, q) || !device_ptr(h, out)) return OKVQ_EINVAL;
   return enqueue_decode(h, q, out, static_cast<cudaStream_t>(stream), h->partials, -1, h->prof, nullptr);
 }
 
@@ -776,7 +779,7 @@ okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, 
 }
 
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream) {
-  if (!h || !device_ptr(h, q) || !device_ptr(h, out)) return OKVQ_EINVAL;
+  if (!h || !aligned16(q) || !device_ptr(h, q) || !device_ptr(h, out)) return OKVQ_EINVAL;
   float *scratch = nullptr;
   okvq_status st = static_partials(h->device, &scratch);
   if (st != OKVQ_OK) return st;
@@ -788,7 +791,8 @@ okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, 
 okvq_status okvq_decode_pseudo(okvq_cache *h, const void *q, const void *far_k, const void *far_v,
                                const float *far_mass, int32_t num_prototypes, int32_t tokens_per_prototype,
                                void *out, void *stream) {
-  if (!h || !device_ptr(h, q) || !device_ptr(h, out) || num_prototypes < 0 || tokens_per_prototype < 1)
+  if (!h || !aligned16(q) || !device_ptr(h, q) || !device_ptr(h, out) || num_prototypes < 0 ||
+      tokens_per_prototype < 1)
     return OKVQ_EINVAL;
   const long long n_far = (long long)num_prototypes * tokens_per_prototype;
   if (n_far > (1ll << 30)) return OKVQ_EINVAL;

@@ -125,7 +125,8 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
                               const uint8_t *modality, int32_t num_tokens, void *stream);
 
 /* One decode step for every session and layer (section 1, Implementation):
- *   q    device fp16 [num_sessions][num_layers][num_q_heads][128]
+ *   q    device fp16 [num_sessions][num_layers][num_q_heads][128], 16-byte
+ *        aligned (each segment's queries arrive by bulk copy); OKVQ_EINVAL otherwise
  *   out  device fp16 [num_sessions][num_layers][num_q_heads][128]
  * An empty session yields zeros. Two kernel launches (split-K fused
  * attention, then the merge + inverse value rotations), asynchronous on

@@ -269,8 +269,9 @@ def test_decode_host_pageable_and_pinned_outputs_agree():
 
 
 def test_host_and_foreign_pointers_are_rejected_before_any_launch():
-    """Pageable and pinned host memory passed where device memory is expected:
-    OKVQ_EINVAL, nothing launched, the cache unchanged."""
+    """Pageable and pinned host memory passed where device memory is expected, and
+    queries off a 16-byte boundary: OKVQ_EINVAL, nothing launched, the cache
+    unchanged."""
     import torch
     from bit_kv_cache_rht_gb300 import okvq
     w = synth.tiny(seed=51, tokens=64)
@@ -289,6 +290,10 @@ def test_host_and_foreign_pointers_are_rejected_before_any_launch():
     qd, od = q.cuda(), torch.empty_like(q).cuda()
     assert okvq.okvq_decode(c._h, q.data_ptr(), od.data_ptr()) == E
     assert okvq.okvq_decode(c._h, qd.data_ptr(), q.pin_memory().data_ptr()) == E
+    # queries off a 16-byte boundary (the decode stages them by bulk copy)
+    qbuf = torch.zeros(qd.numel() + 8, dtype=torch.float16, device="cuda")
+    assert okvq.okvq_decode(c._h, qbuf[1:].data_ptr(), od.data_ptr()) == E
+    assert okvq.okvq_decode_static_scratch(c._h, qbuf[1:].data_ptr(), od.data_ptr()) == E
     torch.cuda.synchronize()
     assert c.length(0) == 64 and c.check_errors() == 0
     after = c.export_state(0)
