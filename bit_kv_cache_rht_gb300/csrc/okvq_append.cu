@@ -28,7 +28,7 @@ constexpr int ROW_H = ROT_ROW_H;           // padded fp16 row: ldmatrix row read
 struct Smem {
   union {
     struct {
-      __half rh[2][D][ROW_H];      // R_m of one modality, fp16 high and residual parts, [output][channel]
+      __half rh[D][ROW_H];         // one part (fp16 high, then residual) of R_m, [output][channel]
       __half vh[PAGE][ROW_H];      // the page's values, fp16 [token][channel]
     } v;
     float xt[PAGE * D];            // then: keys [token][c] (rotated, fp32)
@@ -247,44 +247,52 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   const int mt = warp & 3, o0 = 64 * (warp >> 2);
   const int g = lane >> 2, t4 = lane & 3;
   uint32_t phase = 0;
-  for (int m = 0; m < a.M; ++m) {
+  bool failed = false;
+  for (int m = 0; m < a.M && !failed; ++m) {
     if (!S.present[m]) continue;  // uniform: smem flag read after a barrier
-    if (tid == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar)),
-                   "r"((uint32_t)sizeof(S.u.v.rh))
-                   : "memory");
-      asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-              smem_addr(&S.u.v.rh[0][0][0])),
-          "l"(a.rot_h + ((long long)lh * a.M + m) * (2 * D * ROW_H)), "r"((uint32_t)sizeof(S.u.v.rh)),
-          "r"(smem_addr(&S.bar))
-          : "memory");
-    }
-    const bool failed = __syncthreads_or(!wait_bar(&S.bar, phase));
-    phase ^= 1u;
-    if (failed) {                                  // the codes of this chunk's values stay unwritten
-      if (tid == 0) atomicOr(a.err, ERR_WAIT);
-      break;
-    }
     float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     const uint32_t va = smem_addr(&S.u.v.vh[16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-    const int bj = lane >> 3;                      // ldmatrix matrix: hi / lo x channel half
-    const uint32_t rb = smem_addr(&S.u.v.rh[bj >> 1][o0 + (lane & 7)][8 * (bj & 1)]);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t A[4];
-      ldsm4(va + 32 * kk, A);
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        uint32_t B[4];
-        ldsm4(rb + (8 * nt * ROW_H) * 2 + 32 * kk, B);
-        mma16816(acc[nt], A, B[0], B[1]);
-        mma16816(acc[nt], A, B[2], B[3]);
+    const int bj = lane >> 3;                      // ldmatrix matrix: output block (nt, nt + 1) x channel half
+    const uint32_t rb = smem_addr(&S.u.v.rh[o0 + 8 * (bj >> 1) + (lane & 7)][8 * (bj & 1)]);
+    // the high part, then the residual, staged in turn (one part of shared memory:
+    // three CTAs fit on an SM); the products accumulate in fp32 across both passes
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar)),
+                     "r"((uint32_t)sizeof(S.u.v.rh))
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_addr(&S.u.v.rh[0][0])),
+            "l"(a.rot_h + (((long long)lh * a.M + m) * 2 + part) * (D * ROW_H)), "r"((uint32_t)sizeof(S.u.v.rh)),
+            "r"(smem_addr(&S.bar))
+            : "memory");
       }
+      failed = __syncthreads_or(!wait_bar(&S.bar, phase));
+      phase ^= 1u;
+      if (failed) {                                // the codes of this chunk's values stay unwritten
+        if (tid == 0) atomicOr(a.err, ERR_WAIT);
+        break;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t A[4];
+        ldsm4(va + 32 * kk, A);
+#pragma unroll
+        for (int nt = 0; nt < 8; nt += 2) {
+          uint32_t B[4];
+          ldsm4(rb + (8 * nt * ROW_H) * 2 + 32 * kk, B);
+          mma16816(acc[nt], A, B[0], B[1]);
+          mma16816(acc[nt + 1], A, B[2], B[3]);
+        }
+      }
+      __syncthreads();                             // rh is rewritten next
     }
+    if (failed) break;
     // rows: tokens 16 mt + g (+8); columns: outputs o0 + 8 nt + 2 t4 (+1)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -300,8 +308,8 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
         }
       }
     }
-    __syncthreads();                               // rh is rewritten for the next modality
   }
+  __syncthreads();                                 // every warp's codes are in S.vc
   // write the value tiles that got new tokens
   for (int tile = ta / TILE; tile * TILE < tb; ++tile)
     pack_tile<BITS, 1>(S.vc, pg + PL.off_v + tile * PL.tile_bytes, tile, tb, tid, THREADS);
@@ -448,9 +456,12 @@ cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s) {
   static std::atomic<uint64_t> attr_done{0};
   const size_t smem = sizeof(Smem);
   cudaError_t e = once_per_device(attr_done, [&] {
+    // ~73 KB of shared memory: three CTAs per SM with the largest shared-memory carveout
     cudaError_t r = cudaFuncSetAttribute(append_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (r != cudaSuccess) return r;
-    return cudaFuncSetAttribute(append_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return r;
   });
   if (e != cudaSuccess) return e;
   dim3 grid(n_pages, a.L * a.Hkv);
