@@ -9,9 +9,8 @@
 //   (session, layer, kv head, page) list, cut into segments at unit boundaries
 //   (the host balances pages plus a fixed cost per segment). A segment's
 //   descriptor and queries are staged one segment ahead. Each warp streams whole
-//   pages, one bulk copy each, into a private
-//   2-stage shared-memory ring (mbarrier completion, bounded waits) and works on
-//   32-token half pages:
+//   pages, one bulk copy each, into a private 2-stage shared-memory ring
+//   (mbarrier completion, bounded waits) and works on 32-token half pages:
 //     scores  S^T[16 x 8 tok] = [a_hi; a_lo][16 x 128] * Lambda^T[128 x 8 tok] + [beta; 0]
 //             (mma m16n8k16; rows 0-7 / 8-15 = the 8 query heads' fp16 high and
 //             residual parts of a = q' o range, so the sum is exact to ~2^-22)
