@@ -941,8 +941,9 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
     float p0[OPER], p1[OPER];
 #pragma unroll
     for (int k = 0; k < OPER; ++k) {
-      p0[k] = (s0 < s1 && 32 * k < nr) ? part(s0)[2 + lane + 32 * k] : 0.f;
-      p1[k] = (s0 + 1 < s1 && 32 * k < nr) ? part(s0 + 1)[2 + lane + 32 * k] : 0.f;
+      // lane: channels 2 lane + 64 (k / 2) + (k % 2), as 8-byte pairs
+      p0[k] = (s0 < s1 && 64 * (k >> 1) < nr) ? part(s0)[2 + 2 * lane + 64 * (k >> 1) + (k & 1)] : 0.f;
+      p1[k] = (s0 + 1 < s1 && 64 * (k >> 1) < nr) ? part(s0 + 1)[2 + 2 * lane + 64 * (k >> 1) + (k & 1)] : 0.f;
     }
     float m0 = -INFINITY, l0 = 0.f;
     if (s0 + lane < s1) {
@@ -994,16 +995,21 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
         const float ws = __shfl_sync(0xffffffffu, wt, j);
         const float *p = part(sb + j) + 2 + lane;
 #pragma unroll
-        for (int k = 0; k < OPER; ++k)
-          if (32 * k < nr) o[k] = fmaf(ws, p[32 * k], o[k]);
+        for (int k = 0; k < OPER; k += 2)
+          if (64 * (k >> 1) < nr) {
+            const float2 v = *reinterpret_cast<const float2 *>(p + lane + 64 * (k >> 1));
+            o[k] = fmaf(ws, v.x, o[k]);
+            o[k + 1] = fmaf(ws, v.y, o[k + 1]);
+          }
       }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-    for (int k = 0; k < OPER; ++k)
-      if (32 * k < nr) osh[w * OSTRIDE + lane + 32 * k] = o[k] * inv;
+    for (int k = 0; k < OPER; k += 2)
+      if (64 * (k >> 1) < nr)
+        *reinterpret_cast<float2 *>(osh + w * OSTRIDE + 2 * lane + 64 * (k >> 1)) = make_float2(o[k] * inv, o[k + 1] * inv);
 #pragma unroll
     for (int j = 0; j < CB_CH / 32; ++j) ofar[w * CB_CH + lane + 32 * j] = of[j] * inv;
   } else if (w < MAXGQ) {
