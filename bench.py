@@ -57,9 +57,9 @@ def algorithmic_bytes(w, lengths, key_codec="omni"):
             per_unit_T = T * (2 * d * b // 8 + 2) + (T // G) * 4 * d + (T % G) * 2 * d
         per_unit += per_unit_T * sh.num_layers * sh.num_kv_heads
     mod = sum(lengths)
-    qo = 2 * len(lengths) * sh.num_layers * sh.num_q_heads * d
+    q_bytes = 2 * len(lengths) * sh.num_layers * sh.num_q_heads * d     # fp16 queries in, and as many outputs
     rot = sh.num_layers * sh.num_kv_heads * sh.num_modalities * d * d * 4
-    return per_unit + mod + qo // 2, qo // 2, rot     # split kernel bytes, merge kernel out bytes, R bytes
+    return per_unit + mod + q_bytes, q_bytes, rot     # split kernel bytes, merge kernel out bytes, R bytes
 
 
 def rank_env():

@@ -37,9 +37,12 @@ struct okvq_cache {
   std::vector<int> tail_sel;    // per session: current tail buffer
   bool dirty = true;
   int ncta = 0, nseg = 0;
-  void *host_table = nullptr;   // pinned staging of the work table
-  cudaEvent_t table_ev = nullptr;
-  bool table_ev_pending = false;
+  // pinned staging of the work table, two buffers used in turn: a rebuild waits only
+  // for the upload two rebuilds back, long finished in an append-decode loop
+  void *host_table[2] = {};
+  cudaEvent_t table_ev[2] = {};
+  bool table_ev_pending[2] = {};
+  int table_slot = 0;
   // offsets (bytes) inside the table
   size_t off_segs = 0, off_cta = 0, off_useg = 0, off_ulen = 0, off_utail = 0;
   // codebook
@@ -162,8 +165,10 @@ void release(okvq_cache *h) {
     if (h->ev_used[b]) cudaEventDestroy(h->ev_used[b]);
   }
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
-  if (h->host_table) cudaFreeHost(h->host_table);
-  if (h->table_ev) cudaEventDestroy(h->table_ev);
+  for (int b = 0; b < 2; ++b) {
+    if (h->host_table[b]) cudaFreeHost(h->host_table[b]);
+    if (h->table_ev[b]) cudaEventDestroy(h->table_ev[b]);
+  }
   for (auto e : h->ev) cudaEventDestroy(e);
   delete h;
 }
@@ -264,8 +269,8 @@ SplitPlan plan_split(const long long *pages_u, long long U, int max_cta, int seg
 #endif
 constexpr int SEG_COST_PAGES = OKVQ_SEG_COST;
 
-// Build the decode work table from the session lengths.
-void build_table(okvq_cache *h) {
+// Build the decode work table from the session lengths into pinned buffer `slot`.
+void build_table(okvq_cache *h, int slot) {
   const long long U = h->units;
   std::vector<long long> pages_u(U);
   const int LH = h->L * h->Hkv;
@@ -273,7 +278,7 @@ void build_table(okvq_cache *h) {
     long long T = h->len[u / LH];
     pages_u[u] = (T + PAGE - 1) / PAGE;
   }
-  char *base = static_cast<char *>(h->host_table);
+  char *base = static_cast<char *>(h->host_table[slot]);
   int *segs = reinterpret_cast<int *>(base + h->off_segs);
   int *cta_seg = reinterpret_cast<int *>(base + h->off_cta);
   int *unit_seg = reinterpret_cast<int *>(base + h->off_useg);
@@ -369,11 +374,14 @@ okvq_status push_page_meta(okvq_cache *h, int session, long long p0, long long p
 okvq_status enqueue_decode(okvq_cache *h, const void *q, void *out, cudaStream_t s, float *partials, long long seg_limit,
                            bool profile, const FarArgs *far) {
   if (h->dirty) {
-    if (h->table_ev_pending) OKVQ_TRY(cudaEventSynchronize(h->table_ev));   // staging buffer free again
-    build_table(h);
-    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table, h->table_bytes, cudaMemcpyHostToDevice, s));
-    OKVQ_TRY(cudaEventRecord(h->table_ev, s));
-    h->table_ev_pending = true;
+    const int b = h->table_slot;
+    // the staging buffer is free once the upload made from it two rebuilds back has run
+    if (h->table_ev_pending[b]) OKVQ_TRY(cudaEventSynchronize(h->table_ev[b]));
+    build_table(h, b);
+    OKVQ_TRY(cudaMemcpyAsync(h->table, h->host_table[b], h->table_bytes, cudaMemcpyHostToDevice, s));
+    OKVQ_TRY(cudaEventRecord(h->table_ev[b], s));
+    h->table_ev_pending[b] = true;
+    h->table_slot = b ^ 1;
     h->dirty = false;
   }
   if (seg_limit >= 0 && h->nseg > seg_limit) return OKVQ_ESCRATCH;
@@ -622,8 +630,10 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   h->off_utail = take((size_t)h->units * sizeof(int));
   h->table_bytes = off;
   if ((st = alloc_dev((void **)&h->table, h->table_bytes)) != OKVQ_OK) return fail(st);
-  if (cudaMallocHost(&h->host_table, h->table_bytes) != cudaSuccess) return fail(OKVQ_ENOMEM);
-  if (cudaEventCreateWithFlags(&h->table_ev, cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
+  for (int b = 0; b < 2; ++b) {
+    if (cudaMallocHost(&h->host_table[b], h->table_bytes) != cudaSuccess) return fail(OKVQ_ENOMEM);
+    if (cudaEventCreateWithFlags(&h->table_ev[b], cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
+  }
 
   // contents
   if (cudaMemsetAsync(h->pages, 0, page_total, s) != cudaSuccess) return fail(OKVQ_ECUDA);

@@ -130,8 +130,16 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
  *   out  device fp16 [num_sessions][num_layers][num_q_heads][128]
  * An empty session yields zeros. Two kernel launches (split-K fused
  * attention, then the merge + inverse value rotations), asynchronous on
- * `stream`; the work list is re-uploaded on `stream` after appends changed
- * the lengths. */
+ * `stream`.
+ * Work list: the first decode after appends (or an eviction or compaction)
+ * changed the lengths plans the split on the host and uploads it on `stream`
+ * from one of two page-locked staging buffers used in turn; the call waits
+ * only for the upload made from the same buffer two rebuilds earlier (in an
+ * append-then-decode loop that upload has long finished). That upload reads
+ * host memory when it runs, so such a first decode is not for stream capture;
+ * decodes with unchanged lengths upload nothing. The device copy of the work
+ * list is one per handle: calls on one handle must be ordered on the device
+ * (one stream, or ordered by the caller). */
 okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
 
 /* Capacity, in work-list segments, of the static scratch array used by
