@@ -607,7 +607,6 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   __shared__ __align__(8) uint64_t q_bar;
   __shared__ int sd_unit, sd_pb, sd_pe, sd_tail;
   __shared__ long long sd_T;
-  const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
   const int gq = a.Hq / a.Hkv;
   struct SegDesc {
     int unit, pb, pe, tail;
@@ -633,11 +632,13 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     fence_async_smem();
     bulk_load(qstage, qsrc, (uint32_t)(gq * D * sizeof(__half)), &q_bar);
   };
+  // Launched as a programmatic dependent of the previous kernel on the stream (the
+  // last step's merge): everything up to griddepcontrol.wait reads only the cache's
+  // level table, written at create; the work list, queries and pages come after it.
   if (tid == 0) {
     mbar_init(&lut_bar, 1);
     mbar_init(&q_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (seg_begin < seg_end) stage_segment(load_desc(seg_begin));
     bulk_load(lut, a.lut, LUT_BYTES, &lut_bar);
   }
   if (lane == 0)
@@ -652,6 +653,9 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   }
   // the merge kernel may be scheduled as SMs free up; it waits for this grid's memory
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
+  if (tid == 0 && seg_begin < seg_end) stage_segment(load_desc(seg_begin));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -925,7 +929,10 @@ __global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
     fence_async_smem();
     bulk_load(afr, a.rot_frag + ((long long)lh * 8 + CB_MT * half) * nks * 32 * 2, fbytes, &bar);
   }
-  // everything above only reads the rotations; the partials come from the decode grid
+  // everything above only reads the rotations; the partials come from the decode grid.
+  // The next decode step may launch as this grid's CTAs retire (it waits for this grid
+  // before it reads or writes anything this one touches).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int nr = a.M * D;
   if (w < gq) {
@@ -1069,8 +1076,17 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int n_cta, cudaStream_t s) {
     return cudaFuncSetAttribute(decode_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
-  decode_kernel<BITS, G><<<n_cta, Cfg<BITS>::WARPS * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_cta);
+  cfg.blockDim = dim3(Cfg<BITS>::WARPS * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, G>, a);
 }
 
 }  // namespace
