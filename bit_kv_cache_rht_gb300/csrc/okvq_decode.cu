@@ -634,7 +634,11 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   };
   // Launched as a programmatic dependent of the previous kernel on the stream (the
   // last step's merge): everything up to griddepcontrol.wait reads only the cache's
-  // level table, written at create; the work list, queries and pages come after it.
+  // level table (written at create) and the work list (written by a host copy that
+  // the launch itself follows); queries and pages come after it.
+  const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
+  SegDesc first{};
+  if (tid == 0 && seg_begin < seg_end) first = load_desc(seg_begin);
   if (tid == 0) {
     mbar_init(&lut_bar, 1);
     mbar_init(&q_bar, 1);
@@ -654,8 +658,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   // the merge kernel may be scheduled as SMs free up; it waits for this grid's memory
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
-  if (tid == 0 && seg_begin < seg_end) stage_segment(load_desc(seg_begin));
+  if (tid == 0 && seg_begin < seg_end) stage_segment(first);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
