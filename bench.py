@@ -35,10 +35,12 @@ UNIT = "context tokens/s"
 
 
 def decode_source_sha256():
-    """Hash of the decode kernel sources (compared with the one stored beside the ncu traffic figure)."""
+    """Hash of the decode kernel's own sources (okvq_decode.cu and the two headers it
+    includes; the merge kernel lives in okvq_combine.cu), compared with the one stored
+    beside the ncu traffic figure: a changed kernel makes the stored figure stale."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("okvq_decode.cu", "okvq_internal.h"):
+    for f in ("okvq_decode.cu", "okvq_internal.h", "okvq_device.h"):
         with open(os.path.join(ROOT, "bit_kv_cache_rht_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -99,6 +101,16 @@ def peaks():
             j = json.load(f)
         return float(j["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """fp16 tensor peak (TFLOP/s): the measured bf16 cuBLAS burst figure (fp16 runs at
+    the bf16 rate), else the profiling fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 cuBLAS burst; fp16 at the same rate)"
+    return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -197,7 +209,7 @@ def calibrate(w, torch, device):
     return R, calib
 
 
-def build_cache(w, torch, device, replicas=2, key_codec="omni"):
+def build_cache(w, torch, device, replicas=2, key_codec="omni", keep_layer0=False):
     from bit_kv_cache_rht_gb300.okvq import Cache, OKVQ_KEYS_GROUP_RANGE, OKVQ_KEYS_TURBOQUANT
     sh = w.shape
     st = torch.cuda.current_stream()
@@ -207,12 +219,16 @@ def build_cache(w, torch, device, replicas=2, key_codec="omni"):
                     hadamard_seed=w.hadamard_seed,
                     key_codec=OKVQ_KEYS_TURBOQUANT if key_codec == "turbo" else OKVQ_KEYS_GROUP_RANGE)
               for _ in range(replicas)]
+    for c in caches:
+        c.rotations_used = R          # the value rotations the caches were created with
     append_ms = [[] for _ in range(replicas)]
     for s in range(len(w.sessions)):
         if not w.sessions[s].length:
             continue
         K, V = device_session_kv(w, s, torch, device)
         M = torch.from_numpy(w.sessions[s].modality()).to(device)
+        if keep_layer0 and s == 0:     # the inputs of layer 0, for the CPU leg's state comparison
+            caches[0].layer0_kv = (K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy())
         for rep, c in enumerate(caches):
             ev = []
             for a, b in w.sessions[s].chunk_bounds():
@@ -354,15 +370,84 @@ def pseudo_leg(torch, device, peak, steps=10, near_tokens=8192, prototypes=3072,
                              "note": "far kernel time = (near + far kernels) - (near kernel alone), CUDA events"}}
 
 
-def streaming_run(args, torch, device, peak):
-    """The streaming configuration: 1-s chunks [2,304 video, 25 audio] of the 3B
-    shape appended one by one up to 131,072 tokens, one decode query after every
-    chunk; append and decode latency (CUDA events around each call, host work of
-    the call included) against the context length."""
-    from bit_kv_cache_rht_gb300.okvq import Cache
-    w = make_workload(args)
+
+
+def timed_steps(caches, Q, out, torch, steps, warmup):
+    """Warm-up steps, a profiled pass (per-kernel CUDA events: decode kernel, merge
+    kernel), then `steps` back-to-back decode steps timed with CUDA events on the
+    launching stream (the replicas alternate). Returns (total ms, split ms list,
+    merge ms list)."""
+    st = torch.cuda.current_stream()
+    for i in range(warmup):
+        caches[i % len(caches)].decode(Q, out)
+    torch.cuda.synchronize()
+    for c in caches:
+        c.profile_enable(True)
+    for i in range(steps):
+        caches[i % len(caches)].decode(Q, out)
+    torch.cuda.synchronize()
+    split_ms, merge_ms = [], []
+    for c in caches:
+        a, b = c.profile_read()
+        split_ms += list(a)
+        merge_ms += list(b)
+        c.profile_enable(False)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        caches[i % len(caches)].decode(Q, out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), split_ms, merge_ms
+
+
+def config_summary(w, args, torch, device, peak, steps, warmup, key_codec="omni"):
+    """One extra configuration of the default run: its caches built on the device,
+    decode steps timed as for the headline line (two replicas alternate unless one
+    cache alone is more than four times the L2), every cache freed afterwards."""
     sh = w.shape
-    R, calib = calibrate(w, torch, device)
+    lengths = [s.length for s in w.sessions]
+    split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths, key_codec)
+    replicas = 2 if split_bytes < 4 * 129e6 else 1
+    caches, append_ms, _ = build_cache(w, torch, device, replicas=replicas, key_codec=key_codec)
+    Q = torch.from_numpy(w.queries(0)).to(device)
+    out = torch.empty_like(Q)
+    ms, split_ms, merge_ms = timed_steps(caches, Q, out, torch, steps, warmup)
+    errs = [c.check_errors() for c in caches]
+    ap_ms = sum(x for x, _ in append_ms[0])
+    ap_tokens = sum(n for _, n in append_ms[0])
+    del caches, Q, out
+    torch.cuda.empty_cache()
+    if any(errs):
+        raise RuntimeError("device error word set in %s" % w.name)
+    ms_step = ms / steps
+    avg_split = float(np.mean(split_ms))
+    step_us = 1e3 * (np.asarray(split_ms) + np.asarray(merge_ms))
+    achieved = split_bytes / (avg_split / 1e3) / 1e9
+    return {"workload": config_of(w, args)["workload"], "sessions": len(lengths), "context_tokens": sum(lengths),
+            "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
+            "context_tokens_per_s": sum(lengths) / (ms_step / 1e3),
+            "hbm_gbs_step": (split_bytes + out_bytes) / (ms_step / 1e3) / 1e9,
+            "latency_us": {"p50": float(np.percentile(step_us, 50)), "p99": float(np.percentile(step_us, 99))},
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "bytes_per_launch": split_bytes,
+                         "avg_launch_ms": avg_split, "merge_kernel_avg_ms": float(np.mean(merge_ms))},
+            "append_tokens_per_s": ap_tokens / (ap_ms / 1e3),
+            "l2": "two cache replicas alternate" if replicas == 2 else "one cache, %.1f GB per step" % (
+                split_bytes / 1e9)}
+
+
+def streaming_summary(args, torch, device, peak, tokens=131072):
+    """The streaming configuration: 1-s chunks [2,304 video, 25 audio] of the 3B head
+    shape appended one by one, one decode query after every chunk. Reports append
+    throughput on these chunks, decode latency against context length (CUDA events
+    around the device work of each call, host work included), and plain decodes at
+    the final length for comparison (no append in between)."""
+    from bit_kv_cache_rht_gb300.okvq import Cache
+    w = synth.streaming(tokens=tokens, bits=getattr(args, "bits", 2), group_size=getattr(args, "group_size", 32))
+    sh = w.shape
+    R, _ = calibrate(w, torch, device)
     c = Cache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, w.max_tokens, R, head_dim=sh.head_dim,
               group_size=sh.group_size, bits=sh.bits, num_modalities=sh.num_modalities,
               hadamard_seed=w.hadamard_seed)
@@ -384,39 +469,181 @@ def streaming_run(args, torch, device, peak):
     if c.check_errors() != 0:
         raise RuntimeError("device error word set in the streaming run")
     res = [(T, n, e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for T, n, e in rows]
-    ap_tok = sum(n for _, n, _, _ in res)
-    ap_ms = sum(x for _, _, x, _ in res)
-    T_end, _, _, dec_ms = res[-1]
-    line = {"metric": METRIC, "value": T_end / (dec_ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": len(res),
-            "warmup": 0, "ms_per_step": dec_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16 operands, f32 accumulate", "data": "synthetic", "config": config_of(w, args),
-            "streaming": {"chunks": len(res), "append_tokens_per_s": ap_tok / (ap_ms / 1e3),
-                          "decode_ms_at_context": [[T, round(d, 4)] for T, _, _, d in res[::8]] + [[T_end,
-                                                                                                  round(dec_ms, 4)]],
-                          "append_ms_per_chunk": float(np.median([x for _, _, x, _ in res])),
-                          "note": "first decode after each append rebuilds the work table (host) and uploads it"},
-            "calibration": calib}
+    # plain decodes at the final length
+    for _ in range(5):
+        c.decode(Q, out)
+    torch.cuda.synchronize()
+    plain = []
+    for _ in range(20):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        c.decode(Q, out)
+        e1.record(st)
+        torch.cuda.synchronize()
+        plain.append(e0.elapsed_time(e1))
+    c.close()
+    del K, V, M, c
+    torch.cuda.empty_cache()
+    full = [r for r in res if r[1] == 2329]
+    ap_tok = sum(n for _, n, _, _ in full)
+    ap_ms = sum(x for _, _, x, _ in full)
+    T_end, _, _, dec_last = res[-1]
+    return {"workload": "streaming: 3B head shape, 1-s chunks [2,304 video, 25 audio] appended to %d tokens, a "
+                        "decode after every chunk" % T_end,
+            "chunks": len(res), "append_tokens_per_s_2329": ap_tok / (ap_ms / 1e3),
+            "append_ms_per_2329_chunk": float(np.median([x for _, _, x, _ in full])),
+            "decode_ms_after_append_at_context": [[T, round(d, 4)] for T, _, _, d in res[::8]] + [[T_end,
+                                                                                                  round(dec_last, 4)]],
+            "decode_ms_after_last_append": dec_last, "plain_decode_ms_at_final_length": float(np.median(plain)),
+            "context_tokens_per_s_final": T_end / (float(np.median(plain)) / 1e3),
+            "note": "decode after an append includes the host work split and its upload on the stream"}
+
+
+def streaming_run(args, torch, device, peak):
+    """--workload streaming: the streaming summary as its own JSON line."""
+    s = streaming_summary(args, torch, device, peak)
+    w = make_workload(args)
+    line = {"metric": METRIC, "value": s["context_tokens_per_s_final"], "unit": UNIT, "n_gpus": 1,
+            "steps": 20, "warmup": 5, "ms_per_step": s["plain_decode_ms_at_final_length"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 operands, f32 accumulate",
+            "data": "synthetic", "config": config_of(w, args), "streaming": s}
     print(json.dumps(line))
 
 
-def cpu_baseline_child(args):
-    """Time the CPU oracle, as it stands, on a bounded sample: decode of the
-    (layer 0, kv heads 0..Hkv-1) units of the workload, single-threaded."""
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands (plain numpy, fp64), timed on host cores
+# ---------------------------------------------------------------------------
+
+def cpu_model():
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20)
+        for line in r.stdout.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def _oracle_for_layers(args, layers, R=None, kv=None):
+    """Oracle state of session 0 of the workload for the listed layers (appended in
+    the workload's chunks), the value rotations R (the GPU's, when given) and the
+    inputs kv = (K, V) [T][len(layers)][Hkv][d] (the GPU cache's, when given; else the
+    workload's numpy draw)."""
     from oracle import okvq_oracle as o
     w = make_workload(args)
     sh = w.shape
-    Vc, modc = w.calibration_slice()
-    R = o.calibrate_rotations(Vc, modc, sh.num_modalities)[0].astype(np.float32)
+    if R is None:
+        Vc, modc = w.calibration_slice()
+        R = o.calibrate_rotations(Vc, modc, sh.num_modalities)[0].astype(np.float32)
     oc = o.OracleCache(1, sh.num_layers, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, sh.group_size, sh.bits,
-                       w.max_tokens, w.hadamard_seed, R, layers=[0], key_codec=args.key_codec)
-    K, V = w.session_kv(0, [0])
+                       w.max_tokens, w.hadamard_seed, R, layers=layers, key_codec=args.key_codec)
+    K, V = w.session_kv(0, layers) if kv is None else kv
     mod = w.sessions[0].modality()
     for a, b in w.sessions[0].chunk_bounds():
-        oc.append(0, K[a:b], V[a:b], mod[a:b], layers_in=[0])
+        oc.append(0, K[a:b], V[a:b], mod[a:b], layers_in=layers)
+    return w, oc
+
+
+def _worker(conn, args, layers, R):
+    """One host core: the oracle state of its layers, then full-step decodes on command."""
+    w, oc = _oracle_for_layers(args, layers, R)
+    Q = w.queries(0)
+    conn.send("ready")
+    while True:
+        cmd = conn.recv()
+        if cmd == "stop":
+            break
+        t0 = time.perf_counter()
+        oc.decode(Q)
+        conn.send(time.perf_counter() - t0)
+
+
+def _all_core_steps(args, R, steps, warmup):
+    """Full decode steps of session 0 on every host core: the layers are dealt out
+    to one spawned process per core, each holding its layers' oracle state; a step
+    is all processes decoding their layers, timed from the command to the last
+    answer (wall clock)."""
+    import multiprocessing as mp
+    w = make_workload(args)
+    L = w.shape.num_layers
+    ncores = min(os.cpu_count() or 1, L)
+    ctx = mp.get_context("spawn")
+    procs, conns = [], []
+    for i in range(ncores):
+        a, b = ctx.Pipe()
+        p = ctx.Process(target=_worker, args=(b, args, list(range(i, L, ncores)), R), daemon=True)
+        p.start()
+        procs.append(p)
+        conns.append(a)
+    for c in conns:
+        assert c.recv() == "ready"
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        for c in conns:
+            c.send("step")
+        for c in conns:
+            c.recv()
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    for c in conns:
+        c.send("stop")
+    for p in procs:
+        p.join(timeout=30)
+    return times, ncores
+
+
+def compare_with_oracle(state, oc):
+    """Boundary-code accounting of one GPU-stored layer against the oracle (layer 0,
+    session 0, every kv head): codes whose pre-quantization value lies within 1e-5
+    of a decision threshold are flagged by the oracle; the GPU may pick either side
+    there. Every other code, the statistics and the tail must match bit for bit."""
+    from oracle import okvq_oracle as o
+    r = dict(k_codes=0, k_flagged=0, k_differ_flagged=0, k_differ_strict=0, v_codes=0, v_flagged=0,
+             v_differ_flagged=0, v_differ_strict=0, norms=0, norm_flagged=0, norm_differ_flagged=0,
+             norm_differ_strict=0, stats_equal=True, tail_equal=True)
+    bits = oc.bits
+    for h in range(oc.Hkv):
+        e = oc.units[(0, oc.layers[0], h)].export()
+        for kind in ("k", "v"):
+            g = o.unpack_codes(state[kind + "codes"][h], bits)
+            ref = o.unpack_codes(e[kind + "codes"], bits)
+            bnd = e[kind + "bnd"]
+            d = g != ref
+            r[kind + "_codes"] += int(d.size)
+            r[kind + "_flagged"] += int(bnd.sum())
+            r[kind + "_differ_flagged"] += int((d & bnd).sum())
+            r[kind + "_differ_strict"] += int((d & ~bnd).sum())
+        gn, on = state["vnorm"][h].view(np.uint16), e["vnorm"].view(np.uint16)
+        d = gn != on
+        r["norms"] += int(d.size)
+        r["norm_flagged"] += int(e["nbnd"].sum())
+        r["norm_differ_flagged"] += int((d & e["nbnd"]).sum())
+        r["norm_differ_strict"] += int((d & ~e["nbnd"]).sum())
+        if "kstats" in state:
+            r["stats_equal"] &= bool(np.array_equal(state["kstats"][h].view(np.uint16), e["kstats"].view(np.uint16)))
+            r["tail_equal"] &= bool(np.array_equal(state["ktail"][h].view(np.uint16), e["ktail"].view(np.uint16)))
+    return r
+
+
+def cpu_baseline_child(args):
+    """Time the oracle as it stands on the host cores (no GPU in this process):
+    single-threaded on layer 0 of session 0 (repeated decodes for --cpu-seconds,
+    extrapolated linearly to every layer), then full steps on every core; with
+    --gpu-state, also the boundary-code accounting of the GPU's layer 0."""
+    R = None
+    state = None
+    if args.gpu_state:
+        z = np.load(args.gpu_state)
+        R = z["R"]
+        kv0 = (z["K0"][:, None], z["V0"][:, None])
+        state = {k: z[k] for k in z.files if k not in ("R", "K0", "V0")}
+    w, oc = _oracle_for_layers(args, [0], R, kv0 if state is not None else None)
+    sh = w.shape
     Q = w.queries(0)
     reps, t_total = 0, 0.0
-    budget = args.cpu_seconds
-    while t_total < budget or reps == 0:
+    while t_total < args.cpu_seconds or reps == 0:
         t0 = time.perf_counter()
         oc.decode(Q)
         t_total += time.perf_counter() - t0
@@ -424,53 +651,85 @@ def cpu_baseline_child(args):
         if reps >= args.cpu_max_reps:
             break
     per_sample = t_total / reps
-    units_total = sh.num_layers * sh.num_kv_heads
     T0 = w.sessions[0].length
     T_all = sum(x.length for x in w.sessions)
     step_s = per_sample * sh.num_layers * T_all / T0      # linear in layers and in cached tokens
-    print(json.dumps({"value": T_all / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-                      "sample": "oracle decode of layer 0 of session 0 (%d of %d (layer, kv head) units), %d "
-                                "repetitions, %.1f s of CPU time, extrapolated linearly to all %d layers%s"
-                                % (sh.num_kv_heads, units_total, reps, t_total, sh.num_layers,
-                                   "" if len(w.sessions) == 1 else " and all %d sessions' tokens" % len(w.sessions)),
-                      "step_s": step_s}))
+    res = {"single_core": {"value": T_all / step_s, "unit": UNIT, "cores": 1,
+                           "sample": "oracle decode of layer 0 of session 0 (%d of %d (layer, kv head) units), %d "
+                                     "repetitions, %.1f s of CPU time, extrapolated linearly to all %d layers%s"
+                                     % (sh.num_kv_heads, sh.num_layers * sh.num_kv_heads, reps, t_total,
+                                        sh.num_layers, "" if len(w.sessions) == 1 else
+                                        " and all %d sessions' tokens" % len(w.sessions)),
+                           "step_s_extrapolated": step_s}}
+    if state is not None:
+        res["boundary"] = compare_with_oracle(state, oc)
+    if args.all_cores:
+        times, ncores = _all_core_steps(args, R, args.all_core_steps, 1)
+        st = statistics.median(times)
+        T_s0 = w.sessions[0].length
+        res["all_cores"] = {"value": T_s0 / st, "unit": UNIT, "cores": ncores, "step_s": st,
+                            "steps": len(times),
+                            "sample": "full decode steps of session 0 (%d tokens, all %d layers), layers dealt to %d "
+                                      "spawned processes, one per core, wall clock per step (median of %d)"
+                                      % (T_s0, sh.num_layers, ncores, len(times))
+                                      + ("" if len(w.sessions) == 1 else "; session 0 only")}
+    print(json.dumps(res))
 
 
-def run_cpu_baseline(args):
+def run_cpu_baseline(args, gpu_state=None, all_cores=True, steps=3):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload,
            "--bits", str(getattr(args, "bits", 2)), "--group-size", str(getattr(args, "group_size", 32)),
            "--cpu-seconds", str(args.cpu_seconds), "--cpu-max-reps", str(args.cpu_max_reps),
-           "--key-codec", args.key_codec]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+           "--key-codec", args.key_codec, "--all-core-steps", str(steps)]
+    if all_cores:
+        cmd.append("--all-cores")
+    if gpu_state:
+        cmd += ["--gpu-state", gpu_state]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+        return {"error": "cpu baseline failed: " + r.stderr[-400:]}
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def cpu_baseline_entry(res):
+    """The line's cpu_baseline object: all host cores on full steps when measured,
+    the single-core figure beside it."""
+    model = cpu_model()
+    if "error" in res:
+        return {"value": None, "unit": UNIT, "cores": None, "kind": "oracle", "sample": res["error"]}
+    sc = res["single_core"]
+    ac = res.get("all_cores")
+    head = ac if ac else sc
+    out = {"value": head["value"], "unit": UNIT, "cores": head["cores"], "kind": "oracle", "sample": head["sample"],
+           "cpu_model": model, "nproc": os.cpu_count(), "single_core": sc}
+    if ac:
+        out["all_cores"] = ac
+    return out
+
+
 def reference_arm(args):
+    """--impl reference: the oracle on every host core, timing full decode steps of
+    the workload's session 0 (no extrapolation: every step decodes every layer)."""
     if rank_env()[1] != 0:         # under a multi-rank launch, rank 0 alone times the oracle
         return
-    steps = []
-    base = None
-    for i in range(args.warmup + args.steps):
-        res = run_cpu_baseline(argparse.Namespace(workload=args.workload, bits=args.bits, group_size=args.group_size,
-                                                  cpu_seconds=args.ref_seconds,
-                                                  cpu_max_reps=1, key_codec=args.key_codec))
-        if i >= args.warmup:
-            steps.append(res)
-        base = res
-    vals = [s["value"] for s in steps if s.get("value")]
-    v = statistics.median(vals) if vals else None
+    ns = argparse.Namespace(**vars(args))
+    times, ncores = _all_core_steps(ns, None, args.steps, args.warmup)
     w = make_workload(args)
+    T0 = w.sessions[0].length
+    st = statistics.median(times)
+    v = T0 / st
+    sample = ("full decode steps of session 0 (%d tokens, all %d layers) on %d spawned processes (one per core, "
+              "layers dealt out), wall clock per step, median of %d" % (T0, w.shape.num_layers, ncores, len(times)))
+    if len(w.sessions) > 1:
+        sample += "; session 0 of %d" % len(w.sessions)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": (statistics.median([s["step_s"] for s in steps]) * 1e3) if steps else None,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": st * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, args),
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": base["sample"] if base else None},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": ncores, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model(), "nproc": os.cpu_count()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -490,7 +749,7 @@ def config_of(w, args):
             "l2": "inputs larger than L2: two cache replicas (2 x %.0f MB) alternate between steps"
                   % (algorithmic_bytes(w, [s.length for s in w.sessions], getattr(args, "key_codec", "omni"))[0]
                      / 1e6),
-            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+            "parallelism": "replicas" if getattr(args, "gpus", 1) > 1 else "single GPU"}
 
 
 def main():
@@ -502,13 +761,16 @@ def main():
     ap.add_argument("--workload", default="qwen3b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-reps", type=int, default=1000)
-    ap.add_argument("--ref-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only (no extra configurations)")
     ap.add_argument("--key-codec", default="omni", choices=["omni", "turbo"],
                     help="omni: per-group key ranges (the method); turbo: the TurboQuant comparison codec")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
     ap.add_argument("--group-size", type=int, default=32, choices=[32, 64])
     ap.add_argument("--cpu-baseline-child", action="store_true")
+    ap.add_argument("--all-cores", action="store_true")
+    ap.add_argument("--all-core-steps", type=int, default=3)
+    ap.add_argument("--gpu-state", default=None)
     args = ap.parse_args()
     if args.cpu_baseline_child:
         return cpu_baseline_child(args)
@@ -530,8 +792,8 @@ def main():
         return streaming_run(args, torch, device, peaks()[0])
     w = make_workload(args)
     sh = w.shape
-    caches, append_ms, calib = build_cache(w, torch, device, replicas=2, key_codec=args.key_codec)
-    T = w.sessions[0].length
+    caches, append_ms, calib = build_cache(w, torch, device, replicas=2, key_codec=args.key_codec,
+                                           keep_layer0=not args.no_cpu_baseline)
     lengths = [s.length for s in w.sessions]
     split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths, args.key_codec)
     step_bytes = split_bytes + out_bytes
@@ -539,22 +801,6 @@ def main():
     Q = torch.from_numpy(w.queries(0)).to(device)
     out = torch.empty_like(Q)
     st = torch.cuda.current_stream()
-    for i in range(args.warmup):
-        caches[i % 2].decode(Q, out)
-    torch.cuda.synchronize()
-    # per-kernel split: a separate profiled pass (event records between the two
-    # kernels would keep the merge kernel from overlapping the decode tail)
-    for c in caches:
-        c.profile_enable(True)
-    for i in range(args.steps):
-        caches[i % 2].decode(Q, out)
-    torch.cuda.synchronize()
-    split_ms, merge_ms = [], []
-    for c in caches:
-        a, b = c.profile_read()
-        split_ms += list(a)
-        merge_ms += list(b)
-        c.profile_enable(False)
     sampler = ClockSampler()
     if rank == 0:
         sampler.start()
@@ -562,36 +808,36 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(args.steps):
-        caches[i % 2].decode(Q, out)
-    e1.record(st)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms, split_ms, merge_ms = timed_steps(caches, Q, out, torch, args.steps, args.warmup)
     if world > 1:
         dist.barrier()
 
     # end to end through okvq_decode_host: every step copies the queries from pinned
-    # host memory, decodes and copies the outputs back to pinned host memory
+    # host memory, decodes and delivers the outputs to pinned host memory. Timed two
+    # ways: host wall clock around the calls and a final synchronisation (the line's
+    # value), and CUDA events on the stream (device time only).
     q_host = Q.cpu().pin_memory()
     o_host = torch.empty(Q.shape, dtype=torch.float16).pin_memory()
     for i in range(4):
         caches[i % 2].decode_host(q_host, o_host)
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        caches[i % 2].decode_host(q_host, o_host)
+    torch.cuda.synchronize()
+    e2e_wall_ms = (time.perf_counter() - t0) * 1e3
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(st)
     for i in range(args.steps):
         caches[i % 2].decode_host(q_host, o_host)
     f1.record(st)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
+    e2e_ev_ms = f0.elapsed_time(f1)
     clocks = sampler.stop(local) if rank == 0 else None
 
-    t_max, e2e_max = max_over_ranks([ms, e2e_ms], world, device)
+    t_max, e2e_max, e2e_ev_max = max_over_ranks([ms, e2e_wall_ms, e2e_ev_ms], world, device)
     total_tokens = job_tokens(world, args.steps, lengths)
     value = total_tokens / (t_max / 1e3)
-    e2e_value = total_tokens / (e2e_max / 1e3)
 
     if rank == 0:
         peak, peak_kind = peaks()
@@ -601,18 +847,25 @@ def main():
         ms_step = t_max / args.steps
         ap_ms = sum(x for x, _ in append_ms[0])
         ap_tokens = sum(n for _, n in append_ms[0])
+        # append: reads fp16 K and V, writes codes, norms, statistics; flops of the value
+        # rotation (2 d^2 per token-head) and the key transform; the binding one of the two
         ap_bytes_tok = sh.num_layers * sh.num_kv_heads * (2 * 2 * sh.head_dim + 2 * sh.head_dim * sh.bits // 8 + 2
                                                            + 4 * sh.head_dim / sh.group_size) + 1
+        ap_flops_tok = sh.num_layers * sh.num_kv_heads * (2 * sh.head_dim ** 2 + 10 * sh.head_dim)
+        ap_s = ap_ms / 1e3
+        ap_gbs = ap_tokens * ap_bytes_tok / ap_s / 1e9
+        ap_tfs = ap_tokens * ap_flops_tok / ap_s / 1e12
         traffic = None
         tp = os.path.join(ROOT, "profiles", "decode_traffic.json")
         if os.path.exists(tp):
             with open(tp) as f:
                 tj = json.load(f)
             # DRAM bytes of one decode launch from an ncu capture, valid only while the
-            # kernel sources are the ones that capture measured
+            # decode kernel's sources are the ones that capture measured
             if (tj.get("workload") == args.workload and tj.get("source_sha256") == decode_source_sha256()
                     and args.key_codec == "omni"):
                 traffic = tj.get("bytes_per_launch")
+        tc_peak, tc_kind = tensor_peak()
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -627,24 +880,61 @@ def main():
                          "bytes_per_launch": split_bytes, "avg_launch_ms": avg_split,
                          "merge_kernel_avg_ms": float(np.mean(merge_ms)),
                          "with_R_frac_step": (step_bytes + rot_bytes) / (ms_step / 1e3) / 1e9 / peak},
-            "append": {"tokens_per_s": ap_tokens / (ap_ms / 1e3), "chunks": len(append_ms[0]),
-                       "gbs": ap_tokens * ap_bytes_tok / (ap_ms / 1e3) / 1e9,
-                       "frac": ap_tokens * ap_bytes_tok / (ap_ms / 1e3) / 1e9 / peak},
+            "append": {"tokens_per_s": ap_tokens / ap_s, "chunks": len(append_ms[0]),
+                       "tokens_per_chunk": ap_tokens / max(1, len(append_ms[0])),
+                       "gbs": ap_gbs, "tflops": ap_tfs,
+                       "roofline": {"bound": "hbm" if ap_gbs / peak >= ap_tfs / tc_peak else "tensor",
+                                    "bytes_frac": ap_gbs / peak, "flops_frac": ap_tfs / tc_peak,
+                                    "frac": max(ap_gbs / peak, ap_tfs / tc_peak),
+                                    "flops": "2 d^2 + 10 d per token-head (the value rotation, on the tensor "
+                                             "cores, and the key transform)",
+                                    "flops_peak_tflops": tc_peak, "flops_peak_kind": tc_kind}},
             "calibration": dict(calib, kernel="calib_kernel (value-rotation covariance + Jacobi eigenbasis)"),
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(Q.numel() * 2),
-                    "d2h_bytes_per_step": int(out.numel() * 2),
-                    "how": "okvq_decode_host: pinned-host queries copied in and outputs stored into pinned "
-                           "host memory by the merge kernel, inside the timed region, every step"},
+            "e2e": {"value": total_tokens / (e2e_max / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(Q.numel() * 2),
+                    "d2h_bytes_per_step": int(out.numel() * 2), "ms_per_step_wall": e2e_max / args.steps,
+                    "device_event_value": total_tokens / (e2e_ev_max / 1e3),
+                    "how": "okvq_decode_host: pinned-host queries copied in and outputs stored into pinned host memory "
+                           "by the merge kernel, every step; value = host wall clock around %d calls and a final "
+                           "synchronisation; device_event_value = CUDA events on the stream" % args.steps},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
         }
-        if args.workload == "qwen3b" and sh.bits == 2 and sh.group_size == 32 and args.key_codec == "omni":
-            line["compaction"] = compaction_leg(caches[0], w, torch, Q, out, peak, 10)
-            del caches
-            torch.cuda.empty_cache()
-            line["pseudo_tokens"] = pseudo_leg(torch, device, peak)
+        default = (args.workload == "qwen3b" and sh.bits == 2 and sh.group_size == 32 and args.key_codec == "omni"
+                   and world == 1)
+        gpu_state = None
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = run_cpu_baseline(args)
+            # the GPU-stored state of layer 0 (session 0) and the rotations it used: the
+            # CPU leg compares the oracle's codes with it (boundary-code accounting)
+            st0 = caches[0].export_state(0)
+            fd, gpu_state = tempfile.mkstemp(suffix=".npz")
+            os.close(fd)
+            arrays = {k: np.ascontiguousarray(v[0]) for k, v in st0.items() if k != "mod" and v.ndim >= 2}
+            arrays["R"] = np.asarray(caches[0].rotations_used, np.float32)
+            arrays["K0"], arrays["V0"] = caches[0].layer0_kv
+            np.savez(gpu_state, **arrays)
+        if default:
+            line["compaction"] = compaction_leg(caches[0], w, torch, Q, out, peak, 10)
+        del caches
+        torch.cuda.empty_cache()
+        if default:
+            line["pseudo_tokens"] = pseudo_leg(torch, device, peak)
+            if not args.no_extra:
+                cfg = {}
+                ns = argparse.Namespace(**vars(args))
+                cfg["qwen7b_2bit_g32"] = config_summary(synth.qwen7b(), ns, torch, device, peak, 20, 5)
+                cfg["multisession_2bit_g32"] = config_summary(synth.multisession(), ns, torch, device, peak, 20, 5)
+                cfg["multisession_4bit_g32"] = config_summary(synth.multisession(bits=4), ns, torch, device, peak, 20,
+                                                              5)
+                cfg["streaming"] = streaming_summary(ns, torch, device, peak)
+                line["configs"] = cfg
+        if not args.no_cpu_baseline:
+            res = run_cpu_baseline(args, gpu_state=gpu_state, all_cores=True, steps=3)
+            if gpu_state:
+                os.unlink(gpu_state)
+            line["cpu_baseline"] = cpu_baseline_entry(res)
+            if "boundary" in res:
+                line["boundary_codes"] = dict(res["boundary"], of="layer 0 of session 0, every kv head: GPU state "
+                                              "against the oracle fed the same inputs and rotations")
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

@@ -408,10 +408,6 @@ okvq_status enqueue_decode(okvq_cache *h, const void *q, void *out, cudaStream_t
   a.lut = h->lut;
   a.signs = h->signs;
   a.err = h->err;
-  for (int j = 0; j < 16; ++j) {
-    a.klut_src[j] = h->KG ? h->klev16[j] : h->levels16[j];   // TurboQuant keys use the value levels
-    a.vlut_src[j] = h->levels16[j];
-  }
   CombineArgs cb{};
   cb.partials = partials;
   cb.unit_seg = reinterpret_cast<const int *>(tb + h->off_useg);

@@ -24,11 +24,8 @@
 //   others parked in tensor memory. Evicted tokens (page deletion masks) take no
 //   part in the softmax. Warps merge through tensor memory (the warps of a lane
 //   quarter) and shared memory (the four quarters); one partial (m, l, o_m) per
-//   segment and head goes out.
-// combine_kernel - per (unit, 64 output channels): log-sum-exp merge of the
-//   unit's partials (and of the far-memory partials, if any), then
-//   O = (sum_m R_m^T o_m) / (l sqrt d) on the tensor cores, plus the far-memory
-//   values, fp16 store.
+//   segment and head goes out; the merge kernel (okvq_combine.cu) combines them.
+// lut_kernel - the code-byte -> fp16 level table, built once per cache.
 #include "okvq_device.h"
 
 namespace okvq {
@@ -143,23 +140,6 @@ __device__ __forceinline__ void lut64(const unsigned char *lut, uint32_t off, ui
   b = v.y;
 }
 
-// 2-bit key pair from the register-table layout: `src` holds the pair's two
-// codes at bits s and s+8 (s = 0, 2, 4, 6). Mask it into the mantissa of
-// 2^23 + (x << s) + (y << (s+8)); one fp32 fma turns that into
-// 2^23 + 0x4040 + 0x11*x + 0x1100*y, whose low 16 bits are the byte-permute
-// selector [x, x+4, y, y+4] over the table {lo bytes of the 4 levels, hi bytes}.
-__device__ __forceinline__ uint32_t kreg_pair(uint32_t src, int s, uint32_t lutlo, uint32_t luthi) {
-  constexpr float MUL[4] = {17.0f, 4.25f, 1.0625f, 0.265625f};
-  constexpr float ADD[4] = {-134201280.0f, -27246528.0f, -507840.0f, 6176832.0f};
-  uint32_t t, r;
-  float f;
-  // single lop3 / fma / prmt (the plain C++ form compiles to about twice as many ops)
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(src), "r"(0x0303u << s), "r"(0x4B000000u));
-  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(f) : "f"(__uint_as_float(t)), "f"(MUL[s >> 1]), "f"(ADD[s >> 1]));
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lutlo), "r"(luthi), "r"(__float_as_uint(f)));
-  return r;
-}
-
 // shared-memory table address for code byte `B` (0..3) of word w:
 // byte << 8 | lane part (laneoff holds it in its low byte)
 template <int B>
@@ -206,24 +186,15 @@ __device__ __forceinline__ void value_mma(float (&acc)[8][4], const uint32_t *vw
 // key B fragments of one kb block for one 16-token tile:
 // n-tile 0 (tokens 0-7): (pair 4kb, pair 4kb+2); n-tile 1: (pair 4kb+1, pair 4kb+3)
 template <int BITS>
-__device__ __forceinline__ void key_frags(const uint32_t *kw, int kb, uint32_t lutlo, uint32_t luthi,
-                                          const unsigned char *lut_k, uint32_t laneoff, uint32_t (&bf)[4]) {
+__device__ __forceinline__ void key_frags(const uint32_t *kw, int kb, const unsigned char *lut_k, uint32_t laneoff,
+                                          uint32_t (&bf)[4]) {
   if (BITS == 2) {
-    if ((KREG_WORDS >> (kb >> 1)) & 1u) {
-      uint32_t src = kw[kb >> 1];
-      if (kb & 1) asm("prmt.b32 %0, %1, 0, 0x4432;" : "=r"(src) : "r"(kw[kb >> 1]));
-      bf[0] = kreg_pair(src, 0, lutlo, luthi);
-      bf[1] = kreg_pair(src, 4, lutlo, luthi);
-      bf[2] = kreg_pair(src, 2, lutlo, luthi);
-      bf[3] = kreg_pair(src, 6, lutlo, luthi);
-    } else {
-      // one table entry = one B fragment: (pairs 4kb, 4kb+2), then (4kb+1, 4kb+3)
-      const uint32_t w = kw[kb >> 1];
-      const uint32_t a0 = (kb & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
-      const uint32_t a1 = (kb & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
-      lut64(lut_k, a0, bf[0], bf[1]);
-      lut64(lut_k, a1, bf[2], bf[3]);
-    }
+    // one table entry = one B fragment: (pairs 4kb, 4kb+2), then (4kb+1, 4kb+3)
+    const uint32_t w = kw[kb >> 1];
+    const uint32_t a0 = (kb & 1) ? lut_addr<2>(laneoff, w) : lut_addr<0>(laneoff, w);
+    const uint32_t a1 = (kb & 1) ? lut_addr<3>(laneoff, w) : lut_addr<1>(laneoff, w);
+    lut64(lut_k, a0, bf[0], bf[1]);
+    lut64(lut_k, a1, bf[2], bf[3]);
   } else {
     const uint32_t w = kw[kb];
     bf[0] = lut32(lut_k, lut_addr<0>(laneoff, w));
@@ -240,7 +211,7 @@ struct HalfPageCtx {
   const __half *qraw;        // [8][128] natural order
   const __half *tail;        // this unit's fp16 trailing keys
   const uint8_t *mod;        // this session's modality ids
-  uint32_t laneoff, lutlo, luthi;
+  uint32_t laneoff;
   int T, Tf;
 };
 
@@ -301,7 +272,7 @@ __device__ __forceinline__ void half_page(const HalfPageCtx &c, const PageLayout
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           uint32_t bf[4];
-          key_frags<BITS>(kw[t], kb, c.lutlo, c.luthi, c.lut_k, c.laneoff, bf);
+          key_frags<BITS>(kw[t], kb, c.lut_k, c.laneoff, bf);
           mma16816(sacc[2 * t + 0], afk, bf[0], bf[1]);
           mma16816(sacc[2 * t + 1], afk, bf[2], bf[3]);
         }
@@ -667,15 +638,6 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
 
   const unsigned char *lut_k = lut, *lut_v = lut + 128;
   const uint32_t laneoff = BITS == 2 ? (uint32_t)((lane & 15) << 3) : (uint32_t)(lane << 2);
-  // 4-entry key level table in registers (2-bit register path)
-  uint32_t lutlo = 0, luthi = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t hv = __half_as_ushort(a.klut_src[j]);
-    lutlo |= (hv & 0xFFu) << (8 * j);
-    luthi |= (hv >> 8) << (8 * j);
-  }
-
   int ring_st = 0;          // stage of the next page this warp consumes
   uint32_t ring_par = 0;    // its mbarrier phase parity
   bool wait_failed = false;
@@ -767,8 +729,6 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     hc.tail = tail;
     hc.mod = a.mod + (long long)session * a.cap;
     hc.laneoff = laneoff;
-    hc.lutlo = lutlo;
-    hc.luthi = luthi;
     hc.T = T;
     hc.Tf = Tf;
 
@@ -898,179 +858,6 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   }
 }
 
-// One CTA per (unit, 64 output channels): merge the unit's partials by
-// log-sum-exp (warp w = query head w), then O^T[c][h] = sum_r R^T[c][r] o[h][r] / l
-// on the tensor cores. R^T comes pre-split into fp16 high and residual parts in
-// mma fragment order (one bulk copy per CTA, issued before the wait on the decode
-// grid); o / l is split the same way, and hi*hi + hi*lo + lo*hi carries the
-// product to ~2^-22 relative (fp32 accumulation).
-#ifndef OKVQ_CB_CH
-#define OKVQ_CB_CH 32
-#endif
-constexpr int CB_CH = OKVQ_CB_CH;               // output channels per CTA (32 or 64)
-constexpr int CB_MT = CB_CH / 16;               // m-tiles of 16 channels per CTA
-constexpr int CB_KS = 8 / CB_MT;                // warps sharing an m-tile, each a slice of the k-steps
-constexpr int CB_RED = (CB_KS - 1) * CB_MT * 32 * 4;   // floats of the cross-warp k-slice reduction
-constexpr int OSTRIDE = MAXM * D + 4;           // padded row of the merged o (floats)
-__global__ void __launch_bounds__(256, 1) combine_kernel(const CombineArgs a) {
-  extern __shared__ __align__(128) unsigned char csm[];
-  uint4 *afr = reinterpret_cast<uint4 *>(csm);                                  // [MT][8M][32][2] hi|lo
-  float *osh = reinterpret_cast<float *>(csm + CB_MT * 8 * MAXM * 32 * 32);       // [8][OSTRIDE]
-  float *red = osh + MAXGQ * OSTRIDE;                                             // [KS-1][MT][32][4]
-  float *ofar = red + CB_RED;                                                      // [8][CB_CH] far memory / l
-  __shared__ __align__(8) uint64_t bar;
-  const int unit = blockIdx.x, half = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
-  const int gq = a.Hq / a.Hkv;
-  const int s0 = a.unit_seg[unit], s1 = a.unit_seg[unit + 1];
-  const int lh = unit % (a.L * a.Hkv);
-  const int nks = 8 * a.M;                                // 16-row k-steps over the stacked R_m
-  const uint32_t fbytes = (uint32_t)(CB_MT * nks * 32 * 32);
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    fence_async_smem();
-    bulk_load(afr, a.rot_frag + ((long long)lh * 8 + CB_MT * half) * nks * 32 * 2, fbytes, &bar);
-  }
-  // everything above only reads the rotations; the partials come from the decode grid.
-  // The next decode step may launch as this grid's CTAs retire (it waits for this grid
-  // before it reads or writes anything this one touches).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int nr = a.M * D;
-  if (w < gq) {
-    constexpr int OPER = MAXM * D / 32;
-    float o[OPER];
-#pragma unroll
-    for (int k = 0; k < OPER; ++k) o[k] = 0.f;
-    float L = 0.f;
-    const float *pbase = a.partials + (long long)w * PARTIAL_FLOATS;
-    auto part = [&](int s) { return pbase + (long long)s * MAXGQ * PARTIAL_FLOATS; };
-    // the first two segments' o rows are loaded with the (m, l) pairs: one round
-    // trip to L2 fewer for the common unit of one or two segments
-    float p0[OPER], p1[OPER];
-#pragma unroll
-    for (int k = 0; k < OPER; ++k) {
-      // lane: channels 2 lane + 64 (k / 2) + (k % 2), as 8-byte pairs
-      p0[k] = (s0 < s1 && 64 * (k >> 1) < nr) ? part(s0)[2 + 2 * lane + 64 * (k >> 1) + (k & 1)] : 0.f;
-      p1[k] = (s0 + 1 < s1 && 64 * (k >> 1) < nr) ? part(s0 + 1)[2 + 2 * lane + 64 * (k >> 1) + (k & 1)] : 0.f;
-    }
-    float m0 = -INFINITY, l0 = 0.f;
-    if (s0 + lane < s1) {
-      const float2 ml = *reinterpret_cast<const float2 *>(part(s0 + lane));
-      m0 = ml.x;
-      l0 = ml.y;
-    }
-    float M = m0;
-    for (int s = s0 + 32 + lane; s < s1; s += 32) M = fmaxf(M, part(s)[0]);
-    // far-memory partials of this unit and head: m, l, o[D] in the original value basis
-    const float *fbase = a.far_split ? a.far + ((long long)unit * a.far_split * MAXGQ + w) * FAR_PARTIAL_FLOATS : a.far;
-    auto farp = [&](int f) { return fbase + (long long)f * MAXGQ * FAR_PARTIAL_FLOATS; };
-    for (int f = lane; f < a.far_split; f += 32) M = fmaxf(M, farp(f)[0]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float of[CB_CH / 32] = {};             // channels half * CB_CH + lane (+ 32)
-    for (int f = 0; f < a.far_split; ++f) {
-      const float mf = farp(f)[0];
-      const float wt = mf == -INFINITY ? 0.f : ex2(mf - M);
-      if (lane == 0) L = fmaf(wt, farp(f)[1], L);
-#pragma unroll
-      for (int j = 0; j < CB_CH / 32; ++j) of[j] = fmaf(wt, farp(f)[2 + half * CB_CH + lane + 32 * j], of[j]);
-    }
-    for (int sb = s0; sb < s1; sb += 32) {
-      float wt = 0.f;
-      if (sb + lane < s1) {
-        float m = m0, l = l0;
-        if (sb != s0) {
-          const float2 ml = *reinterpret_cast<const float2 *>(part(sb + lane));
-          m = ml.x;
-          l = ml.y;
-        }
-        wt = m == -INFINITY ? 0.f : ex2(m - M);
-        L = fmaf(wt, l, L);
-      }
-      const int n = min(32, s1 - sb);
-      int j0 = 0;
-      if (sb == s0) {                     // lane 1's weight is 0 (and p1 = 0) without a second segment
-        const float w0 = __shfl_sync(0xffffffffu, wt, 0), w1 = __shfl_sync(0xffffffffu, wt, 1);
-#pragma unroll
-        for (int k = 0; k < OPER; ++k) {
-          o[k] = fmaf(w0, p0[k], o[k]);
-          o[k] = fmaf(w1, p1[k], o[k]);
-        }
-        j0 = 2;
-      }
-#pragma unroll 4
-      for (int j = j0; j < n; ++j) {
-        const float ws = __shfl_sync(0xffffffffu, wt, j);
-        const float *p = part(sb + j) + 2 + lane;
-#pragma unroll
-        for (int k = 0; k < OPER; k += 2)
-          if (64 * (k >> 1) < nr) {
-            const float2 v = *reinterpret_cast<const float2 *>(p + lane + 64 * (k >> 1));
-            o[k] = fmaf(ws, v.x, o[k]);
-            o[k + 1] = fmaf(ws, v.y, o[k + 1]);
-          }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-    for (int k = 0; k < OPER; k += 2)
-      if (64 * (k >> 1) < nr)
-        *reinterpret_cast<float2 *>(osh + w * OSTRIDE + 2 * lane + 64 * (k >> 1)) = make_float2(o[k] * inv, o[k + 1] * inv);
-#pragma unroll
-    for (int j = 0; j < CB_CH / 32; ++j) ofar[w * CB_CH + lane + 32 * j] = of[j] * inv;
-  } else if (w < MAXGQ) {
-    for (int k = lane; k < nr; k += 32) osh[w * OSTRIDE + k] = 0.f;
-#pragma unroll
-    for (int j = 0; j < CB_CH / 32; ++j) ofar[w * CB_CH + lane + 32 * j] = 0.f;
-  }
-  __syncthreads();
-  const bool got = mbar_wait(&bar, 0);
-  if (!got && tid == 0) atomicOr(a.err, ERR_WAIT);
-  // warp w: m-tile w % MT of this CTA's channels, k-step slice w / MT
-  const int mtl = w % CB_MT, kh = w / CB_MT, k0 = kh * (nks / CB_KS), k1 = k0 + nks / CB_KS;
-  float d[4] = {0.f, 0.f, 0.f, 0.f};
-  if (got) {
-    for (int ks = k0; ks < k1; ++ks) {
-      const uint4 ah = afr[((mtl * nks + ks) * 32 + lane) * 2];
-      const uint4 al = afr[((mtl * nks + ks) * 32 + lane) * 2 + 1];
-      const uint32_t Ah[4] = {ah.x, ah.y, ah.z, ah.w}, Al[4] = {al.x, al.y, al.z, al.w};
-      const float2 x01 = *reinterpret_cast<const float2 *>(osh + g * OSTRIDE + 16 * ks + 2 * t4);
-      const float2 x89 = *reinterpret_cast<const float2 *>(osh + g * OSTRIDE + 16 * ks + 2 * t4 + 8);
-      const __half2 h01 = __floats2half2_rn(x01.x, x01.y), h89 = __floats2half2_rn(x89.x, x89.y);
-      const float2 f01 = __half22float2(h01), f89 = __half22float2(h89);
-      const uint32_t bh0 = h2u(h01), bh1 = h2u(h89);
-      const uint32_t bl0 = pack_h2(x01.x - f01.x, x01.y - f01.y), bl1 = pack_h2(x89.x - f89.x, x89.y - f89.y);
-      mma16816(d, Ah, bh0, bh1);
-      mma16816(d, Ah, bl0, bl1);
-      mma16816(d, Al, bh0, bh1);
-    }
-  }
-  if (kh > 0)
-    *reinterpret_cast<float4 *>(red + (((kh - 1) * CB_MT + mtl) * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
-  __syncthreads();
-  if (kh == 0 && got) {
-    float y[4] = {d[0], d[1], d[2], d[3]};
-#pragma unroll
-    for (int k = 1; k < CB_KS; ++k) {
-      const float4 e = *reinterpret_cast<const float4 *>(red + (((k - 1) * CB_MT + mtl) * 32 + lane) * 4);
-      y[0] += e.x; y[1] += e.y; y[2] += e.z; y[3] += e.w;
-    }
-    const int session = unit / (a.L * a.Hkv);
-    const int layer = lh / a.Hkv, kvh = lh % a.Hkv;
-    __half *ob = a.out + (((long long)session * a.L + layer) * a.Hq + kvh * gq) * D;
-    const int c = half * CB_CH + 16 * mtl + g;
-#pragma unroll
-    for (int e2 = 0; e2 < 4; ++e2) {
-      const int h = 2 * t4 + (e2 & 1), cc = c + 8 * (e2 >> 1);
-      if (h < gq) ob[h * D + cc] = __float2half_rn(fmaf(y[e2], INV_SQRT_D, ofar[h * CB_CH + cc - half * CB_CH]));
-    }
-  }
-}
-
 template <int BITS, int G>
 cudaError_t launch_decode_t(const DecodeArgs &a, int n_cta, cudaStream_t s) {
   static std::atomic<uint64_t> attr_done{0};
@@ -1119,30 +906,6 @@ cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s) {
   if (a.bits == 2 && a.G == 64) return launch_decode_t<2, 64>(a, n_cta, s);
   if (a.bits == 4 && a.G == 32) return launch_decode_t<4, 32>(a, n_cta, s);
   return launch_decode_t<4, 64>(a, n_cta, s);
-}
-
-cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
-  if (a.units <= 0) return cudaSuccess;
-  static std::atomic<uint64_t> attr_done{0};
-  const size_t smem = (size_t)CB_MT * 8 * MAXM * 32 * 32 + (MAXGQ * OSTRIDE + CB_RED + MAXGQ * CB_CH) * sizeof(float);
-  cudaError_t ea = once_per_device(attr_done, [&] {
-    cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    // same shared/L1 split as the decode kernel: no reconfiguration between the two
-    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  });
-  if (ea != cudaSuccess) return ea;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.units, D / CB_CH);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace okvq

@@ -28,14 +28,9 @@
 //   4-bit: 8*j + 4*e (pair j = byte j).
 //   2-bit V: 4*j + 2*e (pair j = nibble j); a byte holds two pairs and indexes
 //        the shared-memory level table.
-//   2-bit K words not in KREG_WORDS (table layout): pair j = 8*i + r of word i
-//        sits in byte 2*(r/4) + (r&1), nibble (r/2)&1, so the two pairs of one
-//        table entry are exactly one score-MMA B fragment (pairs 4kb and 4kb+2,
-//        or 4kb+1 and 4kb+3).
-//   2-bit K words in KREG_WORDS (register table path): word i = j/8 holds pairs
-//        q = j%8 with code e at bit 16*(q/4) + 2*(q%4) + 8*e, so one mask picks a
-//        pair as two 2-bit fields 8 bits apart, ready to become a byte-permute
-//        selector.
+//   2-bit K: pair j = 8*i + r of word i sits in byte 2*(r/4) + (r&1), nibble
+//        (r/2)&1, so the two pairs of one table entry are exactly one score-MMA
+//        B fragment (pairs 4kb and 4kb+2, or 4kb+1 and 4kb+3).
 //
 // Stat channel order: position p = 32*(kb/2) + 8*t + 4*(kb%2) + i (t = 0..3,
 // kb = 0..7, i = 0..3) holds channel 16*kb + 2*t + (i&1) + 8*(i>>1): the 8
@@ -100,13 +95,9 @@ __host__ __device__ inline void v_pair_coords(int lane, int j, int e, int &tok, 
   tok = 2 * (lane & 3) + 8 * (reg >> 1) + e;
   ch = 16 * blk + (lane >> 2) + 8 * (reg & 1);
 }
-// 2-bit K chunk words that use the register table layout (bit w = word w)
-constexpr unsigned KREG_WORDS = 0x0u;
-
 __host__ __device__ inline int k_code_bit(int bits, int j, int e) {
   if (bits == 4) return 8 * j + 4 * e;
   const int word = j >> 3, r = j & 7;
-  if ((KREG_WORDS >> word) & 1u) return 32 * word + 16 * (r >> 2) + 2 * (r & 3) + 8 * e;
   return 32 * word + 8 * (2 * (r >> 2) + (r & 1)) + 4 * ((r >> 1) & 1) + 2 * e;
 }
 __host__ __device__ inline int v_code_bit(int bits, int j, int e) { return bits == 4 ? 8 * j + 4 * e : 4 * j + 2 * e; }
@@ -117,10 +108,6 @@ __host__ __device__ inline void chunk_code_at(int kind, int bits, int wi, int b,
   if (bits == 4) {
     j = (32 * wi + b) >> 3;
     e = (b >> 2) & 1;
-  } else if (kind == 0 && ((KREG_WORDS >> wi) & 1u)) {
-    const int half = b >> 4, bb = b & 15;
-    e = bb >> 3;
-    j = 8 * wi + 4 * half + ((bb & 7) >> 1);
   } else if (kind == 0) {
     const int byte = b >> 3, nib = (b >> 2) & 1;
     e = (b >> 1) & 1;
@@ -180,8 +167,6 @@ struct DecodeArgs {
   const unsigned char *lut; // [256 code bytes][K 128 B | V 128 B] level table, built by launch_lut
   const float *signs;       // [D] +-1
   uint32_t *err;
-  __half klut_src[16];      // key levels lambda_j (fp16)
-  __half vlut_src[16];      // value levels l_j (fp16)
 };
 
 // The decode kernel's code-byte -> fp16 level table (64 KB), built once per cache.
