@@ -115,6 +115,31 @@ def test_multisession_full_length_mix_sampled_sessions():
     assert c.check_errors() == 0
 
 
+@pytest.mark.parametrize("bits,G", [(2, 64), (4, 32), (4, 64)])
+def test_multisession_full_length_mix_variants(bits, G):
+    """The 64-session configuration's other code widths and group sizes with the full
+    4 K-64 K length mix (1 layer): the oracle recomputes the shortest and the longest
+    session and one in between, state bit for bit and outputs within tolerance."""
+    import torch
+    w = synth.multisession(layers=1, bits=bits, group_size=G)
+    lens = [x.length for x in w.sessions]
+    pick = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17})
+    oc, R = pu.oracle_cache(w, sessions=pick)
+    pu.feed_oracle(oc, w, sessions=pick)
+    c = pu.gpu_cache(w, R=R)
+    assert c.check_errors() == 0
+    for s in pick:
+        st = c.export_state(s)
+        pu.assert_state_matches(pu.compare_state(st, oc, s, oc.layers, w.shape.bits))
+        pu.adopt_boundary_choices(st, oc, s, oc.layers)
+    for step in (0, 1):
+        Q = w.queries(step)
+        out = c.decode(torch.from_numpy(Q).cuda()).cpu().numpy()
+        ref = oc.decode(Q)
+        pu.assert_outputs_close(out[pick], ref[pick], "sampled sessions, step %d" % step)
+    assert c.check_errors() == 0
+
+
 def test_qwen7b_shape_seven_heads_per_kv():
     w = synth.qwen7b(seed=41, tokens=3000, layers=2)
     _full_check(w, steps=(0,))
