@@ -61,6 +61,8 @@ struct okvq_cache {
   unsigned char *lut = nullptr;                        // decode level table (LEVEL_TABLE_BYTES)
   __half *q_stage[2] = {}, *out_stage = nullptr;       // device staging of okvq_decode_host
   cudaStream_t copy_stream = nullptr;                  // uploads of okvq_decode_host
+  cudaStream_t key_stream = nullptr;                   // the append's key grid, forked from the caller's stream
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaEvent_t ev_in[2] = {}, ev_used[2] = {};          // upload done / staging slot released
   int host_calls = 0;
   const void *dev_ok[8] = {};                          // device pointers already validated
@@ -165,6 +167,9 @@ void release(okvq_cache *h) {
     if (h->ev_used[b]) cudaEventDestroy(h->ev_used[b]);
   }
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+  if (h->key_stream) cudaStreamDestroy(h->key_stream);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
   for (int b = 0; b < 2; ++b) {
     if (h->host_table[b]) cudaFreeHost(h->host_table[b]);
     if (h->table_ev[b]) cudaEventDestroy(h->table_ev[b]);
@@ -598,6 +603,9 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   }
   if ((st = alloc_dev((void **)&h->out_stage, qo_bytes)) != OKVQ_OK) return fail(st);
   if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaStreamCreateWithFlags(&h->key_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
+  if (cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
   // far memory: every unit's pseudo tokens split so that the far grid covers the SMs once
   h->far_nsplit = (int)std::max<long long>(1, (long long)h->num_sms / h->units);
   if ((st = alloc_dev((void **)&h->far_partials,
@@ -747,7 +755,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   }
   const long long last = (T0 + num_tokens - 1) / PAGE;
   const int n_pages = (int)(last - a.page0 + 1);
-  cudaError_t e = launch_append(a, n_pages, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_append(a, n_pages, static_cast<cudaStream_t>(stream), h->key_stream, h->ev_fork, h->ev_join);
   if (e != cudaSuccess) return cuda_status(e);
   h->len[session] = T0 + num_tokens;
   h->tail_sel[session] ^= 1;

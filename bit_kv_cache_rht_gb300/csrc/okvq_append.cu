@@ -25,22 +25,22 @@ constexpr float SQRT_D = 11.3137084989847603904f;
 
 constexpr int ROW_H = ROT_ROW_H;           // padded fp16 row: ldmatrix row reads hit distinct banks
 
-struct Smem {
-  union {
-    struct {
-      __half rh[D][ROW_H];         // one part (fp16 high, then residual) of R_m, [output][channel]
-      __half vh[PAGE][ROW_H];      // the page's values, fp16 [token][channel]
-    } v;
-    float xt[PAGE * D];            // then: keys [token][c] (rotated, fp32)
-  } u;
+// Shared memory of the value role: one part of R_m, the page's values, their codes.
+struct ValueSmem {
+  __half rh[D][ROW_H];             // one part (fp16 high, then residual) of R_m, [output][channel]
+  __half vh[PAGE][ROW_H];          // the page's values, fp16 [token][channel]
   uint64_t bar;                    // completion of the bulk copy of rh
   uint8_t vc[PAGE * D];            // value codes of the page
-  uint8_t kc[PAGE * D];            // key codes of the page
   float vnorm[PAGE];
   int mod[PAGE];
+  int present[MAXM];
+};
+// Shared memory of the key role: rotated keys, their codes and group statistics.
+struct KeySmem {
+  float xt[PAGE * D];              // keys [token][c] (rotated, fp32)
+  uint8_t kc[PAGE * D];            // key codes of the page
   float kmn[2][D], kmx[2][D];     // group min and range (fp16 values held as fp32)
   float red[2][2][D];              // per-half min / max of a group
-  int present[MAXM];
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -149,11 +149,14 @@ __device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int ke
   }
 }
 
-template <int BITS>
+// ROLE 0: the values of the new tokens (modality ids, norms, rotation, codes) and
+// the page's tile masks; ROLE 1: the keys (groups that complete now, or every new
+// token for TurboQuant keys) and the new fp16 tail. The two write disjoint parts of
+// a page and read nothing the other writes, so they run as two concurrent grids.
+template <int BITS, int ROLE>
 __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   constexpr int NTHR = (1 << BITS) - 1;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Smem &S = *reinterpret_cast<Smem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const PageLayout PL = page_layout(BITS, a.G);
 
@@ -167,6 +170,8 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   const int row_stride = a.L * a.Hkv * D;          // between tokens in the input
   uint8_t *pg = a.pages + (unit * a.P_max + page) * (long long)PL.page_bytes;
 
+  if constexpr (ROLE == 0) {
+  ValueSmem &S = *reinterpret_cast<ValueSmem *>(smem_raw);
   // ---- modality ids of the new tokens (validated) ----
   for (int t = tid; t < PAGE; t += THREADS) {
     int m = 0;
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   for (int j = 0; j < VPW; ++j) {
     const int t = warp + j * (THREADS / 32);
     if (t < ta || t >= tb) continue;               // warp-uniform
-    *reinterpret_cast<uint2 *>(&S.u.v.vh[t][4 * lane]) = vraw[j];
+    *reinterpret_cast<uint2 *>(&S.vh[t][4 * lane]) = vraw[j];
     const float2 x01 = __half22float2(*reinterpret_cast<const __half2 *>(&vraw[j].x));
     const float2 x23 = __half22float2(*reinterpret_cast<const __half2 *>(&vraw[j].y));
     float ss = x01.x * x01.x;
@@ -253,9 +258,9 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
     float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const uint32_t va = smem_addr(&S.u.v.vh[16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+    const uint32_t va = smem_addr(&S.vh[16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
     const int bj = lane >> 3;                      // ldmatrix matrix: output block (nt, nt + 1) x channel half
-    const uint32_t rb = smem_addr(&S.u.v.rh[o0 + 8 * (bj >> 1) + (lane & 7)][8 * (bj & 1)]);
+    const uint32_t rb = smem_addr(&S.rh[o0 + 8 * (bj >> 1) + (lane & 7)][8 * (bj & 1)]);
     // the high part, then the residual, staged in turn (one part of shared memory:
     // three CTAs fit on an SM); the products accumulate in fp32 across both passes
 #pragma unroll 1
@@ -263,12 +268,12 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       if (tid == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar)),
-                     "r"((uint32_t)sizeof(S.u.v.rh))
+                     "r"((uint32_t)sizeof(S.rh))
                      : "memory");
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                smem_addr(&S.u.v.rh[0][0])),
-            "l"(a.rot_h + (((long long)lh * a.M + m) * 2 + part) * (D * ROW_H)), "r"((uint32_t)sizeof(S.u.v.rh)),
+                smem_addr(&S.rh[0][0])),
+            "l"(a.rot_h + (((long long)lh * a.M + m) * 2 + part) * (D * ROW_H)), "r"((uint32_t)sizeof(S.rh)),
             "r"(smem_addr(&S.bar))
             : "memory");
       }
@@ -313,11 +318,11 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
   // write the value tiles that got new tokens
   for (int tile = ta / TILE; tile * TILE < tb; ++tile)
     pack_tile<BITS, 1>(S.vc, pg + PL.off_v + tile * PL.tile_bytes, tile, tb, tid, THREADS);
-
+  } else {
+  KeySmem &S = *reinterpret_cast<KeySmem *>(smem_raw);
   if (a.G == 0) {
     // ---- TurboQuant keys (section 2, TurboQuant bullet): every new token now, like a
     // value with the shared Hadamard rotation: n = |k|, w = sqrt(d) k'/n, value levels ----
-    __syncthreads();
     // keep the codes of older tokens that share a 16-token tile with the first new token
     if (ta % TILE != 0) unpack_tile<BITS, 0>(S.kc, pg + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid, THREADS);
     for (int t = ta + warp; t < tb; t += THREADS / 32) {
@@ -346,13 +351,13 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
 
   // ---- keys: groups that complete with this chunk, all of the page's at once ----
   const int G = a.G;
-  float *xk = S.u.xt;             // keys as [token][c], row stride D (the value staging is free now)
-  __syncthreads();
+  float *xk = S.xt;               // keys as [token][c], row stride D
   uint32_t gmask = 0;             // bit gi: group gi of the page completes now
   for (int g0 = 0; g0 < PAGE; g0 += G) {
     const long long gend = P0 + g0 + G;
     if (gend > T0 && gend <= T1) gmask |= 1u << (g0 / G);
   }
+  if (!gmask && blockIdx.x != gridDim.x - 1) return;   // nothing for this CTA
   if (gmask) {
     const __half *told = a.tail_old + unit * (long long)G * D;
     // rotate every member: warp per token (8 tokens per warp, loads issued first),
@@ -448,26 +453,44 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const AppendArgs a) {
       tnew[r * D + c] = v;
     }
   }
+  }
+}
+
+template <int BITS, int ROLE>
+cudaError_t set_append_attrs() {
+  const int smem = ROLE == 0 ? (int)sizeof(ValueSmem) : (int)sizeof(KeySmem);
+  cudaError_t r = cudaFuncSetAttribute(append_kernel<BITS, ROLE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<BITS, ROLE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  return r;
 }
 
 }  // namespace
 
-cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s) {
+// The value grid runs on `s`; the key grid on `aux`, forked from `s` before the
+// value grid and joined back into `s` after it, so the two overlap on the device and
+// everything issued on `s` afterwards sees both.
+cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s, cudaStream_t aux, cudaEvent_t fork,
+                          cudaEvent_t join) {
   static std::atomic<uint64_t> attr_done{0};
-  const size_t smem = sizeof(Smem);
   cudaError_t e = once_per_device(attr_done, [&] {
-    // ~73 KB of shared memory: three CTAs per SM with the largest shared-memory carveout
-    cudaError_t r = cudaFuncSetAttribute(append_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (r == cudaSuccess) r = cudaFuncSetAttribute(append_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaError_t r = set_append_attrs<2, 0>();
+    if (r == cudaSuccess) r = set_append_attrs<2, 1>();
+    if (r == cudaSuccess) r = set_append_attrs<4, 0>();
+    if (r == cudaSuccess) r = set_append_attrs<4, 1>();
     return r;
   });
   if (e != cudaSuccess) return e;
-  dim3 grid(n_pages, a.L * a.Hkv);
-  if (a.bits == 2) append_kernel<2><<<grid, THREADS, smem, s>>>(a);
-  else append_kernel<4><<<grid, THREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  const dim3 grid(n_pages, a.L * a.Hkv);
+  if ((e = cudaEventRecord(fork, s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(aux, fork, 0)) != cudaSuccess) return e;
+  if (a.bits == 2) append_kernel<2, 1><<<grid, THREADS, sizeof(KeySmem), aux>>>(a);
+  else append_kernel<4, 1><<<grid, THREADS, sizeof(KeySmem), aux>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.bits == 2) append_kernel<2, 0><<<grid, THREADS, sizeof(ValueSmem), s>>>(a);
+  else append_kernel<4, 0><<<grid, THREADS, sizeof(ValueSmem), s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(join, aux)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(s, join, 0);
 }
 
 }  // namespace okvq

@@ -266,7 +266,8 @@ cudaError_t once_per_device(std::atomic<uint64_t> &done, Fn set) {
   return e;
 }
 
-cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s, cudaStream_t aux, cudaEvent_t fork,
+                          cudaEvent_t join);
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_lut(int bits, const LutArgs &a, cudaStream_t s);
