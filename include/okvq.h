@@ -120,7 +120,11 @@ void okvq_free(okvq_cache *h);
  *             device: a bad id sets the error word and is stored as modality 0)
  * Shapes and capacity are checked on the host before any launch
  * (OKVQ_EINVAL / OKVQ_ECAPACITY, state unchanged). num_tokens == 0 is a no-op.
- * One kernel launch, asynchronous on `stream`. */
+ * Two kernel grids, asynchronous: the values on `stream`, the keys on a stream
+ * owned by the handle that waits for `stream` before it starts (an event) and
+ * that `stream` waits for afterwards (another event), so work issued on `stream`
+ * after the call sees the whole append. Appends of one handle must be ordered
+ * (one host thread). */
 okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, const void *v,
                               const uint8_t *modality, int32_t num_tokens, void *stream);
 
