@@ -24,7 +24,7 @@ struct okvq_cache {
   __half *tails = nullptr;      // [2][units][G][D]
   uint8_t *mod = nullptr;       // [S][cap]
   uint32_t *rot_frag = nullptr; // R^T in mma fragment order, fp16 high and residual (see CombineArgs)
-  __half *rot_h = nullptr;      // [L*Hkv*M][2][D][ROT_ROW_H] fp16 high / residual parts of R (append)
+  __half *rot_h = nullptr;      // [L*Hkv*M][2][D*D] fp16 high / residual parts of R, tensor-core layout (append)
   float *signs = nullptr;       // [D]
   uint32_t *err = nullptr;
   float *partials = nullptr;
@@ -588,7 +588,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   if ((st = alloc_dev((void **)&h->tails, tails)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->mod, (size_t)h->S * h->cap)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->rot_frag, rot)) != OKVQ_OK) return fail(st);
-  const size_t rot_h_bytes = (size_t)h->L * h->Hkv * h->M * 2 * D * ROT_ROW_H * sizeof(__half);
+  const size_t rot_h_bytes = (size_t)h->L * h->Hkv * h->M * 2 * D * D * sizeof(__half);
   if ((st = alloc_dev((void **)&h->rot_h, rot_h_bytes)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->signs, D * sizeof(float))) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->err, sizeof(uint32_t))) != OKVQ_OK) return fail(st);
@@ -656,17 +656,18 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   }
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
-    // R as fp16 high + residual parts, rows padded (the append kernel's tensor-core rotation)
-    std::vector<__half> rh(nmat * 2 * D * ROT_ROW_H, __float2half_rn(0.f));
+    // R as fp16 high + residual parts in the tensor core's K-major layout (the
+    // append kernel's A operand, rows = output channels)
+    std::vector<__half> rh(nmat * 2 * D * D);
     for (size_t mtx = 0; mtx < nmat; ++mtx) {
       const float *R = c.value_rot + mtx * D * D;
-      __half *H = rh.data() + mtx * 2 * D * ROT_ROW_H;
+      __half *H = rh.data() + mtx * 2 * D * D;
       for (int i = 0; i < D; ++i)
         for (int cc = 0; cc < D; ++cc) {
           const float v = R[i * D + cc];
           const __half hi = __float2half_rn(v);
-          H[i * ROT_ROW_H + cc] = hi;
-          H[(D + i) * ROT_ROW_H + cc] = __float2half_rn(v - __half2float(hi));
+          H[kmajor_off(i, cc)] = hi;
+          H[D * D + kmajor_off(i, cc)] = __float2half_rn(v - __half2float(hi));
         }
     }
     // R^T as m16n8k16 A fragments: m-tile mt (16 output channels), k-step ks (16 rows
@@ -723,6 +724,7 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   if (!h || session < 0 || session >= h->S || num_tokens < 0) return OKVQ_EINVAL;
   if (num_tokens == 0) return OKVQ_OK;
   if (!device_ptr(h, k) || !device_ptr(h, v) || !device_ptr(h, modality)) return OKVQ_EINVAL;
+  if (!aligned16(k) || !aligned16(v)) return OKVQ_EINVAL;
   const long long T0 = h->len[session];
   if (T0 + num_tokens > h->max_tokens) return OKVQ_ECAPACITY;
   AppendArgs a{};
@@ -755,6 +757,11 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   }
   const long long last = (T0 + num_tokens - 1) / PAGE;
   const int n_pages = (int)(last - a.page0 + 1);
+  // value CTAs: about two per SM (each holds R_m, ~97 KB of shared memory), at most
+  // V_MAX_PPC pages each
+  const int upl = h->L * h->Hkv;
+  const int cpu = std::max(1, std::min(n_pages, 2 * h->num_sms / std::max(1, upl)));
+  a.vppc = std::min(V_MAX_PPC, (n_pages + cpu - 1) / cpu);
   cudaError_t e = launch_append(a, n_pages, static_cast<cudaStream_t>(stream), h->key_stream, h->ev_fork, h->ev_join);
   if (e != cudaSuccess) return cuda_status(e);
   h->len[session] = T0 + num_tokens;
