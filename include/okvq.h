@@ -115,10 +115,11 @@ void okvq_free(okvq_cache *h);
 
 /* Append num_tokens tokens to `session` (section 2: values are quantized at
  * once; each key group is quantized when its last token arrives).
- *   k, v      device fp16 [num_tokens][num_layers][num_kv_heads][128], token-major
+ *   k, v      device fp16 [num_tokens][num_layers][num_kv_heads][128], token-major,
+ *             16-byte aligned (the value rows are copied in 16-byte pieces)
  *   modality  device uint8 [num_tokens], each < num_modalities (checked on the
  *             device: a bad id sets the error word and is stored as modality 0)
- * Shapes and capacity are checked on the host before any launch
+ * Shapes, alignment and capacity are checked on the host before any launch
  * (OKVQ_EINVAL / OKVQ_ECAPACITY, state unchanged). num_tokens == 0 is a no-op.
  * Two kernel grids, asynchronous: the values on `stream`, the keys on a stream
  * owned by the handle that waits for `stream` before it starts (an event) and
