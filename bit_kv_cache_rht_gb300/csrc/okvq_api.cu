@@ -24,7 +24,7 @@ struct okvq_cache {
   __half *tails = nullptr;      // [2][units][G][D]
   uint8_t *mod = nullptr;       // [S][cap]
   uint32_t *rot_frag = nullptr; // R^T in mma fragment order, fp16 high and residual (see CombineArgs)
-  __half *rot_h = nullptr;      // [L*Hkv*M][2][D*D] fp16 high / residual parts of R, tensor-core layout (append)
+  __half *rot_h = nullptr;      // [L*Hkv*M][2][D][D] fp16 high / residual parts of R (append)
   float *signs = nullptr;       // [D]
   uint32_t *err = nullptr;
   float *partials = nullptr;
@@ -656,8 +656,8 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
   }
   {
     const size_t nmat = (size_t)h->L * h->Hkv * h->M;
-    // R as fp16 high + residual parts in the tensor core's K-major layout (the
-    // append kernel's A operand, rows = output channels)
+    // R as fp16 high + residual parts, row-major [output][channel] (the append
+    // kernel's tensor-memory A operand: row o to lane o)
     std::vector<__half> rh(nmat * 2 * D * D);
     for (size_t mtx = 0; mtx < nmat; ++mtx) {
       const float *R = c.value_rot + mtx * D * D;
@@ -666,8 +666,8 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
         for (int cc = 0; cc < D; ++cc) {
           const float v = R[i * D + cc];
           const __half hi = __float2half_rn(v);
-          H[kmajor_off(i, cc)] = hi;
-          H[D * D + kmajor_off(i, cc)] = __float2half_rn(v - __half2float(hi));
+          H[i * D + cc] = hi;
+          H[D * D + i * D + cc] = __float2half_rn(v - __half2float(hi));
         }
     }
     // R^T as m16n8k16 A fragments: m-tile mt (16 output channels), k-step ks (16 rows
@@ -757,10 +757,10 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   }
   const long long last = (T0 + num_tokens - 1) / PAGE;
   const int n_pages = (int)(last - a.page0 + 1);
-  // value CTAs: about two per SM (each holds R_m, ~97 KB of shared memory), at most
-  // V_MAX_PPC pages each
+  // value CTAs: about one per SM (the key CTAs of the chunk share the SMs with them),
+  // at most V_MAX_PPC pages each
   const int upl = h->L * h->Hkv;
-  const int cpu = std::max(1, std::min(n_pages, 2 * h->num_sms / std::max(1, upl)));
+  const int cpu = std::max(1, std::min(n_pages, h->num_sms / std::max(1, upl)));
   a.vppc = std::min(V_MAX_PPC, (n_pages + cpu - 1) / cpu);
   cudaError_t e = launch_append(a, n_pages, static_cast<cudaStream_t>(stream), h->key_stream, h->ev_fork, h->ev_join);
   if (e != cudaSuccess) return cuda_status(e);

@@ -21,6 +21,8 @@
 //     quantized by the CTA whose page holds it when its last token arrives,
 //     reading earlier members from the fp16 tail buffer; the CTA owning the last
 //     touched page writes the new fp16 tail into the other tail buffer.
+#include <cuda.h>
+
 #include "okvq_internal.h"
 
 namespace okvq {
@@ -130,43 +132,41 @@ __device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int ke
 // ---------------------------------------------------------------------------
 // Values: w = sqrt(d) R_m v / |v| on the 5th-generation tensor cores, then codes
 // ---------------------------------------------------------------------------
-constexpr int VTHREADS = 128;              // epilogue: thread o = output channel o = tensor-memory lane o
-constexpr uint32_t V_TMEM_COLS = 64;       // the accumulator: one fp32 column per token of a page
+constexpr int VTHREADS = 256;              // 8 warps: warp w reads accumulator lanes 32 (w % 4) .., tokens 32 (w / 4) ..
+constexpr uint32_t V_TMEM_COLS = 256;      // two accumulators of 64 fp32 columns, then R_m (2 x 64 columns of fp16 pairs)
+constexpr uint32_t V_TMEM_R = 128;         // first column of R_m: high part, then residual
+constexpr int V_NBUF = 3;                  // pages in flight
 constexpr int V_MAX_ROUNDS = V_MAX_PPC * MAXM;
+constexpr int V_HALF_BYTES = PAGE * 64 * 2;    // one 64-channel half of a page: 64 rows of 128 B
 
-// Shared memory of the value kernel. R_m and a page's values use the K-major
-// layout without swizzle (kmajor_off): core matrices of 8 rows x 8 channels.
+// Shared memory of the value kernel (1024-byte aligned: the pages use the 128-byte
+// swizzle, whose pattern repeats every 8 rows of 128 B).
 struct ValueSmem {
-  __half r[2][D * D];              // R_m, fp16 high part then residual; rows = output channels
-  __half v[2][PAGE * D];           // values of a page (two buffers); rows = tokens
-  float sc[PAGE];                  // sqrt(d) / |v| of the current round's tokens (0: zero vector)
+  __half v[V_NBUF][PAGE * D];      // pages as the TMA writes them: two halves [64 tokens][64 channels], swizzled
+  float sc[2][PAGE];               // sqrt(d) / |v| of a round's tokens (0: zero vector)
   uint8_t mod[V_MAX_PPC * PAGE];   // modality of each new token of the run, 0xff for the others
   uint8_t rpage[V_MAX_ROUNDS];     // rounds: (page of the run, modality)
   uint8_t rmod[V_MAX_ROUNDS];
   int pm[V_MAX_PPC];               // modalities present among a page's new tokens
-  uint32_t mmask[2];               // tokens of the current round
+  uint32_t mmask[2][2];            // a round's tokens
   int nround;
   uint32_t tmem;
-  uint64_t bar_r, bar_mma;
+  uint64_t bar_v[V_NBUF], bar_mma[2];
 };
+constexpr size_t V_SMEM_BYTES = sizeof(ValueSmem) + 1024;   // + alignment slack
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Shared-memory matrix descriptor of a K-major operand without swizzle: core
-// matrices adjacent along K 128 B apart, along M/N 2 KB apart (kmajor_off).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(2048u >> 4) << 32) |
-         (1ull << 46);
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte swizzle:
+// rows of 64 fp16 (128 B), 8-row groups 1024 B apart; a K step of 16 inside the
+// 64-channel span advances the start by 32 B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
 
-// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes
+// 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
   asm volatile(
@@ -179,6 +179,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
       : "r"(taddr));
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
 
 // Bits of one V-layout chunk word (lane group t4) that belong to tokens below
@@ -197,25 +207,29 @@ __device__ __forceinline__ uint32_t v_keep_mask(int t4, int keep_end) {
   return m;
 }
 
-// One CTA per (run of a.vppc touched pages, layer * Hkv + kv head). A round is one
-// (page, modality) pair: the page's new tokens of that modality are copied into
-// shared memory (the next round's while this one computes), their norms taken,
-// and one thread issues D[o][t] = sum_c (R_hi[o][c] + R_lo[o][c]) v[t][c] (16 MMAs,
-// M = 128, N = 64, K = 16, fp32 accumulation in tensor memory). The thread of
-// lane o then quantizes w = D[o][t] * sqrt(d) / |v_t| for the round's tokens.
+// One CTA per (run of a.vppc touched pages, layer * Hkv + kv head). Pages arrive by
+// TMA (two 64-channel boxes each, 128-byte swizzle, three pages ahead); R_m sits in
+// tensor memory (row o = lane o, fp16 pairs). A round is one (page, modality) pair:
+// one thread issues D[o][t] = sum_c (R_hi[o][c] + R_lo[o][c]) v[t][c] (16 MMAs,
+// M = 128, N = 64, K = 16, A from tensor memory, B from shared memory, fp32
+// accumulation in tensor memory) and the round's norms are taken meanwhile. The
+// MMAs of round r + 1 run while the warps quantize round r from the other
+// accumulator: w = D[o][t] * sqrt(d) / |v_t| against the value thresholds.
 //
-// Packing: thread o = 32 w + 8 i + g holds channel o of every token; in the V
-// layout channel o of decode lane (g, t4) sits in chunk word w (2-bit) or
-// 2 w + i/2 (4-bit), at a bit offset set by i, the token's half and parity. The
-// four (2-bit) or two (4-bit) threads that share a word are lanes g + 8 i of one
-// warp, so two (one) xor-shuffles complete it.
+// Packing: the thread of accumulator lane o = 32 quarter + 8 i + g holds channel o
+// of its 32 tokens; in the V layout channel o of decode lane (g, t4) sits in chunk
+// word `quarter` (2-bit) or 2 quarter + i/2 (4-bit), at a bit offset set by i, the
+// token's half and parity. The four (2-bit) or two (4-bit) threads that share a
+// word are lanes g + 8 i of one warp, so two (one) xor-shuffles complete it.
 template <int BITS>
-__global__ void __launch_bounds__(VTHREADS, 2) append_value_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(VTHREADS, 2)
+    append_value_kernel(const AppendArgs a, const __grid_constant__ CUtensorMap tmv) {
   constexpr int NTHR = (1 << BITS) - 1;
   constexpr int PW = BITS / 2;                     // chunk words a thread stores per tile
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  ValueSmem &S = *reinterpret_cast<ValueSmem *>(smem_raw);
+  ValueSmem &S = *reinterpret_cast<ValueSmem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quarter = warp & 3, half = warp >> 2;
   const int gq = lane & 7, iq = lane >> 3;
   const PageLayout PL = page_layout(BITS, a.G);
   const int lh = blockIdx.y;
@@ -223,27 +237,70 @@ __global__ void __launch_bounds__(VTHREADS, 2) append_value_kernel(const AppendA
   const long long T0 = a.T0, T1 = a.T0 + a.n;
   const long long pbeg = a.page0 + (long long)blockIdx.x * a.vppc;
   const int npg = (int)(min(pbeg + a.vppc, (T1 - 1) / PAGE + 1) - pbeg);
-  const long long row_stride = (long long)a.L * a.Hkv * D;
+  // one thread: page p of the run (all 64 rows; rows outside the input read as zeros)
+  auto issue_page = [&](int p) {
+    const int buf = p % V_NBUF;
+    const int y = (int)((pbeg + p) * PAGE - T0);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar_v[buf])),
+                 "r"((uint32_t)(2 * V_HALF_BYTES))
+                 : "memory");
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+              smem_addr(&S.v[buf][0]) + (uint32_t)(h * V_HALF_BYTES)),
+          "l"(reinterpret_cast<uint64_t>(&tmv)), "r"(lh * D + 64 * h), "r"(y), "r"(smem_addr(&S.bar_v[buf]))
+          : "memory");
+  };
 
-  // ---- the run's modality ids (validated) and the session's copy of them ----
-  for (int i = tid; i < npg * PAGE; i += VTHREADS) {
-    const long long t = pbeg * PAGE + i;
-    int m = 0xff;
-    if (t >= T0 && t < T1) {
-      m = a.mod_in[t - T0];
-      if (m >= a.M) {
-        if (lh == 0) atomicOr(a.err, ERR_MODALITY);
-        m = 0;
-      }
-      if (lh == 0) a.mod[(long long)a.session * a.cap + t] = (uint8_t)m;
+  // R_m into tensor memory: warp w writes part w / 4 of rows 32 (w % 4) .. (row o =
+  // lane o, fp16 pairs); every load of the row is issued before the stores
+  const int rpart = warp >> 2, rrow = 32 * quarter + lane;
+  auto fetch_r = [&](int m, uint4 (&rr)[16]) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.rot_h + ((long long)(lh * a.M + m) * 2 + rpart) * D * D +
+                                                       (long long)rrow * D);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) rr[k] = src[k];
+  };
+
+  // the rotation of modality 0 (usually the first round's) is on its way during the
+  // bookkeeping below
+  uint4 rfirst[16];
+  fetch_r(0, rfirst);
+
+  // ---- the run's modality ids (validated) and the session's copy of them; every
+  // load issued before the first store ----
+  {
+    constexpr int PER = V_MAX_PPC * PAGE / VTHREADS;
+    int mv[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const long long t = pbeg * PAGE + tid + k * VTHREADS;
+      mv[k] = (tid + k * VTHREADS < npg * PAGE && t >= T0 && t < T1) ? (int)a.mod_in[t - T0] : 0xff;
     }
-    S.mod[i] = (uint8_t)m;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid + k * VTHREADS;
+      if (i >= npg * PAGE) break;
+      int m = mv[k];
+      if (m != 0xff) {
+        if (m >= a.M) {
+          if (lh == 0) atomicOr(a.err, ERR_MODALITY);
+          m = 0;
+        }
+        if (lh == 0) a.mod[(long long)a.session * a.cap + pbeg * PAGE + i] = (uint8_t)m;
+      }
+      S.mod[i] = (uint8_t)m;
+    }
   }
   if (tid < V_MAX_PPC) S.pm[tid] = 0;
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_r)));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_mma)));
+    for (int b = 0; b < V_NBUF; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_v[b])));
+    for (int b = 0; b < 2; ++b) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_mma[b])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int p = 0; p < V_NBUF && p < npg; ++p) issue_page(p);    // the first pages, before the bookkeeping
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&S.tmem)),
@@ -254,22 +311,25 @@ __global__ void __launch_bounds__(VTHREADS, 2) append_value_kernel(const AppendA
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem;
+  auto store_r = [&](const uint4 (&rr)[16]) {
+    const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + V_TMEM_R + 64 * rpart;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t r[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        r[4 * k] = rr[8 * hh + k].x;
+        r[4 * k + 1] = rr[8 * hh + k].y;
+        r[4 * k + 2] = rr[8 * hh + k].z;
+        r[4 * k + 3] = rr[8 * hh + k].w;
+      }
+      tmem_st32(ta + 32 * hh, r);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  };
   for (int i = tid; i < npg * PAGE; i += VTHREADS)
     if (S.mod[i] != 0xff) atomicOr(&S.pm[i / PAGE], 1 << S.mod[i]);
   __syncthreads();
-  // the pages' own copy of their tile modality masks (decode reads them with the page)
-  for (int i = tid; i < npg * (PAGE / TILE); i += VTHREADS) {
-    const int p = i / (PAGE / TILE), tile = i % (PAGE / TILE);
-    const long long P0 = (pbeg + p) * PAGE;
-    const int ta = (int)(max(P0, T0) - P0), tb = (int)(min(P0 + PAGE, T1) - P0);
-    const int t0 = tile * TILE, t1 = t0 + TILE;
-    if (t1 > ta && t0 < tb) {
-      uint8_t *tm = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes + PL.off_tmask + tile;
-      uint8_t bitsm = (t0 < ta) ? *tm : 0;        // tile already partly filled
-      for (int t = max(t0, ta); t < min(t1, tb); ++t) bitsm |= (uint8_t)(1u << S.mod[p * PAGE + t]);
-      *tm = bitsm;
-    }
-  }
   // ---- rounds: a page's modalities, the resident rotation's first, so that R_m is
   // copied again only when the modality changes ----
   if (tid == 0) {
@@ -294,65 +354,53 @@ __global__ void __launch_bounds__(VTHREADS, 2) append_value_kernel(const AppendA
   __syncthreads();
   const int nr = S.nround;
 
-  auto issue_r = [&](int m) {                      // one thread: both parts of R_m, one bulk copy
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&S.bar_r)),
-                 "r"((uint32_t)sizeof(S.r))
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(&S.r[0][0])),
-        "l"(a.rot_h + (long long)(lh * a.M + m) * 2 * D * D), "r"((uint32_t)sizeof(S.r)), "r"(smem_addr(&S.bar_r))
-        : "memory");
-  };
-  auto issue_v = [&](int r, int buf) {             // every thread: the round's tokens, 16-byte copies
-    const int p = S.rpage[r], m = S.rmod[r];
-    const long long P0 = (pbeg + p) * PAGE;
-    for (int i = tid; i < PAGE * (D / 8); i += VTHREADS) {
-      const int t = i & (PAGE - 1), c = i >> 6;    // a warp: 32 tokens, one 8-channel block
-      if (S.mod[p * PAGE + t] == m)
-        cp_async16(&S.v[buf][kmajor_off(t, 8 * c)], a.v + (P0 + t - T0) * row_stride + (long long)lh * D + 8 * c);
-    }
-    cp_async_commit();
-  };
-
-  uint32_t ph_r = 0, ph_mma = 0;
-  bool failed = false, r_pending = false, mma_pending = false;
-  uint32_t pw[4][PW];
-  if (nr > 0) {
-    if (tid == 0) issue_r(S.rmod[0]);
-    r_pending = true;
-    issue_v(0, 0);
-  }
-  for (int r = 0; r < nr; ++r) {
-    const int buf = r & 1, p = S.rpage[r], m = S.rmod[r];
-    const long long P0 = (pbeg + p) * PAGE;
-    const int ta = (int)(max(P0, T0) - P0), tb = (int)(min(P0 + PAGE, T1) - P0);
-    uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
-    if (r == 0 || S.rpage[r - 1] != p) {
+  bool failed = false;
+  int issued = 0, waited = 0;                      // rounds whose MMAs were issued / seen complete
+  int pages_seen = 0;                              // pages whose copy completed
+  // stage A: the round's values and rotation are in; MMAs into accumulator r % 2,
+  // then the round's token mask and norms
+  auto stage_a = [&](int r) -> bool {
+    const int p = S.rpage[r], m = S.rmod[r], buf = p % V_NBUF;
+    const bool ok = wait_bar(&S.bar_v[buf], (uint32_t)(p / V_NBUF) & 1u);
+    if (ok) pages_seen = max(pages_seen, p + 1);
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) return false;
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(PAGE >> 3) << 17) | ((uint32_t)(D >> 4) << 24);
+      const uint32_t vb = smem_addr(&S.v[buf][0]);
+      const uint32_t dt = tmem + (uint32_t)((r & 1) * PAGE);
 #pragma unroll
-      for (int tau = 0; tau < 4; ++tau)
+      for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int k = 0; k < PW; ++k) pw[tau][k] = 0u;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t at = tmem + V_TMEM_R + (uint32_t)(64 * part + 8 * ks);
+          const uint64_t bd = sw128_desc(vb + (uint32_t)((ks >> 2) * V_HALF_BYTES + (ks & 3) * 32));
+          asm volatile(
+              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dt),
+              "r"(at), "l"(bd), "r"(idesc), "r"((part | ks) ? 1u : 0u));
+        }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_addr(&S.bar_mma[r & 1]))
+                   : "memory");
     }
-    // the next round's values go to the other buffer (its MMA has completed)
-    if (r + 1 < nr) {
-      issue_v(r + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    issued = r + 1;
     if (warp < 2) {
       const uint32_t b = __ballot_sync(0xffffffffu, S.mod[p * PAGE + tid] == m);
-      if (lane == 0) S.mmask[warp] = b;
+      if (lane == 0) S.mmask[r & 1][warp] = b;
     }
-    __syncthreads();                               // the round's values (every thread's copies) landed
-    // norms: thread t = token t, partial sums of 4 channels combined in the order of a
-    // 32-lane xor-shuffle tree (lane l holding channels 4l .. 4l+3)
-    if (tid < PAGE && S.mod[p * PAGE + tid] == m) {
-      float q[32];
+    // norms: 4 threads per token (thread q: channels 32q .. 32q+31), partial sums of 4
+    // channels combined in the order of a 32-lane xor-shuffle tree over lanes holding
+    // channels 4l .. 4l+3 (levels 16 and 8 across the token's threads, 4, 2, 1 inside)
+    {
+      const int t = tid >> 2, q = tid & 3;
+      float s8[8];
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(&S.v[buf][kmajor_off(tid, 8 * c)]);
+      for (int k = 0; k < 4; ++k) {
+        const int c = 4 * q + k;
+        const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(&S.v[buf][0]) +
+                                                          (c >> 3) * V_HALF_BYTES + t * 128 + (((c & 7) ^ (t & 7)) << 4));
         const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
         const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
         const float2 x2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
@@ -365,157 +413,267 @@ __global__ void __launch_bounds__(VTHREADS, 2) append_value_kernel(const AppendA
         s1 = fmaf(x2.y, x2.y, s1);
         s1 = fmaf(x3.x, x3.x, s1);
         s1 = fmaf(x3.y, x3.y, s1);
-        q[2 * c] = s0;
-        q[2 * c + 1] = s1;
+        s8[2 * k] = s0;                          // partial 8q + 2k
+        s8[2 * k + 1] = s1;
       }
 #pragma unroll
-      for (int s = 16; s >= 1; s >>= 1)
+      for (int i = 0; i < 8; ++i) s8[i] = __fadd_rn(s8[i], __shfl_xor_sync(0xffffffffu, s8[i], 2));   // l, l + 16
 #pragma unroll
-        for (int l = 0; l < s; ++l) q[l] = __fadd_rn(q[l], q[l + s]);
-      const float n = sqrtf(q[0]);
-      S.sc[tid] = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
-      reinterpret_cast<__half *>(pg + PL.off_norm)[tid] = __float2half_rn(n);
-    }
-    bool ok = true;
-    if (r_pending) {                               // R_m resident
-      ok = wait_bar(&S.bar_r, ph_r);
-      if (ok) {
-        ph_r ^= 1u;
-        r_pending = false;
+      for (int i = 0; i < 8; ++i) s8[i] = __fadd_rn(s8[i], __shfl_xor_sync(0xffffffffu, s8[i], 1));   // l, l + 8
+#pragma unroll
+      for (int st = 4; st >= 1; st >>= 1)
+#pragma unroll
+        for (int i = 0; i < st; ++i) s8[i] = __fadd_rn(s8[i], s8[i + st]);
+      if (q == 0 && S.mod[p * PAGE + t] == m) {
+        const float n = sqrtf(s8[0]);
+        S.sc[r & 1][t] = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
+        uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
+        reinterpret_cast<__half *>(pg + PL.off_norm)[t] = __float2half_rn(n);
       }
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the copied values, for the tensor core
+    return true;
+  };
+
+  uint32_t pw[2][PW];
+  if (nr > 0) {
+    if (S.rmod[0] != 0) fetch_r(S.rmod[0], rfirst);
+    store_r(rfirst);
     tc_fence_before();
-    if (__syncthreads_or(!ok)) {
+    __syncthreads();
+    tc_fence_after();
+    failed = !stage_a(0);
+  }
+  for (int r = 0; r < nr && !failed; ++r) {
+    const int p = S.rpage[r];
+    const long long P0 = (pbeg + p) * PAGE;
+    const int ta = (int)(max(P0, T0) - P0), tb = (int)(min(P0 + PAGE, T1) - P0);
+    uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
+    const bool next_same = r + 1 < nr && S.rmod[r + 1] == S.rmod[r];
+    // the next round's MMAs overlap this round's codes
+    if (next_same && !stage_a(r + 1)) {
       failed = true;
       break;
     }
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(PAGE >> 3) << 17) | ((uint32_t)(D >> 4) << 24);
-      const uint32_t ra = smem_addr(&S.r[0][0]), va = smem_addr(&S.v[buf][0]);
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t ad = kmajor_desc(ra + part * D * D * 2 + 256 * ks);
-          const uint64_t bd = kmajor_desc(va + 256 * ks);
-          asm volatile(
-              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-              "l"(ad), "l"(bd), "r"(idesc), "r"((part | ks) ? 1u : 0u));
-        }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_addr(&S.bar_mma))
-                   : "memory");
-    }
-    mma_pending = true;
-    ok = wait_bar(&S.bar_mma, ph_mma);
-    if (ok) {
-      ph_mma ^= 1u;
-      mma_pending = false;
-    }
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
+    // ---- stage B: codes of round r ----
+    __syncthreads();                               // the round's mask and norms
+    {
+      const bool ok = wait_bar(&S.bar_mma[r & 1], (uint32_t)(r >> 1) & 1u);
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      waited = r + 1;
     }
     tc_fence_after();
-    // the next round's rotation, if it differs, while this round's codes are made
-    if (r + 1 < nr && S.rmod[r + 1] != m) {
-      if (tid == 0) issue_r(S.rmod[r + 1]);
-      r_pending = true;
+    if (r == 0 || S.rpage[r - 1] != p) {
+#pragma unroll
+      for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+        for (int k = 0; k < PW; ++k) pw[tl][k] = 0u;
     }
-
-    // ---- epilogue: lane o of the accumulator = output channel o ----
-    float acc[PAGE];
-    const uint32_t ta_addr = tmem + ((uint32_t)(32 * warp) << 16);
-    tmem_ld32(ta_addr, acc);
-    tmem_ld32(ta_addr + 32, acc + 32);
+    float acc[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)((r & 1) * PAGE + 32 * half), acc);
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    const uint32_t mm0 = S.mmask[0], mm1 = S.mmask[1];
-    uint32_t wr[4][4];
+    const uint32_t mm = S.mmask[r & 1][half];
+    uint32_t wr[2][4];
 #pragma unroll
-    for (int tau = 0; tau < 4; ++tau)
+    for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4) wr[tau][t4] = 0u;
+      for (int t4 = 0; t4 < 4; ++t4) wr[tl][t4] = 0u;
 #pragma unroll
-    for (int t = 0; t < PAGE; ++t) {
-      const uint32_t sel = ((t < 32 ? mm0 >> t : mm1 >> (t - 32)) & 1u);
-      const uint32_t code = (uint32_t)code_of<NTHR>(acc[t] * S.sc[t], a.vthr) & (0u - sel);
-      const int tt = t & 15;
-      wr[t >> 4][(tt & 7) >> 1] |= code << (BITS == 2 ? 8 * (tt >> 3) + 2 * (tt & 1) : 16 * (tt >> 3) + 4 * (tt & 1));
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t sel = (mm >> j) & 1u;
+      const uint32_t code = (uint32_t)code_of<NTHR>(acc[j] * S.sc[r & 1][32 * half + j], a.vthr) & (0u - sel);
+      const int tt = j & 15;
+      wr[j >> 4][(tt & 7) >> 1] |= code << (BITS == 2 ? 8 * (tt >> 3) + 2 * (tt & 1) : 16 * (tt >> 3) + 4 * (tt & 1));
     }
     if constexpr (BITS == 2) {
       const int sh = 16 * (iq >> 1) + 4 * (iq & 1);
 #pragma unroll
-      for (int tau = 0; tau < 4; ++tau)
+      for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
-          uint32_t w = wr[tau][t4] << sh;
+          uint32_t w = wr[tl][t4] << sh;
           w |= __shfl_xor_sync(0xffffffffu, w, 8);
           w |= __shfl_xor_sync(0xffffffffu, w, 16);
-          if (t4 == iq) pw[tau][0] |= w;
+          if (t4 == iq) pw[tl][0] |= w;
         }
     } else {
       const int sh = 8 * (iq & 1);
 #pragma unroll
-      for (int tau = 0; tau < 4; ++tau)
+      for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
-          uint32_t w = wr[tau][t4] << sh;
+          uint32_t w = wr[tl][t4] << sh;
           w |= __shfl_xor_sync(0xffffffffu, w, 8);
-          if ((t4 >> 1) == (iq & 1)) pw[tau][t4 & 1] |= w;
+          if ((t4 >> 1) == (iq & 1)) pw[tl][t4 & 1] |= w;
         }
     }
+    tc_fence_before();
     // the page's last round: store its chunk words (older tokens of a tile kept)
     if (r + 1 == nr || S.rpage[r + 1] != p) {
 #pragma unroll
-      for (int tau = 0; tau < 4; ++tau) {
+      for (int tl = 0; tl < 2; ++tl) {
+        const int tau = 2 * half + tl;
         if (TILE * tau + TILE <= ta || TILE * tau >= tb) continue;
         uint32_t *tw = reinterpret_cast<uint32_t *>(pg + PL.off_v + tau * PL.tile_bytes);
 #pragma unroll
         for (int k = 0; k < PW; ++k) {
           const int t4 = BITS == 2 ? iq : 2 * (iq & 1) + k;
-          uint32_t *dst = BITS == 2 ? tw + (4 * gq + t4) * 4 + warp : tw + (4 * gq + t4) * 8 + 2 * warp + (iq >> 1);
-          uint32_t val = pw[tau][k];
+          uint32_t *dst =
+              BITS == 2 ? tw + (4 * gq + t4) * 4 + quarter : tw + (4 * gq + t4) * 8 + 2 * quarter + (iq >> 1);
+          uint32_t val = pw[tl][k];
           if (TILE * tau < ta) val |= *dst & v_keep_mask<BITS>(t4, ta - TILE * tau);
           *dst = val;
         }
       }
     }
-    tc_fence_before();
-    __syncthreads();                               // accumulator and per-round arrays free again
+    // page p's last round: its buffer is free (MMAs completed, norms taken before the
+    // barrier above) for the page three ahead
+    if (tid == 0 && (r + 1 == nr || S.rpage[r + 1] != p) && p + V_NBUF < npg) issue_page(p + V_NBUF);
+    // a new rotation: written once round r's MMAs (the last readers of R) completed
+    if (r + 1 < nr && !next_same) {
+      {
+        uint4 rr[16];
+        fetch_r(S.rmod[r + 1], rr);
+        store_r(rr);
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (!stage_a(r + 1)) {
+        failed = true;
+        break;
+      }
+    }
   }
-  cp_async_wait<0>();
+  // the pages' own copy of their tile modality masks (decode reads them with the page)
+  for (int i = tid; i < npg * (PAGE / TILE); i += VTHREADS) {
+    const int p = i / (PAGE / TILE), tile = i % (PAGE / TILE);
+    const long long P0 = (pbeg + p) * PAGE;
+    const int ta = (int)(max(P0, T0) - P0), tb = (int)(min(P0 + PAGE, T1) - P0);
+    const int t0 = tile * TILE, t1 = t0 + TILE;
+    if (t1 > ta && t0 < tb) {
+      uint8_t *tm = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes + PL.off_tmask + tile;
+      uint8_t bitsm = (t0 < ta) ? *tm : 0;        // tile already partly filled
+      for (int t = max(t0, ta); t < min(t1, tb); ++t) bitsm |= (uint8_t)(1u << S.mod[p * PAGE + t]);
+      *tm = bitsm;
+    }
+  }
   if (failed) {
     if (tid == 0) atomicOr(a.err, ERR_WAIT);
-    if (r_pending) (void)wait_bar(&S.bar_r, ph_r);
-    if (mma_pending) (void)wait_bar(&S.bar_mma, ph_mma);
+    // MMAs still in flight: wait (bounded) before their accumulator columns are freed
+    for (int r = waited; r < issued; ++r) (void)wait_bar(&S.bar_mma[r & 1], (uint32_t)(r >> 1) & 1u);
+    // pages still on their way: issued up to the third after the last one consumed
+    if (tid == 0)
+      for (int p = pages_seen; p < npg && p < pages_seen + V_NBUF; ++p)
+        (void)wait_bar(&S.bar_v[p % V_NBUF], (uint32_t)(p / V_NBUF) & 1u);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(V_TMEM_COLS));
 }
 
-// Shared memory of the key kernel: rotated keys, their codes and group statistics.
-struct KeySmem {
-  float xt[PAGE * D];              // keys [token][c] (rotated, fp32)
-  uint8_t kc[PAGE * D];            // key codes of the page
-  float kmn[2][D], kmx[2][D];     // group min and range (fp16 values held as fp32)
-  float red[2][2][D];              // per-half min / max of a group
-};
-
 // ---------------------------------------------------------------------------
 // Keys: the groups that complete with this chunk (or every new token for
 // TurboQuant keys), and the new fp16 tail
 // ---------------------------------------------------------------------------
+constexpr int XS = D + 4;                  // padded row (floats) of the rotated keys in shared memory
+
+// Shared memory of the key kernel: rotated keys (or TurboQuant codes), and per
+// (group, channel) the record [min, code thresholds on k' - min].
+template <int BITS, int GT>
+struct KeySmem {
+  static constexpr int NREC = 1 << BITS;   // min + (levels - 1) thresholds
+  static constexpr int RSLOT = D + 6;      // record slots: channel c at c + 2 (c / 32)
+  float xt[GT * XS];               // rotated keys [token][channel ^ 16 (token / 8 % 2)], fp32
+  float rec[RSLOT][NREC];
+  float red[2][2][D];              // per-half min / max of a 64-token group
+  uint32_t sgn[D / 2];             // Hadamard signs of channel pairs as fp16x2 sign bits
+};
+// Column of channel c in row r of KeySmem::xt: the rows 8 apart that one warp writes
+// land in different banks.
+__device__ __forceinline__ int xt_col(int c, int r) { return c ^ (16 * ((r >> 3) & 1)); }
+// Record slot of channel c: the four channels 32 apart that one warp reads together
+// sit in different banks.
+__device__ __forceinline__ int rec_slot(int c) { return c + 2 * (c >> 5); }
+
+// The smallest fp32 d >= 0 with fl(d / rng) > t (IEEE division, round to nearest
+// even), +inf when no d qualifies (rng 0 or infinite: every code is 0). The quotient
+// is non-decreasing in d, so d >= key_threshold(t, rng) <=> fl(d / rng) > t, and a
+// code taken as the count of thresholds below d equals the count of midpoints
+// below the correctly rounded scaled key. The start fl(t * rng) is within a few
+// ulps of the answer; the walks are bounded.
+__device__ float key_threshold(float t, float rng) {
+  if (!(rng > 0.f) || isinf(rng)) return __int_as_float(0x7f800000);
+  float d = fmaxf(__fmul_rn(t, rng), 0.f);
+  for (int it = 0; it < 64 && !(__fdiv_rn(d, rng) > t); ++it) d = __int_as_float(__float_as_int(d) + 1);
+  for (int it = 0; it < 64 && d > 0.f; ++it) {
+    const float dp = __int_as_float(__float_as_int(d) - 1);
+    if (!(__fdiv_rn(dp, rng) > t)) break;
+    d = dp;
+  }
+  return d;
+}
+
+// Canonical fp32 rotation of one key, four threads per token: thread q holds
+// channels 32q .. 32q+31 as 16 channel pairs; strides 1 .. 16 inside the thread,
+// 32 and 64 across the token's threads (lanes q ^ 1, q ^ 2). Round-to-nearest
+// adds and subtracts (a - b as fma(b, -1, a)), then one multiply by fp32(1/sqrt d):
+// the same operations on the same operands as the warp-per-token form.
+__device__ __forceinline__ void rotate_key_quarter(const uint4 (&raw)[4], const uint32_t *sgn, int q,
+                                                   float2 (&x)[16]) {
+  const float2 NEG1 = make_float2(-1.f, -1.f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t h = w[m] ^ sgn[16 * q + 4 * k + m];      // s o k on the fp16 pair (exact)
+      x[4 * k + m] = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {                               // stride 1: the two halves of a pair
+    const float a0 = x[p].x, b0 = x[p].y;
+    x[p] = make_float2(__fadd_rn(a0, b0), __fsub_rn(a0, b0));
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)                             // strides 2 .. 16: pairs h apart
+#pragma unroll
+    for (int p = 0; p < 16; ++p)
+      if (!(p & h)) {
+        const float2 a0 = x[p], b0 = x[p + h];
+        x[p] = __fadd2_rn(a0, b0);
+        x[p + h] = __ffma2_rn(b0, NEG1, a0);
+      }
+#pragma unroll
+  for (int sm = 1; sm <= 2; sm <<= 1) {                        // strides 32, 64: partner lane q ^ sm
+    const float s = (q & sm) ? -1.f : 1.f;                     // upper: partner - own, lower: own + partner
+    const float2 s2 = make_float2(s, s);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[p].x, sm), __shfl_xor_sync(0xffffffffu, x[p].y, sm));
+      x[p] = __ffma2_rn(s2, x[p], o);
+    }
+  }
+  const float2 sc = make_float2(INV_SQRT_D, INV_SQRT_D);
+#pragma unroll
+  for (int p = 0; p < 16; ++p) x[p] = __fmul2_rn(x[p], sc);
+}
+
+// TurboQuant keys (section 2, TurboQuant bullet): every new token now, like a value
+// with the shared Hadamard rotation: n = |k|, w = sqrt(d) k'/n, value levels. One CTA
+// per (touched page, layer * Hkv + kv head); no groups, no fp16 tail.
+struct TurboSmem {
+  uint8_t kc[PAGE * D];            // key codes [token][channel]
+};
 template <int BITS>
-__global__ void __launch_bounds__(THREADS) append_key_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(THREADS) append_turbo_kernel(const AppendArgs a) {
   constexpr int NTHR = (1 << BITS) - 1;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PageLayout PL = page_layout(BITS, a.G);
-
+  const PageLayout PL = page_layout(BITS, 0);
   const long long page = a.page0 + blockIdx.x;
   const int lh = blockIdx.y;                       // layer * Hkv + kv head
   const long long unit = (long long)a.session * a.L * a.Hkv + lh;
@@ -525,152 +683,215 @@ __global__ void __launch_bounds__(THREADS) append_key_kernel(const AppendArgs a)
   const int tb = (int)(min(P0 + PAGE, T1) - P0);
   const int row_stride = a.L * a.Hkv * D;          // between tokens in the input
   uint8_t *pg = a.pages + (unit * a.P_max + page) * (long long)PL.page_bytes;
+  TurboSmem &S = *reinterpret_cast<TurboSmem *>(smem_raw);
+  // ---- TurboQuant keys (section 2, TurboQuant bullet): every new token now, like a
+  // value with the shared Hadamard rotation: n = |k|, w = sqrt(d) k'/n, value levels ----
+  // keep the codes of older tokens that share a 16-token tile with the first new token
+  if (ta % TILE != 0) unpack_tile<BITS, 0>(S.kc, pg + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid, THREADS);
+  for (int t = ta + warp; t < tb; t += THREADS / 32) {
+    const __half *src = a.k + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = __half2float(src[4 * lane + j]);
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float n = sqrtf(ss);
+    float x[4];
+    rotate_key_row(*reinterpret_cast<const uint2 *>(src + 4 * lane), a.signs, lane, x);
+    const float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) S.kc[t * D + 4 * lane + j] = (uint8_t)code_of<NTHR>(x[j] * sc, a.vthr);
+    if (lane == 0) reinterpret_cast<__half *>(pg + PL.off_stats)[t] = __float2half_rn(n);
+  }
+  __syncthreads();
+  for (int tile = ta / TILE; tile * TILE < tb; ++tile)
+    pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, tb, tid, THREADS);
+}
 
-  KeySmem &S = *reinterpret_cast<KeySmem *>(smem_raw);
-  if (a.G == 0) {
-    // ---- TurboQuant keys (section 2, TurboQuant bullet): every new token now, like a
-    // value with the shared Hadamard rotation: n = |k|, w = sqrt(d) k'/n, value levels ----
-    // keep the codes of older tokens that share a 16-token tile with the first new token
-    if (ta % TILE != 0) unpack_tile<BITS, 0>(S.kc, pg + (ta / TILE) * PL.tile_bytes, ta / TILE, ta, tid, THREADS);
-    for (int t = ta + warp; t < tb; t += THREADS / 32) {
-      const __half *src = a.k + (P0 + t - T0) * (long long)row_stride + (long long)lh * D;
-      float ss = 0.f;
+// Grouped keys: one CTA per (key group touched by the chunk, layer * Hkv + kv head),
+// GT = group size tokens, 4 threads per token. A group is quantized when its last
+// token arrives, earlier members read from the fp16 tail buffer; the CTA of the last
+// touched group writes the new fp16 tail into the other tail buffer.
+template <int BITS, int GT>
+__global__ void __launch_bounds__(4 * GT) append_key_kernel(const AppendArgs a) {
+  constexpr int NTHR = (1 << BITS) - 1;
+  constexpr int NT = 4 * GT;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  KeySmem<BITS, GT> &S = *reinterpret_cast<KeySmem<BITS, GT> *>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const PageLayout PL = page_layout(BITS, GT);
+  const long long T0 = a.T0, T1 = a.T0 + a.n;
+  const long long gs = (T0 / GT + blockIdx.x) * GT;         // the group: tokens [gs, gs + GT)
+  const int lh = blockIdx.y;                                 // layer * Hkv + kv head
+  const long long unit = (long long)a.session * a.L * a.Hkv + lh;
+  const long long page = gs / PAGE;
+  const int g0 = (int)(gs - page * PAGE);                    // the group's first token in its page
+  const int row_stride = a.L * a.Hkv * D;                    // between tokens in the input
+  uint8_t *pg = a.pages + (unit * a.P_max + page) * (long long)PL.page_bytes;
+  const __half *told = a.tail_old + unit * (long long)GT * D;
+
+  if (gs + GT <= T1) {                                       // the group completes now
+    if (tid < D / 2)
+      S.sgn[tid] = (a.signs[2 * tid] < 0.f ? 0x8000u : 0u) | (a.signs[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
+    __syncthreads();
+    // rotate every member: thread q of a token holds channels 32q .. 32q+31; warp w
+    // takes tokens g = 4 (w % 2) .. + 3 and g + 8 of the group's tile w / 2
+    const int q = lane & 3, tk = lane >> 4;
+    const int tile = warp >> 1, g = 4 * (warp & 1) + ((lane >> 2) & 3);
+    const int r = TILE * tile + g + 8 * tk;
+    float2 x[16];
+    {
+      const long long t = gs + r;
+      const __half *src = (t < T0 ? told + (t - gs) * D : a.k + (t - T0) * (long long)row_stride + (long long)lh * D) +
+                          32 * q;
+      uint4 raw[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float v = __half2float(src[4 * lane + j]);
-        ss = fmaf(v, v, ss);
-      }
+      for (int k = 0; k < 4; ++k) raw[k] = reinterpret_cast<const uint4 *>(src)[k];
+      rotate_key_quarter(raw, S.sgn, q, x);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float n = sqrtf(ss);
-      float x[4];
-      rotate_key_row(*reinterpret_cast<const uint2 *>(src + 4 * lane), a.signs, lane, x);
-      const float sc = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) S.kc[t * D + 4 * lane + j] = (uint8_t)code_of<NTHR>(x[j] * sc, a.vthr);
-      if (lane == 0) reinterpret_cast<__half *>(pg + PL.off_stats)[t] = __float2half_rn(n);
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<float4 *>(&S.xt[r * XS + xt_col(32 * q + 4 * k, r)]) =
+            make_float4(x[2 * k].x, x[2 * k].y, x[2 * k + 1].x, x[2 * k + 1].y);
     }
     __syncthreads();
-    for (int tile = ta / TILE; tile * TILE < tb; ++tile)
-      pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, tb, tid, THREADS);
-    return;                       // no key groups, no fp16 tail
-  }
-
-  // ---- keys: groups that complete with this chunk, all of the page's at once ----
-  const int G = a.G;
-  float *xk = S.xt;               // keys as [token][c], row stride D
-  uint32_t gmask = 0;             // bit gi: group gi of the page completes now
-  for (int g0 = 0; g0 < PAGE; g0 += G) {
-    const long long gend = P0 + g0 + G;
-    if (gend > T0 && gend <= T1) gmask |= 1u << (g0 / G);
-  }
-  if (!gmask && blockIdx.x != gridDim.x - 1) return;   // nothing for this CTA
-  if (gmask) {
-    const __half *told = a.tail_old + unit * (long long)G * D;
-    // rotate every member: warp per token (8 tokens per warp, loads issued first),
-    // lane holds channels 4*lane .. 4*lane+3
-    constexpr int PER_WARP = PAGE / (THREADS / 32);
-    uint2 raw[PER_WARP];
-#pragma unroll
-    for (int j = 0; j < PER_WARP; ++j) {
-      const int r = warp + j * (THREADS / 32);
-      raw[j] = make_uint2(0u, 0u);
-      if ((gmask >> (r / G)) & 1u) {
-        const long long t = P0 + r, gs = P0 + (r / G) * G;
-        const __half *src = t < T0 ? told + (t - gs) * D : a.k + (t - T0) * (long long)row_stride + (long long)lh * D;
-        raw[j] = *reinterpret_cast<const uint2 *>(src + 4 * lane);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < PER_WARP; ++j) {
-      const int r = warp + j * (THREADS / 32);
-      if (!((gmask >> (r / G)) & 1u)) continue;     // warp-uniform
-      float x[4];
-      rotate_key_row(raw[j], a.signs, lane, x);
-      *reinterpret_cast<float4 *>(&xk[r * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
-    }
-    __syncthreads();
-    // per-channel statistics: thread (c, h) scans 32 members (G = 32: group h;
-    // G = 64: half h of the group); then min rounded down, range rounded up
+    // per-channel statistics: thread (c, h) scans members 32h .. 32h + 31
     {
       const int c = tid & (D - 1), h = tid / D;
-      if ((gmask >> ((32 * h) / G)) & 1u) {
-        float mn = xk[(32 * h) * D + c], mx = mn;
+      float mn = S.xt[(32 * h) * XS + xt_col(c, 0)], mx = mn;
 #pragma unroll 8
-        for (int r = 1; r < 32; ++r) {
-          const float v = xk[(32 * h + r) * D + c];
-          mn = fminf(mn, v);
-          mx = fmaxf(mx, v);
-        }
-        S.red[h][0][c] = mn;
-        S.red[h][1][c] = mx;
+      for (int rr = 1; rr < 32; ++rr) {
+        const float v = S.xt[(32 * h + rr) * XS + xt_col(c, rr)];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
       }
+      S.red[h][0][c] = mn;
+      S.red[h][1][c] = mx;
     }
     __syncthreads();
-    for (int i = tid; i < (PAGE / G) * D; i += THREADS) {
-      const int gi = i / D, c = i % D;
-      if (!((gmask >> gi) & 1u)) continue;
-      float mn, mx;
-      if (G == 32) {
-        mn = S.red[gi][0][c];
-        mx = S.red[gi][1][c];
-      } else {
-        mn = fminf(S.red[0][0][c], S.red[1][0][c]);
-        mx = fmaxf(S.red[0][1][c], S.red[1][1][c]);
+    // min rounded down, range rounded up (fp16, stored), and the code thresholds
+    if (tid < D) {
+      const int c = tid;
+      float mn = S.red[0][0][c], mx = S.red[0][1][c];
+      if (GT == 64) {
+        mn = fminf(mn, S.red[1][0][c]);
+        mx = fmaxf(mx, S.red[1][1][c]);
       }
       const __half hmn = __float2half_rd(mn);
       const __half hrg = __float2half_ru(__fsub_ru(mx, __half2float(hmn)));
-      S.kmn[gi][c] = __half2float(hmn);
-      S.kmx[gi][c] = __half2float(hrg);
-      __half *st = reinterpret_cast<__half *>(pg + PL.off_stats + gi * 2 * D * 2);
+      __half *st = reinterpret_cast<__half *>(pg + PL.off_stats + (g0 / GT) * 2 * D * 2);
       st[stat_pos(c)] = hmn;
       st[D + stat_pos(c)] = hrg;
+      const float rng = __half2float(hrg);
+      float *rec = S.rec[rec_slot(c)];
+      rec[0] = __half2float(hmn);
+#pragma unroll
+      for (int j = 0; j < NTHR; ++j) rec[1 + j] = key_threshold(a.kthr[j], rng);
     }
     __syncthreads();
-    {
-      // thread (c, h): channel c of rows 32h .. 32h + 31, one group's statistics
-      const int c = tid & (D - 1), h = tid / D, gi = (32 * h) / G;
-      if ((gmask >> gi) & 1u) {
-        const float mn = S.kmn[gi][c], rng = S.kmx[gi][c];
-#pragma unroll 4
-        for (int r = 32 * h; r < 32 * h + 32; ++r) {
-          int code = 0;
-          if (rng != 0.f) code = code_of<NTHR>(__fdiv_rn(__fsub_rn(xk[r * D + c], mn), rng), a.kthr);
-          S.kc[r * D + c] = (uint8_t)code;
+    // codes from the registers, straight into chunk words (k_pair_coords, k_code_bit):
+    // channel 32q + i of token g + 8 tk goes to decode lane (g, t4) at
+    //   2-bit: word q,           i = 2 t4 + e + 8 s + 16 hb, bit 8 (2 hb + tk) + 4 s + 2 e
+    //   4-bit: word 2q + i / 16, i = 2 t4 + e + 8 s + 16 hb, bit 8 (2 s + tk) + 4 e
+    // and the partner token (tk ^ 1) is lane ^ 16.
+    uint32_t pw[2][4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) pw[hh][t4] = 0u;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float4 *rv = reinterpret_cast<const float4 *>(S.rec[rec_slot(32 * q + i)]);
+      const float4 r0 = rv[0];
+      const float xv = (i & 1) ? x[i >> 1].y : x[i >> 1].x;
+      const float dm = __fsub_rn(xv, r0.x);
+      uint32_t code = (dm >= r0.y) + (dm >= r0.z) + (dm >= r0.w);
+      if constexpr (BITS == 4) {
+#pragma unroll
+        for (int kk = 1; kk < 4; ++kk) {
+          const float4 rk = rv[kk];
+          code += (dm >= rk.x) + (dm >= rk.y) + (dm >= rk.z) + (dm >= rk.w);
         }
       }
+      const int e = i & 1, t4 = (i >> 1) & 3, sb = (i >> 3) & 1, hb = i >> 4;
+      if (BITS == 2) pw[0][t4] |= code << (16 * hb + 4 * sb + 2 * e);
+      else pw[hb][t4] |= code << (16 * sb + 4 * e);
     }
-    __syncthreads();
-    for (int tile = 0; tile < PAGE / TILE; ++tile)
-      if ((gmask >> ((TILE * tile) / G)) & 1u) pack_tile<BITS, 0>(S.kc, pg + tile * PL.tile_bytes, tile, PAGE, tid, THREADS);
-    __syncthreads();
+    uint32_t *tw = reinterpret_cast<uint32_t *>(pg + (g0 / TILE + tile) * PL.tile_bytes);
+#pragma unroll
+    for (int hh = 0; hh < BITS / 2; ++hh)
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) {
+        uint32_t w = pw[hh][t4] << (8 * tk);
+        w |= __shfl_xor_sync(0xffffffffu, w, 16);
+        if ((t4 >> 1) == tk) {
+          if (BITS == 2) tw[(4 * g + t4) * 4 + q] = w;
+          else tw[(4 * g + t4) * 8 + 2 * q + hh] = w;
+        }
+      }
   }
 
-  // ---- new fp16 tail (only the CTA of the last touched page) ----
+  // ---- new fp16 tail (only the CTA of the last touched group): 16-byte pieces, every
+  // load issued before the first store ----
   if (blockIdx.x == gridDim.x - 1) {
-    long long tstart = (T1 / G) * G;
-    const __half *told = a.tail_old + unit * (long long)G * D;
-    __half *tnew = a.tail_new + unit * (long long)G * D;
-    int ntail = (int)(T1 - tstart);
-    for (int i = tid; i < ntail * D; i += THREADS) {
-      int r = i / D, c = i % D;
-      long long t = tstart + r;
-      __half v = t < T0 ? told[(t - (T0 / G) * G) * D + c]
-                        : a.k[(t - T0) * (long long)row_stride + (long long)lh * D + c];
-      tnew[r * D + c] = v;
+    const long long tstart = (T1 / GT) * GT, ts0 = (T0 / GT) * GT;
+    __half *tnew = a.tail_new + unit * (long long)GT * D;
+    const int npc = (int)(T1 - tstart) * (D / 8);
+    constexpr int PER = (GT * (D / 8) + NT - 1) / NT;
+    uint4 v[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid + k * NT;
+      if (i < npc) {
+        const long long t = tstart + (i >> 4);
+        const int c = 8 * (i & 15);
+        v[k] = *reinterpret_cast<const uint4 *>(t < T0 ? told + (t - ts0) * D + c
+                                                       : a.k + (t - T0) * (long long)row_stride + (long long)lh * D + c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid + k * NT;
+      if (i < npc) *reinterpret_cast<uint4 *>(tnew + (i >> 4) * D + 8 * (i & 15)) = v[k];
     }
   }
 }
 
+// Shared-memory sizes, and one carveout (all shared) for every append kernel: CTAs of
+// kernels whose L1 / shared split differs do not share an SM, and the key CTAs are
+// meant to run beside the value CTAs.
+template <class K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (r == cudaSuccess)
+    r = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  return r;
+}
 template <int BITS>
 cudaError_t set_append_attrs() {
-  cudaError_t r = cudaFuncSetAttribute(append_value_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(ValueSmem));
-  if (r == cudaSuccess)
-    r = cudaFuncSetAttribute(append_key_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(KeySmem));
-  if (r == cudaSuccess)
-    r = cudaFuncSetAttribute(append_key_kernel<BITS>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  cudaError_t r = set_smem(append_value_kernel<BITS>, V_SMEM_BYTES);
+  if (r == cudaSuccess) r = set_smem(append_key_kernel<BITS, 32>, sizeof(KeySmem<BITS, 32>));
+  if (r == cudaSuccess) r = set_smem(append_key_kernel<BITS, 64>, sizeof(KeySmem<BITS, 64>));
+  if (r == cudaSuccess) r = set_smem(append_turbo_kernel<BITS>, sizeof(TurboSmem));
   return r;
+}
+
+// cuTensorMapEncodeTiled, looked up in the driver once
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
 }
 
 }  // namespace
@@ -688,14 +909,42 @@ cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s, cuda
   });
   if (e != cudaSuccess) return e;
   if (a.vppc < 1 || a.vppc > V_MAX_PPC) return cudaErrorInvalidValue;
-  const dim3 kgrid(n_pages, a.L * a.Hkv), vgrid((n_pages + a.vppc - 1) / a.vppc, a.L * a.Hkv);
+  // the chunk's values as a 2-D tensor [n tokens][L * Hkv * 128 channels]; a box is
+  // 64 channels x 64 tokens, written to shared memory with the 128-byte swizzle
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tmv;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.L * a.Hkv * D, (cuuint64_t)a.n};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.L * a.Hkv * D * sizeof(__half)};
+  const cuuint32_t box[2] = {64, PAGE}, estr[2] = {1, 1};
+  if (enc(&tmv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(a.v), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int upl = a.L * a.Hkv;
+  const dim3 vgrid((n_pages + a.vppc - 1) / a.vppc, upl);
+  // the value grid first (about one CTA per SM), then the key grid on `aux` fills the
+  // room the value CTAs leave
   if ((e = cudaEventRecord(fork, s)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(aux, fork, 0)) != cudaSuccess) return e;
-  if (a.bits == 2) append_key_kernel<2><<<kgrid, THREADS, sizeof(KeySmem), aux>>>(a);
-  else append_key_kernel<4><<<kgrid, THREADS, sizeof(KeySmem), aux>>>(a);
+  if (a.bits == 2) append_value_kernel<2><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
+  else append_value_kernel<4><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.bits == 2) append_value_kernel<2><<<vgrid, VTHREADS, sizeof(ValueSmem), s>>>(a);
-  else append_value_kernel<4><<<vgrid, VTHREADS, sizeof(ValueSmem), s>>>(a);
+  if ((e = cudaStreamWaitEvent(aux, fork, 0)) != cudaSuccess) return e;
+  if (a.G == 0) {
+    const dim3 tgrid(n_pages, upl);
+    if (a.bits == 2) append_turbo_kernel<2><<<tgrid, THREADS, sizeof(TurboSmem), aux>>>(a);
+    else append_turbo_kernel<4><<<tgrid, THREADS, sizeof(TurboSmem), aux>>>(a);
+  } else {
+    const long long T1 = a.T0 + a.n;
+    const dim3 kgrid((unsigned)((T1 - 1) / a.G - a.T0 / a.G + 1), upl);
+    if (a.G == 32) {
+      if (a.bits == 2) append_key_kernel<2, 32><<<kgrid, 128, sizeof(KeySmem<2, 32>), aux>>>(a);
+      else append_key_kernel<4, 32><<<kgrid, 128, sizeof(KeySmem<4, 32>), aux>>>(a);
+    } else {
+      if (a.bits == 2) append_key_kernel<2, 64><<<kgrid, 256, sizeof(KeySmem<2, 64>), aux>>>(a);
+      else append_key_kernel<4, 64><<<kgrid, 256, sizeof(KeySmem<4, 64>), aux>>>(a);
+    }
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = cudaEventRecord(join, aux)) != cudaSuccess) return e;
   return cudaStreamWaitEvent(s, join, 0);

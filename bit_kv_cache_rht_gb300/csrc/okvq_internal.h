@@ -54,15 +54,8 @@ constexpr int PAGE = 64;
 constexpr int TILE = 16;
 constexpr int MAXM = 3;
 constexpr int MAXGQ = 8;
-constexpr int V_MAX_PPC = 16;      // pages one CTA of the value append takes at most
-
-// Offset (fp16 elements) of (row x, channel c) of a 128-channel matrix in the tensor
-// core's K-major layout without swizzle: 8 x 8 core matrices of 128 B (8 consecutive
-// channels per 16-byte row), channel-block neighbours 128 B apart, 8-row blocks 2 KB
-// apart.
-__host__ __device__ constexpr int kmajor_off(int x, int c) {
-  return ((x >> 3) * (D / 8) + (c >> 3)) * 64 + (x & 7) * 8 + (c & 7);
-}
+constexpr int V_MAX_PPC = 32;      // pages one CTA of the value append takes at most
+constexpr int MAX_G = 64;          // largest key group (group sizes are 32 or 64)
 
 enum : uint32_t { ERR_MODALITY = 1u, ERR_WAIT = 2u };
 
@@ -150,7 +143,7 @@ struct AppendArgs {
   __half *tail_new;         // [units][G][D] buffer written (next)
   uint8_t *mod;             // [S][cap] session modality ids
   long long cap;            // max_tokens rounded up to a page
-  const __half *rot_h;      // [L][Hkv][M][2][D * D]: R[i][c] as fp16 high, then residual part, each at kmajor_off(i, c)
+  const __half *rot_h;      // [L][Hkv][M][2][D][D]: R[i][c] as fp16 high, then residual part
   const float *signs;       // [D] +-1 Hadamard signs
   uint32_t *err;
   long long page0;          // first page touched
