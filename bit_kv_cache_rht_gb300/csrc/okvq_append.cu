@@ -132,7 +132,8 @@ __device__ void unpack_tile(uint8_t *codes, const uint8_t *src, int tile, int ke
 // ---------------------------------------------------------------------------
 // Values: w = sqrt(d) R_m v / |v| on the 5th-generation tensor cores, then codes
 // ---------------------------------------------------------------------------
-constexpr int VTHREADS = 256;              // 8 warps: warp w reads accumulator lanes 32 (w % 4) .., tokens 32 (w / 4) ..
+constexpr int VWARPS = 8;                  // warp w reads accumulator lanes 32 (w % 4) .. (all 64 tokens when 4 warps)
+constexpr int VTHREADS = 32 * VWARPS;
 constexpr uint32_t V_TMEM_COLS = 256;      // two accumulators of 64 fp32 columns, then R_m (2 x 64 columns of fp16 pairs)
 constexpr uint32_t V_TMEM_R = 128;         // first column of R_m: high part, then residual
 constexpr int V_NBUF = 3;                  // pages in flight
@@ -217,7 +218,7 @@ __device__ __forceinline__ uint32_t v_keep_mask(int t4, int keep_end) {
 // accumulator: w = D[o][t] * sqrt(d) / |v_t| against the value thresholds.
 //
 // Packing: the thread of accumulator lane o = 32 quarter + 8 i + g holds channel o
-// of its 32 tokens; in the V layout channel o of decode lane (g, t4) sits in chunk
+// of its tokens; in the V layout channel o of decode lane (g, t4) sits in chunk
 // word `quarter` (2-bit) or 2 quarter + i/2 (4-bit), at a bit offset set by i, the
 // token's half and parity. The four (2-bit) or two (4-bit) threads that share a
 // word are lanes g + 8 i of one warp, so two (one) xor-shuffles complete it.
@@ -256,9 +257,9 @@ __global__ void __launch_bounds__(VTHREADS, 2)
 
   // R_m into tensor memory: warp w writes part w / 4 of rows 32 (w % 4) .. (row o =
   // lane o, fp16 pairs); every load of the row is issued before the stores
-  const int rpart = warp >> 2, rrow = 32 * quarter + lane;
-  auto fetch_r = [&](int m, uint4 (&rr)[16]) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.rot_h + ((long long)(lh * a.M + m) * 2 + rpart) * D * D +
+  const int rpart = half, rrow = 32 * quarter + lane;     // 8 warps: part w / 4; 4 warps: both parts in turn
+  auto fetch_r = [&](int m, int part, uint4 (&rr)[16]) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.rot_h + ((long long)(lh * a.M + m) * 2 + part) * D * D +
                                                        (long long)rrow * D);
 #pragma unroll
     for (int k = 0; k < 16; ++k) rr[k] = src[k];
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(VTHREADS, 2)
   // the rotation of modality 0 (usually the first round's) is on its way during the
   // bookkeeping below
   uint4 rfirst[16];
-  fetch_r(0, rfirst);
+  fetch_r(0, rpart, rfirst);
 
   // ---- the run's modality ids (validated) and the session's copy of them; every
   // load issued before the first store ----
@@ -311,8 +312,8 @@ __global__ void __launch_bounds__(VTHREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem;
-  auto store_r = [&](const uint4 (&rr)[16]) {
-    const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + V_TMEM_R + 64 * rpart;
+  auto store_r = [&](int part, const uint4 (&rr)[16]) {
+    const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + V_TMEM_R + 64 * part;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t r[32];
@@ -393,8 +394,8 @@ __global__ void __launch_bounds__(VTHREADS, 2)
     // norms: 4 threads per token (thread q: channels 32q .. 32q+31), partial sums of 4
     // channels combined in the order of a 32-lane xor-shuffle tree over lanes holding
     // channels 4l .. 4l+3 (levels 16 and 8 across the token's threads, 4, 2, 1 inside)
-    {
-      const int t = tid >> 2, q = tid & 3;
+    for (int t0 = 0; t0 < PAGE; t0 += VTHREADS / 4) {
+      const int t = t0 + (tid >> 2), q = tid & 3;
       float s8[8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -434,10 +435,14 @@ __global__ void __launch_bounds__(VTHREADS, 2)
     return true;
   };
 
-  uint32_t pw[2][PW];
+  uint32_t pw[16 / VWARPS][PW];                   // chunk words of the page's tiles this warp packs
   if (nr > 0) {
-    if (S.rmod[0] != 0) fetch_r(S.rmod[0], rfirst);
-    store_r(rfirst);
+    if (S.rmod[0] != 0) fetch_r(S.rmod[0], rpart, rfirst);
+    store_r(rpart, rfirst);
+    for (int part = rpart + VWARPS / 4; part < 2; part += VWARPS / 4) {
+      fetch_r(S.rmod[0], part, rfirst);
+      store_r(part, rfirst);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -465,56 +470,75 @@ __global__ void __launch_bounds__(VTHREADS, 2)
       waited = r + 1;
     }
     tc_fence_after();
+    constexpr int NHC = 8 / VWARPS;                // 32-token column blocks a warp takes
     if (r == 0 || S.rpage[r - 1] != p) {
 #pragma unroll
-      for (int tl = 0; tl < 2; ++tl)
+      for (int tl = 0; tl < 2 * NHC; ++tl)
 #pragma unroll
         for (int k = 0; k < PW; ++k) pw[tl][k] = 0u;
     }
-    float acc[32];
-    tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)((r & 1) * PAGE + 32 * half), acc);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    const uint32_t mm = S.mmask[r & 1][half];
-    uint32_t wr[2][4];
 #pragma unroll
-    for (int tl = 0; tl < 2; ++tl)
-#pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4) wr[tl][t4] = 0u;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t sel = (mm >> j) & 1u;
-      const uint32_t code = (uint32_t)code_of<NTHR>(acc[j] * S.sc[r & 1][32 * half + j], a.vthr) & (0u - sel);
-      const int tt = j & 15;
-      wr[j >> 4][(tt & 7) >> 1] |= code << (BITS == 2 ? 8 * (tt >> 3) + 2 * (tt & 1) : 16 * (tt >> 3) + 4 * (tt & 1));
-    }
-    if constexpr (BITS == 2) {
-      const int sh = 16 * (iq >> 1) + 4 * (iq & 1);
+    for (int hb = 0; hb < NHC; ++hb) {
+      const int hc = NHC == 1 ? half : hb;         // tokens 32 hc .. 32 hc + 31 (tiles 2 hc, 2 hc + 1)
+      float acc[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)((r & 1) * PAGE + 32 * hc), acc);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const uint32_t mm = S.mmask[r & 1][hc];
+      const float4 *scv = reinterpret_cast<const float4 *>(&S.sc[r & 1][32 * hc]);
+      uint32_t wr[2][4];
 #pragma unroll
       for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
-        for (int t4 = 0; t4 < 4; ++t4) {
-          uint32_t w = wr[tl][t4] << sh;
-          w |= __shfl_xor_sync(0xffffffffu, w, 8);
-          w |= __shfl_xor_sync(0xffffffffu, w, 16);
-          if (t4 == iq) pw[tl][0] |= w;
-        }
-    } else {
-      const int sh = 8 * (iq & 1);
+        for (int t4 = 0; t4 < 4; ++t4) wr[tl][t4] = 0u;
 #pragma unroll
-      for (int tl = 0; tl < 2; ++tl)
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 sc4 = scv[j4];
+        const float scj[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
 #pragma unroll
-        for (int t4 = 0; t4 < 4; ++t4) {
-          uint32_t w = wr[tl][t4] << sh;
-          w |= __shfl_xor_sync(0xffffffffu, w, 8);
-          if ((t4 >> 1) == (iq & 1)) pw[tl][t4 & 1] |= w;
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * j4 + jj;
+          const float x = acc[j] * scj[jj];
+          uint32_t code;
+          if constexpr (BITS == 2) {                 // sorted thresholds: one compare picks the half
+            const bool up = x > a.vthr[1];
+            code = (up ? 2u : 0u) + (x > (up ? a.vthr[2] : a.vthr[0]) ? 1u : 0u);
+          } else {
+            code = (uint32_t)code_of<NTHR>(x, a.vthr);
+          }
+          code &= 0u - ((mm >> j) & 1u);
+          const int tt = j & 15;
+          wr[j >> 4][(tt & 7) >> 1] |= code << (BITS == 2 ? 8 * (tt >> 3) + 2 * (tt & 1) : 16 * (tt >> 3) + 4 * (tt & 1));
         }
+      }
+      if constexpr (BITS == 2) {
+        const int sh = 16 * (iq >> 1) + 4 * (iq & 1);
+#pragma unroll
+        for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            uint32_t w = wr[tl][t4] << sh;
+            w |= __shfl_xor_sync(0xffffffffu, w, 8);
+            w |= __shfl_xor_sync(0xffffffffu, w, 16);
+            if (t4 == iq) pw[2 * hb + tl][0] |= w;
+          }
+      } else {
+        const int sh = 8 * (iq & 1);
+#pragma unroll
+        for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            uint32_t w = wr[tl][t4] << sh;
+            w |= __shfl_xor_sync(0xffffffffu, w, 8);
+            if ((t4 >> 1) == (iq & 1)) pw[2 * hb + tl][t4 & 1] |= w;
+          }
+      }
     }
     tc_fence_before();
     // the page's last round: store its chunk words (older tokens of a tile kept)
     if (r + 1 == nr || S.rpage[r + 1] != p) {
 #pragma unroll
-      for (int tl = 0; tl < 2; ++tl) {
-        const int tau = 2 * half + tl;
+      for (int tl = 0; tl < 2 * NHC; ++tl) {
+        const int tau = NHC == 1 ? 2 * half + tl : tl;
         if (TILE * tau + TILE <= ta || TILE * tau >= tb) continue;
         uint32_t *tw = reinterpret_cast<uint32_t *>(pg + PL.off_v + tau * PL.tile_bytes);
 #pragma unroll
@@ -533,10 +557,10 @@ __global__ void __launch_bounds__(VTHREADS, 2)
     if (tid == 0 && (r + 1 == nr || S.rpage[r + 1] != p) && p + V_NBUF < npg) issue_page(p + V_NBUF);
     // a new rotation: written once round r's MMAs (the last readers of R) completed
     if (r + 1 < nr && !next_same) {
-      {
+      for (int part = rpart; part < 2; part += VWARPS / 4) {
         uint4 rr[16];
-        fetch_r(S.rmod[r + 1], rr);
-        store_r(rr);
+        fetch_r(S.rmod[r + 1], part, rr);
+        store_r(part, rr);
       }
       tc_fence_before();
       __syncthreads();
