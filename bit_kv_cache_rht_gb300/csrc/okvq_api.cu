@@ -757,11 +757,15 @@ okvq_status okvq_append_chunk(okvq_cache *h, int32_t session, const void *k, con
   }
   const long long last = (T0 + num_tokens - 1) / PAGE;
   const int n_pages = (int)(last - a.page0 + 1);
-  // value CTAs: about one per SM (the key CTAs of the chunk share the SMs with them),
-  // at most V_MAX_PPC pages each
+  // value CTAs: one per SM for short chunks, two per SM (each holds half of the tensor
+  // memory) once a unit's chunk spans 24 pages or more (measured: 665-token chunks
+  // are faster with one, 2,329-token chunks with two); the key CTAs of the chunk
+  // share the SMs with them; at most V_MAX_PPC pages each
   const int upl = h->L * h->Hkv;
-  const int cpu = std::max(1, std::min(n_pages, h->num_sms / std::max(1, upl)));
+  const int per_sm = n_pages >= 24 ? 2 : 1;
+  const int cpu = std::max(1, std::min(n_pages, per_sm * h->num_sms / std::max(1, upl)));
   a.vppc = std::min(V_MAX_PPC, (n_pages + cpu - 1) / cpu);
+  a.vwide = per_sm == 2 ? 1 : 0;
   cudaError_t e = launch_append(a, n_pages, static_cast<cudaStream_t>(stream), h->key_stream, h->ev_fork, h->ev_join);
   if (e != cudaSuccess) return cuda_status(e);
   h->len[session] = T0 + num_tokens;

@@ -222,8 +222,10 @@ __device__ __forceinline__ uint32_t v_keep_mask(int t4, int keep_end) {
 // word `quarter` (2-bit) or 2 quarter + i/2 (4-bit), at a bit offset set by i, the
 // token's half and parity. The four (2-bit) or two (4-bit) threads that share a
 // word are lanes g + 8 i of one warp, so two (one) xor-shuffles complete it.
-template <int BITS>
-__global__ void __launch_bounds__(VTHREADS, 2)
+// WIDE: the register budget of two value CTAs per SM beside the key CTAs (long
+// chunks); otherwise one per SM, with the first part of R_m fetched whole at start.
+template <int BITS, bool WIDE>
+__global__ void __launch_bounds__(VTHREADS, WIDE ? 3 : 2)
     append_value_kernel(const AppendArgs a, const __grid_constant__ CUtensorMap tmv) {
   constexpr int NTHR = (1 << BITS) - 1;
   constexpr int PW = BITS / 2;                     // chunk words a thread stores per tile
@@ -258,17 +260,19 @@ __global__ void __launch_bounds__(VTHREADS, 2)
   // R_m into tensor memory: warp w writes part w / 4 of rows 32 (w % 4) .. (row o =
   // lane o, fp16 pairs); every load of the row is issued before the stores
   const int rpart = half, rrow = 32 * quarter + lane;     // 8 warps: part w / 4; 4 warps: both parts in turn
-  auto fetch_r = [&](int m, int part, uint4 (&rr)[16]) {
+  auto fetch_r = [&](int m, int part, int hh, uint4 (&rr)[8]) {   // half row hh of part `part`
     const uint4 *src = reinterpret_cast<const uint4 *>(a.rot_h + ((long long)(lh * a.M + m) * 2 + part) * D * D +
-                                                       (long long)rrow * D);
+                                                       (long long)rrow * D) + 8 * hh;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) rr[k] = src[k];
+    for (int k = 0; k < 8; ++k) rr[k] = src[k];
   };
 
   // the rotation of modality 0 (usually the first round's) is on its way during the
   // bookkeeping below
-  uint4 rfirst[16];
-  fetch_r(0, rpart, rfirst);
+  constexpr int NPRE = WIDE ? 1 : 2;               // half rows of R_m fetched at kernel start
+  uint4 rfirst[NPRE][8];
+#pragma unroll
+  for (int h = 0; h < NPRE; ++h) fetch_r(0, rpart, h, rfirst[h]);
 
   // ---- the run's modality ids (validated) and the session's copy of them; every
   // load issued before the first store ----
@@ -312,20 +316,27 @@ __global__ void __launch_bounds__(VTHREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem;
-  auto store_r = [&](int part, const uint4 (&rr)[16]) {
-    const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + V_TMEM_R + 64 * part;
+  auto store_r = [&](int part, int hh, const uint4 (&rr)[8]) {
+    uint32_t r[32];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t r[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        r[4 * k] = rr[8 * hh + k].x;
-        r[4 * k + 1] = rr[8 * hh + k].y;
-        r[4 * k + 2] = rr[8 * hh + k].z;
-        r[4 * k + 3] = rr[8 * hh + k].w;
-      }
-      tmem_st32(ta + 32 * hh, r);
+    for (int k = 0; k < 8; ++k) {
+      r[4 * k] = rr[k].x;
+      r[4 * k + 1] = rr[k].y;
+      r[4 * k + 2] = rr[k].z;
+      r[4 * k + 3] = rr[k].w;
     }
+    tmem_st32(tmem + ((uint32_t)(32 * quarter) << 16) + V_TMEM_R + 64 * part + 32 * hh, r);
+  };
+  // R_m of modality m into tensor memory (this warp's parts, half rows in turn); the
+  // first NPRE half rows may already be in `first`
+  auto load_r = [&](int m, uint4 (&first)[NPRE][8], bool have_first) {
+    for (int part = rpart; part < 2; part += VWARPS / 4)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint4 (&buf)[8] = first[hh % NPRE];
+        if (!(have_first && part == rpart && hh < NPRE)) fetch_r(m, part, hh, buf);
+        store_r(part, hh, buf);
+      }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   };
   for (int i = tid; i < npg * PAGE; i += VTHREADS)
@@ -437,12 +448,7 @@ __global__ void __launch_bounds__(VTHREADS, 2)
 
   uint32_t pw[16 / VWARPS][PW];                   // chunk words of the page's tiles this warp packs
   if (nr > 0) {
-    if (S.rmod[0] != 0) fetch_r(S.rmod[0], rpart, rfirst);
-    store_r(rpart, rfirst);
-    for (int part = rpart + VWARPS / 4; part < 2; part += VWARPS / 4) {
-      fetch_r(S.rmod[0], part, rfirst);
-      store_r(part, rfirst);
-    }
+    load_r(S.rmod[0], rfirst, S.rmod[0] == 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -557,11 +563,7 @@ __global__ void __launch_bounds__(VTHREADS, 2)
     if (tid == 0 && (r + 1 == nr || S.rpage[r + 1] != p) && p + V_NBUF < npg) issue_page(p + V_NBUF);
     // a new rotation: written once round r's MMAs (the last readers of R) completed
     if (r + 1 < nr && !next_same) {
-      for (int part = rpart; part < 2; part += VWARPS / 4) {
-        uint4 rr[16];
-        fetch_r(S.rmod[r + 1], part, rr);
-        store_r(part, rr);
-      }
+      load_r(S.rmod[r + 1], rfirst, false);
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
@@ -895,7 +897,8 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }
 template <int BITS>
 cudaError_t set_append_attrs() {
-  cudaError_t r = set_smem(append_value_kernel<BITS>, V_SMEM_BYTES);
+  cudaError_t r = set_smem(append_value_kernel<BITS, false>, V_SMEM_BYTES);
+  if (r == cudaSuccess) r = set_smem(append_value_kernel<BITS, true>, V_SMEM_BYTES);
   if (r == cudaSuccess) r = set_smem(append_key_kernel<BITS, 32>, sizeof(KeySmem<BITS, 32>));
   if (r == cudaSuccess) r = set_smem(append_key_kernel<BITS, 64>, sizeof(KeySmem<BITS, 64>));
   if (r == cudaSuccess) r = set_smem(append_turbo_kernel<BITS>, sizeof(TurboSmem));
@@ -950,8 +953,13 @@ cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s, cuda
   // the value grid first (about one CTA per SM), then the key grid on `aux` fills the
   // room the value CTAs leave
   if ((e = cudaEventRecord(fork, s)) != cudaSuccess) return e;
-  if (a.bits == 2) append_value_kernel<2><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
-  else append_value_kernel<4><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
+  if (a.bits == 2) {
+    if (a.vwide) append_value_kernel<2, true><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
+    else append_value_kernel<2, false><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
+  } else {
+    if (a.vwide) append_value_kernel<4, true><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
+    else append_value_kernel<4, false><<<vgrid, VTHREADS, V_SMEM_BYTES, s>>>(a, tmv);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = cudaStreamWaitEvent(aux, fork, 0)) != cudaSuccess) return e;
   if (a.G == 0) {

@@ -148,6 +148,7 @@ struct AppendArgs {
   uint32_t *err;
   long long page0;          // first page touched
   int vppc;                 // pages per CTA of the value kernel (1 .. V_MAX_PPC)
+  int vwide;                // 1: two value CTAs per SM (their register budget), 0: one
   int nlev;
   float vthr[15];           // fp32 value thresholds (midpoints of the fp16 levels)
   float kthr[15];           // fp32 key thresholds (midpoints of the fp16 key levels)
