@@ -8,6 +8,7 @@
 #include <new>
 #include <vector>
 
+#include "okvq_append.h"
 #include "okvq_internal.h"
 
 using namespace okvq;

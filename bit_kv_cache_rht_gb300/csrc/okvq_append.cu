@@ -23,7 +23,7 @@
 //     touched page writes the new fp16 tail into the other tail buffer.
 #include <cuda.h>
 
-#include "okvq_internal.h"
+#include "okvq_append.h"
 
 namespace okvq {
 

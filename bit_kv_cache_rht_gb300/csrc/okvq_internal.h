@@ -54,8 +54,6 @@ constexpr int PAGE = 64;
 constexpr int TILE = 16;
 constexpr int MAXM = 3;
 constexpr int MAXGQ = 8;
-constexpr int V_MAX_PPC = 32;      // pages one CTA of the value append takes at most
-constexpr int MAX_G = 64;          // largest key group (group sizes are 32 or 64)
 
 enum : uint32_t { ERR_MODALITY = 1u, ERR_WAIT = 2u };
 
@@ -128,31 +126,6 @@ __host__ __device__ inline int stat_pos(int c) {
   const int t = (r & 7) >> 1, i = (r & 1) | ((r >> 3) << 1);
   return 32 * (kb >> 1) + 8 * t + 4 * (kb & 1) + i;
 }
-
-struct AppendArgs {
-  const __half *k;          // [n][L][Hkv][D]
-  const __half *v;
-  const uint8_t *mod_in;    // [n]
-  int n;                    // tokens in this chunk
-  long long T0;             // session length before the append
-  int session;
-  int L, Hkv, M, bits, G;   // G: key group size, 0 = TurboQuant keys (per-token norms)
-  long long P_max;
-  uint8_t *pages;           // all units
-  __half *tail_old;         // [units][G][D] buffer read (current)
-  __half *tail_new;         // [units][G][D] buffer written (next)
-  uint8_t *mod;             // [S][cap] session modality ids
-  long long cap;            // max_tokens rounded up to a page
-  const __half *rot_h;      // [L][Hkv][M][2][D][D]: R[i][c] as fp16 high, then residual part
-  const float *signs;       // [D] +-1 Hadamard signs
-  uint32_t *err;
-  long long page0;          // first page touched
-  int vppc;                 // pages per CTA of the value kernel (1 .. V_MAX_PPC)
-  int vwide;                // 1: two value CTAs per SM (their register budget), 0: one
-  int nlev;
-  float vthr[15];           // fp32 value thresholds (midpoints of the fp16 levels)
-  float kthr[15];           // fp32 key thresholds (midpoints of the fp16 key levels)
-};
 
 struct DecodeArgs {
   const __half *q;          // [S][L][Hq][D]
@@ -269,8 +242,6 @@ cudaError_t once_per_device(std::atomic<uint64_t> &done, Fn set) {
   return e;
 }
 
-cudaError_t launch_append(const AppendArgs &a, int n_pages, cudaStream_t s, cudaStream_t aux, cudaEvent_t fork,
-                          cudaEvent_t join);
 cudaError_t launch_decode(const DecodeArgs &a, int n_cta, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_lut(int bits, const LutArgs &a, cudaStream_t s);
