@@ -173,6 +173,13 @@ def test_capacity_and_argument_errors():
     assert c.length(0) == 100                   # unchanged
     st = okvq.okvq_append_chunk(c._h, 1, K.data_ptr(), K.data_ptr(), M.data_ptr(), 4)
     assert st == okvq.OKVQ_EINVAL               # no such session
+    # keys or values not 16-byte aligned (the value rows are copied in 16-byte pieces)
+    B = torch.zeros(4 * 256 + 16, dtype=torch.uint8, device="cuda")
+    for koff, voff in ((2, 0), (0, 8)):
+        st = okvq.okvq_append_chunk(c._h, 0, B.data_ptr() + koff, B.data_ptr() + voff, M.data_ptr(), 4)
+        assert st == okvq.OKVQ_EINVAL
+    assert c.length(0) == 100                   # nothing appended
+    assert c.check_errors() == 0
 
 
 def test_bad_modality_sets_error_word():
