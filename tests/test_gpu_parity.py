@@ -174,7 +174,7 @@ def test_capacity_and_argument_errors():
     st = okvq.okvq_append_chunk(c._h, 1, K.data_ptr(), K.data_ptr(), M.data_ptr(), 4)
     assert st == okvq.OKVQ_EINVAL               # no such session
     # keys or values not 16-byte aligned (the value rows are copied in 16-byte pieces)
-    B = torch.zeros(4 * 256 + 16, dtype=torch.uint8, device="cuda")
+    B = torch.zeros(4 * 2 * 2 * 128 * 2 + 16, dtype=torch.uint8, device="cuda")   # room for 4 tokens either way
     for koff, voff in ((2, 0), (0, 8)):
         st = okvq.okvq_append_chunk(c._h, 0, B.data_ptr() + koff, B.data_ptr() + voff, M.data_ptr(), 4)
         assert st == okvq.OKVQ_EINVAL
