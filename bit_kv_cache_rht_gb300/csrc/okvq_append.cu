@@ -152,7 +152,10 @@ struct ValueSmem {
   uint32_t mmask[2][2];            // a round's tokens
   int nround;
   uint32_t tmem;
+  int mma_issued;                  // rounds whose MMAs were issued (producer thread 0)
+  int pages_seen;                  // pages whose copy a producer saw complete
   uint64_t bar_v[V_NBUF], bar_mma[2];
+  uint64_t bar_full[2], bar_empty[2], bar_rload;   // producer / consumer handshakes
 };
 constexpr size_t V_SMEM_BYTES = sizeof(ValueSmem) + 1024;   // + alignment slack
 
@@ -227,7 +230,6 @@ __device__ __forceinline__ uint32_t v_keep_mask(int t4, int keep_end) {
 template <int BITS, bool WIDE>
 __global__ void __launch_bounds__(VTHREADS, WIDE ? 3 : 2)
     append_value_kernel(const AppendArgs a, const __grid_constant__ CUtensorMap tmv) {
-  constexpr int NTHR = (1 << BITS) - 1;
   constexpr int PW = BITS / 2;                     // chunk words a thread stores per tile
   extern __shared__ __align__(128) unsigned char smem_raw[];
   ValueSmem &S = *reinterpret_cast<ValueSmem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
@@ -303,7 +305,14 @@ __global__ void __launch_bounds__(VTHREADS, WIDE ? 3 : 2)
   if (tid == 0) {
     for (int b = 0; b < V_NBUF; ++b)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_v[b])));
-    for (int b = 0; b < 2; ++b) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_mma[b])));
+    for (int b = 0; b < 2; ++b) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar_mma[b])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&S.bar_full[b])), "r"(VTHREADS / 2));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&S.bar_empty[b])), "r"(VTHREADS / 2));
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&S.bar_rload)), "r"(VTHREADS / 2));
+    S.mma_issued = 0;
+    S.pages_seen = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int p = 0; p < V_NBUF && p < npg; ++p) issue_page(p);    // the first pages, before the bookkeeping
   }
@@ -366,213 +375,219 @@ __global__ void __launch_bounds__(VTHREADS, WIDE ? 3 : 2)
   __syncthreads();
   const int nr = S.nround;
 
-  bool failed = false;
-  int issued = 0, waited = 0;                      // rounds whose MMAs were issued / seen complete
-  int pages_seen = 0;                              // pages whose copy completed
-  // stage A: the round's values and rotation are in; MMAs into accumulator r % 2,
-  // then the round's token mask and norms
-  auto stage_a = [&](int r) -> bool {
-    const int p = S.rpage[r], m = S.rmod[r], buf = p % V_NBUF;
-    const bool ok = wait_bar(&S.bar_v[buf], (uint32_t)(p / V_NBUF) & 1u);
-    if (ok) pages_seen = max(pages_seen, p + 1);
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) return false;
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(PAGE >> 3) << 17) | ((uint32_t)(D >> 4) << 24);
-      const uint32_t vb = smem_addr(&S.v[buf][0]);
-      const uint32_t dt = tmem + (uint32_t)((r & 1) * PAGE);
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t at = tmem + V_TMEM_R + (uint32_t)(64 * part + 8 * ks);
-          const uint64_t bd = sw128_desc(vb + (uint32_t)((ks >> 2) * V_HALF_BYTES + (ks & 3) * 32));
-          asm volatile(
-              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dt),
-              "r"(at), "l"(bd), "r"(idesc), "r"((part | ks) ? 1u : 0u));
-        }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_addr(&S.bar_mma[r & 1]))
-                   : "memory");
-    }
-    issued = r + 1;
-    if (warp < 2) {
-      const uint32_t b = __ballot_sync(0xffffffffu, S.mod[p * PAGE + tid] == m);
-      if (lane == 0) S.mmask[r & 1][warp] = b;
-    }
-    // norms: 4 threads per token (thread q: channels 32q .. 32q+31), partial sums of 4
-    // channels combined in the order of a 32-lane xor-shuffle tree over lanes holding
-    // channels 4l .. 4l+3 (levels 16 and 8 across the token's threads, 4, 2, 1 inside)
-    for (int t0 = 0; t0 < PAGE; t0 += VTHREADS / 4) {
-      const int t = t0 + (tid >> 2), q = tid & 3;
-      float s8[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = 4 * q + k;
-        const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(&S.v[buf][0]) +
-                                                          (c >> 3) * V_HALF_BYTES + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-        const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
-        const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
-        const float2 x2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
-        const float2 x3 = __half22float2(*reinterpret_cast<const __half2 *>(&u.w));
-        float s0 = x0.x * x0.x;
-        s0 = fmaf(x0.y, x0.y, s0);
-        s0 = fmaf(x1.x, x1.x, s0);
-        s0 = fmaf(x1.y, x1.y, s0);
-        float s1 = x2.x * x2.x;
-        s1 = fmaf(x2.y, x2.y, s1);
-        s1 = fmaf(x3.x, x3.x, s1);
-        s1 = fmaf(x3.y, x3.y, s1);
-        s8[2 * k] = s0;                          // partial 8q + 2k
-        s8[2 * k + 1] = s1;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s8[i] = __fadd_rn(s8[i], __shfl_xor_sync(0xffffffffu, s8[i], 2));   // l, l + 16
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s8[i] = __fadd_rn(s8[i], __shfl_xor_sync(0xffffffffu, s8[i], 1));   // l, l + 8
-#pragma unroll
-      for (int st = 4; st >= 1; st >>= 1)
-#pragma unroll
-        for (int i = 0; i < st; ++i) s8[i] = __fadd_rn(s8[i], s8[i + st]);
-      if (q == 0 && S.mod[p * PAGE + t] == m) {
-        const float n = sqrtf(s8[0]);
-        S.sc[r & 1][t] = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
-        uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
-        reinterpret_cast<__half *>(pg + PL.off_norm)[t] = __float2half_rn(n);
-      }
-    }
-    return true;
-  };
-
-  uint32_t pw[16 / VWARPS][PW];                   // chunk words of the page's tiles this warp packs
+  // ---- warp roles. Producers (warps 4-7): wait for a round's page, issue its MMAs
+  // into accumulator r % 2 (once the consumers freed it), take the round's token mask
+  // and norms, signal `full`. Consumers (warps 0-3, one accumulator lane quarter each,
+  // all 64 tokens): wait for `full` and the MMAs, make and pack the codes, free the
+  // accumulator (`empty`), store a page's words after its last round and copy in the
+  // page three ahead. Every handshake is an mbarrier with a bounded wait. ----
+  constexpr int NR = VTHREADS / 2;                 // threads per role
+  const bool producer = warp >= VWARPS / 2;
+  int c_waited = 0, pages_issued = min(npg, V_NBUF);
   if (nr > 0) {
     load_r(S.rmod[0], rfirst, S.rmod[0] == 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    failed = !stage_a(0);
   }
-  for (int r = 0; r < nr && !failed; ++r) {
-    const int p = S.rpage[r];
-    const long long P0 = (pbeg + p) * PAGE;
-    const int ta = (int)(max(P0, T0) - P0), tb = (int)(min(P0 + PAGE, T1) - P0);
-    uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
-    const bool next_same = r + 1 < nr && S.rmod[r + 1] == S.rmod[r];
-    // the next round's MMAs overlap this round's codes
-    if (next_same && !stage_a(r + 1)) {
-      failed = true;
-      break;
-    }
-    // ---- stage B: codes of round r ----
-    __syncthreads();                               // the round's mask and norms
-    {
-      const bool ok = wait_bar(&S.bar_mma[r & 1], (uint32_t)(r >> 1) & 1u);
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-      waited = r + 1;
-    }
-    tc_fence_after();
-    constexpr int NHC = 8 / VWARPS;                // 32-token column blocks a warp takes
-    if (r == 0 || S.rpage[r - 1] != p) {
-#pragma unroll
-      for (int tl = 0; tl < 2 * NHC; ++tl)
-#pragma unroll
-        for (int k = 0; k < PW; ++k) pw[tl][k] = 0u;
-    }
-#pragma unroll
-    for (int hb = 0; hb < NHC; ++hb) {
-      const int hc = NHC == 1 ? half : hb;         // tokens 32 hc .. 32 hc + 31 (tiles 2 hc, 2 hc + 1)
-      float acc[32];
-      tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)((r & 1) * PAGE + 32 * hc), acc);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const uint32_t mm = S.mmask[r & 1][hc];
-      const float4 *scv = reinterpret_cast<const float4 *>(&S.sc[r & 1][32 * hc]);
-      uint32_t wr[2][4];
-#pragma unroll
-      for (int tl = 0; tl < 2; ++tl)
-#pragma unroll
-        for (int t4 = 0; t4 < 4; ++t4) wr[tl][t4] = 0u;
-#pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
-        const float4 sc4 = scv[j4];
-        const float scj[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = 4 * j4 + jj;
-          const float x = acc[j] * scj[jj];
-          uint32_t code;
-          if constexpr (BITS == 2) {                 // sorted thresholds: one compare picks the half
-            const bool up = x > a.vthr[1];
-            code = (up ? 2u : 0u) + (x > (up ? a.vthr[2] : a.vthr[0]) ? 1u : 0u);
-          } else {
-            code = (uint32_t)code_of<NTHR>(x, a.vthr);
+  if (producer) {
+    const int ptid = tid - NR;
+    int reloads = 0;
+    for (int r = 0; r < nr; ++r) {
+      const int p = S.rpage[r], m = S.rmod[r], buf = p % V_NBUF;
+      bool ok = true;
+      if (r > 0 && m != S.rmod[r - 1]) {
+        // a new rotation, written once the previous round's MMAs (its last readers) are done
+        ok = __all_sync(0xffffffffu, wait_bar(&S.bar_mma[(r - 1) & 1], (uint32_t)((r - 1) >> 1) & 1u));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+            fetch_r(m, part, hh, rfirst[0]);
+            store_r(part, hh, rfirst[0]);
           }
-          code &= 0u - ((mm >> j) & 1u);
-          const int tt = j & 15;
-          wr[j >> 4][(tt & 7) >> 1] |= code << (BITS == 2 ? 8 * (tt >> 3) + 2 * (tt & 1) : 16 * (tt >> 3) + 4 * (tt & 1));
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&S.bar_rload)) : "memory");
+        ++reloads;
+      }
+      // every wait is taken by the whole warp (warp-uniform outcome: the .aligned
+      // tensor-memory instructions need converged warps)
+      ok = __all_sync(0xffffffffu, wait_bar(&S.bar_v[buf], (uint32_t)(p / V_NBUF) & 1u));
+      if (ok && ptid == 0) S.pages_seen = max(S.pages_seen, p + 1);
+      if (ok && r >= 2) ok = __all_sync(0xffffffffu, wait_bar(&S.bar_empty[r & 1], (uint32_t)((r >> 1) - 1) & 1u));
+      if (ok && reloads) ok = __all_sync(0xffffffffu, wait_bar(&S.bar_rload, (uint32_t)(reloads - 1) & 1u));
+      if (!ok) break;
+      if (ptid == 0) {
+        tc_fence_after();
+        const uint32_t idesc = (1u << 4) | ((uint32_t)(PAGE >> 3) << 17) | ((uint32_t)(D >> 4) << 24);
+        const uint32_t vb = smem_addr(&S.v[buf][0]);
+        const uint32_t dt = tmem + (uint32_t)((r & 1) * PAGE);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t at = tmem + V_TMEM_R + (uint32_t)(64 * part + 8 * ks);
+            const uint64_t bd = sw128_desc(vb + (uint32_t)((ks >> 2) * V_HALF_BYTES + (ks & 3) * 32));
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dt),
+                "r"(at), "l"(bd), "r"(idesc), "r"((part | ks) ? 1u : 0u));
+          }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_addr(&S.bar_mma[r & 1]))
+                     : "memory");
+        S.mma_issued = r + 1;
+      }
+      // the round's tokens
+      if (ptid < PAGE) {
+        const uint32_t b = __ballot_sync(0xffffffffu, S.mod[p * PAGE + ptid] == m);
+        if (lane == 0) S.mmask[r & 1][ptid >> 5] = b;
+      }
+      // norms: 2 threads per token (thread q: channels 64q .. 64q+63), partial sums of 4
+      // channels combined in the order of a 32-lane xor-shuffle tree over lanes holding
+      // channels 4l .. 4l+3 (level 16 across the token's two threads, 8 .. 1 inside)
+      {
+        const int t = ptid >> 1, q = ptid & 1;
+        float s16[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = 8 * q + k;
+          const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(&S.v[buf][0]) +
+                                                            (c >> 3) * V_HALF_BYTES + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+          const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+          const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+          const float2 x2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
+          const float2 x3 = __half22float2(*reinterpret_cast<const __half2 *>(&u.w));
+          float s0 = x0.x * x0.x;
+          s0 = fmaf(x0.y, x0.y, s0);
+          s0 = fmaf(x1.x, x1.x, s0);
+          s0 = fmaf(x1.y, x1.y, s0);
+          float s1 = x2.x * x2.x;
+          s1 = fmaf(x2.y, x2.y, s1);
+          s1 = fmaf(x3.x, x3.x, s1);
+          s1 = fmaf(x3.y, x3.y, s1);
+          s16[2 * k] = s0;                         // partial 16q + 2k
+          s16[2 * k + 1] = s1;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s16[i] = __fadd_rn(s16[i], __shfl_xor_sync(0xffffffffu, s16[i], 1));   // l, l + 16
+#pragma unroll
+        for (int st = 8; st >= 1; st >>= 1)
+#pragma unroll
+          for (int i = 0; i < st; ++i) s16[i] = __fadd_rn(s16[i], s16[i + st]);
+        if (q == 0 && S.mod[p * PAGE + t] == m) {
+          const float n = sqrtf(s16[0]);
+          S.sc[r & 1][t] = n > 0.f ? __fdiv_rn(SQRT_D, n) : 0.f;
+          uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
+          reinterpret_cast<__half *>(pg + PL.off_norm)[t] = __float2half_rn(n);
         }
       }
-      if constexpr (BITS == 2) {
-        const int sh = 16 * (iq >> 1) + 4 * (iq & 1);
-#pragma unroll
-        for (int tl = 0; tl < 2; ++tl)
-#pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            uint32_t w = wr[tl][t4] << sh;
-            w |= __shfl_xor_sync(0xffffffffu, w, 8);
-            w |= __shfl_xor_sync(0xffffffffu, w, 16);
-            if (t4 == iq) pw[2 * hb + tl][0] |= w;
-          }
-      } else {
-        const int sh = 8 * (iq & 1);
-#pragma unroll
-        for (int tl = 0; tl < 2; ++tl)
-#pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            uint32_t w = wr[tl][t4] << sh;
-            w |= __shfl_xor_sync(0xffffffffu, w, 8);
-            if ((t4 >> 1) == (iq & 1)) pw[2 * hb + tl][t4 & 1] |= w;
-          }
-      }
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&S.bar_full[r & 1])) : "memory");
     }
-    tc_fence_before();
-    // the page's last round: store its chunk words (older tokens of a tile kept)
-    if (r + 1 == nr || S.rpage[r + 1] != p) {
-#pragma unroll
-      for (int tl = 0; tl < 2 * NHC; ++tl) {
-        const int tau = NHC == 1 ? 2 * half + tl : tl;
-        if (TILE * tau + TILE <= ta || TILE * tau >= tb) continue;
-        uint32_t *tw = reinterpret_cast<uint32_t *>(pg + PL.off_v + tau * PL.tile_bytes);
-#pragma unroll
-        for (int k = 0; k < PW; ++k) {
-          const int t4 = BITS == 2 ? iq : 2 * (iq & 1) + k;
-          uint32_t *dst =
-              BITS == 2 ? tw + (4 * gq + t4) * 4 + quarter : tw + (4 * gq + t4) * 8 + 2 * quarter + (iq >> 1);
-          uint32_t val = pw[tl][k];
-          if (TILE * tau < ta) val |= *dst & v_keep_mask<BITS>(t4, ta - TILE * tau);
-          *dst = val;
-        }
-      }
-    }
-    // page p's last round: its buffer is free (MMAs completed, norms taken before the
-    // barrier above) for the page three ahead
-    if (tid == 0 && (r + 1 == nr || S.rpage[r + 1] != p) && p + V_NBUF < npg) issue_page(p + V_NBUF);
-    // a new rotation: written once round r's MMAs (the last readers of R) completed
-    if (r + 1 < nr && !next_same) {
-      load_r(S.rmod[r + 1], rfirst, false);
-      tc_fence_before();
-      __syncthreads();
+  } else {
+    uint32_t pw[4][PW];                            // chunk words of the page's four tiles (this lane quarter)
+    for (int r = 0; r < nr; ++r) {
+      const int p = S.rpage[r];
+      const long long P0 = (pbeg + p) * PAGE;
+      const int ta = (int)(max(P0, T0) - P0), tb = (int)(min(P0 + PAGE, T1) - P0);
+      uint8_t *pg = a.pages + (unit * a.P_max + pbeg + p) * (long long)PL.page_bytes;
+      if (!__all_sync(0xffffffffu, wait_bar(&S.bar_full[r & 1], (uint32_t)(r >> 1) & 1u))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(&S.bar_mma[r & 1], (uint32_t)(r >> 1) & 1u))) break;
+      c_waited = r + 1;
       tc_fence_after();
-      if (!stage_a(r + 1)) {
-        failed = true;
-        break;
+      if (r == 0 || S.rpage[r - 1] != p) {
+#pragma unroll
+        for (int tl = 0; tl < 4; ++tl)
+#pragma unroll
+          for (int k = 0; k < PW; ++k) pw[tl][k] = 0u;
+      }
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {             // tokens 32 hc .. 32 hc + 31 (tiles 2 hc, 2 hc + 1)
+        float acc[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)((r & 1) * PAGE + 32 * hc), acc);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const uint32_t mm = S.mmask[r & 1][hc];
+        const float4 *scv = reinterpret_cast<const float4 *>(&S.sc[r & 1][32 * hc]);
+        uint32_t wr[2][4];
+#pragma unroll
+        for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) wr[tl][t4] = 0u;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 sc4 = scv[j4];
+          const float scj[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * j4 + jj;
+            const float x = acc[j] * scj[jj];
+            uint32_t code;
+            if constexpr (BITS == 2) {               // sorted thresholds: one compare picks the half
+              const bool up = x > a.vthr[1];
+              code = (up ? 2u : 0u) + (x > (up ? a.vthr[2] : a.vthr[0]) ? 1u : 0u);
+            } else {
+              code = (uint32_t)code_of<(1 << BITS) - 1>(x, a.vthr);
+            }
+            code &= 0u - ((mm >> j) & 1u);
+            const int tt = j & 15;
+            wr[j >> 4][(tt & 7) >> 1] |= code << (BITS == 2 ? 8 * (tt >> 3) + 2 * (tt & 1) : 16 * (tt >> 3) + 4 * (tt & 1));
+          }
+        }
+        if constexpr (BITS == 2) {
+          const int sh = 16 * (iq >> 1) + 4 * (iq & 1);
+#pragma unroll
+          for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+            for (int t4 = 0; t4 < 4; ++t4) {
+              uint32_t w = wr[tl][t4] << sh;
+              w |= __shfl_xor_sync(0xffffffffu, w, 8);
+              w |= __shfl_xor_sync(0xffffffffu, w, 16);
+              if (t4 == iq) pw[2 * hc + tl][0] |= w;
+            }
+        } else {
+          const int sh = 8 * (iq & 1);
+#pragma unroll
+          for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+            for (int t4 = 0; t4 < 4; ++t4) {
+              uint32_t w = wr[tl][t4] << sh;
+              w |= __shfl_xor_sync(0xffffffffu, w, 8);
+              if ((t4 >> 1) == (iq & 1)) pw[2 * hc + tl][t4 & 1] |= w;
+            }
+        }
+      }
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&S.bar_empty[r & 1])) : "memory");
+      // the page's last round: store its chunk words (older tokens of a tile kept), and
+      // its buffer (MMAs done, norms taken) takes the page three ahead
+      if (r + 1 == nr || S.rpage[r + 1] != p) {
+#pragma unroll
+        for (int tau = 0; tau < 4; ++tau) {
+          if (TILE * tau + TILE <= ta || TILE * tau >= tb) continue;
+          uint32_t *tw = reinterpret_cast<uint32_t *>(pg + PL.off_v + tau * PL.tile_bytes);
+#pragma unroll
+          for (int k = 0; k < PW; ++k) {
+            const int t4 = BITS == 2 ? iq : 2 * (iq & 1) + k;
+            uint32_t *dst =
+                BITS == 2 ? tw + (4 * gq + t4) * 4 + quarter : tw + (4 * gq + t4) * 8 + 2 * quarter + (iq >> 1);
+            uint32_t val = pw[tau][k];
+            if (TILE * tau < ta) val |= *dst & v_keep_mask<BITS>(t4, ta - TILE * tau);
+            *dst = val;
+          }
+        }
+        if (tid == 0 && p + V_NBUF < npg) {
+          issue_page(p + V_NBUF);
+          pages_issued = p + V_NBUF + 1;
+        }
       }
     }
   }
+  const bool mine_failed = producer ? false : c_waited < nr;
+  // a producer that stopped early leaves the consumers waiting: they give up too
+  __syncthreads();
   // the pages' own copy of their tile modality masks (decode reads them with the page)
   for (int i = tid; i < npg * (PAGE / TILE); i += VTHREADS) {
     const int p = i / (PAGE / TILE), tile = i % (PAGE / TILE);
@@ -586,14 +601,13 @@ __global__ void __launch_bounds__(VTHREADS, WIDE ? 3 : 2)
       *tm = bitsm;
     }
   }
-  if (failed) {
-    if (tid == 0) atomicOr(a.err, ERR_WAIT);
+  if (tid == 0 && mine_failed) {
+    atomicOr(a.err, ERR_WAIT);
     // MMAs still in flight: wait (bounded) before their accumulator columns are freed
-    for (int r = waited; r < issued; ++r) (void)wait_bar(&S.bar_mma[r & 1], (uint32_t)(r >> 1) & 1u);
-    // pages still on their way: issued up to the third after the last one consumed
-    if (tid == 0)
-      for (int p = pages_seen; p < npg && p < pages_seen + V_NBUF; ++p)
-        (void)wait_bar(&S.bar_v[p % V_NBUF], (uint32_t)(p / V_NBUF) & 1u);
+    for (int r = c_waited; r < S.mma_issued; ++r) (void)wait_bar(&S.bar_mma[r & 1], (uint32_t)(r >> 1) & 1u);
+    // pages still on their way
+    for (int p = S.pages_seen; p < pages_issued; ++p)
+      (void)wait_bar(&S.bar_v[p % V_NBUF], (uint32_t)(p / V_NBUF) & 1u);
   }
   tc_fence_before();
   __syncthreads();
