@@ -11,16 +11,17 @@
 // Two grids that write disjoint parts of the touched pages and read nothing the
 // other writes, so they run concurrently:
 //   append_value_kernel - one CTA per (run of touched pages, layer, kv head): the
-//     modality ids, tile masks, value norms and value codes. R_m (fp16 high and
-//     residual parts) and the page's values sit in shared memory in the tensor
-//     core's layout; one thread issues the 5th-generation MMAs
-//     D[128 outputs x 64 tokens] = R_m V^T into tensor memory, and the thread of
-//     output lane o quantizes its row and packs the codes straight into the
-//     decode's lane chunks (the accumulator's lane/column order is the chunk's).
-//   append_key_kernel - one CTA per (touched page, layer, kv head): a key group is
-//     quantized by the CTA whose page holds it when its last token arrives,
-//     reading earlier members from the fp16 tail buffer; the CTA owning the last
-//     touched page writes the new fp16 tail into the other tail buffer.
+//     modality ids, tile masks, value norms and value codes. Pages arrive by TMA
+//     (128-byte swizzle) and R_m (fp16 high and residual parts) sits in tensor
+//     memory; producer warps issue the 5th-generation MMAs D[128 outputs x 64
+//     tokens] = R_m V^T and take the norms, consumer warps quantize the accumulator
+//     (lane o = output channel o) and pack the codes straight into the decode's lane
+//     chunks.
+//   append_key_kernel - one CTA per (key group touched, layer, kv head): a group is
+//     quantized when its last token arrives, earlier members read from the fp16 tail
+//     buffer; the CTA of the last touched group writes the new fp16 tail into the
+//     other tail buffer. append_turbo_kernel - TurboQuant keys (one CTA per touched
+//     page): every new token coded on arrival.
 #include <cuda.h>
 
 #include "okvq_append.h"
