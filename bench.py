@@ -414,7 +414,7 @@ def append_rates(chunks):
             "tokens_per_s_all_chunks": sum(n for _, n in chunks) / (sum(x for x, _ in chunks) / 1e3)}
 
 
-def config_summary(w, args, torch, device, peak, steps, warmup, key_codec="omni"):
+def config_summary(w, args, torch, device, peak, steps, warmup, key_codec="omni", workload=None):
     """One extra configuration of the default run: its caches built on the device,
     decode steps timed as for the headline line (two replicas alternate unless one
     cache alone is more than four times the L2), every cache freed afterwards."""
@@ -422,12 +422,18 @@ def config_summary(w, args, torch, device, peak, steps, warmup, key_codec="omni"
     lengths = [s.length for s in w.sessions]
     split_bytes, out_bytes, rot_bytes = algorithmic_bytes(w, lengths, key_codec)
     replicas = 2 if split_bytes < 4 * 129e6 else 1
-    caches, append_ms, _ = build_cache(w, torch, device, replicas=replicas, key_codec=key_codec)
+    caches, append_ms, _ = build_cache(w, torch, device, replicas=replicas, key_codec=key_codec,
+                                       keep_layer0=workload is not None)
     Q = torch.from_numpy(w.queries(0)).to(device)
     out = torch.empty_like(Q)
     ms, split_ms, merge_ms = timed_steps(caches, Q, out, torch, steps, warmup)
     errs = [c.check_errors() for c in caches]
     ap = append_rates(append_ms[0])
+    bnd = None
+    if workload is not None and not args.no_cpu_baseline:
+        bnd = dict(boundary_counts(workload, sh.bits, sh.group_size, caches[0]),
+                   of="layer 0 of session 0 (%d tokens), every kv head: GPU state against the oracle fed the same "
+                      "inputs and rotations" % lengths[0])
     del caches, Q, out
     torch.cuda.empty_cache()
     if any(errs):
@@ -444,6 +450,7 @@ def config_summary(w, args, torch, device, peak, steps, warmup, key_codec="omni"
             "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "bytes_per_launch": split_bytes,
                          "avg_launch_ms": avg_split, "merge_kernel_avg_ms": float(np.mean(merge_ms))},
+            "boundary_codes": bnd,
             "append_tokens_per_s": ap["tokens_per_s"], "append_ms_per_chunk_median": ap["ms_per_chunk_median"],
             "append_tokens_per_chunk_median": ap["tokens_per_chunk_median"],
             "l2": "two cache replicas alternate" if replicas == 2 else "one cache, %.1f GB per step" % (
@@ -688,6 +695,42 @@ def cpu_baseline_child(args):
     print(json.dumps(res))
 
 
+def save_layer0_state(cache, path):
+    """Layer 0 of session 0 as the GPU stored it, with the rotations and inputs it was
+    built from (the CPU side's boundary-code accounting reads this file)."""
+    st0 = cache.export_state(0)
+    arrays = {k: np.ascontiguousarray(v[0]) for k, v in st0.items() if k != "mod" and v.ndim >= 2}
+    arrays["R"] = np.asarray(cache.rotations_used, np.float32)
+    arrays["K0"], arrays["V0"] = cache.layer0_kv
+    np.savez(path, **arrays)
+
+
+def boundary_child(args):
+    """The oracle's layer 0 of session 0, fed the GPU cache's inputs and rotations, and
+    the boundary-code accounting of the GPU's stored state against it."""
+    z = np.load(args.gpu_state)
+    kv0 = (z["K0"][:, None], z["V0"][:, None])
+    state = {k: z[k] for k in z.files if k not in ("R", "K0", "V0")}
+    _, oc = _oracle_for_layers(args, [0], z["R"], kv0)
+    print(json.dumps(compare_with_oracle(state, oc)))
+
+
+def boundary_counts(workload, bits, group_size, cache):
+    """Boundary-code accounting of one configuration (CPU child, no GPU)."""
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    try:
+        save_layer0_state(cache, path)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                   CUDA_VISIBLE_DEVICES="")
+        cmd = [sys.executable, os.path.abspath(__file__), "--boundary-child", "--workload", workload, "--bits",
+               str(bits), "--group-size", str(group_size), "--key-codec", "omni", "--gpu-state", path]
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, check=True).stdout
+        return json.loads(out.strip().splitlines()[-1])
+    finally:
+        os.unlink(path)
+
+
 def run_cpu_baseline(args, gpu_state=None, all_cores=True, steps=3):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -780,12 +823,15 @@ def main():
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
     ap.add_argument("--group-size", type=int, default=32, choices=[32, 64])
     ap.add_argument("--cpu-baseline-child", action="store_true")
+    ap.add_argument("--boundary-child", action="store_true")
     ap.add_argument("--all-cores", action="store_true")
     ap.add_argument("--all-core-steps", type=int, default=3)
     ap.add_argument("--gpu-state", default=None)
     args = ap.parse_args()
     if args.cpu_baseline_child:
         return cpu_baseline_child(args)
+    if args.boundary_child:
+        return boundary_child(args)
     if args.impl == "reference":
         return reference_arm(args)
     args.warmup = max(args.warmup, 3)
@@ -919,13 +965,9 @@ def main():
         if not args.no_cpu_baseline:
             # the GPU-stored state of layer 0 (session 0) and the rotations it used: the
             # CPU leg compares the oracle's codes with it (boundary-code accounting)
-            st0 = caches[0].export_state(0)
             fd, gpu_state = tempfile.mkstemp(suffix=".npz")
             os.close(fd)
-            arrays = {k: np.ascontiguousarray(v[0]) for k, v in st0.items() if k != "mod" and v.ndim >= 2}
-            arrays["R"] = np.asarray(caches[0].rotations_used, np.float32)
-            arrays["K0"], arrays["V0"] = caches[0].layer0_kv
-            np.savez(gpu_state, **arrays)
+            save_layer0_state(caches[0], gpu_state)
         if default:
             line["compaction"] = compaction_leg(caches[0], w, torch, Q, out, peak, 10)
         del caches
@@ -935,10 +977,12 @@ def main():
             if not args.no_extra:
                 cfg = {}
                 ns = argparse.Namespace(**vars(args))
-                cfg["qwen7b_2bit_g32"] = config_summary(synth.qwen7b(), ns, torch, device, peak, 20, 5)
-                cfg["multisession_2bit_g32"] = config_summary(synth.multisession(), ns, torch, device, peak, 20, 5)
+                cfg["qwen7b_2bit_g32"] = config_summary(synth.qwen7b(), ns, torch, device, peak, 20, 5,
+                                                        workload="qwen7b")
+                cfg["multisession_2bit_g32"] = config_summary(synth.multisession(), ns, torch, device, peak, 20, 5,
+                                                              workload="multisession")
                 cfg["multisession_4bit_g32"] = config_summary(synth.multisession(bits=4), ns, torch, device, peak, 20,
-                                                              5)
+                                                              5, workload="multisession")
                 cfg["streaming"] = streaming_summary(ns, torch, device, peak)
                 line["configs"] = cfg
         if not args.no_cpu_baseline:
