@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libokvq.so")
 SOURCES = ["okvq_api.cu", "okvq_append.cu", "okvq_decode.cu", "okvq_combine.cu", "okvq_calib.cu", "okvq_evict.cu",
-           "okvq_far.cu"]
+           "okvq_far.cu", "okvq_hostio.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

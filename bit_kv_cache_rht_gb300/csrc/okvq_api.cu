@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "okvq_append.h"
+#include "okvq_hostio.h"
 #include "okvq_internal.h"
 
 using namespace okvq;
@@ -61,11 +62,12 @@ struct okvq_cache {
   float *far_partials = nullptr;                       // [units][far_nsplit][MAXGQ][FAR_PARTIAL_FLOATS]
   unsigned char *lut = nullptr;                        // decode level table (LEVEL_TABLE_BYTES)
   __half *q_stage[2] = {}, *out_stage = nullptr;       // device staging of okvq_decode_host
+  __half *q_pin = nullptr;                             // its staging of page-locked queries (stage_queries_kernel)
   cudaStream_t copy_stream = nullptr;                  // uploads of okvq_decode_host
   cudaStream_t key_stream = nullptr;                   // the append's key grid, forked from the caller's stream
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaEvent_t ev_in[2] = {}, ev_used[2] = {};          // upload done / staging slot released
-  int host_calls = 0;
+  int host_calls = 0;                                  // okvq_decode_host calls that uploaded on copy_stream
   const void *dev_ok[8] = {};                          // device pointers already validated
   int dev_ok_next = 0;
   int far_nsplit = 1;
@@ -162,6 +164,7 @@ void release(okvq_cache *h) {
   cudaFree(h->lut);
   cudaFree(h->q_stage[0]);
   cudaFree(h->q_stage[1]);
+  cudaFree(h->q_pin);
   cudaFree(h->out_stage);
   for (int b = 0; b < 2; ++b) {
     if (h->ev_in[b]) cudaEventDestroy(h->ev_in[b]);
@@ -602,6 +605,7 @@ okvq_status okvq_create(const okvq_config *cfg, void *stream, okvq_cache **out) 
     if (cudaEventCreateWithFlags(&h->ev_in[b], cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
     if (cudaEventCreateWithFlags(&h->ev_used[b], cudaEventDisableTiming) != cudaSuccess) return fail(OKVQ_ECUDA);
   }
+  if ((st = alloc_dev((void **)&h->q_pin, qo_bytes)) != OKVQ_OK) return fail(st);
   if ((st = alloc_dev((void **)&h->out_stage, qo_bytes)) != OKVQ_OK) return fail(st);
   if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(OKVQ_ECUDA);
   if (cudaStreamCreateWithFlags(&h->key_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(OKVQ_ECUDA);
@@ -784,23 +788,34 @@ okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, 
   if (!h || !q_host || !out_host) return OKVQ_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t qo_bytes = (size_t)h->S * h->L * h->Hq * D * sizeof(__half);
-  // the upload runs on the handle's copy stream into one of two staging slots, so it
-  // overlaps the decode the previous call left on `stream`; the slot is reused only
-  // after the decode two calls back has read it
+  // page-locked queries: a kernel on `stream` copies them in (zero-copy reads), so the
+  // decode stays a programmatic dependent of the kernel before it and its prologue
+  // still overlaps the previous step's merge (stage_queries_kernel)
+  const void *q_mapped = aligned16(q_host) ? mapped_host(const_cast<void *>(q_host)) : nullptr;
   const int b = h->host_calls & 1;
-  if (h->host_calls >= 2) OKVQ_TRY(cudaStreamWaitEvent(h->copy_stream, h->ev_used[b], 0));
-  OKVQ_TRY(cudaMemcpyAsync(h->q_stage[b], q_host, qo_bytes, cudaMemcpyHostToDevice, h->copy_stream));
-  OKVQ_TRY(cudaEventRecord(h->ev_in[b], h->copy_stream));
-  OKVQ_TRY(cudaStreamWaitEvent(s, h->ev_in[b], 0));
+  const __half *q_dev = h->q_pin;
+  if (q_mapped) {
+    OKVQ_TRY(launch_stage_queries(q_mapped, h->q_pin, (long long)(qo_bytes / 16), s));
+  } else {
+    // pageable queries: the upload runs on the handle's copy stream into one of two
+    // staging slots, so it overlaps the decode the previous call left on `stream`; the
+    // slot is reused only after the decode two uploads back has read it
+    if (h->host_calls >= 2) OKVQ_TRY(cudaStreamWaitEvent(h->copy_stream, h->ev_used[b], 0));
+    OKVQ_TRY(cudaMemcpyAsync(h->q_stage[b], q_host, qo_bytes, cudaMemcpyHostToDevice, h->copy_stream));
+    OKVQ_TRY(cudaEventRecord(h->ev_in[b], h->copy_stream));
+    OKVQ_TRY(cudaStreamWaitEvent(s, h->ev_in[b], 0));
+    q_dev = h->q_stage[b];
+  }
   // page-locked output: the merge kernel stores into it directly (no copy after the
   // decode); pageable output: device staging, then a copy
   void *out_dev = mapped_host(out_host);
-  okvq_status st = enqueue_decode(h, h->q_stage[b], out_dev ? out_dev : h->out_stage, s, h->partials, -1, h->prof,
-                                  nullptr);
+  okvq_status st = enqueue_decode(h, q_dev, out_dev ? out_dev : h->out_stage, s, h->partials, -1, h->prof, nullptr);
   if (st != OKVQ_OK) return st;
-  OKVQ_TRY(cudaEventRecord(h->ev_used[b], s));
+  if (!q_mapped) {
+    OKVQ_TRY(cudaEventRecord(h->ev_used[b], s));
+    ++h->host_calls;
+  }
   if (!out_dev) OKVQ_TRY(cudaMemcpyAsync(out_host, h->out_stage, qo_bytes, cudaMemcpyDeviceToHost, s));
-  ++h->host_calls;
   return OKVQ_OK;
 }
 

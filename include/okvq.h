@@ -182,21 +182,27 @@ okvq_status okvq_decode(okvq_cache *h, const void *q, void *out, void *stream);
  * rebuilt and uploaded on `stream`); otherwise as okvq_decode. */
 okvq_status okvq_decode_static_scratch(okvq_cache *h, const void *q, void *out, void *stream);
 
-/* okvq_decode on HOST buffers: copies the queries (host, same layout as
+/* okvq_decode on HOST buffers: brings the queries (host, same layout as
  * okvq_decode's q) into the handle's device staging, decodes, and delivers the
  * outputs to `out_host`, all asynchronously on `stream` (the host buffers must
- * stay valid, and `out_host` unread, until the stream reaches that point). When
- * `out_host` is page-locked host memory (cudaHostAlloc, cudaHostRegister, a
- * pinned torch tensor; checked with cudaPointerGetAttributes on every call), the
- * merge kernel stores the outputs into it directly, with no copy after the
- * decode; otherwise they go through device staging and a copy. Pinned host
- * memory makes the query upload asynchronous, pageable memory makes it
- * synchronous. The upload runs on a copy stream owned by the handle, into one
- * of two staging slots, so it overlaps the decode a previous call left on
- * `stream`; `stream` waits for it, so the call's effects are complete when
- * `stream` reaches that point. Staging (3 x S*L*Hq*128 fp16), the copy stream and
- * its events are created by okvq_create; calls on one handle must be ordered
- * (one host thread). Errors as okvq_decode. */
+ * stay valid, and `out_host` unread, until the stream reaches that point).
+ * Page-locked host memory (cudaHostAlloc, cudaHostRegister, a pinned torch
+ * tensor; checked with cudaPointerGetAttributes on every call):
+ *  - queries (16-byte aligned): a small kernel on `stream` reads them through
+ *    their mapped device address and writes the staging once every earlier
+ *    kernel on `stream` has completed; it runs, like the decode, as a programmatic
+ *    dependent of the kernel before it, so the decode's prologue still overlaps
+ *    the previous call's merge;
+ *  - outputs: the merge kernel stores them into `out_host` directly, with no copy
+ *    after the decode.
+ * Pageable memory: the queries are uploaded (synchronously with respect to the
+ * host) on a copy stream owned by the handle, into one of two staging slots, so
+ * the upload overlaps the decode a previous call left on `stream`; `stream` waits
+ * for it. The outputs go through device staging and a copy on `stream`. The
+ * call's effects are complete when `stream` reaches that point. Staging
+ * (4 x S*L*Hq*128 fp16), the copy stream and its events are created by
+ * okvq_create; calls on one handle must be ordered (one host thread). Errors as
+ * okvq_decode. */
 okvq_status okvq_decode_host(okvq_cache *h, const void *q_host, void *out_host, void *stream);
 
 /* Decode with far-memory pseudo tokens ("ProtoKV: Streaming Video Understanding

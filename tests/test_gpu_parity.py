@@ -262,9 +262,10 @@ def test_turbo_keys_qwen3b_shape_and_multisession():
 
 
 def test_decode_host_equals_decode_on_device_buffers():
-    """okvq_decode_host (pinned host queries and outputs, the uploads on the handle's
-    copy stream into alternating slots) gives okvq_decode's outputs bit for bit,
-    with four calls queued before any synchronisation."""
+    """okvq_decode_host with pinned host queries and outputs (the queries read by the
+    staging kernel on the decode's stream, the outputs stored by the merge kernel)
+    gives okvq_decode's outputs bit for bit, with four calls queued before any
+    synchronisation."""
     import torch
     w = synth.multisession(seed=45, sessions=3, lo=100, hi=2500, layers=2)
     c = pu.gpu_cache(w)
@@ -298,6 +299,39 @@ def test_decode_host_pageable_and_pinned_outputs_agree():
     torch.cuda.synchronize()
     for o, ref in zip(outs, refs):
         assert torch.equal(o, ref)
+
+
+def test_decode_host_pinned_pageable_and_unaligned_queries_alternate():
+    """The three query paths of okvq_decode_host on one handle, six calls queued
+    before any synchronisation: pinned (the staging kernel), pageable (the copy
+    stream into alternating slots) and pinned but off a 16-byte boundary (also the
+    copy stream). Every call gives okvq_decode's outputs bit for bit."""
+    import torch
+    w = synth.qwen3b(seed=47, tokens=1800, layers=2)
+    c = pu.gpu_cache(w)
+    Qs = [w.queries(step) for step in range(6)]
+    refs = [c.decode(torch.from_numpy(Q).cuda()).cpu() for Q in Qs]
+    keep, outs = [], []
+    for i, Q in enumerate(Qs):
+        kind = i % 3
+        if kind == 0:
+            q = torch.from_numpy(Q).pin_memory()
+        elif kind == 1:
+            q = torch.from_numpy(Q.copy())
+        else:
+            buf = torch.empty(Q.size + 4, dtype=torch.float16).pin_memory()
+            q = buf[4:].view(Q.shape)                  # 8 bytes past a 16-byte boundary
+            q.copy_(torch.from_numpy(Q))
+            assert q.data_ptr() % 16 == 8
+            keep.append(buf)
+        o = torch.full(Q.shape, float("nan"), dtype=torch.float16).pin_memory()
+        c.decode_host(q, o)
+        keep.append(q)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for o, ref in zip(outs, refs):
+        assert torch.equal(o, ref)
+    assert c.check_errors() == 0
 
 
 def test_host_and_foreign_pointers_are_rejected_before_any_launch():
