@@ -953,8 +953,9 @@ def main():
             "e2e": {"value": total_tokens / (e2e_max / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(Q.numel() * 2),
                     "d2h_bytes_per_step": int(out.numel() * 2), "ms_per_step_wall": e2e_max / args.steps,
                     "device_event_value": total_tokens / (e2e_ev_max / 1e3),
-                    "how": "okvq_decode_host: pinned-host queries copied in and outputs stored into pinned host memory "
-                           "by the merge kernel, every step; value = host wall clock around %d calls and a final "
+                    "how": "okvq_decode_host: pinned-host queries read over the host link by the query staging "
+                           "kernel and outputs stored into pinned host memory by the merge kernel, every step (3 "
+                           "launches a step); value = host wall clock around %d calls and a final "
                            "synchronisation; device_event_value = CUDA events on the stream" % args.steps},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
