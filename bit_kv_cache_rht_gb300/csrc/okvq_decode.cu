@@ -577,6 +577,8 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   // current one runs, so a segment starts without global latency
   __shared__ __align__(8) uint64_t q_bar;
   __shared__ int sd_unit, sd_pb, sd_pe, sd_tail;
+  // the Hadamard signs (written at create), staged before the dependency wait
+  __shared__ __align__(16) float sgn[D];
   __shared__ long long sd_T;
   const int gq = a.Hq / a.Hkv;
   struct SegDesc {
@@ -605,8 +607,8 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   };
   // Launched as a programmatic dependent of the previous kernel on the stream (the
   // last step's merge): everything up to griddepcontrol.wait reads only the cache's
-  // level table (written at create) and the work list (written by a host copy that
-  // the launch itself follows); queries and pages come after it.
+  // level table and Hadamard signs (written at create) and the work list (written by
+  // a host copy that the launch itself follows); queries and pages come after it.
   const int seg_begin = a.cta_seg[blockIdx.x], seg_end = a.cta_seg[blockIdx.x + 1];
   SegDesc first{};
   if (tid == 0 && seg_begin < seg_end) first = load_desc(seg_begin);
@@ -618,6 +620,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   }
   if (lane == 0)
     for (int s = 0; s < STAGES; ++s) mbar_init(&my_bars[s], 1);
+  if (tid < D / 4) reinterpret_cast<float4 *>(sgn)[tid] = reinterpret_cast<const float4 *>(a.signs)[tid];
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   // tensor memory for the parked modality accumulators: 2 warps per lane quarter,
   // 3 x 32 columns each
@@ -660,12 +663,12 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     const int Tf = KT ? T : (T / GG) * GG;
     const unsigned char *unit_pages = a.pages + (long long)unit * a.P_max * PL.page_bytes;
     const __half *tail = a.tails + ((long long)tail_sel * a.units + unit) * (long long)G * D;
-    // the segment's first pages are on their way while the query is rotated (the
-    // ring is free: the previous segment's merge ended with a barrier)
+    // each warp's first page is on its way while the query is rotated (the ring is
+    // free: the previous segment's merge ended with a barrier)
     const int npages = pe - pb;
     const int my_n = npages > warp ? (npages - warp + WARPS - 1) / WARPS : 0;
     if (lane == 0) {
-      for (int k = 0; k < min(my_n, STAGES); ++k) {
+      for (int k = 0; k < min(my_n, 1); ++k) {
         const int st = (ring_st + k) % STAGES;
         fence_async_smem();
         bulk_load(my_stage0 + (size_t)st * PL.page_bytes,
@@ -678,12 +681,14 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     if (warp < MAXGQ) {
       const int hh = warp;
       float x[4];
+      const float4 sg4 = reinterpret_cast<const float4 *>(sgn)[lane];
+      const float sg[4] = {sg4.x, sg4.y, sg4.z, sg4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = 4 * lane + j;
         const __half hv = hh < gq ? qstage[hh * D + c] : __float2half(0.f);
         qraw[hh * D + c] = hv;
-        x[j] = __half2float(hv) * a.signs[c];
+        x[j] = __half2float(hv) * sg[j];
       }
       float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
       x[0] = y0 + y2; x[2] = y0 - y2; x[1] = y1 + y3; x[3] = y1 - y3;
@@ -717,6 +722,16 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     __syncthreads();
     // the descriptor and queries of this CTA's next segment, staged while this one runs
     if (stager) stage_segment(next);
+    // the rest of the ring: one page per warp went out first, so that the first
+    // pages of all warps arrive before any second page competes with them
+    if (lane == 0) {
+      for (int k = 1; k < min(my_n, STAGES); ++k) {
+        const int st = (ring_st + k) % STAGES;
+        fence_async_smem();
+        bulk_load(my_stage0 + (size_t)st * PL.page_bytes,
+                  unit_pages + (long long)(pb + warp + k * WARPS) * PL.page_bytes, PL.page_bytes, &my_bars[st]);
+      }
+    }
 
     HalfPageCtx hc;
     hc.lut_k = lut_k;
