@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <queue>
 #include <vector>
 
 #include "okvq_append.h"
@@ -278,6 +279,142 @@ SplitPlan plan_split(const long long *pages_u, long long U, int max_cta, int seg
 #endif
 constexpr int SEG_COST_PAGES = OKVQ_SEG_COST;
 
+// Row cost model of a decode CTA. Its W warps take the CTA's pages in turn, so a
+// segment of n pages costs ceil(n / W) whole rows of W pages, plus ROW_SEG_COST pages
+// for the segment itself (query rotation, the page ring started empty, the merge).
+// Measured on the 3B shape: a CTA running nine 8-page segments takes ~5.1 us per
+// segment, about 24 pages of a loaded CTA's time (one row of 12 plus 12).
+constexpr int ROW_SEG_COST = 12;
+
+long long row_cost(long long n, int W) { return ROW_SEG_COST + (long long)W * ((n + W - 1) / W); }
+
+// The costliest CTA of a split under the row cost model.
+long long split_row_cost(const int *segs, const int *cta_seg, int ncta, int W) {
+  long long worst = 0;
+  for (int c = 0; c < ncta; ++c) {
+    long long t = 0;
+    for (int i = cta_seg[c]; i < cta_seg[c + 1]; ++i) t += row_cost(segs[4 * i + 2] - segs[4 * i + 1], W);
+    worst = std::max(worst, t);
+  }
+  return worst;
+}
+
+// Row-aligned split: every unit is cut into pieces of R whole rows (R W pages), one
+// CTA each, and what is left of each unit (its last pages) goes, costliest first, to
+// the least loaded CTA that holds no piece. The smallest R is taken (from the fewest
+// rows that could hold every page, trying up to 64 values and at most max_rows) for
+// which the pieces fit in max_cta CTAs and every CTA stays within a piece's cost.
+// It uses SMs the contiguous split leaves idle, and it makes every piece whole rows
+// (one 512-page unit over two CTAs: pieces of 252 pages, 21 rows, instead of 256
+// pages, 22 rows, with the units' 8-page remainders on the idle SMs). Returns the
+// CTAs used (0: no R fits); segs [nseg][4] = unit, first page, end page, 0, in CTA
+// order; *cost = the costliest CTA's cost.
+int plan_rows(const long long *pages_u, long long U, int max_cta, int W, long long max_rows, int *segs, int *cta_seg,
+              int *nseg_out, long long *cost) {
+  long long P = 0;
+  for (long long u = 0; u < U; ++u) P += pages_u[u];
+  if (P == 0 || max_cta < 1 || W < 1) return 0;
+  const long long R0 = std::max<long long>(1, (P + (long long)W * max_cta - 1) / ((long long)W * max_cta));
+  for (long long R = R0; R <= std::min(max_rows, R0 + 63); ++R) {
+    const long long piece = R * W, B = row_cost(piece, W);
+    long long main = 0;
+    for (long long u = 0; u < U; ++u) main += pages_u[u] / piece;
+    if (main > max_cta) continue;
+    struct Rest {
+      long long cost;
+      long long unit;
+    };
+    std::vector<Rest> rest;
+    for (long long u = 0; u < U; ++u)
+      if (pages_u[u] % piece) rest.push_back({row_cost(pages_u[u] % piece, W), u});
+    const long long bins = max_cta - main;
+    if (!rest.empty() && bins == 0) continue;
+    std::stable_sort(rest.begin(), rest.end(), [](const Rest &x, const Rest &y) { return x.cost > y.cost; });
+    std::vector<std::vector<long long>> held(bins);
+    // least loaded bin first (ties: lowest index)
+    std::priority_queue<std::pair<long long, long long>, std::vector<std::pair<long long, long long>>,
+                        std::greater<std::pair<long long, long long>>>
+        heap;
+    for (long long b = 0; b < bins; ++b) heap.push({0, b});
+    bool ok = true;
+    for (const Rest &r : rest) {
+      const auto top = heap.top();
+      if (top.first + r.cost > B) {
+        ok = false;
+        break;
+      }
+      heap.pop();
+      heap.push({top.first + r.cost, top.second});
+      held[top.second].push_back(r.unit);
+    }
+    if (!ok) continue;
+    int ns = 0, c = 0;
+    for (long long u = 0; u < U; ++u)
+      for (long long k = 0; k < pages_u[u] / piece; ++k) {
+        cta_seg[c++] = ns;
+        segs[4 * ns + 0] = (int)u;
+        segs[4 * ns + 1] = (int)(k * piece);
+        segs[4 * ns + 2] = (int)((k + 1) * piece);
+        segs[4 * ns + 3] = 0;
+        ++ns;
+      }
+    for (long long b = 0; b < bins; ++b) {
+      if (held[b].empty()) continue;
+      std::sort(held[b].begin(), held[b].end());
+      cta_seg[c++] = ns;
+      for (long long u : held[b]) {
+        segs[4 * ns + 0] = (int)u;
+        segs[4 * ns + 1] = (int)(pages_u[u] / piece * piece);
+        segs[4 * ns + 2] = (int)pages_u[u];
+        segs[4 * ns + 3] = 0;
+        ++ns;
+      }
+    }
+    cta_seg[c] = ns;
+    *nseg_out = ns;
+    *cost = split_row_cost(segs, cta_seg, c, W);
+    return c;
+  }
+  return 0;
+}
+
+// Partial slots: a unit's segments get consecutive slots in page order, so the merge
+// kernel reads a unit's partials as one range; unit_seg [units + 1] = first slot.
+void assign_slots(int *segs, int nseg, long long U, int *unit_seg) {
+  std::vector<int> order(nseg);
+  for (int i = 0; i < nseg; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    return segs[4 * x] != segs[4 * y] ? segs[4 * x] < segs[4 * y] : segs[4 * x + 1] < segs[4 * y + 1];
+  });
+  for (int r = 0; r < nseg; ++r) segs[4 * order[r] + 3] = r;
+  int sl = 0;
+  for (long long uu = 0; uu <= U; ++uu) {
+    while (sl < nseg && segs[4 * order[sl]] < uu) ++sl;
+    unit_seg[uu] = sl;
+  }
+}
+
+// The decode's work split: the contiguous split, or the row-aligned one when the row
+// cost model puts it at least one row lower.
+SplitPlan plan_decode_work(const long long *pages_u, long long U, int max_cta, int W, int *segs, int *cta_seg) {
+  SplitPlan sp = plan_split(pages_u, U, max_cta, SEG_COST_PAGES, segs, cta_seg);
+  if (sp.ncta == 0) return sp;
+  cta_seg[sp.ncta] = sp.nseg;
+  const long long contiguous = split_row_cost(segs, cta_seg, sp.ncta, W);
+  const long long max_rows = (contiguous - W - ROW_SEG_COST) / W;
+  std::vector<int> rsegs(4 * ((size_t)U + max_cta + 1)), rcta(max_cta + 2);
+  int rnseg = 0;
+  long long rcost = 0;
+  const int rn = plan_rows(pages_u, U, max_cta, W, max_rows, rsegs.data(), rcta.data(), &rnseg, &rcost);
+  if (rn > 0 && rcost + W <= contiguous) {
+    std::copy(rsegs.begin(), rsegs.begin() + 4 * (size_t)rnseg, segs);
+    std::copy(rcta.begin(), rcta.begin() + rn + 1, cta_seg);
+    sp.ncta = rn;
+    sp.nseg = rnseg;
+  }
+  return sp;
+}
+
 // Build the decode work table from the session lengths into pinned buffer `slot`.
 void build_table(okvq_cache *h, int slot) {
   const long long U = h->units;
@@ -297,15 +434,10 @@ void build_table(okvq_cache *h, int slot) {
     ulen[u] = h->len[u / LH];
     utail[u] = h->tail_sel[u / LH];
   }
-  const SplitPlan sp = plan_split(pages_u.data(), U, h->max_cta, SEG_COST_PAGES, segs, cta_seg);
+  const SplitPlan sp = plan_decode_work(pages_u.data(), U, h->max_cta, decode_warps(h->bits), segs, cta_seg);
   const int ncta = sp.ncta, nseg = sp.nseg;
   cta_seg[ncta] = nseg;
-  // unit -> first segment (segments are ordered by unit)
-  int s = 0;
-  for (long long uu = 0; uu <= U; ++uu) {
-    while (s < nseg && segs[4 * s] < uu) ++s;
-    unit_seg[uu] = s;
-  }
+  assign_slots(segs, nseg, U, unit_seg);
   h->ncta = ncta;
   h->nseg = nseg;
 }
@@ -965,6 +1097,31 @@ okvq_status okvq_plan_decode(const int64_t *unit_pages, int64_t units, int32_t m
   cta_first[sp.ncta] = sp.nseg;
   for (int i = 0; i < sp.nseg; ++i)
     for (int j = 0; j < 3; ++j) segments[3 * i + j] = segs[4 * i + j];
+  *num_ctas = sp.ncta;
+  *num_segments = sp.nseg;
+  return OKVQ_OK;
+}
+
+okvq_status okvq_plan_decode_work(const int64_t *unit_pages, int64_t units, int32_t max_ctas, int32_t bits,
+                                  int32_t *segments, int32_t *cta_first, int32_t *unit_first, int32_t *num_ctas,
+                                  int32_t *num_segments) {
+  if (units < 0 || (units > 0 && !unit_pages) || max_ctas < 1 || (bits != 2 && bits != 4) || !segments ||
+      !cta_first || !unit_first || !num_ctas || !num_segments)
+    return OKVQ_EINVAL;
+  if (units > INT32_MAX) return OKVQ_EINVAL;
+  std::vector<long long> pages(units);
+  for (long long u = 0; u < units; ++u) {
+    if (unit_pages[u] < 0 || unit_pages[u] > INT32_MAX) return OKVQ_EINVAL;
+    pages[u] = unit_pages[u];
+  }
+  std::vector<int> segs(4 * ((size_t)units + max_ctas + 1)), cta(max_ctas + 2);
+  const SplitPlan sp = plan_decode_work(pages.data(), units, max_ctas, decode_warps(bits), segs.data(), cta.data());
+  cta[sp.ncta] = sp.nseg;
+  std::vector<int> useg(units + 1);
+  assign_slots(segs.data(), sp.nseg, units, useg.data());
+  for (int i = 0; i < 4 * sp.nseg; ++i) segments[i] = segs[i];
+  for (int c = 0; c <= sp.ncta; ++c) cta_first[c] = cta[c];
+  for (long long u = 0; u <= units; ++u) unit_first[u] = useg[u];
   *num_ctas = sp.ncta;
   *num_segments = sp.nseg;
   return OKVQ_OK;

@@ -576,13 +576,14 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
   // the next segment's descriptor and queries (bulk copy) are staged while the
   // current one runs, so a segment starts without global latency
   __shared__ __align__(8) uint64_t q_bar;
-  __shared__ int sd_unit, sd_pb, sd_pe, sd_tail;
+  __shared__ int sd_unit, sd_pb, sd_pe, sd_tail, sd_slot;
+  __shared__ int cur_slot;    // the running segment's partial slot, read by its merge
   // the Hadamard signs (written at create), staged before the dependency wait
   __shared__ __align__(16) float sgn[D];
   __shared__ long long sd_T;
   const int gq = a.Hq / a.Hkv;
   struct SegDesc {
-    int unit, pb, pe, tail;
+    int unit, pb, pe, slot, tail;
     long long T;
   };
   auto load_desc = [&](int sg) {
@@ -590,6 +591,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     d.unit = a.segs[4 * sg + 0];
     d.pb = a.segs[4 * sg + 1];
     d.pe = a.segs[4 * sg + 2];
+    d.slot = a.segs[4 * sg + 3];
     d.T = a.unit_len[d.unit];
     d.tail = a.unit_tail[d.unit];
     return d;
@@ -598,6 +600,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     sd_unit = d.unit;
     sd_pb = d.pb;
     sd_pe = d.pe;
+    sd_slot = d.slot;
     sd_T = d.T;
     sd_tail = d.tail;
     const int ss = d.unit / (a.L * a.Hkv), lh = d.unit % (a.L * a.Hkv);
@@ -653,6 +656,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     const int session = unit / (a.L * a.Hkv);
     const int T = (int)sd_T;
     const int tail_sel = sd_tail;
+    if (tid == 0) cur_slot = sd_slot;     // before the stager overwrites sd_* (barriers below)
     // the next segment's descriptor: loaded now by a thread whose warp has no head
     // to rotate (at 2-bit), staged with its queries once the rotation is done
     const bool stager = tid == THREADS - 32 && seg + 1 < seg_end;
@@ -856,7 +860,7 @@ __global__ void __launch_bounds__(Cfg<BITS>::WARPS * 32, 1) decode_kernel(const 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    segment_merge<WARPS>(&MG, a.partials + (long long)seg * MAXGQ * PARTIAL_FLOATS, tbase, a.M);
+    segment_merge<WARPS>(&MG, a.partials + (long long)cur_slot * MAXGQ * PARTIAL_FLOATS, tbase, a.M);
     __syncthreads();              // merge area is the stage ring of the next segment
   }
   // the level table's and a staged query copy must land before the CTA's shared
@@ -911,6 +915,8 @@ cudaError_t launch_lut(int bits, const LutArgs &a, cudaStream_t s) {
   else lut_kernel<4><<<32, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
+
+int decode_warps(int bits) { return bits == 2 ? Cfg<2>::WARPS : Cfg<4>::WARPS; }
 
 size_t decode_smem_bytes(int bits, int G) { return bits == 2 ? decode_smem_bytes_t<2>(G) : decode_smem_bytes_t<4>(G); }
 

@@ -132,7 +132,7 @@ struct DecodeArgs {
   const uint8_t *pages;
   const __half *tails;      // [2][units][G][D]
   const uint8_t *mod;       // [S][cap]
-  const int *segs;          // [nseg][4] = unit, page_begin, page_end, 0
+  const int *segs;          // [nseg][4] = unit, page_begin, page_end, partial slot
   const int *cta_seg;       // [ncta+1]
   const long long *unit_len;// [units] token count
   const int *unit_tail;     // [units] 0/1 current tail buffer
@@ -247,6 +247,7 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_lut(int bits, const LutArgs &a, cudaStream_t s);
 constexpr size_t LEVEL_TABLE_BYTES = 256 * 256;
 size_t decode_smem_bytes(int bits, int G);
+int decode_warps(int bits);   // warps per decode CTA: a CTA takes its pages in turns of this many
 cudaError_t launch_move(const MoveArgs &a, cudaStream_t s);
 cudaError_t launch_far(const FarArgs &a, cudaStream_t s);
 int far_pass_tokens();        // pseudo tokens one pass of the far kernel's warps takes

@@ -26,7 +26,7 @@ EXPORTS = (
     "okvq_codebook", "okvq_check_errors", "okvq_profile_enable", "okvq_profile_read", "okvq_status_string",
     "okvq_decode_static_scratch", "okvq_calibrate_rotations", "okvq_live_length", "okvq_evict",
     "okvq_compaction_granule", "okvq_plan_compaction", "okvq_compact", "okvq_decode_pseudo", "okvq_decode_host",
-    "okvq_test_fail_alloc", "okvq_plan_decode",
+    "okvq_test_fail_alloc", "okvq_plan_decode", "okvq_plan_decode_work",
 )
 
 
@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
                                        ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(i32)]
     L.okvq_compact.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(i32), vp]
     L.okvq_plan_decode.argtypes = [vp, ctypes.c_int64, i32, i32, vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.okvq_plan_decode_work.argtypes = [vp, ctypes.c_int64, i32, i32, vp, vp, vp, ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32)]
     L.okvq_length.argtypes = [vp, i32, ctypes.POINTER(i64)]
     L.okvq_export_state.argtypes = [vp, i32, vp, ctypes.POINTER(ctypes.c_size_t)]
     L.okvq_codebook.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
@@ -224,6 +226,21 @@ def okvq_plan_decode(unit_pages, max_ctas: int, segment_cost: int):
                                  seg.ctypes.data_as(ctypes.c_void_p), first.ctypes.data_as(ctypes.c_void_p),
                                  ctypes.byref(nc), ctypes.byref(ns))
     return st, seg[:ns.value].copy(), first[:nc.value + 1].copy()
+
+
+def okvq_plan_decode_work(unit_pages, max_ctas: int, bits: int):
+    """The split okvq_decode uses. Returns (status, segments [n][4] = (unit, first page,
+    end page, partial slot), cta_first [ctas + 1], unit_first [units + 1])."""
+    p = np.ascontiguousarray(np.asarray(unit_pages, np.int64))
+    units = p.shape[0]
+    seg = np.zeros((units + max(max_ctas, 1) + 1, 4), np.int32)
+    first = np.zeros(max(max_ctas, 1) + 1, np.int32)
+    ufirst = np.zeros(units + 1, np.int32)
+    nc, ns = ctypes.c_int32(), ctypes.c_int32()
+    st = load().okvq_plan_decode_work(p.ctypes.data_as(ctypes.c_void_p) if units else None, units, max_ctas, bits,
+                                      seg.ctypes.data_as(ctypes.c_void_p), first.ctypes.data_as(ctypes.c_void_p),
+                                      ufirst.ctypes.data_as(ctypes.c_void_p), ctypes.byref(nc), ctypes.byref(ns))
+    return st, seg[:ns.value].copy(), first[:nc.value + 1].copy(), ufirst
 
 
 def okvq_compact(h, session: int, min_pages_saved: int, stream: int = 0):

@@ -293,6 +293,28 @@ okvq_status okvq_plan_compaction(const uint8_t *dead, int64_t length, int32_t gr
 okvq_status okvq_plan_decode(const int64_t *unit_pages, int64_t units, int32_t max_ctas, int32_t segment_cost,
                              int32_t *segments, int32_t *cta_first, int32_t *num_ctas, int32_t *num_segments);
 
+/* The split okvq_decode itself uses (host only; no handle, no GPU). A decode CTA's
+ * warps (12 at bits 2, 8 at bits 4) take its pages in turn, so a segment of n
+ * pages costs ceil(n / warps) whole rows. Two candidates: the contiguous split of
+ * okvq_plan_decode with segment_cost 48, and a row-aligned split, in which every
+ * unit is cut into pieces of R whole rows, one CTA each, and each unit's last pages
+ * (fewer than a piece) go, costliest first, to the least loaded CTA holding no
+ * piece. Under the model "a segment costs 12 + warps * ceil(n / warps) pages" the
+ * row-aligned split is taken when its costliest CTA is at least one row cheaper
+ * (the smallest fitting R, trying up to 64 values). Example: 72 units of 512 pages
+ * on 152 CTAs at bits 2: 144 CTAs take 252 pages (21 rows, not 22) and 8 CTAs take
+ * nine 8-page remainders each. A unit's segments get consecutive partial slots in
+ * page order. Inputs as okvq_plan_decode, and bits (2 or 4). Outputs: segments
+ * [*num_segments][4] = unit, first page, end page, partial slot (caller room for
+ * units + max_ctas + 1 segments), in CTA order; cta_first [*num_ctas + 1] = first
+ * segment of each CTA, then *num_segments (room for max_ctas + 1); unit_first
+ * [units + 1] = first partial slot of each unit, then *num_segments. No pages:
+ * *num_ctas = *num_segments = 0. OKVQ_EINVAL for NULL pointers, units < 0,
+ * max_ctas < 1, bits other than 2 or 4, or a count outside [0, 2^31). */
+okvq_status okvq_plan_decode_work(const int64_t *unit_pages, int64_t units, int32_t max_ctas, int32_t bits,
+                                  int32_t *segments, int32_t *cta_first, int32_t *unit_first, int32_t *num_ctas,
+                                  int32_t *num_segments);
+
 /* Plan (as okvq_plan_compaction, with the handle's granule and its deletions)
  * and apply the ordered-suffix compaction of `session`: the moved granules'
  * codes, statistics, norms, modality ids, masks and deletion bits are gathered
