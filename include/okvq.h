@@ -282,9 +282,10 @@ okvq_status okvq_plan_compaction(const uint8_t *dead, int64_t length, int32_t gr
  * range into segments at unit boundaries (one split-K partial each). A page
  * costs 1 and a segment segment_cost more; the split minimises the largest
  * CTA cost (the smallest budget with which a greedy walk covers every page,
- * found by bisection), and no segment is empty. okvq_decode plans with
- * segment_cost 48 (a segment's query rotation, its empty page ring at the
- * start and its cross-warp merge at the end cost about that many pages).
+ * found by bisection), and no segment is empty. okvq_decode's own split
+ * (okvq_plan_decode_work, below) starts from this one with segment_cost 48 (a
+ * segment's query rotation, its empty page ring at the start and its cross-warp
+ * merge at the end cost about that many pages in this model).
  * Outputs: segments [*num_segments][3] = unit, first page, end page (caller
  * room for units + max_ctas segments); cta_first [*num_ctas + 1] = first
  * segment of each CTA, then *num_segments (caller room for max_ctas + 1).
