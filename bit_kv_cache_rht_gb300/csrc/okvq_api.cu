@@ -6,7 +6,6 @@
 #include <cstring>
 #include <mutex>
 #include <new>
-#include <queue>
 #include <vector>
 
 #include "okvq_append.h"
@@ -314,40 +313,71 @@ int plan_rows(const long long *pages_u, long long U, int max_cta, int W, long lo
   long long P = 0;
   for (long long u = 0; u < U; ++u) P += pages_u[u];
   if (P == 0 || max_cta < 1 || W < 1) return 0;
+  std::vector<long long> whole(U);                 // a whole unit as one remainder
+  for (long long u = 0; u < U; ++u) whole[u] = pages_u[u] ? row_cost(pages_u[u], W) : 0;
+  struct Rest {
+    long long cost, unit;
+  };
+  std::vector<Rest> rest;
+  std::vector<std::pair<long long, long long>> placed;   // (bin, unit)
+  long long Pmax = 0, total_whole = 0;
+  for (long long u = 0; u < U; ++u) {
+    Pmax = std::max(Pmax, pages_u[u]);
+    total_whole += whole[u];
+  }
+  bool rest_whole = false;      // `rest` holds every unit whole, sorted (reused while pieces exceed every unit)
   const long long R0 = std::max<long long>(1, (P + (long long)W * max_cta - 1) / ((long long)W * max_cta));
   for (long long R = R0; R <= std::min(max_rows, R0 + 63); ++R) {
     const long long piece = R * W, B = row_cost(piece, W);
-    long long main = 0;
-    for (long long u = 0; u < U; ++u) main += pages_u[u] / piece;
-    if (main > max_cta) continue;
-    struct Rest {
-      long long cost;
-      long long unit;
-    };
-    std::vector<Rest> rest;
-    for (long long u = 0; u < U; ++u)
-      if (pages_u[u] % piece) rest.push_back({row_cost(pages_u[u] % piece, W), u});
+    long long main = 0, total = 0;
+    if (Pmax < piece) {
+      total = total_whole;                  // every unit whole: no pieces
+    } else {
+      for (long long u = 0; u < U; ++u) {
+        const long long p = pages_u[u];
+        if (p < piece) {
+          total += whole[u];
+          continue;
+        }
+        const long long q = p / piece, r = p - q * piece;
+        main += q;
+        if (r) total += row_cost(r, W);
+      }
+    }
+    // every CTA holds at most B, and the greedy packing needs some slack: R whose
+    // cost fills more than 99.8 % of max_cta CTAs of cost B is not tried
+    if (main > max_cta || 1000 * (main * B + total) > 998 * (long long)max_cta * B) continue;
     const long long bins = max_cta - main;
+    if (!(Pmax < piece && rest_whole)) {
+      rest.clear();
+      for (long long u = 0; u < U; ++u) {
+        const long long r = pages_u[u] % piece;
+        if (r) rest.push_back({pages_u[u] < piece ? whole[u] : row_cost(r, W), u});
+      }
+      std::stable_sort(rest.begin(), rest.end(), [](const Rest &x, const Rest &y) { return x.cost > y.cost; });
+      rest_whole = Pmax < piece;
+    }
     if (!rest.empty() && bins == 0) continue;
-    std::stable_sort(rest.begin(), rest.end(), [](const Rest &x, const Rest &y) { return x.cost > y.cost; });
-    std::vector<std::vector<long long>> held(bins);
-    // least loaded bin first (ties: lowest index)
-    std::priority_queue<std::pair<long long, long long>, std::vector<std::pair<long long, long long>>,
-                        std::greater<std::pair<long long, long long>>>
-        heap;
-    for (long long b = 0; b < bins; ++b) heap.push({0, b});
+    // least loaded bin first (ties: lowest index); key = load << 24 | bin
+    std::vector<unsigned long long> heap;
+    heap.reserve(bins);
+    for (long long b = 0; b < bins; ++b) heap.push_back((unsigned long long)b);
+    placed.clear();
     bool ok = true;
     for (const Rest &r : rest) {
-      const auto top = heap.top();
-      if (top.first + r.cost > B) {
+      const unsigned long long top = heap.front();
+      const long long load = (long long)(top >> 24), bin = (long long)(top & 0xFFFFFFull);
+      if (load + r.cost > B) {
         ok = false;
         break;
       }
-      heap.pop();
-      heap.push({top.first + r.cost, top.second});
-      held[top.second].push_back(r.unit);
+      std::pop_heap(heap.begin(), heap.end(), std::greater<unsigned long long>());
+      heap.back() = ((unsigned long long)(load + r.cost) << 24) | (unsigned long long)bin;
+      std::push_heap(heap.begin(), heap.end(), std::greater<unsigned long long>());
+      placed.push_back({bin, r.unit});
     }
     if (!ok) continue;
+    std::sort(placed.begin(), placed.end());
     int ns = 0, c = 0;
     for (long long u = 0; u < U; ++u)
       for (long long k = 0; k < pages_u[u] / piece; ++k) {
@@ -358,17 +388,14 @@ int plan_rows(const long long *pages_u, long long U, int max_cta, int W, long lo
         segs[4 * ns + 3] = 0;
         ++ns;
       }
-    for (long long b = 0; b < bins; ++b) {
-      if (held[b].empty()) continue;
-      std::sort(held[b].begin(), held[b].end());
-      cta_seg[c++] = ns;
-      for (long long u : held[b]) {
-        segs[4 * ns + 0] = (int)u;
-        segs[4 * ns + 1] = (int)(pages_u[u] / piece * piece);
-        segs[4 * ns + 2] = (int)pages_u[u];
-        segs[4 * ns + 3] = 0;
-        ++ns;
-      }
+    for (size_t i = 0; i < placed.size(); ++i) {
+      if (i == 0 || placed[i].first != placed[i - 1].first) cta_seg[c++] = ns;
+      const long long u = placed[i].second;
+      segs[4 * ns + 0] = (int)u;
+      segs[4 * ns + 1] = (int)(pages_u[u] / piece * piece);
+      segs[4 * ns + 2] = (int)pages_u[u];
+      segs[4 * ns + 3] = 0;
+      ++ns;
     }
     cta_seg[c] = ns;
     *nseg_out = ns;
