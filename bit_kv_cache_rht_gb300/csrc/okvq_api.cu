@@ -301,8 +301,9 @@ long long split_row_cost(const int *segs, const int *cta_seg, int ncta, int W) {
 // Row-aligned split: every unit is cut into pieces of R whole rows (R W pages), one
 // CTA each, and what is left of each unit (its last pages) goes, costliest first, to
 // the least loaded CTA that holds no piece. The smallest R is taken (from the fewest
-// rows that could hold every page, trying up to 64 values and at most max_rows) for
-// which the pieces fit in max_cta CTAs and every CTA stays within a piece's cost.
+// rows that could hold every page, trying up to 64 values and at most max_rows, and
+// skipping those whose cost fills more than 99.8 % of the CTAs) for which the pieces
+// fit in max_cta CTAs and every CTA stays within a piece's cost.
 // It uses SMs the contiguous split leaves idle, and it makes every piece whole rows
 // (one 512-page unit over two CTAs: pieces of 252 pages, 21 rows, instead of 256
 // pages, 22 rows, with the units' 8-page remainders on the idle SMs). Returns the

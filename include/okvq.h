@@ -302,7 +302,8 @@ okvq_status okvq_plan_decode(const int64_t *unit_pages, int64_t units, int32_t m
  * (fewer than a piece) go, costliest first, to the least loaded CTA holding no
  * piece. Under the model "a segment costs 12 + warps * ceil(n / warps) pages" the
  * row-aligned split is taken when its costliest CTA is at least one row cheaper
- * (the smallest fitting R, trying up to 64 values). Example: 72 units of 512 pages
+ * (the smallest R that fits, trying up to 64 values and skipping those whose cost
+ * fills more than 99.8 % of the CTAs: the greedy packing needs slack). Example: 72 units of 512 pages
  * on 152 CTAs at bits 2: 144 CTAs take 252 pages (21 rows, not 22) and 8 CTAs take
  * nine 8-page remainders each. A unit's segments get consecutive partial slots in
  * page order. Inputs as okvq_plan_decode, and bits (2 or 4). Outputs: segments
