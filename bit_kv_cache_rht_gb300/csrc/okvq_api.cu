@@ -281,8 +281,9 @@ constexpr int SEG_COST_PAGES = OKVQ_SEG_COST;
 // Row cost model of a decode CTA. Its W warps take the CTA's pages in turn, so a
 // segment of n pages costs ceil(n / W) whole rows of W pages, plus ROW_SEG_COST pages
 // for the segment itself (query rotation, the page ring started empty, the merge).
-// Measured on the 3B shape: a CTA running nine 8-page segments takes ~5.1 us per
-// segment, about 24 pages of a loaded CTA's time (one row of 12 plus 12).
+// Measured with 12 warps (2-bit codes, 8 query heads per kv head): a CTA running
+// nine 8-page segments takes ~5.1 us per segment, about 24 pages of a loaded CTA's
+// time (one row of 12 plus 12).
 constexpr int ROW_SEG_COST = 12;
 
 long long row_cost(long long n, int W) { return ROW_SEG_COST + (long long)W * ((n + W - 1) / W); }
